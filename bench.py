@@ -1,0 +1,472 @@
+"""Benchmark of the GDN layer core on GB300.
+
+Prints ONE JSON line (rank 0).  A step is one pass of the layer core's
+prefill path -- gdn_conv1d_fwd + gdn_chunk_prefill + gdn_rmsnorm_gated --
+over the Qwen3.6-27B prefill workload (B=1, T=4096, 16 QK / 48 V heads,
+d=128, bf16 activations, f32 state).  `value` is prefill tokens/s with inputs
+resident in HBM; the same line carries the decode path (gdn_conv1d_update +
+gdn_recurrent_decode + gdn_rmsnorm_gated on the 27B decode workload: 64
+sequences, one token each per step) under "decode", each with the roofline
+of its dominant kernel, the end-to-end rate through host buffers ("e2e"), the
+oracle's CPU rate ("cpu_baseline") and the SM clocks seen while timing.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload (replicas:
+the layer core has no exchange step), so scaling is weak and `value` is the
+sum over ranks of tokens divided by the slowest rank's time.
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "GDN prefill tokens/s and decode tokens/s per layer; % tensor-core / HBM roofline"
+PREFILL = "qwen36_27b_prefill"
+DECODE = "qwen36_27b_decode"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+FLOP_PER_TOKEN_HEAD = 5 * 64 * 128 + 6 * 128 * 128  # 139,264 (chunked delta rule, C=64, d=128)
+
+
+def decode_kernel_bytes_per_seq(s: W.GDNShape) -> int:
+    """Algorithmic bytes of the recurrent-decode kernel per sequence-step: read
+    and write each f32 state once, read q/k/v (bf16) and a, b, write o."""
+    state = s.H_v * 2 * s.d_k * s.d_v * 4
+    return state + (s.conv_dim + 2 * s.H_v + s.H_v * s.d_v) * 2
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary of `kernel`, valid
+    only while the kernel's source is unchanged (sha256 recorded with it)."""
+    path = os.path.join(ROOT, "profiles", f"ncu_traffic_{kernel}.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            m = re.match(r"^(\w+)\s*=\s*(\S+)", line.strip())
+            if m:
+                kv[m.group(1)] = m.group(2)
+    src = os.path.join(ROOT, "gated_deltanet_linear_core_gb300", "csrc", kv.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != kv.get("source_sha256"):
+            return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled every 200 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.rows = []
+        self.proc = None
+        self.marks = []
+        args = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                "-lms", "200"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            if uuid and not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+            args += ["-i", uuid]
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(args, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append((time.time(), parts))
+
+    def mark(self, on: bool):
+        self.marks.append((time.time(), on))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        spans, start = [], None
+        for t, on in self.marks:
+            if on:
+                start = t
+            elif start is not None:
+                spans.append((start - 0.25, t + 0.25))
+                start = None
+        rows = [p for t, p in self.rows if any(a <= t <= b for a, b in spans)] or \
+            [p for _, p in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+def max_over_ranks(dist, x: float, dev) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, dev):
+    if dist is not None:
+        dist.barrier(device_ids=[dev.index] if dev.type == "cuda" else None)
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import gated_deltanet_linear_core_gb300 as gdn
+    from gated_deltanet_linear_core_gb300 import build as gbuild
+    gbuild.build()
+
+    dist, rank, world, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    pk = peaks()
+
+    wp = W.WORKLOADS[PREFILL]
+    s = wp.shape
+    dims = gdn.GDNDims(s.H_k, s.H_v, s.d_k, s.d_v)
+    inp = W.workload_inputs(PREFILL)
+    T = int(inp["mixed_qkv"].shape[0])
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.empty_like(d["mixed_qkv"])
+    conv_out = torch.empty((1, s.conv_dim, 3), dtype=wp.dtype, device=dev)
+    S = torch.empty((1, s.H_v, s.d_k, s.d_v), dtype=torch.float32, device=dev)
+    o = torch.empty((T, s.H_v, s.d_v), dtype=wp.dtype, device=dev)
+    out = torch.empty((T, s.H_v * s.d_v), dtype=wp.dtype, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def prefill_step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        gdn.gdn_conv1d_fwd(d["mixed_qkv"], d["conv_w"], dims, None, None, conv_out, y=y)
+        if ev:
+            ev[1].record(stream)
+        gdn.gdn_chunk_prefill(y, dims, d["a"], d["b"], d["A_log"], d["dt_bias"], final_state=S,
+                              o=o)
+        if ev:
+            ev[2].record(stream)
+        gdn.gdn_rmsnorm_gated(o, d["z"], d["norm_w"], dims, out=out)
+        if ev:
+            ev[3].record(stream)
+
+    clocks = ClockSampler(local)
+    launches = 0
+
+    # ---- prefill, device-resident inputs
+    for _ in range(args.warmup):
+        flush.zero_()
+        prefill_step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    clocks.mark(True)
+    for k in range(args.steps):
+        flush.zero_()  # L2 flush between steps, outside the timed events
+        prefill_step(evs[k])
+    torch.cuda.synchronize(dev)
+    clocks.mark(False)
+    barrier(dist, dev)
+    launches += args.steps * 4  # conv (2 kernels), chunk, norm
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    chunk_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    norm_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_s = max_over_ranks(dist, sum(step_ms) / 1e3, dev)
+    value = world * T * args.steps / total_s
+    chunk_avg = sum(chunk_ms) / len(chunk_ms) / 1e3
+    flops = FLOP_PER_TOKEN_HEAD * T * s.H_v
+    achieved_tf = flops / chunk_avg / 1e12
+    ncu_bytes = traffic_record("chunk_prefill")
+    roofline = {"kernel": "gdn_chunk_prefill", "bound": "tensor", "achieved": round(achieved_tf, 2),
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved_tf / pk["bf16_tflops"], 4),
+                "peak_source": pk["source"] + " (bf16 burst)",
+                "traffic": ncu_bytes, "algorithmic_flop_per_launch": flops}
+
+    # ---- decode (64 sequences x one token per step)
+    wd = W.WORKLOADS[DECODE]
+    B = wd.decode_batch
+    nd = min(wd.decode_steps, args.decode_steps)
+    dinp = W.workload_inputs(DECODE)
+    dd = {k: v.to(dev) for k, v in dinp.items()}
+    Sd = dd["S0"].clone()
+    csd = dd["conv_state0"].clone()
+    yd = torch.empty((B, s.conv_dim), dtype=wd.dtype, device=dev)
+    od = torch.empty((B, s.H_v, s.d_v), dtype=wd.dtype, device=dev)
+    outd = torch.empty((B, s.H_v * s.d_v), dtype=wd.dtype, device=dev)
+
+    def decode_step(t, ev=None):
+        if ev:
+            ev[0].record(stream)
+        gdn.gdn_conv1d_update(dd["qkv"][t], dd["conv_w"], csd, dims, y=yd)
+        if ev:
+            ev[1].record(stream)
+        gdn.gdn_recurrent_decode(yd, Sd, dims, dd["a"][t], dd["b"][t], dd["A_log"], dd["dt_bias"],
+                                 o=od)
+        if ev:
+            ev[2].record(stream)
+        gdn.gdn_rmsnorm_gated(od, dd["z"][t], dd["norm_w"], dims, out=outd)
+        if ev:
+            ev[3].record(stream)
+
+    for t in range(min(args.warmup, nd)):
+        flush.zero_()
+        decode_step(t)
+    devs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nd)]
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    clocks.mark(True)
+    for t in range(nd):
+        flush.zero_()
+        decode_step(t, devs[t])
+    torch.cuda.synchronize(dev)
+    clocks.mark(False)
+    barrier(dist, dev)
+    launches += nd * 3
+    dstep_ms = [e[0].elapsed_time(e[3]) for e in devs]
+    dker_ms = [e[1].elapsed_time(e[2]) for e in devs]
+    dtotal = max_over_ranks(dist, sum(dstep_ms) / 1e3, dev)
+    dec_value = world * B * nd / dtotal
+    dbytes = B * decode_kernel_bytes_per_seq(s)
+    dker_avg = sum(dker_ms) / len(dker_ms) / 1e3
+    d_gbs = dbytes / dker_avg / 1e9
+    decode = {
+        "workload": DECODE, "value": round(dec_value, 1), "unit": "tokens/s",
+        "ms_per_step": round(sum(dstep_ms) / nd, 4), "steps": nd, "batch": B,
+        "per_kernel_ms": {"conv1d_update": round(statistics.mean(
+            [e[0].elapsed_time(e[1]) for e in devs]), 4),
+            "recurrent_decode": round(dker_avg * 1e3, 4),
+            "rmsnorm_gated": round(statistics.mean([e[2].elapsed_time(e[3]) for e in devs]), 4)},
+        "roofline": {"kernel": "gdn_recurrent_decode", "bound": "hbm", "achieved": round(d_gbs, 1),
+                     "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(d_gbs / pk["hbm_gbs"], 4),
+                     "peak_source": pk["source"] + " (HBM copy)",
+                     "traffic": traffic_record("recurrent_decode"),
+                     "algorithmic_bytes_per_launch": dbytes},
+        "l2": "flushed between steps",
+    }
+
+    # ---- end to end through the public API with pinned host buffers
+    names = ("mixed_qkv", "z", "a", "b")
+    hin = {k: inp[k].pin_memory() for k in names}
+    hout = torch.empty((T, s.H_v * s.d_v), dtype=wp.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = hout.numel() * hout.element_size()
+    dev_in = {k: torch.empty_like(hin[k], device=dev) for k in names}
+
+    def e2e_step():
+        for k in names:
+            dev_in[k].copy_(hin[k], non_blocking=True)
+        r = gdn.gdn_layer_prefill(dev_in["mixed_qkv"], dev_in["z"], dev_in["a"], dev_in["b"],
+                                  d["conv_w"], d["A_log"], d["dt_bias"], d["norm_w"], dims)
+        hout.copy_(r["out"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    clocks.mark(True)
+    for k in range(args.steps):
+        flush.zero_()
+        eev[k][0].record(stream)
+        e2e_step()
+        eev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark(False)
+    barrier(dist, dev)
+    launches += args.steps * 4
+    e_total = max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in eev) / 1e3, dev)
+    e2e = {"value": round(world * T * args.steps / e_total, 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": round(e_total * 1e3 / args.steps, 4)}
+    clocks.stop()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, s, args.cpu_tokens)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_s * 1e3 / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, random layer parameters)",
+            "config": {"workload": PREFILL, "tokens_per_step": T, "H_k": s.H_k, "H_v": s.H_v,
+                       "d_k": s.d_k, "d_v": s.d_v, "chunk": 64, "state": "f32",
+                       "l2": "flushed (512 MiB write) between timed steps",
+                       "parallelism": f"replicas x{world}"},
+            "per_kernel_ms": {"conv1d_fwd": round(statistics.mean(conv_ms), 4),
+                              "chunk_prefill": round(statistics.mean(chunk_ms), 4),
+                              "rmsnorm_gated": round(statistics.mean(norm_ms), 4)},
+            "roofline": roofline,
+            "decode": decode,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": launches,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(inp, s, tokens):
+    """The oracle (as it stands) on the first `tokens` tokens of the workload,
+    all heads, on this host's cores."""
+    import oracle
+    f = W.to_f64
+    args = [f(inp[k][:tokens]) for k in ("mixed_qkv", "z", "a", "b")]
+    params = [f(inp[k]) for k in ("conv_w", "A_log", "dt_bias", "norm_w")]
+    t0 = time.perf_counter()
+    oracle.layer_prefill(*args, *params, s.H_k, s.H_v, s.d_k, s.d_v)
+    dt = time.perf_counter() - t0
+    return {"value": round(tokens / dt, 2), "unit": "tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"first {tokens} tokens of {PREFILL} (all {s.H_v} heads), f64, {dt:.2f} s"}
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The CPU oracle timed as the reference implementation, on a bounded
+    sample per step of the same workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wp = W.WORKLOADS[PREFILL]
+    s = wp.shape
+    inp = W.workload_inputs(PREFILL)
+    tokens = args.ref_tokens
+    f = W.to_f64
+    params = [f(inp[k]) for k in ("conv_w", "A_log", "dt_bias", "norm_w")]
+    T = int(inp["mixed_qkv"].shape[0])
+
+    def step(k):
+        t0 = (k * tokens) % max(1, T - tokens)
+        xs = [f(inp[n][t0:t0 + tokens]) for n in ("mixed_qkv", "z", "a", "b")]
+        a = time.perf_counter()
+        oracle.layer_prefill(*xs, *params, s.H_k, s.H_v, s.d_k, s.d_v)
+        return time.perf_counter() - a
+
+    for k in range(args.warmup):
+        step(k)
+    times = [step(k) for k in range(args.steps)]
+    total = sum(times)
+    value = tokens * args.steps / total
+    cores = oracle.max_threads()
+    sample = (f"{tokens} tokens per step (all {s.H_v} heads) of {PREFILL}, f64 oracle, "
+              f"{cores} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) activations, random layer parameters)",
+        "config": {"workload": PREFILL, "tokens_per_step": tokens, "H_k": s.H_k, "H_v": s.H_v,
+                   "d_k": s.d_k, "d_v": s.d_v},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--cpu-tokens", type=int, default=512)
+    ap.add_argument("--ref-tokens", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,253 @@
+"""Gated DeltaNet (GDN) linear-attention layer core for GB300 (sm_103a).
+
+A thin binding of the C ABI in include/gdn.h (libgdn.so, hand-written CUDA
+kernels).  The functions below only marshal arguments: they check tensor
+placement and layout, allocate outputs with torch when the caller passes none,
+and call the library on the current CUDA stream.  Every step of the layer runs
+in the library's kernels; if libgdn.so is missing, every call raises.
+
+Layer core (cortex commit "feat(stage-8c): linear-attention layer (Qwen3-Next
+GatedDeltaNet)"): conv1d(k=4)+SiLU -> split [q|k|v] -> l2norm(q,k), gates
+g = -exp(A_log) softplus(a+dt_bias), beta = sigmoid(b) -> gated delta rule
+(chunked prefill or per-token decode) -> RMSNormGated(o, z).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import GDNError, GDN_QK_L2NORM  # noqa: F401
+
+__all__ = [
+    "GDNDims", "GDNError", "gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
+    "gdn_chunk_prefill_workspace_size", "gdn_recurrent_decode", "gdn_rmsnorm_gated",
+    "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_layer_prefill", "gdn_layer_decode",
+    "library_path",
+]
+
+RMSNORM_EPS = 1e-6
+
+
+@dataclass(frozen=True)
+class GDNDims:
+    """H_k query/key heads, H_v value heads, head dims d_k = d_v, conv width 4."""
+    H_k: int
+    H_v: int
+    d_k: int
+    d_v: int
+    conv_k: int = 4
+
+    @property
+    def conv_dim(self) -> int:
+        return 2 * self.H_k * self.d_k + self.H_v * self.d_v
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _dims(d) -> _lib.Dims:
+    return _lib.Dims(int(d.H_k), int(d.H_v), int(d.d_k), int(d.d_v), int(getattr(d, "conv_k", 4)))
+
+
+def _conv_dim(d) -> int:
+    return 2 * int(d.H_k) * int(d.d_k) + int(d.H_v) * int(d.d_v)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _lib.GDN_BF16
+    if t.dtype == torch.float32:
+        return _lib.GDN_F32
+    raise TypeError(f"unsupported activation dtype {t.dtype} (bfloat16 or float32)")
+
+
+def _ptr(t, name, dtype=None, shape=None):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor (got {t.device})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr() if t.numel() else None
+
+
+def _stream(t: torch.Tensor, stream):
+    if stream is not None:
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _nseq(cu_seqlens):
+    return 1 if cu_seqlens is None else int(cu_seqlens.numel()) - 1
+
+
+def gdn_ckpt_count(cu_seqlens, every: int) -> int:
+    """Checkpoint rows for packed sequences (host offsets: list, numpy or CPU tensor)."""
+    cu = torch.as_tensor(cu_seqlens, dtype=torch.int32, device="cpu").contiguous()
+    r = _lib.load().gdn_ckpt_count(cu.data_ptr(), int(cu.numel()) - 1, int(every))
+    if r < 0:
+        raise ValueError("invalid cu_seqlens or checkpoint interval")
+    return int(r)
+
+
+def gdn_check_cu_seqlens(cu_seqlens: torch.Tensor, T_tot: int, stream=None) -> None:
+    """Validates device offsets (synchronises the stream)."""
+    p = _ptr(cu_seqlens, "cu_seqlens", torch.int32)
+    _lib.check(_lib.load().gdn_check_cu_seqlens(p, _nseq(cu_seqlens), int(T_tot),
+                                               _stream(cu_seqlens, stream)),
+               "gdn_check_cu_seqlens")
+
+
+def gdn_conv1d_fwd(x, w, dims, cu_seqlens=None, conv_state_in=None, conv_state_out=None,
+                   ckpt_every=0, conv_ckpt_out=None, apply_silu=True, y=None, stream=None):
+    """Prefill depthwise causal conv1d(k=4) with state prepend (+SiLU).
+    x [T, conv_dim]; w [conv_dim, 4]; states [n_seq, conv_dim, 3];
+    checkpoints [rows, conv_dim, 3].  Returns y [T, conv_dim]."""
+    dt = x.dtype
+    T, C = x.shape
+    if C != _conv_dim(dims):
+        raise ValueError(f"x has {C} channels, dims give {_conv_dim(dims)}")
+    if y is None:
+        y = torch.empty_like(x)
+    rows = 0 if conv_ckpt_out is None else int(conv_ckpt_out.shape[0])
+    st = _lib.load().gdn_conv1d_fwd(
+        _ptr(x, "x", dt), _ptr(w, "w", dt, (C, 4)), _ptr(cu_seqlens, "cu_seqlens", torch.int32),
+        _nseq(cu_seqlens), T, _ptr(conv_state_in, "conv_state_in", dt),
+        _ptr(conv_state_out, "conv_state_out", dt), int(ckpt_every),
+        _ptr(conv_ckpt_out, "conv_ckpt_out", dt), rows, int(bool(apply_silu)),
+        _ptr(y, "y", dt, (T, C)), _dims(dims), _dtype_code(x), _stream(x, stream))
+    _lib.check(st, "gdn_conv1d_fwd")
+    return y
+
+
+def gdn_conv1d_update(x, w, conv_state, dims, apply_silu=True, y=None, stream=None):
+    """Decode conv for B sequences; conv_state [B, conv_dim, 3] shifted in place."""
+    dt = x.dtype
+    B, C = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    st = _lib.load().gdn_conv1d_update(
+        _ptr(x, "x", dt), _ptr(w, "w", dt, (C, 4)), _ptr(conv_state, "conv_state", dt, (B, C, 3)),
+        B, int(bool(apply_silu)), _ptr(y, "y", dt, (B, C)), _dims(dims), _dtype_code(x),
+        _stream(x, stream))
+    _lib.check(st, "gdn_conv1d_update")
+    return y
+
+
+def gdn_chunk_prefill_workspace_size(n_seq: int, T_tot: int, dims, dtype) -> int:
+    code = _lib.GDN_BF16 if dtype == torch.bfloat16 else _lib.GDN_F32
+    return int(_lib.load().gdn_chunk_prefill_workspace_size(int(n_seq), int(T_tot), _dims(dims),
+                                                            code))
+
+
+def _gate_ptrs(a, b, A_log, dt_bias, g, beta, dt):
+    return (_ptr(a, "a", dt), _ptr(b, "b", dt), _ptr(A_log, "A_log", torch.float32),
+            _ptr(dt_bias, "dt_bias", torch.float32), _ptr(g, "g", torch.float32),
+            _ptr(beta, "beta", torch.float32))
+
+
+def gdn_chunk_prefill(qkv, dims, a=None, b=None, A_log=None, dt_bias=None, g=None, beta=None,
+                      cu_seqlens=None, initial_state=None, final_state=None, ckpt_every=0,
+                      state_ckpt_out=None, scale=0.0, l2norm_qk=True, o=None, workspace=None,
+                      stream=None):
+    """Chunked gated delta rule over packed sequences.  qkv [T, conv_dim]
+    (post-conv); states [n_seq, H_v, d_k, d_v] f32; returns o [T, H_v, d_v]."""
+    dt = qkv.dtype
+    T = int(qkv.shape[0])
+    if o is None:
+        o = torch.empty((T, dims.H_v, dims.d_v), dtype=dt, device=qkv.device)
+    rows = 0 if state_ckpt_out is None else int(state_ckpt_out.shape[0])
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lib = _lib.load()
+    st = lib.gdn_chunk_prefill(
+        _ptr(qkv, "qkv", dt), *_gate_ptrs(a, b, A_log, dt_bias, g, beta, dt),
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32), _nseq(cu_seqlens), T,
+        _ptr(initial_state, "initial_state", torch.float32),
+        _ptr(final_state, "final_state", torch.float32), int(ckpt_every),
+        _ptr(state_ckpt_out, "state_ckpt_out", torch.float32), rows, float(scale),
+        _lib.GDN_QK_L2NORM if l2norm_qk else 0, _ptr(o, "o", dt), _ptr(workspace, "workspace"),
+        ws, _dims(dims), _dtype_code(qkv), _stream(qkv, stream))
+    _lib.check(st, "gdn_chunk_prefill")
+    return o
+
+
+def gdn_recurrent_decode(qkv, state, dims, a=None, b=None, A_log=None, dt_bias=None, g=None,
+                         beta=None, scale=0.0, l2norm_qk=True, o=None, stream=None):
+    """One decode step for B sequences; state [B, H_v, d_k, d_v] f32 in place.
+    Returns o [B, H_v, d_v]."""
+    dt = qkv.dtype
+    B = int(qkv.shape[0])
+    if o is None:
+        o = torch.empty((B, dims.H_v, dims.d_v), dtype=dt, device=qkv.device)
+    st = _lib.load().gdn_recurrent_decode(
+        _ptr(qkv, "qkv", dt), *_gate_ptrs(a, b, A_log, dt_bias, g, beta, dt),
+        _ptr(state, "state", torch.float32, (B, dims.H_v, dims.d_k, dims.d_v)), B, float(scale),
+        _lib.GDN_QK_L2NORM if l2norm_qk else 0, _ptr(o, "o", dt), _dims(dims), _dtype_code(qkv),
+        _stream(qkv, stream))
+    _lib.check(st, "gdn_recurrent_decode")
+    return o
+
+
+def gdn_rmsnorm_gated(o, z, w, dims, eps=RMSNORM_EPS, out=None, stream=None):
+    """RMSNormGated per value head: o [T, H_v, d_v], z [T, H_v*d_v] -> out [T, H_v*d_v]."""
+    dt = o.dtype
+    T = int(o.shape[0])
+    if out is None:
+        out = torch.empty((T, dims.H_v * dims.d_v), dtype=dt, device=o.device)
+    st = _lib.load().gdn_rmsnorm_gated(
+        _ptr(o, "o", dt), _ptr(z, "z", dt), _ptr(w, "w", dt, (dims.d_v,)), float(eps), T,
+        _ptr(out, "out", dt), _dims(dims), _dtype_code(o), _stream(o, stream))
+    _lib.check(st, "gdn_rmsnorm_gated")
+    return out
+
+
+def gdn_layer_prefill(mixed_qkv, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, cu_seqlens=None,
+                      initial_state=None, conv_state=None, ckpt_every=0, scale=0.0,
+                      return_intermediates=False, stream=None):
+    """Whole layer core over packed sequences: conv1d+SiLU -> chunked delta rule
+    -> RMSNormGated.  Returns a dict with out [T, H_v*d_v], final_state
+    [n_seq, H_v, d_k, d_v] f32, conv_state [n_seq, conv_dim, 3] and, when
+    ckpt_every > 0, state_ckpt / conv_ckpt."""
+    dev, dt = mixed_qkv.device, mixed_qkv.dtype
+    n_seq = _nseq(cu_seqlens)
+    C = _conv_dim(dims)
+    rows = 0
+    if ckpt_every:
+        host_cu = (cu_seqlens.to("cpu") if cu_seqlens is not None
+                   else torch.tensor([0, mixed_qkv.shape[0]], dtype=torch.int32))
+        rows = gdn_ckpt_count(host_cu, ckpt_every)
+    conv_out = torch.empty((n_seq, C, 3), dtype=dt, device=dev)
+    conv_ck = torch.empty((rows, C, 3), dtype=dt, device=dev) if rows else None
+    y = gdn_conv1d_fwd(mixed_qkv, conv_w, dims, cu_seqlens, conv_state, conv_out, ckpt_every,
+                       conv_ck, True, stream=stream)
+    S = torch.empty((n_seq, dims.H_v, dims.d_k, dims.d_v), dtype=torch.float32, device=dev)
+    S_ck = (torch.empty((rows, dims.H_v, dims.d_k, dims.d_v), dtype=torch.float32, device=dev)
+            if rows else None)
+    o = gdn_chunk_prefill(y, dims, a, b, A_log, dt_bias, cu_seqlens=cu_seqlens,
+                          initial_state=initial_state, final_state=S, ckpt_every=ckpt_every,
+                          state_ckpt_out=S_ck, scale=scale, stream=stream)
+    out = gdn_rmsnorm_gated(o, z, norm_w, dims, stream=stream)
+    r = {"out": out, "final_state": S, "conv_state": conv_out, "state_ckpt": S_ck,
+         "conv_ckpt": conv_ck}
+    if return_intermediates:
+        r.update({"y": y, "o": o})
+    return r
+
+
+def gdn_layer_decode(x, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, state, conv_state,
+                     scale=0.0, stream=None):
+    """One decode step of the layer core for B sequences (x [B, conv_dim]);
+    state and conv_state are updated in place.  Returns out [B, H_v*d_v]."""
+    y = gdn_conv1d_update(x, conv_w, conv_state, dims, True, stream=stream)
+    o = gdn_recurrent_decode(y, state, dims, a, b, A_log, dt_bias, scale=scale, stream=stream)
+    return gdn_rmsnorm_gated(o, z, norm_w, dims, stream=stream)

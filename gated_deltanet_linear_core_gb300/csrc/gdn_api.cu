@@ -1,0 +1,243 @@
+// C ABI of the GDN layer core: argument validation and dispatch.
+//
+// Every entry point validates all of its arguments on the host before it
+// launches anything; no device memory is read here (except in
+// gdn_check_cu_seqlens, which says so).  No exception crosses the ABI.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <vector>
+
+#include "gdn.h"
+#include "gdn_launch.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_n(const void* p, size_t n) {
+    return p == nullptr || (reinterpret_cast<uintptr_t>(p) % n) == 0;
+}
+size_t elem_size(gdn_dtype_t dt) { return dt == GDN_BF16 ? 2 : 4; }
+
+gdn_status_t check_dims(const gdn_dims_t& d, gdn_dtype_t dt) {
+    if (dt != GDN_F32 && dt != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (d.H_k <= 0 || d.H_v <= 0 || d.d_k <= 0 || d.d_v <= 0 || d.conv_k <= 0)
+        return GDN_ERR_INVALID_ARG;
+    if (d.H_v % d.H_k != 0) return GDN_ERR_INVALID_ARG;
+    if (d.conv_k != 4) return GDN_ERR_UNSUPPORTED;
+    if (d.d_k != d.d_v) return GDN_ERR_UNSUPPORTED;
+    if (d.d_k != 16 && d.d_k != 128) return GDN_ERR_UNSUPPORTED;
+    if ((int64_t)d.H_v * d.d_v > (1 << 24) || (int64_t)d.H_k * d.d_k > (1 << 24))
+        return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+int64_t conv_dim_of(const gdn_dims_t& d) { return 2LL * d.H_k * d.d_k + (int64_t)d.H_v * d.d_v; }
+
+gdn_status_t cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return GDN_OK;
+    g_last_cuda_error = (int)e;
+    return GDN_ERR_CUDA;
+}
+
+gdn_status_t check_ckpt(int32_t every, const void* ckpt, int64_t rows) {
+    if (every < 0) return GDN_ERR_INVALID_ARG;
+    if (every > 0) {
+        if (every % 64 != 0) return GDN_ERR_INVALID_ARG;
+        if (ckpt == nullptr || rows < 0) return GDN_ERR_INVALID_ARG;
+    }
+    return GDN_OK;
+}
+
+gdn_status_t check_seqs(const int32_t* cu, int32_t n_seq, int64_t T) {
+    if (T < 0 || T > (int64_t)INT32_MAX) return GDN_ERR_INVALID_ARG;
+    if (cu == nullptr) return n_seq == 1 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (n_seq < 1 || n_seq > (1 << 24)) return GDN_ERR_INVALID_ARG;
+    if (!aligned_n(cu, 4)) return GDN_ERR_ALIGN;
+    return GDN_OK;
+}
+
+// gates: either (a, b, A_log, dt_bias) or (g, beta)
+gdn_status_t check_gates(const void* a, const void* b, const float* A_log, const float* dt_bias,
+                         const float* g, const float* beta, gdn_dtype_t dt) {
+    const bool raw = a && b && A_log && dt_bias;
+    const bool pre = g && beta;
+    if (!raw && !pre) return GDN_ERR_INVALID_ARG;
+    if (!aligned_n(a, elem_size(dt)) || !aligned_n(b, elem_size(dt)) || !aligned_n(A_log, 4) ||
+        !aligned_n(dt_bias, 4) || !aligned_n(g, 4) || !aligned_n(beta, 4))
+        return GDN_ERR_ALIGN;
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status_t s) {
+    switch (s) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument";
+        case GDN_ERR_ALIGN: return "device pointer not 16-byte aligned";
+        case GDN_ERR_UNSUPPORTED: return "unsupported dimensions";
+        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDN_ERR_CUDA: return "CUDA error";
+        case GDN_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+int gdn_last_cuda_error(void) { return g_last_cuda_error; }
+
+int gdn_version(void) { return (1 << 16) | 0; }
+
+int64_t gdn_ckpt_count(const int32_t* cu, int32_t n_seq, int32_t every) {
+    if (cu == nullptr || n_seq < 1 || every < 0) return -1;
+    if (every == 0) return 0;
+    int64_t r = 0;
+    for (int32_t i = 0; i < n_seq; ++i) {
+        if (cu[i + 1] < cu[i]) return -1;
+        r += (int64_t)(cu[i + 1] - cu[i]) / every;
+    }
+    return r;
+}
+
+gdn_status_t gdn_check_cu_seqlens(const int32_t* cu, int32_t n_seq, int64_t T, void* stream) {
+    if (cu == nullptr || n_seq < 1 || T < 0) return GDN_ERR_INVALID_ARG;
+    std::vector<int32_t> h((size_t)n_seq + 1);
+    cudaError_t e = cudaMemcpyAsync(h.data(), cu, sizeof(int32_t) * h.size(),
+                                    cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (h[0] != 0 || h[(size_t)n_seq] != T) return GDN_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n_seq; ++i)
+        if (h[(size_t)i + 1] < h[(size_t)i]) return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+gdn_status_t gdn_conv1d_fwd(const void* x, const void* w, const int32_t* cu_seqlens, int32_t n_seq,
+                            int64_t T_tot, const void* conv_state_in, void* conv_state_out,
+                            int32_t ckpt_every, void* conv_ckpt_out, int64_t ckpt_rows,
+                            int32_t apply_silu, void* y, gdn_dims_t dims, gdn_dtype_t dtype,
+                            void* stream) {
+    gdn_status_t st = check_dims(dims, dtype);
+    if (st != GDN_OK) return st;
+    if ((st = check_seqs(cu_seqlens, n_seq, T_tot)) != GDN_OK) return st;
+    if ((st = check_ckpt(ckpt_every, conv_ckpt_out, ckpt_rows)) != GDN_OK) return st;
+    if (w == nullptr || (T_tot > 0 && (x == nullptr || y == nullptr))) return GDN_ERR_INVALID_ARG;
+    if (x != nullptr && x == y) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || !aligned16(conv_state_in) ||
+        !aligned16(conv_state_out) || !aligned16(conv_ckpt_out))
+        return GDN_ERR_ALIGN;
+    gdn::ConvArgs a;
+    a.x = x; a.w = w; a.cu = cu_seqlens; a.n_seq = n_seq; a.T = T_tot;
+    a.C = (int)conv_dim_of(dims);
+    a.state_in = conv_state_in; a.state_out = conv_state_out;
+    a.ckpt_every = ckpt_every; a.ckpt = ckpt_every > 0 ? conv_ckpt_out : nullptr;
+    a.ckpt_rows = ckpt_rows; a.silu = apply_silu != 0; a.y = y;
+    return cuda_status(gdn::launch_conv1d_fwd(a, dtype, (cudaStream_t)stream));
+}
+
+gdn_status_t gdn_conv1d_update(const void* x, const void* w, void* conv_state, int32_t B,
+                               int32_t apply_silu, void* y, gdn_dims_t dims, gdn_dtype_t dtype,
+                               void* stream) {
+    gdn_status_t st = check_dims(dims, dtype);
+    if (st != GDN_OK) return st;
+    if (B < 0 || B > INT32_MAX / 2) return GDN_ERR_INVALID_ARG;
+    if (B > 0 && (x == nullptr || w == nullptr || conv_state == nullptr || y == nullptr))
+        return GDN_ERR_INVALID_ARG;
+    if (x != nullptr && x == y) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(conv_state) || !aligned16(y))
+        return GDN_ERR_ALIGN;
+    return cuda_status(gdn::launch_conv1d_update(x, w, conv_state, B, (int)conv_dim_of(dims),
+                                                 apply_silu != 0, y, dtype, (cudaStream_t)stream));
+}
+
+size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t dims,
+                                        gdn_dtype_t dtype) {
+    (void)n_seq; (void)T_tot; (void)dims; (void)dtype;
+    return 0;
+}
+
+gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, const float* A_log,
+                               const float* dt_bias, const float* g, const float* beta,
+                               const int32_t* cu_seqlens, int32_t n_seq, int64_t T_tot,
+                               const float* initial_state, float* final_state, int32_t ckpt_every,
+                               float* state_ckpt_out, int64_t ckpt_rows, float scale,
+                               uint32_t flags, void* o, void* workspace, size_t ws_bytes,
+                               gdn_dims_t dims, gdn_dtype_t dtype, void* stream) {
+    gdn_status_t st = check_dims(dims, dtype);
+    if (st != GDN_OK) return st;
+    if ((st = check_seqs(cu_seqlens, n_seq, T_tot)) != GDN_OK) return st;
+    if ((st = check_ckpt(ckpt_every, state_ckpt_out, ckpt_rows)) != GDN_OK) return st;
+    if (T_tot > 0 && (st = check_gates(a, b, A_log, dt_bias, g, beta, dtype)) != GDN_OK) return st;
+    if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return GDN_ERR_INVALID_ARG;
+    if (T_tot > 0 && (qkv == nullptr || o == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(qkv) || !aligned16(o) || !aligned16(initial_state) || !aligned16(final_state) ||
+        !aligned16(state_ckpt_out))
+        return GDN_ERR_ALIGN;
+    const size_t need = gdn_chunk_prefill_workspace_size(n_seq, T_tot, dims, dtype);
+    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return GDN_ERR_WORKSPACE;
+    if ((int64_t)n_seq * dims.H_v * 8 > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+
+    gdn::DeltaArgs d;
+    memset(&d, 0, sizeof(d));
+    d.qkv = qkv; d.a = a; d.b = b; d.A_log = A_log; d.dt_bias = dt_bias;
+    const bool pre = g && beta;
+    d.g = pre ? g : nullptr; d.beta = pre ? beta : nullptr;
+    d.cu = cu_seqlens; d.n_seq = n_seq; d.T = T_tot;
+    d.H_k = dims.H_k; d.H_v = dims.H_v; d.D = dims.d_k;
+    d.S0 = initial_state; d.S_final = final_state;
+    d.ckpt_every = ckpt_every; d.ckpt = ckpt_every > 0 ? state_ckpt_out : nullptr;
+    d.ckpt_rows = ckpt_rows;
+    d.scale = scale == 0.f ? 1.0f / sqrtf((float)dims.d_k) : scale;
+    d.l2norm = (flags & GDN_QK_L2NORM) != 0;
+    d.o = o;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (gdn::chunk_tc_supported(d, dtype)) return cuda_status(gdn::launch_chunk_tc(d, s));
+    return cuda_status(gdn::launch_chunk_ffma(d, dtype, s));
+}
+
+gdn_status_t gdn_recurrent_decode(const void* qkv, const void* a, const void* b,
+                                  const float* A_log, const float* dt_bias, const float* g,
+                                  const float* beta, float* state, int32_t B, float scale,
+                                  uint32_t flags, void* o, gdn_dims_t dims, gdn_dtype_t dtype,
+                                  void* stream) {
+    gdn_status_t st = check_dims(dims, dtype);
+    if (st != GDN_OK) return st;
+    if (B < 0 || (int64_t)B * dims.H_v > INT32_MAX) return GDN_ERR_INVALID_ARG;
+    if (B > 0 && (st = check_gates(a, b, A_log, dt_bias, g, beta, dtype)) != GDN_OK) return st;
+    if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return GDN_ERR_INVALID_ARG;
+    if (B > 0 && (qkv == nullptr || state == nullptr || o == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(qkv) || !aligned16(state) || !aligned16(o)) return GDN_ERR_ALIGN;
+    gdn::DeltaArgs d;
+    memset(&d, 0, sizeof(d));
+    d.qkv = qkv; d.a = a; d.b = b; d.A_log = A_log; d.dt_bias = dt_bias;
+    const bool pre = g && beta;
+    d.g = pre ? g : nullptr; d.beta = pre ? beta : nullptr;
+    d.n_seq = B; d.T = B;
+    d.H_k = dims.H_k; d.H_v = dims.H_v; d.D = dims.d_k;
+    d.S0 = state; d.S_final = state;
+    d.scale = scale == 0.f ? 1.0f / sqrtf((float)dims.d_k) : scale;
+    d.l2norm = (flags & GDN_QK_L2NORM) != 0;
+    d.o = o;
+    return cuda_status(gdn::launch_recurrent_decode(d, dtype, (cudaStream_t)stream));
+}
+
+gdn_status_t gdn_rmsnorm_gated(const void* o, const void* z, const void* w, float eps, int64_t T,
+                               void* out, gdn_dims_t dims, gdn_dtype_t dtype, void* stream) {
+    gdn_status_t st = check_dims(dims, dtype);
+    if (st != GDN_OK) return st;
+    if (T < 0 || !(eps > 0.f) || !isfinite(eps)) return GDN_ERR_INVALID_ARG;
+    if (w == nullptr || (T > 0 && (o == nullptr || z == nullptr || out == nullptr)))
+        return GDN_ERR_INVALID_ARG;
+    if (!aligned16(o) || !aligned16(z) || !aligned16(w) || !aligned16(out)) return GDN_ERR_ALIGN;
+    return cuda_status(gdn::launch_rmsnorm_gated(o, z, w, eps, T, dims.H_v, dims.d_v, out, dtype,
+                                                 (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,128 @@
+// Shared device helpers of the GDN layer-core kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------- scalar conversion
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---------------------------------------------------------------- 16-byte vectors
+// VecN<T>::N elements of T fill one 16-byte (128-bit) access.
+template <typename T> struct Vec16 { static constexpr int N = 16 / sizeof(T); };
+
+template <typename T>
+__device__ __forceinline__ void load16(const T* __restrict__ p, float* out) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    if constexpr (sizeof(T) == 4) {
+        out[0] = __uint_as_float(u.x); out[1] = __uint_as_float(u.y);
+        out[2] = __uint_as_float(u.z); out[3] = __uint_as_float(u.w);
+    } else {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            out[2 * i] = __uint_as_float(w[i] << 16);
+            out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+}
+
+// Streaming variant: no L1 allocation (data read once).
+template <typename T>
+__device__ __forceinline__ void load16_stream(const T* __restrict__ p, float* out) {
+    uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
+    if constexpr (sizeof(T) == 4) {
+        out[0] = __uint_as_float(u.x); out[1] = __uint_as_float(u.y);
+        out[2] = __uint_as_float(u.z); out[3] = __uint_as_float(u.w);
+    } else {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            out[2 * i] = __uint_as_float(w[i] << 16);
+            out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <typename T>
+__device__ __forceinline__ void store16(T* __restrict__ p, const float* in) {
+    uint4 u;
+    if constexpr (sizeof(T) == 4) {
+        u.x = __float_as_uint(in[0]); u.y = __float_as_uint(in[1]);
+        u.z = __float_as_uint(in[2]); u.w = __float_as_uint(in[3]);
+    } else {
+        u.x = pack_bf16x2(in[0], in[1]); u.y = pack_bf16x2(in[2], in[3]);
+        u.z = pack_bf16x2(in[4], in[5]); u.w = pack_bf16x2(in[6], in[7]);
+    }
+    *reinterpret_cast<uint4*>(p) = u;
+}
+
+// ---------------------------------------------------------------- math
+// Full-precision CUDA math functions only (no hand-written approximations).
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+// softplus with the identity branch above 20 (cortex unit test "softplus small/large branches")
+__device__ __forceinline__ float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
+
+// g = -exp(A_log) * softplus(a + dt_bias), computed in f32 (cortex "Discretisation")
+__device__ __forceinline__ float gate_g(float a, float A_log, float dt_bias) {
+    return -expf(A_log) * softplus_f(a + dt_bias);
+}
+
+// ---------------------------------------------------------------- packed sequences
+// Clamped bounds of sequence i: 0 <= start <= end <= T.  cu == nullptr means
+// one sequence [0, T).
+__device__ __forceinline__ void seq_bounds(const int32_t* __restrict__ cu, int i, int64_t T,
+                                           int64_t& start, int64_t& end) {
+    if (cu == nullptr) { start = 0; end = T; return; }
+    int64_t s = cu[i], e = cu[i + 1];
+    s = s < 0 ? 0 : (s > T ? T : s);
+    e = e < s ? s : (e > T ? T : e);
+    start = s; end = e;
+}
+
+// Largest i in [0, n_seq) with cu[i] <= t (binary search; cu non-decreasing).
+__device__ __forceinline__ int seq_of_token(const int32_t* __restrict__ cu, int n_seq, int64_t t) {
+    if (cu == nullptr) return 0;
+    int lo = 0, hi = n_seq - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Checkpoint row offset of sequence i: sum_{j<i} floor(L_j / every).
+__device__ __forceinline__ int64_t ckpt_row0(const int32_t* __restrict__ cu, int i, int64_t T,
+                                             int every) {
+    int64_t r = 0;
+    for (int j = 0; j < i; ++j) {
+        int64_t s, e;
+        seq_bounds(cu, j, T, s, e);
+        r += (e - s) / every;
+    }
+    return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace gdn

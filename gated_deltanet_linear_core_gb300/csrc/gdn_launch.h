@@ -1,0 +1,64 @@
+// Host-side launchers of the GDN kernels (one translation unit per kernel
+// family).  Arguments are already validated by the C ABI layer in gdn_api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+struct ConvArgs {
+    const void* x;
+    const void* w;
+    const int32_t* cu;
+    int n_seq;
+    int64_t T;
+    int C;  // conv_dim
+    const void* state_in;
+    void* state_out;
+    int ckpt_every;
+    void* ckpt;
+    int64_t ckpt_rows;
+    int silu;
+    void* y;
+};
+cudaError_t launch_conv1d_fwd(const ConvArgs& a, gdn_dtype_t dt, cudaStream_t s);
+cudaError_t launch_conv1d_update(const void* x, const void* w, void* state, int B, int C,
+                                 int silu, void* y, gdn_dtype_t dt, cudaStream_t s);
+
+struct DeltaArgs {
+    const void* qkv;  // [T, conv_dim]
+    const void* a;
+    const void* b;
+    const float* A_log;
+    const float* dt_bias;
+    const float* g;
+    const float* beta;
+    const int32_t* cu;
+    int n_seq;
+    int64_t T;
+    int H_k, H_v, D;
+    const float* S0;
+    float* S_final;
+    int ckpt_every;
+    float* ckpt;
+    int64_t ckpt_rows;
+    float scale;
+    int l2norm;
+    void* o;  // [T, H_v, D]
+};
+// Chunked prefill on CUDA cores (f32 arithmetic; any supported D and dtype).
+cudaError_t launch_chunk_ffma(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s);
+// Chunked prefill on tcgen05 tensor cores (bf16 operands, f32 state), for the
+// shapes chunk_tc_supported() accepts.
+bool chunk_tc_supported(const DeltaArgs& a, gdn_dtype_t dt);
+cudaError_t launch_chunk_tc(const DeltaArgs& a, cudaStream_t s);
+// Recurrent decode: T = B tokens, sequence i = token i, state in place (S0 == S_final).
+cudaError_t launch_recurrent_decode(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s);
+
+cudaError_t launch_rmsnorm_gated(const void* o, const void* z, const void* w, float eps, int64_t T,
+                                 int H, int D, void* out, gdn_dtype_t dt, cudaStream_t s);
+
+}  // namespace gdn

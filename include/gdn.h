@@ -1,0 +1,216 @@
+/*
+ * gdn.h -- C ABI of the Gated DeltaNet (GDN) linear-attention layer core for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer core sits between the input projections and out_proj of a GDN
+ * layer of the hybrid DeltaNet/GQA models Qwen3.6-27B and Qwen3-Coder-Next:
+ *
+ *   mixed_qkv --conv1d+SiLU--> [q | k | v] --l2norm(q,k), gates g/beta-->
+ *   gated delta rule (chunked prefill or per-token decode) --> o
+ *   --RMSNormGated(o, z)--> out
+ *
+ * Definitions follow the cortex commit "feat(stage-8c): linear-attention layer
+ * (Qwen3-Next GatedDeltaNet)" (sections "Block", "Discretisation", "Delta rule
+ * (recurrent, per-token)", "Output", "State (GatedDeltaNetState)") and the
+ * NxD-Inference PR "Add Qwen3.6-27B hybrid DeltaNet/GQA contrib model and vLLM
+ * serving path" (Summary: chunked context encoding, token generation, GDN
+ * recurrent and convolution state checkpoints for hybrid prefix caching).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers marked (device) are CUDA device pointers; (host) are host memory.
+ *   The caller owns every buffer.  The library allocates nothing persistent;
+ *   the only memory it allocates is a caller-sized workspace it never asks for
+ *   (see gdn_chunk_prefill_workspace_size).
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream), except where a call says it synchronises.
+ * - Tensors are dense, row-major, in the shapes given per argument.  Device
+ *   pointers must be 16-byte aligned (GDN_ERR_ALIGN otherwise).
+ * - Arguments are validated before anything is launched.  On any error
+ *   nothing is written and nothing is launched.  No C++ exception crosses the
+ *   ABI.  GDN_ERR_CUDA means a launch failed: gdn_last_cuda_error() returns
+ *   the cudaError_t of the calling thread's last failure.
+ * - `dtype` gives the element type of the activations (x, y, qkv, z, a, b, o,
+ *   out), the conv weight, the conv state and the RMSNormGated weight.  A_log,
+ *   dt_bias, g, beta and the recurrent state are always float32.
+ * - Dimensions: H_k query/key heads, H_v value heads (a multiple of H_k),
+ *   head dims d_k = d_v = D, conv kernel width conv_k = 4,
+ *   conv_dim = 2*H_k*d_k + H_v*d_v.  Value head h reads key head
+ *   h / (H_v / H_k) (repeat_interleave order).
+ * - Supported: D in {16, 128} for GDN_F32; D = 128 for GDN_BF16 (the tensor-
+ *   core path); conv_k = 4.  Other shapes return GDN_ERR_UNSUPPORTED.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* NULL where a buffer is required, bad size or flag */
+    GDN_ERR_ALIGN = 2,       /* a device pointer is not 16-byte aligned          */
+    GDN_ERR_UNSUPPORTED = 3, /* dims the kernels do not cover                     */
+    GDN_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required        */
+    GDN_ERR_CUDA = 5,        /* a CUDA call or launch failed                      */
+    GDN_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up                */
+} gdn_status_t;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
+
+typedef struct {
+    int32_t H_k, H_v, d_k, d_v, conv_k;
+} gdn_dims_t;
+
+/* flags of gdn_chunk_prefill / gdn_recurrent_decode */
+#define GDN_QK_L2NORM 1u /* l2-normalise q and k per head (eps 1e-6 inside the sqrt) */
+
+/* Text for a status code (static storage, never NULL). */
+const char* gdn_status_string(gdn_status_t status);
+
+/* cudaError_t of the calling thread's last GDN_ERR_CUDA (0 if none). */
+int gdn_last_cuda_error(void);
+
+/* ABI version: (major << 16) | minor. */
+int gdn_version(void);
+
+/*
+ * Number of checkpoint rows for packed sequences: sum_i floor(L_i / every),
+ * L_i = cu_seqlens[i+1] - cu_seqlens[i].  cu_seqlens (host) has n_seq + 1
+ * entries.  Returns -1 on invalid input (NULL, n_seq < 1, every < 0,
+ * decreasing offsets).  every == 0 returns 0.
+ */
+int64_t gdn_ckpt_count(const int32_t* cu_seqlens, int32_t n_seq, int32_t every);
+
+/*
+ * Validates packed-sequence offsets that live on the device: cu_seqlens[0] == 0,
+ * non-decreasing, cu_seqlens[n_seq] == T_tot.  SYNCHRONISES `stream` (copies the
+ * n_seq + 1 offsets to the host).  Returns GDN_OK or GDN_ERR_INVALID_ARG.
+ * The compute calls below do not read offsets on the host; on the device they
+ * clamp every sequence to [0, T_tot) so bad offsets cannot make them access
+ * memory out of bounds, but the results are then meaningless.
+ */
+gdn_status_t gdn_check_cu_seqlens(const int32_t* cu_seqlens, int32_t n_seq, int64_t T_tot,
+                                  void* stream);
+
+/*
+ * Prefill depthwise causal conv1d (width conv_k = 4) with state prepend and
+ * optional SiLU, over packed sequences.
+ * Defined by: cortex GatedDeltaNet commit, "Block" (depthwise causal Conv1d
+ * (k=4) with state-aware prepend; SiLU) and "State" (conv_state, the
+ * left-padded tail of raw inputs); NxD-Inference Qwen3.6-27B PR, Summary
+ * (convolution state checkpoints).
+ *
+ *   x          (device) [T_tot, conv_dim]            raw mixed_qkv
+ *   w          (device) [conv_dim, 4]                tap 3 multiplies the current token
+ *   cu_seqlens (device) [n_seq + 1] int32, or NULL for one sequence of T_tot tokens
+ *   conv_state_in  (device) [n_seq, conv_dim, 3] or NULL (zeros): the 3 raw inputs
+ *                  preceding each sequence, column 0 oldest
+ *   conv_state_out (device) [n_seq, conv_dim, 3] or NULL: the 3 newest raw inputs of
+ *                  [state_in | x] per sequence (bit copies).  May alias conv_state_in.
+ *   ckpt_every     0 (off) or a positive multiple of 64: conv_ckpt_out row r holds the
+ *                  conv state after m*ckpt_every tokens of a sequence, m = 1..floor(L/N),
+ *                  rows in sequence order (gdn_ckpt_count rows), [rows, conv_dim, 3]
+ *   ckpt_rows      rows allocated in conv_ckpt_out; rows past it are never written
+ *   apply_silu     nonzero: y = silu(conv)
+ *   y          (device) [T_tot, conv_dim]  (must not alias x)
+ * Arithmetic: f32 accumulation; y is rounded once to `dtype`.
+ */
+gdn_status_t gdn_conv1d_fwd(const void* x, const void* w, const int32_t* cu_seqlens,
+                            int32_t n_seq, int64_t T_tot, const void* conv_state_in,
+                            void* conv_state_out, int32_t ckpt_every, void* conv_ckpt_out,
+                            int64_t ckpt_rows, int32_t apply_silu, void* y, gdn_dims_t dims, gdn_dtype_t dtype,
+                            void* stream);
+
+/*
+ * Decode conv update for B sequences, one token each.
+ * Defined by: cortex GatedDeltaNet commit, "Block" and "State" (as above).
+ *   x          (device) [B, conv_dim]
+ *   w          (device) [conv_dim, 4]
+ *   conv_state (device) [B, conv_dim, 3], updated in place: shifted left by one
+ *              column, x appended as column 2
+ *   y          (device) [B, conv_dim] = silu(w . [state | x]) (or without SiLU)
+ */
+gdn_status_t gdn_conv1d_update(const void* x, const void* w, void* conv_state, int32_t B,
+                               int32_t apply_silu, void* y, gdn_dims_t dims, gdn_dtype_t dtype,
+                               void* stream);
+
+/*
+ * Workspace bytes gdn_chunk_prefill needs for these sizes (0 = none; then
+ * `workspace` may be NULL).
+ */
+size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t dims,
+                                        gdn_dtype_t dtype);
+
+/*
+ * Chunked gated delta rule (chunk size 64, WY/UT form) over packed sequences.
+ * Defined by: cortex GatedDeltaNet commit, "Discretisation" (g, beta in f32),
+ * "Block" (L2norm on q,k), "Delta rule (recurrent, per-token)" (the result is
+ * that of the per-token rule; "Performance note": the chunked algorithm with
+ * chunk_size=64 keeps the same surface); NxD-Inference Qwen3.6-27B PR, Summary
+ * (chunked context encoding; recurrent state checkpoints).
+ *
+ * Per sequence and value head h (key head kh = h / (H_v/H_k)), token by token:
+ *   q^ = scale * l2norm(q), k^ = l2norm(k)       (l2norm only with GDN_QK_L2NORM)
+ *   g = -exp(A_log[h]) * softplus(a + dt_bias[h]), beta = sigmoid(b)
+ *   S <- exp(g) S;  delta = beta (v - S^T k^);  S <- S + k^ delta^T;  o = S^T q^
+ *
+ *   qkv        (device) [T_tot, conv_dim]   post-conv activations, channels [q|k|v]
+ *   a, b       (device) [T_tot, H_v]        gate inputs, or NULL when g/beta are given
+ *   A_log, dt_bias (device) [H_v] f32       or NULL when g/beta are given
+ *   g, beta    (device) [T_tot, H_v] f32    precomputed gates, or both NULL
+ *   cu_seqlens (device) [n_seq + 1] int32 or NULL (one sequence)
+ *   initial_state (device) [n_seq, H_v, d_k, d_v] f32 or NULL (zeros)
+ *   final_state   (device) [n_seq, H_v, d_k, d_v] f32 or NULL; may alias initial_state
+ *   ckpt_every  0 or a positive multiple of 64; state_ckpt_out (device)
+ *               [gdn_ckpt_count rows, H_v, d_k, d_v] f32: state after m*ckpt_every tokens
+ *   ckpt_rows   rows allocated in state_ckpt_out; rows past it are never written
+ *   scale       query scale; 0 means d_k^-1/2
+ *   flags       GDN_QK_L2NORM or 0
+ *   o          (device) [T_tot, H_v, d_v]   (dtype)
+ *   workspace  (device) >= gdn_chunk_prefill_workspace_size bytes, or NULL if that is 0
+ */
+gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, const float* A_log,
+                               const float* dt_bias, const float* g, const float* beta,
+                               const int32_t* cu_seqlens, int32_t n_seq, int64_t T_tot,
+                               const float* initial_state, float* final_state, int32_t ckpt_every,
+                               float* state_ckpt_out, int64_t ckpt_rows, float scale, uint32_t flags, void* o,
+                               void* workspace, size_t ws_bytes, gdn_dims_t dims,
+                               gdn_dtype_t dtype, void* stream);
+
+/*
+ * One recurrent decode step for B sequences (one token each), state in place.
+ * Defined by: cortex GatedDeltaNet commit, "Delta rule (recurrent, per-token)",
+ * "Discretisation", "Block" (L2norm on q,k); NxD-Inference Qwen3.6-27B PR,
+ * Summary (token generation kernel).
+ *   qkv    (device) [B, conv_dim]  post-conv activations of this step
+ *   a, b   (device) [B, H_v] and A_log, dt_bias (device) [H_v] f32, or g, beta
+ *          (device) [B, H_v] f32 (as in gdn_chunk_prefill)
+ *   state  (device) [B, H_v, d_k, d_v] f32, read and rewritten in place
+ *   scale, flags as in gdn_chunk_prefill
+ *   o      (device) [B, H_v, d_v]
+ */
+gdn_status_t gdn_recurrent_decode(const void* qkv, const void* a, const void* b,
+                                  const float* A_log, const float* dt_bias, const float* g,
+                                  const float* beta, float* state, int32_t B, float scale,
+                                  uint32_t flags, void* o, gdn_dims_t dims, gdn_dtype_t dtype,
+                                  void* stream);
+
+/*
+ * RMSNormGated over each value head.
+ * Defined by: cortex GatedDeltaNet commit, "Output": RMSNormGated(core_attn_out, z).
+ *   out[t, h*d_v + j] = w[j] * o[t,h,j] / sqrt(mean_j o[t,h,j]^2 + eps) * silu(z[t, h*d_v + j])
+ *   o   (device) [T, H_v, d_v];  z, out (device) [T, H_v*d_v];  w (device) [d_v]
+ *   eps > 0 (the layer uses 1e-6).  out may alias o.
+ */
+gdn_status_t gdn_rmsnorm_gated(const void* o, const void* z, const void* w, float eps, int64_t T,
+                               void* out, gdn_dims_t dims, gdn_dtype_t dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H_ */

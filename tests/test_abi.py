@@ -1,0 +1,187 @@
+"""C ABI: the library loads, exports every symbol include/gdn.h declares, and
+rejects bad arguments on the host with the documented status codes (CPU only:
+no call here reaches a launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from conftest import ROOT
+
+import gated_deltanet_linear_core_gb300 as gdn
+from gated_deltanet_linear_core_gb300 import _lib
+
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+# Argument-validation cases hand the library fake (never dereferenced) device
+# addresses.  Each case must be rejected before any launch.  On a machine with
+# a GPU these CPU tests are skipped so that a validation regression can never
+# launch a kernel on fake addresses.
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(),
+                            reason="host-only validation tests use fake device addresses")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_deltanet_linear_core_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def header_symbols():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_boundary():
+    syms = header_symbols()
+    for name in ["gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
+                 "gdn_recurrent_decode", "gdn_rmsnorm_gated"]:
+        assert name in syms
+
+
+def test_library_exports_every_header_symbol(lib):
+    syms = header_symbols()
+    assert syms
+    for name in syms:
+        assert hasattr(lib, name), name
+    assert set(syms) == set(_lib.SIGNATURES), "binding signatures out of sync with gdn.h"
+
+
+def test_no_torch_types_in_header():
+    txt = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    for bad in ("torch", "at::", "Tensor", "c10", "#include <cuda"):
+        assert bad not in txt
+
+
+def test_status_strings_and_version(lib):
+    for code in range(7):
+        s = lib.gdn_status_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert lib.gdn_status_string(99) == b"unknown status"
+    assert lib.gdn_version() >> 16 == 1
+    assert lib.gdn_last_cuda_error() == 0
+
+
+def test_ckpt_count(lib):
+    assert gdn.gdn_ckpt_count([0, 130, 194, 257, 457], 64) == 2 + 1 + 0 + 3
+    assert gdn.gdn_ckpt_count([0, 262144], 4096) == 64
+    assert gdn.gdn_ckpt_count([0, 100], 0) == 0
+    with pytest.raises(ValueError):
+        gdn.gdn_ckpt_count([0, 100, 50], 64)
+    cu = (ctypes.c_int32 * 2)(0, 10)
+    assert lib.gdn_ckpt_count(None, 1, 64) == -1
+    assert lib.gdn_ckpt_count(cu, 0, 64) == -1
+    assert lib.gdn_ckpt_count(cu, 1, -1) == -1
+
+
+DIMS = _lib.Dims(16, 48, 128, 128, 4)
+A = 0x7f0000000000  # fake 16-byte-aligned address (never dereferenced)
+
+
+def conv_fwd(lib, **kw):
+    args = dict(x=A, w=A + 0x10000, cu=None, n_seq=1, T=64, si=None, so=None, every=0, ck=None,
+                rows=0, silu=1, y=A + 0x20000, dims=DIMS, dt=_lib.GDN_BF16)
+    args.update(kw)
+    return lib.gdn_conv1d_fwd(args["x"], args["w"], args["cu"], args["n_seq"], args["T"],
+                              args["si"], args["so"], args["every"], args["ck"], args["rows"],
+                              args["silu"], args["y"], args["dims"], args["dt"], None)
+
+
+@no_gpu
+def test_conv1d_fwd_validation(lib):
+    E = _lib
+    assert conv_fwd(lib, dims=_lib.Dims(16, 48, 128, 128, 3)) == E.GDN_ERR_UNSUPPORTED
+    assert conv_fwd(lib, dims=_lib.Dims(16, 48, 64, 64, 4)) == E.GDN_ERR_UNSUPPORTED
+    assert conv_fwd(lib, dims=_lib.Dims(16, 40, 128, 128, 4)) == E.GDN_ERR_INVALID_ARG
+    assert conv_fwd(lib, dims=_lib.Dims(0, 48, 128, 128, 4)) == E.GDN_ERR_INVALID_ARG
+    assert conv_fwd(lib, dt=7) == E.GDN_ERR_INVALID_ARG
+    assert conv_fwd(lib, x=None) == E.GDN_ERR_INVALID_ARG
+    assert conv_fwd(lib, w=None) == E.GDN_ERR_INVALID_ARG
+    assert conv_fwd(lib, y=A) == E.GDN_ERR_INVALID_ARG  # y aliases x
+    assert conv_fwd(lib, x=A + 8) == E.GDN_ERR_ALIGN
+    assert conv_fwd(lib, so=A + 0x30004) == E.GDN_ERR_ALIGN
+    assert conv_fwd(lib, T=-1) == E.GDN_ERR_INVALID_ARG
+    assert conv_fwd(lib, n_seq=2) == E.GDN_ERR_INVALID_ARG  # n_seq > 1 needs cu_seqlens
+    assert conv_fwd(lib, cu=A + 0x40000, n_seq=0) == E.GDN_ERR_INVALID_ARG
+    assert conv_fwd(lib, cu=A + 0x40002, n_seq=2) == E.GDN_ERR_ALIGN
+    assert conv_fwd(lib, every=100, ck=A + 0x50000, rows=1) == E.GDN_ERR_INVALID_ARG
+    assert conv_fwd(lib, every=64, ck=None, rows=1) == E.GDN_ERR_INVALID_ARG
+    assert conv_fwd(lib, every=-64) == E.GDN_ERR_INVALID_ARG
+
+
+def chunk(lib, **kw):
+    args = dict(qkv=A, a=A + 0x1000, b=A + 0x2000, A_log=A + 0x3000, dt_bias=A + 0x4000,
+                g=None, beta=None, cu=None, n_seq=1, T=64, S0=None, Sf=None, every=0,
+                ck=None, rows=0, scale=0.0, flags=_lib.GDN_QK_L2NORM, o=A + 0x10000, ws=None,
+                ws_bytes=0, dims=DIMS, dt=_lib.GDN_BF16)
+    args.update(kw)
+    return lib.gdn_chunk_prefill(
+        args["qkv"], args["a"], args["b"], args["A_log"], args["dt_bias"], args["g"],
+        args["beta"], args["cu"], args["n_seq"], args["T"], args["S0"], args["Sf"],
+        args["every"], args["ck"], args["rows"], args["scale"], args["flags"], args["o"],
+        args["ws"], args["ws_bytes"], args["dims"], args["dt"], None)
+
+
+@no_gpu
+def test_chunk_prefill_validation(lib):
+    E = _lib
+    assert chunk(lib, a=None) == E.GDN_ERR_INVALID_ARG      # neither raw gates ...
+    assert chunk(lib, a=None, g=A + 0x5000) == E.GDN_ERR_INVALID_ARG  # ... nor g AND beta
+    assert chunk(lib, A_log=A + 0x3002) == E.GDN_ERR_ALIGN
+    assert chunk(lib, a=A + 0x1001) == E.GDN_ERR_ALIGN       # bf16 needs 2-byte alignment
+    assert chunk(lib, flags=2) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, scale=float("nan")) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, scale=float("inf")) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, o=None) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, qkv=A + 4) == E.GDN_ERR_ALIGN
+    assert chunk(lib, S0=A + 0x6008) == E.GDN_ERR_ALIGN
+    assert chunk(lib, Sf=A + 0x6004) == E.GDN_ERR_ALIGN
+    assert chunk(lib, every=4000, ck=A + 0x7000, rows=1) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, every=4096, ck=None) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, dims=_lib.Dims(16, 48, 128, 64, 4)) == E.GDN_ERR_UNSUPPORTED
+    assert chunk(lib, dims=_lib.Dims(16, 48, 32, 32, 4)) == E.GDN_ERR_UNSUPPORTED
+
+
+@no_gpu
+def test_decode_update_norm_validation(lib):
+    E = _lib
+    dec = lambda **kw: lib.gdn_recurrent_decode(
+        kw.get("qkv", A), kw.get("a", A + 0x1000), kw.get("b", A + 0x2000),
+        kw.get("A_log", A + 0x3000), kw.get("dt_bias", A + 0x4000), None, None,
+        kw.get("state", A + 0x10000), kw.get("B", 4), kw.get("scale", 0.0),
+        kw.get("flags", 1), kw.get("o", A + 0x20000), kw.get("dims", DIMS), _lib.GDN_BF16, None)
+    assert dec(B=-1) == E.GDN_ERR_INVALID_ARG
+    assert dec(state=None) == E.GDN_ERR_INVALID_ARG
+    assert dec(state=A + 0x10008) == E.GDN_ERR_ALIGN
+    assert dec(flags=4) == E.GDN_ERR_INVALID_ARG
+    assert dec(a=None) == E.GDN_ERR_INVALID_ARG
+    upd = lambda **kw: lib.gdn_conv1d_update(
+        kw.get("x", A), kw.get("w", A + 0x1000), kw.get("st", A + 0x2000), kw.get("B", 4), 1,
+        kw.get("y", A + 0x3000), kw.get("dims", DIMS), _lib.GDN_BF16, None)
+    assert upd(B=-2) == E.GDN_ERR_INVALID_ARG
+    assert upd(st=None) == E.GDN_ERR_INVALID_ARG
+    assert upd(y=A + 2) == E.GDN_ERR_ALIGN
+    assert upd(dims=_lib.Dims(16, 48, 128, 128, 2)) == E.GDN_ERR_UNSUPPORTED
+    norm = lambda **kw: lib.gdn_rmsnorm_gated(
+        kw.get("o", A), kw.get("z", A + 0x1000), kw.get("w", A + 0x2000), kw.get("eps", 1e-6),
+        kw.get("T", 8), kw.get("out", A + 0x3000), DIMS, _lib.GDN_BF16, None)
+    assert norm(eps=0.0) == E.GDN_ERR_INVALID_ARG
+    assert norm(eps=-1.0) == E.GDN_ERR_INVALID_ARG
+    assert norm(w=None) == E.GDN_ERR_INVALID_ARG
+    assert norm(T=-3) == E.GDN_ERR_INVALID_ARG
+    assert norm(z=A + 0x1008) == E.GDN_ERR_ALIGN
+
+
+def test_workspace_size_is_zero_for_the_fused_kernels(lib):
+    assert gdn.gdn_chunk_prefill_workspace_size(8, 32768, gdn.GDNDims(16, 32, 128, 128),
+                                                torch.bfloat16) == 0
+
+
+def test_binding_rejects_host_tensors_before_the_library():
+    x = torch.zeros(4, 128)
+    with pytest.raises(ValueError, match="CUDA"):
+        gdn.gdn_conv1d_fwd(x, torch.zeros(128, 4), gdn.GDNDims(2, 4, 16, 16), y=torch.zeros(4, 128))

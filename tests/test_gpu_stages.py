@@ -1,0 +1,259 @@
+"""GPU parity of each C-ABI call against the CPU oracle on seeded inputs.
+
+Sizes span several 64-token chunks, column blocks and a ragged tail; varlen
+cases include sequences of length 1, 63, 64, 65 and 0.  Tolerances: rel-L2
+1e-4 for f32 activations, 5e-3 for bf16 activations (f32 state); conv state
+and checkpoints bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_core_gb300 as gdn
+import oracle
+import workloads as W
+from gpu_util import TOL, assert_close, host, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = [torch.float32, torch.bfloat16]
+SMALL_128 = W.GDNShape(H_k=2, H_v=6, d_k=128, d_v=128)
+LENGTHS = [1, 63, 64, 65, 0, 200, 3]
+
+
+def _dims(s):
+    return gdn.GDNDims(s.H_k, s.H_v, s.d_k, s.d_v)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [W.TINY, SMALL_128], ids=["d16", "d128"])
+def test_conv1d_fwd(dtype, shape):
+    inp = W.layer_inputs(shape, dtype, LENGTHS, seed=11, init_state=True)
+    cu = inp["cu_seqlens"]
+    x, w, st = (inp[k].cuda() for k in ("mixed_qkv", "conv_w", "conv_state0"))
+    rows = gdn.gdn_ckpt_count(cu, 64)
+    ck = torch.full((rows, shape.conv_dim, 3), float("nan"), dtype=dtype, device="cuda")
+    st_out = st.clone()  # in place: conv_state_out aliases conv_state_in
+    y = gdn.gdn_conv1d_fwd(x, w, _dims(shape), cu.cuda(), st_out, st_out, 64, ck)
+    torch.cuda.synchronize()
+    f = W.to_f64
+    y_ref, st_ref, ck_ref = oracle.conv1d(f(inp["mixed_qkv"]), f(inp["conv_w"]), cu.numpy(),
+                                          f(inp["conv_state0"]), True, 64)
+    assert_close("y", host(y), y_ref, 1e-6 if dtype == torch.float32 else TOL[dtype])
+    assert np.array_equal(host(st_out), st_ref), "conv state out not bit-exact"
+    assert np.array_equal(host(ck), ck_ref), "conv checkpoints not bit-exact"
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_conv1d_fwd_zero_state_and_no_silu(dtype):
+    shape = SMALL_128
+    inp = W.layer_inputs(shape, dtype, [5, 2, 130], seed=12)
+    cu = inp["cu_seqlens"]
+    x, w = inp["mixed_qkv"].cuda(), inp["conv_w"].cuda()
+    st_out = torch.empty((3, shape.conv_dim, 3), dtype=dtype, device="cuda")
+    y = gdn.gdn_conv1d_fwd(x, w, _dims(shape), cu.cuda(), None, st_out, apply_silu=False)
+    torch.cuda.synchronize()
+    f = W.to_f64
+    y_ref, st_ref, _ = oracle.conv1d(f(inp["mixed_qkv"]), f(inp["conv_w"]), cu.numpy(), None,
+                                     False)
+    assert_close("y", host(y), y_ref, 1e-6 if dtype == torch.float32 else TOL[dtype])
+    assert np.array_equal(host(st_out), st_ref)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [W.TINY, SMALL_128], ids=["d16", "d128"])
+def test_conv1d_update(dtype, shape):
+    B = 5
+    d = W.decode_inputs(shape, dtype, B, 1, seed=13)
+    p = W.layer_params(shape, dtype, seed=13)
+    st = W.draw((B, shape.conv_dim, 3), seed=13, stream=99, dtype=dtype)
+    x = d["qkv"][0]
+    st_dev = st.cuda()
+    y = gdn.gdn_conv1d_update(x.cuda(), p["conv_w"].cuda(), st_dev, _dims(shape))
+    torch.cuda.synchronize()
+    f = W.to_f64
+    y_ref, st_ref, _ = oracle.conv1d(f(x), f(p["conv_w"]), np.arange(B + 1), f(st), True)
+    assert_close("y", host(y), y_ref, 1e-6 if dtype == torch.float32 else TOL[dtype])
+    assert np.array_equal(host(st_dev), st_ref)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [W.TINY, SMALL_128], ids=["d16", "d128"])
+def test_rmsnorm_gated(dtype, shape):
+    T = 77
+    o = W.draw((T, shape.H_v, shape.d_v), seed=14, stream=1, dtype=dtype)
+    z = W.draw((T, shape.z_dim), seed=14, stream=2, dtype=dtype)
+    w = W.draw((shape.d_v,), seed=14, stream=3, dtype=dtype, p0=1.0, p1=0.1)
+    out = gdn.gdn_rmsnorm_gated(o.cuda(), z.cuda(), w.cuda(), _dims(shape))
+    torch.cuda.synchronize()
+    ref = oracle.rmsnorm_gated(W.to_f64(o), W.to_f64(z), W.to_f64(w))
+    assert_close("out", host(out), ref, 1e-6 if dtype == torch.float32 else TOL[dtype])
+    # in place (out aliases o)
+    o2 = o.cuda()
+    gdn.gdn_rmsnorm_gated(o2, z.cuda(), w.cuda(), _dims(shape), out=o2.view(T, -1))
+    torch.cuda.synchronize()
+    assert torch.equal(o2.view(T, -1).cpu(), out.cpu())
+
+
+def _delta_inputs(shape, dtype, lengths, seed, init_state=True):
+    """Synthetic post-conv activations (N(0,1)) and gate inputs."""
+    return W.layer_inputs(shape, dtype, lengths, seed=seed, init_state=init_state)
+
+
+def _oracle_delta(inp, shape, ckpt_every=0, scale=None, g=None, beta=None, l2norm=True):
+    f = W.to_f64
+    q, k, v = oracle.split_qkv(f(inp["mixed_qkv"]), shape.H_k, shape.H_v, shape.d_k, shape.d_v)
+    if g is None:
+        g, beta = oracle.gates(f(inp["a"]), f(inp["b"]), f(inp["A_log"]), f(inp["dt_bias"]))
+    return oracle.delta_rule(q, k, v, g, beta, inp["cu_seqlens"].numpy(), f(inp["S0"]), scale,
+                             l2norm, ckpt_every)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [W.TINY, SMALL_128], ids=["d16", "d128"])
+def test_chunk_prefill_varlen_states_ckpts(dtype, shape):
+    inp = _delta_inputs(shape, dtype, LENGTHS, seed=15)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    N = len(LENGTHS)
+    rows = gdn.gdn_ckpt_count(inp["cu_seqlens"], 64)
+    ck = torch.full((rows, shape.H_v, shape.d_k, shape.d_v), float("nan"), device="cuda")
+    Sf = torch.full((N, shape.H_v, shape.d_k, shape.d_v), float("nan"), device="cuda")
+    o = gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(shape), d["a"], d["b"], d["A_log"],
+                              d["dt_bias"], cu_seqlens=d["cu_seqlens"], initial_state=d["S0"],
+                              final_state=Sf, ckpt_every=64, state_ckpt_out=ck)
+    torch.cuda.synchronize()
+    o_ref, S_ref, ck_ref = _oracle_delta(inp, shape, ckpt_every=64)
+    tol = TOL[dtype]
+    assert_close("o", host(o), o_ref, tol, per_head_axis=1)
+    assert_close("S_final", host(Sf), S_ref, tol, per_head_axis=1)
+    assert_close("ckpt", host(ck), ck_ref, tol)
+    # zero-length sequence: final state is its initial state, bit for bit
+    z = LENGTHS.index(0)
+    assert torch.equal(Sf[z].cpu(), inp["S0"][z])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_chunk_prefill_in_place_state_and_zero_init(dtype):
+    shape = SMALL_128
+    inp = _delta_inputs(shape, dtype, [150, 40], seed=16, init_state=False)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    S = torch.zeros((2, shape.H_v, shape.d_k, shape.d_v), device="cuda")
+    o = gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(shape), d["a"], d["b"], d["A_log"],
+                              d["dt_bias"], cu_seqlens=d["cu_seqlens"], initial_state=S,
+                              final_state=S)
+    o2 = gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(shape), d["a"], d["b"], d["A_log"],
+                               d["dt_bias"], cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    o_ref, S_ref, _ = _oracle_delta(inp, shape)
+    assert_close("o", host(o), o_ref, TOL[dtype])
+    assert_close("S", host(S), S_ref, TOL[dtype])
+    assert torch.equal(o, o2)  # NULL initial state == zeros
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_chunk_prefill_precomputed_gates_closed_forms(dtype):
+    """beta = 0: the state only decays (S_T = e^{sum g} S0); with g = 0,
+    beta = 1, scale 1, pre-normalised unit keys and q = k, o_t = v_t."""
+    shape = SMALL_128
+    T = 130
+    inp = _delta_inputs(shape, dtype, [T], seed=17)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    g = -0.05 * torch.rand((T, shape.H_v), generator=torch.Generator().manual_seed(5))
+    beta = torch.zeros((T, shape.H_v))
+    Sf = torch.empty_like(d["S0"])
+    gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(shape), g=g.cuda(), beta=beta.cuda(),
+                          initial_state=d["S0"], final_state=Sf)
+    torch.cuda.synchronize()
+    want = torch.exp(g.double().sum(0))[None, :, None, None] * inp["S0"].double()
+    assert rel_l2(host(Sf), want.numpy()) < 1e-5
+    # retrieval with f32 activations (exact unit keys need f32)
+    if dtype == torch.float32:
+        qkv = inp["mixed_qkv"].clone()
+        D = shape.d_k
+        kk = qkv[:, shape.H_k * D:2 * shape.H_k * D].view(T, shape.H_k, D)
+        kk /= kk.norm(dim=-1, keepdim=True)
+        qkv[:, :shape.H_k * D] = kk.reshape(T, -1)
+        o = gdn.gdn_chunk_prefill(qkv.cuda(), _dims(shape), g=torch.zeros_like(g).cuda(),
+                                  beta=torch.ones_like(beta).cuda(), initial_state=d["S0"],
+                                  scale=1.0, l2norm_qk=False)
+        torch.cuda.synchronize()
+        v = qkv[:, 2 * shape.H_k * D:].view(T, shape.H_v, D)
+        assert rel_l2(host(o), v.double().numpy()) < 1e-4
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [W.TINY, SMALL_128], ids=["d16", "d128"])
+def test_recurrent_decode(dtype, shape):
+    B = 7
+    d = W.decode_inputs(shape, dtype, B, 1, seed=18)
+    p = W.layer_params(shape, dtype, seed=18)
+    S0 = W.draw((B, shape.H_v, shape.d_k, shape.d_v), seed=18, stream=50, dtype=torch.float32,
+                p1=0.02)
+    S = S0.cuda()
+    o = gdn.gdn_recurrent_decode(d["qkv"][0].cuda(), S, _dims(shape), d["a"][0].cuda(),
+                                 d["b"][0].cuda(), p["A_log"].cuda(), p["dt_bias"].cuda())
+    torch.cuda.synchronize()
+    f = W.to_f64
+    q, k, v = oracle.split_qkv(f(d["qkv"][0]), shape.H_k, shape.H_v, shape.d_k, shape.d_v)
+    g, beta = oracle.gates(f(d["a"][0]), f(d["b"][0]), f(p["A_log"]), f(p["dt_bias"]))
+    o_ref, S_ref, _ = oracle.delta_rule(q, k, v, g, beta, np.arange(B + 1), f(S0))
+    assert_close("o", host(o), o_ref, TOL[dtype], per_head_axis=1)
+    assert_close("S", host(S), S_ref, TOL[dtype], per_head_axis=1)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_prefill_then_decode_equals_longer_prefill(dtype):
+    """Continuation: prefill(T1) then per-token decode steps from the handed-off
+    states == one prefill over the longer sequence (GPU against GPU, and
+    against the oracle)."""
+    shape = SMALL_128
+    T, T1 = 100, 70
+    inp = _delta_inputs(shape, dtype, [T], seed=19)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    dims = _dims(shape)
+    S_full = torch.empty_like(d["S0"])
+    o_full = gdn.gdn_chunk_prefill(d["mixed_qkv"], dims, d["a"], d["b"], d["A_log"],
+                                   d["dt_bias"], initial_state=d["S0"], final_state=S_full)
+    S = torch.empty_like(d["S0"])
+    o1 = gdn.gdn_chunk_prefill(d["mixed_qkv"][:T1].contiguous(), dims, d["a"][:T1].contiguous(),
+                               d["b"][:T1].contiguous(), d["A_log"], d["dt_bias"],
+                               initial_state=d["S0"], final_state=S)
+    outs = [o1]
+    for t in range(T1, T):
+        outs.append(gdn.gdn_recurrent_decode(d["mixed_qkv"][t:t + 1].contiguous(), S, dims,
+                                             d["a"][t:t + 1].contiguous(),
+                                             d["b"][t:t + 1].contiguous(), d["A_log"],
+                                             d["dt_bias"]))
+    torch.cuda.synchronize()
+    o_cat = torch.cat(outs)
+    tol = TOL[dtype]
+    assert rel_l2(host(o_cat), host(o_full)) <= tol
+    assert rel_l2(host(S), host(S_full)) <= tol
+    o_ref, S_ref, _ = _oracle_delta(inp, shape)
+    assert_close("o (prefill+decode)", host(o_cat), o_ref, tol)
+    assert_close("S (prefill+decode)", host(S), S_ref, tol)
+
+
+def test_empty_inputs_are_no_ops():
+    shape = SMALL_128
+    dims = _dims(shape)
+    x = torch.empty((0, shape.conv_dim), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((shape.conv_dim, 4), dtype=torch.bfloat16, device="cuda")
+    st = torch.randn((1, shape.conv_dim, 3), device="cuda").to(torch.bfloat16)
+    st_out = torch.empty_like(st)
+    y = gdn.gdn_conv1d_fwd(x, w, dims, None, st, st_out)
+    S0 = torch.randn((1, shape.H_v, 128, 128), device="cuda")
+    Sf = torch.empty_like(S0)
+    A = torch.zeros(shape.H_v, device="cuda")
+    ab = torch.empty((0, shape.H_v), dtype=torch.bfloat16, device="cuda")
+    o = gdn.gdn_chunk_prefill(x, dims, ab, ab, A, A, initial_state=S0, final_state=Sf)
+    torch.cuda.synchronize()
+    assert y.shape == (0, shape.conv_dim) and o.shape == (0, shape.H_v, 128)
+    assert torch.equal(st_out, st) and torch.equal(Sf, S0)
