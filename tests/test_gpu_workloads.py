@@ -189,12 +189,16 @@ def test_qwen36_27b_long_prefill_ckpts_then_decode():
     for h in heads:
         ch = head_channels(s, h)
         S_h, cs_h = refs[h]["S"], refs[h]["conv_state"]
+        ref_steps = []
         for t in range(w.decode_steps):
             o_ref, S_h, cs_h, _ = oracle.layer_decode_step(
                 f(dec["qkv"][t][:, ch]), f(dec["z"][t][:, h * s.d_v:(h + 1) * s.d_v]),
                 f(dec["a"][t][:, h:h + 1]), f(dec["b"][t][:, h:h + 1]), f(inp["conv_w"][ch]),
                 f(inp["A_log"][h:h + 1]), f(inp["dt_bias"][h:h + 1]), f(inp["norm_w"]), 1, 1,
                 s.d_k, s.d_v, S_h, cs_h)
-            e = rel_l2(host(outs[t, h]), o_ref[0])
-            assert e <= tol, f"decode step {t} head {h}: rel-L2 {e:.3e}"
+            ref_steps.append(o_ref[0])
+        # rel-L2 per output tensor (this head's 128-step decode output), and
+        # every single step within twice that bound
+        assert_close(f"decode out head {h}", host(outs[:, h]), np.stack(ref_steps), tol,
+                     per_head_axis=0)
         assert_close(f"decode S head {h}", host(S[0, h]), S_h[0, 0], tol)
