@@ -23,7 +23,7 @@ from ._lib import GDNError, GDN_QK_L2NORM  # noqa: F401
 __all__ = [
     "GDNDims", "GDNError", "gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
     "gdn_chunk_prefill_workspace_size", "gdn_recurrent_decode", "gdn_rmsnorm_gated",
-    "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_layer_prefill", "gdn_layer_decode",
+    "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_sync_status", "gdn_layer_prefill", "gdn_layer_decode",
     "library_path",
 ]
 
@@ -106,6 +106,15 @@ def gdn_check_cu_seqlens(cu_seqlens: torch.Tensor, T_tot: int, stream=None) -> N
     _lib.check(_lib.load().gdn_check_cu_seqlens(p, _nseq(cu_seqlens), int(T_tot),
                                                _stream(cu_seqlens, stream)),
                "gdn_check_cu_seqlens")
+
+
+def gdn_sync_status(device=None, stream=None) -> None:
+    """Synchronises the stream and raises GDNError if a kernel gave up a
+    bounded device-side wait (GDN_ERR_TIMEOUT) or the stream holds a CUDA error."""
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _lib.check(_lib.load().gdn_sync_status(s), "gdn_sync_status")
 
 
 def gdn_conv1d_fwd(x, w, dims, cu_seqlens=None, conv_state_in=None, conv_state_out=None,

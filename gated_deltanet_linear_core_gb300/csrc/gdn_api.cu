@@ -117,6 +117,13 @@ gdn_status_t gdn_check_cu_seqlens(const int32_t* cu, int32_t n_seq, int64_t T, v
     return GDN_OK;
 }
 
+gdn_status_t gdn_sync_status(void* stream) {
+    int flags = 0;
+    cudaError_t e = gdn::read_and_clear_device_error((cudaStream_t)stream, &flags);
+    if (e != cudaSuccess) return cuda_status(e);
+    return (flags & 1) ? GDN_ERR_TIMEOUT : GDN_OK;
+}
+
 gdn_status_t gdn_conv1d_fwd(const void* x, const void* w, const int32_t* cu_seqlens, int32_t n_seq,
                             int64_t T_tot, const void* conv_state_in, void* conv_state_out,
                             int32_t ckpt_every, void* conv_ckpt_out, int64_t ckpt_rows,

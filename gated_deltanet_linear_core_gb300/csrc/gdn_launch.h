@@ -58,6 +58,9 @@ cudaError_t launch_chunk_tc(const DeltaArgs& a, cudaStream_t s);
 // Recurrent decode: T = B tokens, sequence i = token i, state in place (S0 == S_final).
 cudaError_t launch_recurrent_decode(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s);
 
+// Reads (synchronising `s`) and clears the library's device error word.
+cudaError_t read_and_clear_device_error(cudaStream_t s, int* flags);
+
 cudaError_t launch_rmsnorm_gated(const void* o, const void* z, const void* w, float eps, int64_t T,
                                  int H, int D, void* out, gdn_dtype_t dt, cudaStream_t s);
 

@@ -98,6 +98,15 @@ gdn_status_t gdn_check_cu_seqlens(const int32_t* cu_seqlens, int32_t n_seq, int6
                                   void* stream);
 
 /*
+ * SYNCHRONISES `stream`, then reports failures that happened on the device
+ * after the calls above returned: GDN_ERR_TIMEOUT if a kernel of this library
+ * gave up one of its bounded waits (about 1 s each) since the last call -- its
+ * outputs are then incomplete -- and clears that record; GDN_ERR_CUDA if the
+ * stream holds a CUDA error; GDN_OK otherwise.
+ */
+gdn_status_t gdn_sync_status(void* stream);
+
+/*
  * Prefill depthwise causal conv1d (width conv_k = 4) with state prepend and
  * optional SiLU, over packed sequences.
  * Defined by: cortex GatedDeltaNet commit, "Block" (depthwise causal Conv1d

@@ -257,3 +257,9 @@ def test_empty_inputs_are_no_ops():
     torch.cuda.synchronize()
     assert y.shape == (0, shape.conv_dim) and o.shape == (0, shape.H_v, 128)
     assert torch.equal(st_out, st) and torch.equal(Sf, S0)
+
+
+def test_no_kernel_gave_up_a_bounded_wait():
+    """Every chunked-prefill launch above completed its waits: the library's
+    device error word is clear (gdn_sync_status raises on GDN_ERR_TIMEOUT)."""
+    gdn.gdn_sync_status()
