@@ -67,8 +67,8 @@ constexpr int SM_UT = SM_ST + 32768;      // U'^T [v][j]      K-major A operand
 constexpr int SM_UTD = SM_UT + 16384;     // U'^T diag(e^{G_n-G_j} rk_j)
 constexpr int SM_A = SM_UTD + 16384;      // A matrix, f32
 constexpr int A_PITCH = 68;
-constexpr int SM_VEC = SM_A + 64 * A_PITCH * 4;  // G, e^G, beta, dec, rk, rq, misc
-constexpr int SM_BAR = SM_VEC + 7 * 64 * 4;
+constexpr int SM_VEC = SM_A + 64 * A_PITCH * 4;  // G, e^G, beta, dec, rk, rq, misc, fw
+constexpr int SM_BAR = SM_VEC + 8 * 64 * 4;
 constexpr int SM_TOTAL = SM_BAR + 64;
 constexpr int SMEM_BYTES = SM_TOTAL + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -98,6 +98,12 @@ __device__ __forceinline__ void store_row_bf16(uint8_t* blk, int row, int c0, co
     }
 }
 
+// Element (i, j) of a 64 x 64 f32 table whose float4 groups are XOR-swizzled
+// by row, so that a warp reading one float4 per row hits distinct banks.
+__device__ __forceinline__ int ftab(int i, int j) {
+    return i * 64 + ((((j >> 2) ^ (i & 15)) & 15) << 2) + (j & 3);
+}
+
 // Sum of squares of a 128-element bf16 row stored as two 128-byte swizzled rows.
 __device__ __forceinline__ float row_sumsq(const uint8_t* blk0, const uint8_t* blk1, int row) {
     float s = 0.f;
@@ -106,7 +112,7 @@ __device__ __forceinline__ float row_sumsq(const uint8_t* blk0, const uint8_t* b
         const uint4* p = reinterpret_cast<const uint4*>((half ? blk1 : blk0) + row * 128);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const uint4 u = p[q];
+            const uint4 u = p[q ^ (row & 7)];  // same chunks, bank-conflict-free order
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -120,7 +126,8 @@ __device__ __forceinline__ float row_sumsq(const uint8_t* blk0, const uint8_t* b
 }
 
 __global__ void __launch_bounds__(NT, 1)
-chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
+chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                DeltaArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float* Gs = reinterpret_cast<float*>(sm + SM_VEC);
@@ -130,6 +137,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
     float* RKs = Gs + 256;
     float* RQs = Gs + 320;
     float* misc = Gs + 384;
+    float* FWs = Gs + 448;  // beta_j e^{G_j} rk_j
     float* Am = reinterpret_cast<float*>(sm + SM_A);
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + SM_BAR);  // [0], [1]
     uint64_t* bar_mma = bar_tma + 2;
@@ -153,6 +161,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
         mbar_init(bar_mma, 1);
         fence_mbar_init();
         prefetch_tmap(&qmap);
+        prefetch_tmap(&omap);
     }
     if (warp == 0) {
         tmem_alloc(tslot, TMEM_COLS);
@@ -164,8 +173,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
     const uint32_t tb = *tslot;
     const uint32_t lo = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quarter
 
-    int issued[2] = {0, 0};    // TMA issues per buffer (thread 0)
-    int consumed[2] = {0, 0};  // completed TMA phases waited on, per buffer
+    int issued0 = 0, issued1 = 0;      // TMA issues per buffer (thread 0)
+    int consumed0 = 0, consumed1 = 0;  // completed TMA phases waited on, per buffer
     auto issue_tma = [&](int c) {
         const int b = c & 1;
         const int y = (int)(s0 + (int64_t)c * C);
@@ -178,7 +187,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
         tma_load_2d(kq + 24576, &qmap, &bar_tma[b], xq + 64, y);
         tma_load_2d(vv, &qmap, &bar_tma[b], xv, y);
         tma_load_2d(vv + 8192, &qmap, &bar_tma[b], xv + 64, y);
-        ++issued[b];
+        if (b) ++issued1; else ++issued0;
     };
     if (tid == 0) {
         if (nchunks > 0) issue_tma(0);
@@ -201,6 +210,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
     __syncthreads();
     tc_fence_after();
 
+    // raw gate inputs of a chunk's token `tid` (tid < 64), loaded one chunk ahead
+    float ga = 0.f, gb = 0.f;
+    auto load_gates = [&](int cc) {
+        ga = 0.f;
+        gb = 0.f;
+        const int64_t tok = (int64_t)cc * C + tid;
+        if (tid < 64 && tok < L) {
+            const int64_t gi = (s0 + tok) * a.H_v + h;
+            if (a.g != nullptr) {
+                ga = a.g[gi];
+                gb = a.beta[gi];
+            } else {
+                ga = to_f(static_cast<const bf16*>(a.a)[gi]);
+                gb = to_f(static_cast<const bf16*>(a.b)[gi]);
+            }
+        }
+    };
+    if (nchunks > 0) load_gates(0);
+    const float A_log_h = a.g == nullptr ? a.A_log[h] : 0.f;
+    const float dt_bias_h = a.g == nullptr ? a.dt_bias[h] : 0.f;
+    constexpr float kLog2e = 1.4426950408889634f;
+
     uint32_t mma_phase = 0;
     bool mma_pending = false;
     bool ok = true;
@@ -212,20 +243,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
         uint8_t* kq = sm + SM_KQ + b * KQ_BYTES;
         uint8_t* vv = sm + SM_V + b * V_BYTES;
 
-        // ---- gates and their in-warp cumulative sums (tokens 0-31, 32-63)
+        // ---- gates (log2 domain) and their in-warp cumulative sums (tokens 0-31, 32-63)
         if (tid < 64) {
             float g = 0.f, bt = 0.f;
             if (tid < n) {
-                const int64_t gi = (t0 + tid) * a.H_v + h;
                 if (a.g != nullptr) {
-                    g = a.g[gi];
-                    bt = a.beta[gi];
+                    g = ga;
+                    bt = gb;
                 } else {
-                    g = gate_g(to_f(static_cast<const bf16*>(a.a)[gi]), a.A_log[h], a.dt_bias[h]);
-                    bt = sigmoid_f(to_f(static_cast<const bf16*>(a.b)[gi]));
+                    g = gate_g(ga, A_log_h, dt_bias_h);
+                    bt = sigmoid_f(gb);
                 }
             }
-            float x = g;
+            if (c + 1 < nchunks) load_gates(c + 1);  // lands while this chunk computes
+            float x = g * kLog2e;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, x, o);
@@ -234,10 +265,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
             Gs[tid] = x;
             Bs[tid] = bt;
         }
-        ok = mbar_wait(&bar_tma[b], (uint32_t)(consumed[b] & 1), kWaitNs);
+        ok = mbar_wait(&bar_tma[b], (uint32_t)((b ? consumed1 : consumed0) & 1), kWaitNs);
         ok = __syncthreads_and(ok);
         if (!ok) break;
-        ++consumed[b];
+        if (b) ++consumed1; else ++consumed0;
         if (tid >= 32 && tid < 64) Gs[tid] += Gs[31];
         // l2-norm factors from the tiles
         {
@@ -251,9 +282,35 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
         __syncthreads();
         if (tid < 64) {
             const float Gn = Gs[n - 1];
-            eGs[tid] = expf(Gs[tid]);
-            DECs[tid] = tid < n ? expf(Gn - Gs[tid]) : 0.f;
-            if (tid == 0) misc[0] = expf(Gn);
+            const float eg = exp2f(Gs[tid]);
+            eGs[tid] = eg;
+            FWs[tid] = Bs[tid] * eg * RKs[tid];
+            DECs[tid] = tid < n ? exp2f(Gn - Gs[tid]) : 0.f;
+            if (tid == 0) misc[0] = exp2f(Gn);
+        }
+        // decay-and-norm factor tables for A and P: thread t fills half of row t/2
+        {
+            float* FA = reinterpret_cast<float*>(sm + SM_UT);
+            float* FP = FA + 64 * 64;
+            const int i = tid >> 1, j0 = (tid & 1) * 32;
+            const float Gi = Gs[i], fa = Bs[i] * RKs[i], fq = RQs[i];
+            const bool live = i < n;
+#pragma unroll 2
+            for (int g4 = 0; g4 < 8; ++g4) {
+                const int j = j0 + 4 * g4;
+                const float4 G4 = *reinterpret_cast<const float4*>(Gs + j);
+                const float4 R4 = *reinterpret_cast<const float4*>(RKs + j);
+                const float gj[4] = {G4.x, G4.y, G4.z, G4.w}, rj[4] = {R4.x, R4.y, R4.z, R4.w};
+                float va[4], vp[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float e = (live && j + q <= i) ? exp2f(fminf(Gi - gj[q], 0.f)) : 0.f;
+                    vp[q] = fq * rj[q] * e;
+                    va[q] = (j + q < i) ? fa * rj[q] * e : 0.f;
+                }
+                *reinterpret_cast<float4*>(FA + ftab(i, j)) = make_float4(va[0], va[1], va[2], va[3]);
+                *reinterpret_cast<float4*>(FP + ftab(i, j)) = make_float4(vp[0], vp[1], vp[2], vp[3]);
+            }
         }
         __syncthreads();
 
@@ -276,65 +333,103 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
         mma_pending = false;
         tc_fence_after();
 
-        // ---- A (rows 0-63, f32) and P (rows 64-127, bf16 operand)
+        // ---- A (rows 0-63, f32) and P (rows 64-127, bf16 operand) = D1 * factor table
         {
             float d1[64];
             tmem_ld32(tb + lo + T_D1, d1);
             tmem_ld32(tb + lo + T_D1 + 32, d1 + 32);
             tmem_wait_ld();
+            const int i = tid & 63;
+            const float* F = reinterpret_cast<const float*>(sm + SM_UT) + (tid < 64 ? 0 : 64 * 64);
+#pragma unroll
+            for (int g4 = 0; g4 < 16; ++g4) {
+                const float4 f = *reinterpret_cast<const float4*>(F + ftab(i, 4 * g4));
+                d1[4 * g4 + 0] *= f.x;
+                d1[4 * g4 + 1] *= f.y;
+                d1[4 * g4 + 2] *= f.z;
+                d1[4 * g4 + 3] *= f.w;
+            }
             if (tid < 64) {
-                const int i = tid;
-                const float gi = Gs[i], fi = Bs[i] * RKs[i];
-                const bool live = i < n;
 #pragma unroll
-                for (int j0 = 0; j0 < 64; j0 += 4) {
-                    float w4[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int j = j0 + q;
-                        w4[q] = (live && j < i) ? fi * expf(gi - Gs[j]) * d1[j] * RKs[j] : 0.f;
-                    }
-                    *reinterpret_cast<float4*>(&Am[i * A_PITCH + j0]) =
-                        make_float4(w4[0], w4[1], w4[2], w4[3]);
-                }
+                for (int g4 = 0; g4 < 16; ++g4)
+                    *reinterpret_cast<float4*>(&Am[i * A_PITCH + 4 * g4]) =
+                        make_float4(d1[4 * g4], d1[4 * g4 + 1], d1[4 * g4 + 2], d1[4 * g4 + 3]);
             } else {
-                const int i = tid - 64;
-                const float gi = Gs[i], fi = RQs[i];
-                const bool live = i < n;
-#pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    d1[j] = (live && j <= i) ? fi * expf(gi - Gs[j]) * d1[j] * RKs[j] : 0.f;
                 store_row_bf16(sm + SM_P, i, 0, d1, 64);
             }
         }
         fence_async_smem();
         __syncthreads();
 
-        // ---- T' = (I + A)^-1 by forward substitution, one column per thread
-        if (tid < 64) {
-            const int col = tid;
-            float x[64];
+        // ---- T' = (I + A)^-1, blocked by 16 (f32): the four diagonal blocks by
+        //      forward substitution, then by block distance d = 1, 2, 3:
+        //      T'_{b+d,b} = -T'_{b+d,b+d} sum_{c=b}^{b+d-1} A_{b+d,c} T'_{c,b}
+        {
+            float* Tm = reinterpret_cast<float*>(sm + SM_UT);  // [64][A_PITCH]
+            float* Mt = Tm + 64 * A_PITCH;                     // <= 3 blocks of 16 x 16
+            if (tid == 0) bulk_wait_read_all();  // the previous O tile store has left B_W/B_U
+            if (tid < 64) {
+                const int r0 = (tid >> 4) * 16, cl = tid & 15;
+                float x[16];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const float* Ai = &Am[i * A_PITCH];
-                float p0 = (i == col) ? 1.f : 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+                for (int r = 0; r < 16; ++r) {
+                    const float* Ar = &Am[(r0 + r) * A_PITCH + r0];
+                    float acc = (r == cl) ? 1.f : 0.f;
 #pragma unroll
-                for (int j = 0; j + 4 <= i; j += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(Ai + j);
-                    p0 = fmaf(-a4.x, x[j], p0);
-                    p1 = fmaf(-a4.y, x[j + 1], p1);
-                    p2 = fmaf(-a4.z, x[j + 2], p2);
-                    p3 = fmaf(-a4.w, x[j + 3], p3);
+                    for (int q = 0; q < r; ++q) acc = fmaf(-Ar[q], x[q], acc);
+                    x[r] = acc;
                 }
 #pragma unroll
-                for (int j = i & ~3; j < i; ++j) p0 = fmaf(-Ai[j], x[j], p0);
-                x[i] = (p0 + p1) + (p2 + p3);
+                for (int r = 0; r < 16; ++r) Tm[(r0 + r) * A_PITCH + r0 + cl] = x[r];
+            } else {
+                // strictly upper blocks are zero: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+                for (int e = tid - 64; e < 6 * 256; e += 64) {
+                    const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+                    const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                    const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                    Tm[(br * 16 + r) * A_PITCH + bc * 16 + cc] = 0.f;
+                }
             }
-            const float fw = Bs[col] * eGs[col] * RKs[col], fu = Bs[col];
+            __syncthreads();
+            for (int dd = 1; dd < 4; ++dd) {
+                const int nel = (4 - dd) * 256;
+                for (int e = tid; e < nel; e += NT) {
+                    const int bl = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+                    const float* Ar = &Am[((bl + dd) * 16 + r) * A_PITCH];
+                    const float* Tc = &Tm[bl * 16 + cc];
+                    float acc = 0.f;
+                    for (int k = bl * 16; k < (bl + dd) * 16; ++k) acc = fmaf(Ar[k], Tc[k * A_PITCH], acc);
+                    Mt[e] = acc;
+                }
+                __syncthreads();
+                for (int e = tid; e < nel; e += NT) {
+                    const int bl = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+                    const int a0 = (bl + dd) * 16;
+                    const float* Ta = &Tm[(a0 + r) * A_PITCH + a0];
+                    const float* Mb = &Mt[(bl << 8) + cc];
+                    float acc = 0.f;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                *reinterpret_cast<bf16*>(sm + SM_BW + sw128_off(i, col)) = __float2bfloat16_rn(x[i] * fw);
-                *reinterpret_cast<bf16*>(sm + SM_BU + sw128_off(i, col)) = __float2bfloat16_rn(x[i] * fu);
+                    for (int k = 0; k < 16; ++k) acc = fmaf(Ta[k], Mb[k * 16], acc);
+                    Tm[(a0 + r) * A_PITCH + bl * 16 + cc] = -acc;
+                }
+                __syncthreads();
+            }
+            // B_W = T' diag(beta e^G rk) (threads 0-63), B_U = T' diag(beta) (64-127), bf16
+            {
+                const int i = tid & 63;
+                const float* Ti = &Tm[i * A_PITCH];
+                const float* Fc = tid < 64 ? FWs : Bs;
+                float row[64];
+#pragma unroll
+                for (int g4 = 0; g4 < 16; ++g4) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(Ti + 4 * g4);
+                    const float4 f4 = *reinterpret_cast<const float4*>(Fc + 4 * g4);
+                    row[4 * g4 + 0] = t4.x * f4.x;
+                    row[4 * g4 + 1] = t4.y * f4.y;
+                    row[4 * g4 + 2] = t4.z * f4.z;
+                    row[4 * g4 + 3] = t4.w * f4.w;
+                }
+                store_row_bf16(sm + (tid < 64 ? SM_BW : SM_BU), i, 0, row, 64);
             }
         }
         fence_async_smem();
@@ -457,11 +552,29 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
             tmem_ld32(tb + lo + T_DO, po);
             tmem_ld32(tb + lo + T_DO + 32, po + 32);
             tmem_wait_ld();
-            bf16* o = static_cast<bf16*>(a.o) + (t0 * a.H_v + h) * D + tid;
-            const int64_t ostride = (int64_t)a.H_v * D;
+            if (n == C) {
+                // stage the 64 x 128 tile (128B-swizzled, in the B_W/B_U buffers, free
+                // until the next solve) and write it with two TMA stores
+                uint8_t* stg = sm + SM_BW + (tid >> 6) * 8192;
+                const int cc = tid & 63;
 #pragma unroll
-            for (int i = 0; i < 64; ++i)
-                if (i < n) o[i * ostride] = __float2bfloat16_rn(eGs[i] * RQs[i] * qs[i] + po[i]);
+                for (int i = 0; i < 64; ++i)
+                    *reinterpret_cast<bf16*>(stg + sw128_off(i, cc)) =
+                        __float2bfloat16_rn(eGs[i] * RQs[i] * qs[i] + po[i]);
+                fence_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    tma_store_2d(&omap, sm + SM_BW, h * D, (int)t0);
+                    tma_store_2d(&omap, sm + SM_BW + 8192, h * D + 64, (int)t0);
+                    bulk_commit();
+                }
+            } else {
+                bf16* o = static_cast<bf16*>(a.o) + (t0 * a.H_v + h) * D + tid;
+                const int64_t ostride = (int64_t)a.H_v * D;
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (i < n) o[i * ostride] = __float2bfloat16_rn(eGs[i] * RQs[i] * qs[i] + po[i]);
+            }
         }
         // ---- new state -> bf16 S^T operand (and checkpoint)
         {
@@ -503,10 +616,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a) {
         atomicOr(&g_device_error, 1);
         // let copies and MMAs still in flight land before the memory is released
         if (mma_pending) mbar_wait(bar_mma, mma_phase, kWaitNs);
-        for (int bb = 0; bb < 2; ++bb)
-            for (int k = consumed[bb]; k < issued[bb]; ++k)
-                mbar_wait(&bar_tma[bb], (uint32_t)(k & 1), kWaitNs);
+        for (int k = consumed0; k < issued0; ++k) mbar_wait(&bar_tma[0], (uint32_t)(k & 1), kWaitNs);
+        for (int k = consumed1; k < issued1; ++k) mbar_wait(&bar_tma[1], (uint32_t)(k & 1), kWaitNs);
     }
+    if (tid == 0) bulk_wait_all();  // O tile stores complete before the CTA's memory goes
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, TMEM_COLS);
@@ -545,12 +658,19 @@ cudaError_t launch_chunk_tc(const DeltaArgs& a, cudaStream_t s) {
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    CUtensorMap omap;
+    cuuint64_t odim[2] = {(cuuint64_t)a.H_v * D, (cuuint64_t)a.T};
+    cuuint64_t ostr[1] = {(cuuint64_t)a.H_v * D * 2};
+    if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.o, odim, ostr, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(a.n_seq * a.H_v);
     if (grid == 0) return cudaSuccess;
-    chunk_tc_kernel<<<grid, NT, SMEM_BYTES, s>>>(map, a);
+    chunk_tc_kernel<<<grid, NT, SMEM_BYTES, s>>>(map, omap, a);
     return cudaGetLastError();
 }
 
