@@ -176,8 +176,13 @@ def gdn_chunk_prefill(qkv, dims, a=None, b=None, A_log=None, dt_bias=None, g=Non
     if o is None:
         o = torch.empty((T, dims.H_v, dims.d_v), dtype=dt, device=qkv.device)
     rows = 0 if state_ckpt_out is None else int(state_ckpt_out.shape[0])
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     lib = _lib.load()
+    if workspace is None:
+        need = lib.gdn_chunk_prefill_workspace_size(_nseq(cu_seqlens), T, _dims(dims),
+                                                    _dtype_code(qkv))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=qkv.device)
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib.gdn_chunk_prefill(
         _ptr(qkv, "qkv", dt), *_gate_ptrs(a, b, A_log, dt_bias, g, beta, dt),
         _ptr(cu_seqlens, "cu_seqlens", torch.int32), _nseq(cu_seqlens), T,

@@ -164,8 +164,9 @@ gdn_status_t gdn_conv1d_update(const void* x, const void* w, void* conv_state, i
 
 size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t dims,
                                         gdn_dtype_t dtype) {
-    (void)n_seq; (void)T_tot; (void)dims; (void)dtype;
-    return 0;
+    if (check_dims(dims, dtype) != GDN_OK || n_seq < 1 || T_tot <= 0) return 0;
+    if (dtype != GDN_BF16 || dims.d_k != 128) return 0;  // the CUDA-core path needs none
+    return gdn::chunk_split_workspace_bytes(n_seq, T_tot, dims.H_v);
 }
 
 gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, const float* A_log,
@@ -204,7 +205,7 @@ gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, co
     d.l2norm = (flags & GDN_QK_L2NORM) != 0;
     d.o = o;
     cudaStream_t s = (cudaStream_t)stream;
-    if (gdn::chunk_tc_supported(d, dtype)) return cuda_status(gdn::launch_chunk_tc(d, s));
+    if (need > 0) return cuda_status(gdn::launch_chunk_split(d, workspace, ws_bytes, s));
     return cuda_status(gdn::launch_chunk_ffma(d, dtype, s));
 }
 

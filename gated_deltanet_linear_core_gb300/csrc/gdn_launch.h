@@ -7,6 +7,8 @@
 
 #include "gdn.h"
 
+#include <cudaTypedefs.h>
+
 namespace gdn {
 
 struct ConvArgs {
@@ -51,12 +53,18 @@ struct DeltaArgs {
 };
 // Chunked prefill on CUDA cores (f32 arithmetic; any supported D and dtype).
 cudaError_t launch_chunk_ffma(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s);
-// Chunked prefill on tcgen05 tensor cores (bf16 operands, f32 state), for the
-// shapes chunk_tc_supported() accepts.
-bool chunk_tc_supported(const DeltaArgs& a, gdn_dtype_t dt);
-cudaError_t launch_chunk_tc(const DeltaArgs& a, cudaStream_t s);
 // Recurrent decode: T = B tokens, sequence i = token i, state in place (S0 == S_final).
 cudaError_t launch_recurrent_decode(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s);
+
+// cuTensorMapEncodeTiled from the driver (nullptr if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensormap_encoder();
+
+// Chunked prefill on tcgen05 tensor cores (bf16 operands, f32 state, D = 128)
+// in two kernels: the state-independent work of every chunk in parallel (into
+// `workspace`), then the sequential state recurrence.
+size_t chunk_split_workspace_bytes(int n_seq, int64_t T, int H_v);
+cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes,
+                               cudaStream_t s);
 
 // Reads (synchronising `s`) and clears the library's device error word.
 cudaError_t read_and_clear_device_error(cudaStream_t s, int* flags);
