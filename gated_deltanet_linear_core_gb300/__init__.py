@@ -22,7 +22,7 @@ from ._lib import GDNError, GDN_QK_L2NORM  # noqa: F401
 
 __all__ = [
     "GDNDims", "GDNError", "gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
-    "gdn_chunk_prefill_workspace_size", "gdn_recurrent_decode", "gdn_rmsnorm_gated",
+    "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode", "gdn_rmsnorm_gated",
     "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_sync_status", "gdn_layer_prefill", "gdn_layer_decode",
     "library_path",
 ]
@@ -192,6 +192,32 @@ def gdn_chunk_prefill(qkv, dims, a=None, b=None, A_log=None, dt_bias=None, g=Non
         _lib.GDN_QK_L2NORM if l2norm_qk else 0, _ptr(o, "o", dt), _ptr(workspace, "workspace"),
         ws, _dims(dims), _dtype_code(qkv), _stream(qkv, stream))
     _lib.check(st, "gdn_chunk_prefill")
+    return o
+
+
+def gdn_chunk_prefill_noalloc(qkv, dims, o, final_state, a=None, b=None, A_log=None,
+                              dt_bias=None, g=None, beta=None, cu_seqlens=None,
+                              initial_state=None, ckpt_every=0, state_ckpt_out=None, scale=0.0,
+                              l2norm_qk=True, stream=None):
+    """gdn_chunk_prefill for callers that cannot allocate device memory: its
+    scratch is a fixed array inside the library, and this binding allocates
+    nothing either -- the caller passes every output (o [T, H_v, d_v] and
+    final_state [n_seq, H_v, d_k, d_v] f32, plus state_ckpt_out when
+    checkpointing).  bf16, d = 128 only.  Calls that overlap on the GPU share
+    the array and race; the first call on a device should precede any stream
+    capture."""
+    dt = qkv.dtype
+    T = int(qkv.shape[0])
+    rows = 0 if state_ckpt_out is None else int(state_ckpt_out.shape[0])
+    st = _lib.load().gdn_chunk_prefill_noalloc(
+        _ptr(qkv, "qkv", dt), *_gate_ptrs(a, b, A_log, dt_bias, g, beta, dt),
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32), _nseq(cu_seqlens), T,
+        _ptr(initial_state, "initial_state", torch.float32),
+        _ptr(final_state, "final_state", torch.float32), int(ckpt_every),
+        _ptr(state_ckpt_out, "state_ckpt_out", torch.float32), rows, float(scale),
+        _lib.GDN_QK_L2NORM if l2norm_qk else 0, _ptr(o, "o", dt, (T, dims.H_v, dims.d_v)),
+        _dims(dims), _dtype_code(qkv), _stream(qkv, stream))
+    _lib.check(st, "gdn_chunk_prefill_noalloc")
     return o
 
 

@@ -823,3 +823,87 @@ cudaError_t read_and_clear_device_error(cudaStream_t s, int* flags) {
 }
 
 }  // namespace gdn
+
+// ===================================================================== no-allocation variant
+// gdn_chunk_prefill_noalloc runs the same two kernels with their scratch in a
+// fixed array that is part of the library image, for callers that cannot
+// allocate device memory.  Smaller segments than the workspace variant (the
+// array is 24 MiB) mean more launches; the arithmetic is the same.
+namespace gdn {
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = 24ull << 20;
+constexpr int kStaticMaxSeq = 16384;
+
+static __device__ __align__(256) uint8_t g_prefill_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[128];  // device address of g_prefill_scratch, per device ordinal
+
+}  // namespace
+
+bool chunk_split_static_fits(int n_seq, int H_v) {
+    const size_t coff_bytes = ((size_t)4 * (kStaticMaxSeq + 1) + 255) & ~(size_t)255;
+    return n_seq >= 1 && n_seq <= kStaticMaxSeq &&
+           (size_t)H_v * UNIT_BYTES <= kStaticScratchBytes - coff_bytes;
+}
+
+cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s) {
+    if (!chunk_split_static_fits(a.n_seq, a.H_v) || a.S_final == nullptr) return cudaErrorInvalidValue;
+    // set-up once per device, with that device current: the host-side name of
+    // the array is not a device address
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    uint8_t* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (g_scratch_ptr[dev] == nullptr) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_prefill_scratch);
+            if (e != cudaSuccess) return e;
+            g_scratch_ptr[dev] = p;
+        }
+        base = static_cast<uint8_t*>(g_scratch_ptr[dev]);
+    }
+    // layout inside the fixed array: chunk offsets, then as many chunks per
+    // segment as fit; final_state carries the state between segments
+    const size_t coff_bytes = ((size_t)4 * (kStaticMaxSeq + 1) + 255) & ~(size_t)255;
+    const int64_t max_chunks = a.T / C + a.n_seq;
+    int64_t segc = (int64_t)((kStaticScratchBytes - coff_bytes) / ((size_t)a.H_v * UNIT_BYTES));
+    if (segc > max_chunks) segc = max_chunks;
+    if (segc > 65535) segc = 65535;
+    const int64_t n_seg = (max_chunks + segc - 1) / segc;
+    const size_t U = (size_t)segc * a.H_v;
+    Work w;
+    w.coff = reinterpret_cast<int32_t*>(base);
+    w.wt = reinterpret_cast<bf16*>(base + coff_bytes);
+    w.ut = reinterpret_cast<bf16*>(base + coff_bytes + U * U_WT);
+    w.p = reinterpret_cast<bf16*>(base + coff_bytes + U * (U_WT + U_UT));
+    w.vec = reinterpret_cast<float*>(base + coff_bytes + U * (U_WT + U_UT + U_P));
+    w.carry = a.S_final;
+
+    const uint64_t conv_dim = 2ull * a.H_k * D + (uint64_t)a.H_v * D;
+    CUtensorMap qmap, omap, wtmap, utmap, pmap;
+    if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) ||
+        !encode2d(&omap, a.o, (uint64_t)a.H_v * D, (uint64_t)a.T, 64, 64) ||
+        !encode2d(&wtmap, w.wt, 64, U * 128, 64, 128) || !encode2d(&utmap, w.ut, 64, U * 128, 64, 128) ||
+        !encode2d(&pmap, w.p, 64, U * 64, 64, 64))
+        return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CSMEM);
+    if (e != cudaSuccess) return e;
+    chunk_offsets_kernel<<<1, 1024, 0, s>>>(a.cu, a.n_seq, a.T, w.coff);
+    for (int64_t seg = 0; seg < n_seg; ++seg) {
+        const int64_t C0 = seg * segc;
+        chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)segc), NT_I, ISMEM, s>>>(qmap, a, w, C0);
+        chunk_chain_kernel<<<(unsigned)(a.n_seq * a.H_v), NT_C, CSMEM, s>>>(qmap, omap, wtmap, utmap,
+                                                                          pmap, a, w, C0, segc);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -209,6 +209,54 @@ gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, co
     return cuda_status(gdn::launch_chunk_ffma(d, dtype, s));
 }
 
+gdn_status_t gdn_chunk_prefill_noalloc(const void* qkv, const void* a, const void* b,
+                                       const float* A_log, const float* dt_bias, const float* g,
+                                       const float* beta, const int32_t* cu_seqlens, int32_t n_seq,
+                                       int64_t T_tot, const float* initial_state, float* final_state,
+                                       int32_t ckpt_every, float* state_ckpt_out, int64_t ckpt_rows,
+                                       float scale, uint32_t flags, void* o, gdn_dims_t dims,
+                                       gdn_dtype_t dtype, void* stream) {
+    gdn_status_t st = check_dims(dims, dtype);
+    if (st != GDN_OK) return st;
+    if (dtype != GDN_BF16 || dims.d_k != 128) return GDN_ERR_UNSUPPORTED;
+    if ((st = check_seqs(cu_seqlens, n_seq, T_tot)) != GDN_OK) return st;
+    if ((st = check_ckpt(ckpt_every, state_ckpt_out, ckpt_rows)) != GDN_OK) return st;
+    if (T_tot > 0 && (st = check_gates(a, b, A_log, dt_bias, g, beta, dtype)) != GDN_OK) return st;
+    if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return GDN_ERR_INVALID_ARG;
+    if (final_state == nullptr) return GDN_ERR_INVALID_ARG;
+    if (T_tot > 0 && (qkv == nullptr || o == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(qkv) || !aligned16(o) || !aligned16(initial_state) || !aligned16(final_state) ||
+        !aligned16(state_ckpt_out))
+        return GDN_ERR_ALIGN;
+    if (!gdn::chunk_split_static_fits(n_seq, dims.H_v)) return GDN_ERR_WORKSPACE;
+    if (T_tot == 0) {
+        // nothing to compute: the final state of every (empty) sequence is its initial state
+        const size_t bytes = (size_t)n_seq * dims.H_v * dims.d_k * dims.d_v * sizeof(float);
+        cudaError_t e = initial_state != nullptr
+                            ? (initial_state == final_state
+                                   ? cudaSuccess
+                                   : cudaMemcpyAsync(final_state, initial_state, bytes,
+                                                     cudaMemcpyDeviceToDevice, (cudaStream_t)stream))
+                            : cudaMemsetAsync(final_state, 0, bytes, (cudaStream_t)stream);
+        return cuda_status(e);
+    }
+    gdn::DeltaArgs d;
+    memset(&d, 0, sizeof(d));
+    d.qkv = qkv; d.a = a; d.b = b; d.A_log = A_log; d.dt_bias = dt_bias;
+    const bool pre = g && beta;
+    d.g = pre ? g : nullptr; d.beta = pre ? beta : nullptr;
+    d.cu = cu_seqlens; d.n_seq = n_seq; d.T = T_tot;
+    d.H_k = dims.H_k; d.H_v = dims.H_v; d.D = dims.d_k;
+    d.S0 = initial_state; d.S_final = final_state;
+    d.ckpt_every = ckpt_every; d.ckpt = ckpt_every > 0 ? state_ckpt_out : nullptr;
+    d.ckpt_rows = ckpt_rows;
+    d.scale = scale == 0.f ? 1.0f / sqrtf((float)dims.d_k) : scale;
+    d.l2norm = (flags & GDN_QK_L2NORM) != 0;
+    d.o = o;
+    return cuda_status(gdn::launch_chunk_split_static(d, (cudaStream_t)stream));
+}
+
 gdn_status_t gdn_recurrent_decode(const void* qkv, const void* a, const void* b,
                                   const float* A_log, const float* dt_bias, const float* g,
                                   const float* beta, float* state, int32_t B, float scale,

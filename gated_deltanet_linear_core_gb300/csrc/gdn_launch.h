@@ -66,6 +66,11 @@ size_t chunk_split_workspace_bytes(int n_seq, int64_t T, int H_v);
 cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes,
                                cudaStream_t s);
 
+// The same chunked prefill with its scratch in a fixed device array of the
+// library (gdn_chunk_prefill_noalloc): no allocation; final_state required.
+bool chunk_split_static_fits(int n_seq, int H_v);
+cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s);
+
 // Reads (synchronising `s`) and clears the library's device error word.
 cudaError_t read_and_clear_device_error(cudaStream_t s, int* flags);
 

@@ -192,6 +192,43 @@ gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, co
                                gdn_dtype_t dtype, void* stream);
 
 /*
+ * gdn_chunk_prefill without a workspace, for callers that cannot allocate
+ * device memory.  The pages have no counterpart for this call: it exists for
+ * library users whose device memory is owned by someone else -- for example a
+ * plugin inside a host runtime that has partitioned all device memory up front,
+ * or a serving loop that must not allocate on its hot path -- and who therefore
+ * cannot provide the scratch gdn_chunk_prefill_workspace_size asks for.
+ *
+ * The scratch is a fixed 24 MiB array compiled into this library: every GPU
+ * that loads the library holds it until the process exits.  Arguments and
+ * results are those of gdn_chunk_prefill, with these differences:
+ *   - only the tensor-core path: dtype GDN_BF16 and d_k = d_v = 128
+ *     (GDN_ERR_UNSUPPORTED otherwise; gdn_chunk_prefill needs no workspace for
+ *     the other shapes);
+ *   - final_state is required (it carries the state between the call's
+ *     segments); it may alias initial_state;
+ *   - limits: n_seq <= 16384 and H_v * 41,984 bytes must fit in the array
+ *     (H_v <= 597); calls beyond them return GDN_ERR_WORKSPACE;
+ *   - the first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture;
+ *   - all calls share the one array: calls whose kernels overlap on the GPU
+ *     (other streams, other host threads) race and corrupt each other's
+ *     results.  Nothing in the array has to start at zero -- every value a
+ *     call reads is written earlier in the same call -- so the contents left
+ *     by the previous call do no harm.
+ * The arithmetic is the same as gdn_chunk_prefill's; the chunks are processed
+ * in smaller segments (more kernel launches).
+ */
+gdn_status_t gdn_chunk_prefill_noalloc(const void* qkv, const void* a, const void* b,
+                                       const float* A_log, const float* dt_bias, const float* g,
+                                       const float* beta, const int32_t* cu_seqlens, int32_t n_seq,
+                                       int64_t T_tot, const float* initial_state, float* final_state,
+                                       int32_t ckpt_every, float* state_ckpt_out, int64_t ckpt_rows,
+                                       float scale, uint32_t flags, void* o, gdn_dims_t dims,
+                                       gdn_dtype_t dtype, void* stream);
+
+/*
  * One recurrent decode step for B sequences (one token each), state in place.
  * Defined by: cortex GatedDeltaNet commit, "Delta rule (recurrent, per-token)",
  * "Discretisation", "Block" (L2norm on q,k); NxD-Inference Qwen3.6-27B PR,
