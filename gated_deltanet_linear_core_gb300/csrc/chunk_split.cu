@@ -468,17 +468,22 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a, Work w
 // ============================================================== chain kernel
 constexpr int NT_C = 512;
 constexpr int CS_ST = 0;                           // S^T bf16 [v][d], 2 blocks of 16 KB
-constexpr int STAGE = 73728;                       // WT 16K | UT 16K | P 8K | Q 16K | K 16K
+constexpr int STAGE = 74752;                       // WT 16K | UT 16K | P 8K | Q 16K | K 16K | vec 1K
 constexpr int CS_STAGE = CS_ST + 32768;
-constexpr int SG_WT = 0, SG_UT = 16384, SG_P = 32768, SG_Q = 40960, SG_K = 57344;
+constexpr int SG_WT = 0, SG_UT = 16384, SG_P = 32768, SG_Q = 40960, SG_K = 57344, SG_VEC = 73728;
 constexpr int CS_UTC = CS_STAGE + 2 * STAGE;       // U'^T bf16 (then the O staging tile)
 constexpr int CS_UTD = CS_UTC + 16384;             // U'^T diag(e^{G_n-G_j} rk)
 constexpr int CS_BAR = CS_UTD + 16384;
 constexpr int CS_TOTAL = CS_BAR + 64;
 constexpr int CSMEM = CS_TOTAL + 1024;
 static_assert(CSMEM <= 232448, "chain kernel shared memory");
-constexpr uint32_t TC_S = 0, TC_WS = 128, TC_QS = 192, TC_O = 256, TC_COLS = 512;
+// TMEM: state, (W S)^T, and two buffers each of (Q S)^T and U'^T P^T
+constexpr uint32_t TC_S = 0, TC_WS = 128, TC_QS = 192, TC_O = 320, TC_COLS = 512;
 
+// Per chunk: MMA(S^T W^T, S^T Q^T) -> U' -> MMA(state update, U'^T P^T) -> state
+// read-back (bf16 operand for the next chunk, the next chunk's decay applied in
+// TMEM) -> the next chunk's first MMAs are issued -> this chunk's O epilogue
+// runs while they execute.
 __global__ void __launch_bounds__(NT_C, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
                    const __grid_constant__ CUtensorMap wtmap, const __grid_constant__ CUtensorMap utmap,
@@ -489,7 +494,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     const int64_t cs = w.coff[seq], ce = w.coff[seq + 1];
     const int64_t c_lo = cs > C0 ? cs : C0, c_hi = ce < C0 + segc ? ce : C0 + segc;
     const int64_t sbase = ((int64_t)seq * a.H_v + h) * D * D;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     if (c_lo >= c_hi) {
         // no chunk of this sequence in this segment; an empty sequence's final
         // state is its initial state (written once, by the first segment)
@@ -498,7 +503,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 a.S_final[sbase + e] = a.S0 != nullptr ? a.S0[sbase + e] : 0.f;
         return;
     }
-    (void)lane;
     const int quarter = warp & 3, cg = warp >> 2;
     const int row = quarter * 32 + (tid & 31);
     const uint32_t lo = (uint32_t)(quarter * 32) << 16;
@@ -536,16 +540,42 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         const int b = (int)((gcc - c_lo) & 1);
         uint8_t* st = sm + CS_STAGE + b * STAGE;
         const int y = (int)(s0 + (gcc - cs) * C);
-        const int uu = (int)((gcc - C0) * a.H_v + h);
+        const int64_t uu = (gcc - C0) * a.H_v + h;
         mbar_arrive_expect_tx(&bar_tma[b], STAGE);
-        tma_load_2d(st + SG_WT, &wtmap, &bar_tma[b], 0, uu * 128);
-        tma_load_2d(st + SG_UT, &utmap, &bar_tma[b], 0, uu * 128);
-        tma_load_2d(st + SG_P, &pmap, &bar_tma[b], 0, uu * 64);
+        tma_load_2d(st + SG_WT, &wtmap, &bar_tma[b], 0, (int)(uu * 128));
+        tma_load_2d(st + SG_UT, &utmap, &bar_tma[b], 0, (int)(uu * 128));
+        tma_load_2d(st + SG_P, &pmap, &bar_tma[b], 0, (int)(uu * 64));
         tma_load_2d(st + SG_Q, &qmap, &bar_tma[b], xq, y);
         tma_load_2d(st + SG_Q + 8192, &qmap, &bar_tma[b], xq + 64, y);
         tma_load_2d(st + SG_K, &qmap, &bar_tma[b], xk, y);
         tma_load_2d(st + SG_K + 8192, &qmap, &bar_tma[b], xk + 64, y);
+        bulk_load(st + SG_VEC, w.vec + uu * (int64_t)(U_VEC / 4), (uint32_t)U_VEC, &bar_tma[b]);
         if (b) ++issued1; else ++issued0;
+    };
+    auto wait_stage = [&](int64_t gcc) -> bool {  // every thread, in chunk order
+        const int b = (int)((gcc - c_lo) & 1);
+        const bool r = mbar_wait(&bar_tma[b], (uint32_t)((b ? consumed1 : consumed0) & 1), kWaitNs);
+        if (r) {
+            if (b) ++consumed1; else ++consumed0;
+        }
+        return r;
+    };
+    auto issue_mma45 = [&](int64_t gcc) {  // thread 0: (W S)^T and (Q S)^T of chunk gcc
+        const int b = (int)((gcc - c_lo) & 1);
+        uint8_t* st = sm + CS_STAGE + b * STAGE;
+        tc_fence_after();
+        const uint32_t ast = smem_u32(sm + CS_ST), bwt = smem_u32(st + SG_WT);
+        const uint32_t bq = smem_u32(st + SG_Q);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t offA = (k >> 2) * 16384 + (k & 3) * 32;
+            const uint32_t offQ = (k >> 2) * 8192 + (k & 3) * 32;
+            mma_bf16(tb + TC_WS, sdesc_sw128(ast + offA, 16, 1024),
+                     sdesc_sw128(bwt + k * 2048, 16384, 1024), idesc_bf16_f32(128, 64, 0, 1), k > 0);
+            mma_bf16(tb + TC_QS + 64 * b, sdesc_sw128(ast + offA, 16, 1024),
+                     sdesc_sw128(bq + offQ, 16, 1024), idesc_bf16_f32(128, 64, 0, 0), k > 0);
+        }
+        mma_commit(bar_mma);
     };
     if (tid == 0) {
         issue(c_lo);
@@ -554,61 +584,50 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 
     // initial state of this segment: the sequence's initial state at its first
     // chunk, else what the previous segment left in the carry
+    bool ok;
     {
         const float* src = (c_lo == cs) ? a.S0 : w.carry;
         float sv[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             sv[j] = src != nullptr ? src[sbase + (int64_t)(32 * cg + j) * D + row] : 0.f;
-        tmem_st32(tb + lo + TC_S + 32 * cg, sv);
         store_row_bf16(sm + CS_ST + (cg >> 1) * 16384, row, (cg & 1) * 32, sv, 32);
+        ok = __syncthreads_and(wait_stage(c_lo));
+        if (ok) {
+            // TMEM holds e^{G_n} S for the coming state update
+            const float eGn = reinterpret_cast<const float*>(sm + CS_STAGE + SG_VEC)[128];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sv[j] *= eGn;
+            tmem_st32(tb + lo + TC_S + 32 * cg, sv);
+            tmem_wait_st();
+        }
     }
-    tmem_wait_st();
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-
     uint32_t mma_phase = 0;
     bool mma_pending = false;
-    bool ok = true;
-    for (int64_t gcc = c_lo; gcc < c_hi; ++gcc) {
+    if (ok && tid == 0) issue_mma45(c_lo);
+    mma_pending = ok;
+
+    for (int64_t gcc = c_lo; ok && gcc < c_hi; ++gcc) {
         const int b = (int)((gcc - c_lo) & 1);
         uint8_t* st = sm + CS_STAGE + b * STAGE;
+        const float* vs = reinterpret_cast<const float*>(st + SG_VEC);
         const int64_t lc = gcc - cs;
         const int64_t t0 = s0 + lc * C;
         const int n = (int)(L - lc * C < C ? L - lc * C : C);
-        const float* vec = w.vec + ((gcc - C0) * a.H_v + h) * (int64_t)(U_VEC / 4);
+        const int i0 = 16 * cg;
 
-        ok = __syncthreads_and(mbar_wait(&bar_tma[b], (uint32_t)((b ? consumed1 : consumed0) & 1), kWaitNs));
-        if (!ok) break;
-        if (b) ++consumed1; else ++consumed0;
-
-        // (W S)^T = S^T W^T,  (Q S)^T = S^T Q^T     (M = v, N = i, K = d)
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t ast = smem_u32(sm + CS_ST), bwt = smem_u32(st + SG_WT);
-            const uint32_t bq = smem_u32(st + SG_Q);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t offA = (k >> 2) * 16384 + (k & 3) * 32;
-                const uint32_t offQ = (k >> 2) * 8192 + (k & 3) * 32;
-                mma_bf16(tb + TC_WS, sdesc_sw128(ast + offA, 16, 1024),
-                         sdesc_sw128(bwt + k * 2048, 16384, 1024), idesc_bf16_f32(128, 64, 0, 1), k > 0);
-                mma_bf16(tb + TC_QS, sdesc_sw128(ast + offA, 16, 1024),
-                         sdesc_sw128(bq + offQ, 16, 1024), idesc_bf16_f32(128, 64, 0, 0), k > 0);
-            }
-            mma_commit(bar_mma);
-            bulk_wait_read_all();  // the previous O tile store has left the U'^T buffer
-        }
-        mma_pending = true;
+        if (tid == 0) bulk_wait_read_all();  // the previous O tile store has left U'^T's buffer
         ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase, kWaitNs));
         if (!ok) break;
         mma_phase ^= 1;
         mma_pending = false;
         tc_fence_after();
 
-        // U'^T = U^T - (W S)^T (bf16, and scaled by e^{G_n-G_j} rk_j); S^T *= e^{G_n}
+        // U'^T = U^T - (W S)^T (bf16, and scaled by e^{G_n-G_j} rk_j)
+        float erq[16];  // e^{G_i} rq_i of this thread's O rows (the stage is reloaded below)
         {
             const int j0 = 16 * cg;
             float ws[16], ui[16];
@@ -621,21 +640,15 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 #pragma unroll
                 for (int e = 0; e < 8; ++e) ui[8 * g + e] = t8[e];
             }
+#pragma unroll
+            for (int q = 0; q < 16; ++q) erq[q] = vs[i0 + q];
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; ++j) ui[j] -= ws[j];
             store_row_bf16(sm + CS_UTC, row, j0, ui, 16);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) ws[j] = ui[j] * vec[64 + j0 + j];
+            for (int j = 0; j < 16; ++j) ws[j] = ui[j] * vs[64 + j0 + j];
             store_row_bf16(sm + CS_UTD, row, j0, ws, 16);
-            const float eGn = vec[128];
-            float sv[32];
-            tmem_ld32(tb + lo + TC_S + 32 * cg, sv);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sv[j] *= eGn;
-            tmem_st32(tb + lo + TC_S + 32 * cg, sv);
-            tmem_wait_st();
         }
         fence_async_smem();
         tc_fence_before();
@@ -650,7 +663,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             for (int k = 0; k < 4; ++k) {
                 mma_bf16(tb + TC_S, sdesc_sw128(autd + k * 32, 16, 1024),
                          sdesc_sw128(bk + k * 2048, 8192, 1024), idesc_bf16_f32(128, 128, 0, 1), 1);
-                mma_bf16(tb + TC_O, sdesc_sw128(aut + k * 32, 16, 1024),
+                mma_bf16(tb + TC_O + 64 * b, sdesc_sw128(aut + k * 32, 16, 1024),
                          sdesc_sw128(bp + k * 32, 16, 1024), idesc_bf16_f32(128, 64, 0, 0), k > 0);
             }
             mma_commit(bar_mma);
@@ -661,9 +674,11 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         mma_phase ^= 1;
         mma_pending = false;
         tc_fence_after();
-        if (tid == 0 && gcc + 2 < c_hi) issue(gcc + 2);
+        if (tid == 0 && gcc + 2 < c_hi) issue(gcc + 2);  // this chunk's stage is consumed
 
-        // new state -> bf16 S^T operand (and checkpoint)
+        // new state -> bf16 S^T operand (and checkpoint); TMEM <- e^{G_n'} S for the next chunk
+        const bool more = gcc + 1 < c_hi;
+        bool landed = true;
         {
             const int64_t done = lc * C + n;
             float* ck = nullptr;
@@ -678,21 +693,39 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             if (ck != nullptr)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ck[(int64_t)(32 * cg + j) * D + row] = sv[j];
+            if (more) {
+                landed = wait_stage(gcc + 1);
+                if (landed) {
+                    const float eGn = reinterpret_cast<const float*>(sm + CS_STAGE + (b ^ 1) * STAGE +
+                                                                     SG_VEC)[128];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sv[j] *= eGn;
+                    tmem_st32(tb + lo + TC_S + 32 * cg, sv);
+                    tmem_wait_st();
+                }
+            }
         }
-        // O = (Q S) diag(e^G rq) + P U'   (thread (v, cg) holds O[i][v], i in [16 cg, 16 cg + 16))
+        fence_async_smem();
+        tc_fence_before();
+        ok = __syncthreads_and(landed);
+        if (!ok) break;
+        if (more && tid == 0) issue_mma45(gcc + 1);
+        mma_pending = more;
+
+        // O = (Q S) diag(e^G rq) + P U' of this chunk, while the next chunk's MMAs run
         {
+            tc_fence_after();
             float qs[16], po[16];
-            tmem_ld16(tb + lo + TC_QS + 16 * cg, qs);
-            tmem_ld16(tb + lo + TC_O + 16 * cg, po);
+            tmem_ld16(tb + lo + TC_QS + 64 * b + i0, qs);
+            tmem_ld16(tb + lo + TC_O + 64 * b + i0, po);
             tmem_wait_ld();
-            const int i0 = 16 * cg;
             if (n == C) {
                 uint8_t* stg = sm + CS_UTC + (row >> 6) * 8192;
                 const int cc = row & 63;
 #pragma unroll
                 for (int q = 0; q < 16; ++q)
                     *reinterpret_cast<bf16*>(stg + sw128_off(i0 + q, cc)) =
-                        __float2bfloat16_rn(vec[i0 + q] * qs[q] + po[q]);
+                        __float2bfloat16_rn(erq[q] * qs[q] + po[q]);
                 fence_async_smem();
                 __syncthreads();
                 if (tid == 0) {
@@ -705,18 +738,17 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 const int64_t ostride = (int64_t)a.H_v * D;
 #pragma unroll
                 for (int q = 0; q < 16; ++q)
-                    if (i0 + q < n) o[(i0 + q) * ostride] = __float2bfloat16_rn(vec[i0 + q] * qs[q] + po[q]);
+                    if (i0 + q < n) o[(i0 + q) * ostride] = __float2bfloat16_rn(erq[q] * qs[q] + po[q]);
             }
         }
-        fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        tc_fence_after();
     }
 
     if (ok) {
         float* dst = a.S_final != nullptr ? a.S_final : w.carry;
         if (dst != nullptr) {
+            tc_fence_after();
             float sv[32];
             tmem_ld32(tb + lo + TC_S + 32 * cg, sv);
             tmem_wait_ld();
