@@ -13,7 +13,7 @@
 //   intra (independent per chunk, all chunks of all heads in parallel):
 //     D1 = [K; Q] K^T,  A = beta rk e^{G_i-G_j} rk k.k (j<i),  P = rq e^{G_i-G_j} rk q.k (j<=i)
 //     W^T = K^T (T' diag(beta e^G rk))^T,  U^T = V^T (T' diag(beta))^T
-//     -> workspace: W^T, U^T, P (bf16) and e^G rq, e^{G_n-G_j} rk, e^{G_n} (f32)
+//     -> workspace: W (row-major), U^T, P (bf16) and e^G rq, e^{G_n-G_j} rk, e^{G_n} (f32)
 //   chain (sequential per sequence and value head):
 //     U'^T = U^T - S^T W^T;  O^T = (S^T Q^T) diag(e^G rq) + U'^T P^T
 //     S^T <- e^{G_n} S^T + U'^T diag(e^{G_n-G_j} rk) K
@@ -74,7 +74,7 @@ Layout layout_of(int n_seq, int64_t T, int H_v) {
 }
 
 struct Work {
-    bf16* wt;       // [U][128][64]
+    bf16* wt;       // W, [U][64][128] (row i of W = 128 d-values)
     bf16* ut;       // [U][128][64]
     bf16* p;        // [U][64][64]
     float* vec;     // [U][256]: e^G rq (0..63), e^{G_n-G_j} rk (64..127), e^{G_n} (128)
@@ -141,7 +141,8 @@ constexpr int ISMEM = IS_TOTAL + 1024;
 constexpr uint32_t TI_D1 = 0, TI_DW = 64, TI_DU = 128, TI_COLS = 256;
 
 __global__ void __launch_bounds__(NT_I, 2)
-chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a, Work w, int64_t C0) {
+chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
+                   DeltaArgs a, Work w, int64_t C0) {
     const int h = blockIdx.x;
     const int64_t gc = C0 + blockIdx.y;
     const int n_seq = a.n_seq;
@@ -436,18 +437,22 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a, Work w
     if (ok) {
         mma_pending = false;
         tc_fence_after();
-        {   // W^T and U^T rows -> workspace (bf16, 32 columns per thread)
+        {   // W (row-major, staged 128B-swizzled in the consumed V tile, stored by TMA)
+            // and U^T rows (bf16, 32 columns per thread)
             float v32[32];
             tmem_ld32(tb + lo + TI_DW + 32 * half, v32);
             tmem_wait_ld();
-            bf16* dst = w.wt + u * (U_WT / 2) + row * 64 + 32 * half;
+            uint8_t* stg = vv + (row >> 6) * 8192;
+            const int dc = row & 63;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) store16(dst + 8 * g, v32 + 8 * g);
+            for (int q = 0; q < 32; ++q)
+                *reinterpret_cast<bf16*>(stg + sw128_off(32 * half + q, dc)) = __float2bfloat16_rn(v32[q]);
             tmem_ld32(tb + lo + TI_DU + 32 * half, v32);
             tmem_wait_ld();
-            dst = w.ut + u * (U_UT / 2) + row * 64 + 32 * half;
+            bf16* dst = w.ut + u * (U_UT / 2) + row * 64 + 32 * half;
 #pragma unroll
             for (int g = 0; g < 4; ++g) store16(dst + 8 * g, v32 + 8 * g);
+            fence_async_smem();
         }
         if (tid < 64) {
             float* vec = w.vec + u * (U_VEC / 4);
@@ -462,23 +467,29 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, DeltaArgs a, Work w
     }
     tc_fence_before();
     __syncthreads();
+    if (ok && tid == 0) {
+        tma_store_2d(&wmap, vv, 0, (int)(u * 64));
+        tma_store_2d(&wmap, vv + 8192, 64, (int)(u * 64));
+        bulk_commit();
+        bulk_wait_all();
+    }
     if (warp == 0) tmem_dealloc(tb, TI_COLS);
 }
 
 // ============================================================== chain kernel
 constexpr int NT_C = 512;
 constexpr int CS_ST = 0;                           // S^T bf16 [v][d], 2 blocks of 16 KB
-constexpr int STAGE = 74752;                       // WT 16K | UT 16K | P 8K | Q 16K | K 16K | vec 1K
+constexpr int STAGE = 74752;  // [W|Q] 32K (per 64-column block: W rows, Q rows) | UT 16K | P 8K | K 16K | vec 1K
 constexpr int CS_STAGE = CS_ST + 32768;
-constexpr int SG_WT = 0, SG_UT = 16384, SG_P = 32768, SG_Q = 40960, SG_K = 57344, SG_VEC = 73728;
+constexpr int SG_WQ = 0, SG_UT = 32768, SG_P = 49152, SG_K = 57344, SG_VEC = 73728;
 constexpr int CS_UTC = CS_STAGE + 2 * STAGE;       // U'^T bf16 (then the O staging tile)
 constexpr int CS_UTD = CS_UTC + 16384;             // U'^T diag(e^{G_n-G_j} rk)
 constexpr int CS_BAR = CS_UTD + 16384;
 constexpr int CS_TOTAL = CS_BAR + 64;
 constexpr int CSMEM = CS_TOTAL + 1024;
 static_assert(CSMEM <= 232448, "chain kernel shared memory");
-// TMEM: state, (W S)^T, and two buffers each of (Q S)^T and U'^T P^T
-constexpr uint32_t TC_S = 0, TC_WS = 128, TC_QS = 192, TC_O = 320, TC_COLS = 512;
+// TMEM: state, two buffers of [(W S)^T | (Q S)^T] and two of U'^T P^T
+constexpr uint32_t TC_S = 0, TC_WQS = 128, TC_O = 384, TC_COLS = 512;
 
 // Per chunk: MMA(S^T W^T, S^T Q^T) -> U' -> MMA(state update, U'^T P^T) -> state
 // read-back (bf16 operand for the next chunk, the next chunk's decay applied in
@@ -486,7 +497,7 @@ constexpr uint32_t TC_S = 0, TC_WS = 128, TC_QS = 192, TC_O = 320, TC_COLS = 512
 // runs while they execute.
 __global__ void __launch_bounds__(NT_C, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-                   const __grid_constant__ CUtensorMap wtmap, const __grid_constant__ CUtensorMap utmap,
+                   const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap utmap,
                    const __grid_constant__ CUtensorMap pmap, DeltaArgs a, Work w, int64_t C0,
                    int64_t segc) {
     const int h = blockIdx.x % a.H_v;
@@ -542,11 +553,12 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         const int y = (int)(s0 + (gcc - cs) * C);
         const int64_t uu = (gcc - C0) * a.H_v + h;
         mbar_arrive_expect_tx(&bar_tma[b], STAGE);
-        tma_load_2d(st + SG_WT, &wtmap, &bar_tma[b], 0, (int)(uu * 128));
+        tma_load_2d(st + SG_WQ, &wmap, &bar_tma[b], 0, (int)(uu * 64));
+        tma_load_2d(st + SG_WQ + 16384, &wmap, &bar_tma[b], 64, (int)(uu * 64));
+        tma_load_2d(st + SG_WQ + 8192, &qmap, &bar_tma[b], xq, y);
+        tma_load_2d(st + SG_WQ + 24576, &qmap, &bar_tma[b], xq + 64, y);
         tma_load_2d(st + SG_UT, &utmap, &bar_tma[b], 0, (int)(uu * 128));
         tma_load_2d(st + SG_P, &pmap, &bar_tma[b], 0, (int)(uu * 64));
-        tma_load_2d(st + SG_Q, &qmap, &bar_tma[b], xq, y);
-        tma_load_2d(st + SG_Q + 8192, &qmap, &bar_tma[b], xq + 64, y);
         tma_load_2d(st + SG_K, &qmap, &bar_tma[b], xk, y);
         tma_load_2d(st + SG_K + 8192, &qmap, &bar_tma[b], xk + 64, y);
         bulk_load(st + SG_VEC, w.vec + uu * (int64_t)(U_VEC / 4), (uint32_t)U_VEC, &bar_tma[b]);
@@ -560,20 +572,16 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         }
         return r;
     };
-    auto issue_mma45 = [&](int64_t gcc) {  // thread 0: (W S)^T and (Q S)^T of chunk gcc
+    auto issue_mma45 = [&](int64_t gcc) {  // thread 0: [(W S)^T | (Q S)^T] of chunk gcc, one N=128 MMA
         const int b = (int)((gcc - c_lo) & 1);
         uint8_t* st = sm + CS_STAGE + b * STAGE;
         tc_fence_after();
-        const uint32_t ast = smem_u32(sm + CS_ST), bwt = smem_u32(st + SG_WT);
-        const uint32_t bq = smem_u32(st + SG_Q);
+        const uint32_t ast = smem_u32(sm + CS_ST), bwq = smem_u32(st + SG_WQ);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const uint32_t offA = (k >> 2) * 16384 + (k & 3) * 32;
-            const uint32_t offQ = (k >> 2) * 8192 + (k & 3) * 32;
-            mma_bf16(tb + TC_WS, sdesc_sw128(ast + offA, 16, 1024),
-                     sdesc_sw128(bwt + k * 2048, 16384, 1024), idesc_bf16_f32(128, 64, 0, 1), k > 0);
-            mma_bf16(tb + TC_QS + 64 * b, sdesc_sw128(ast + offA, 16, 1024),
-                     sdesc_sw128(bq + offQ, 16, 1024), idesc_bf16_f32(128, 64, 0, 0), k > 0);
+            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+            mma_bf16(tb + TC_WQS + 128 * b, sdesc_sw128(ast + off, 16, 1024),
+                     sdesc_sw128(bwq + off, 16, 1024), idesc_bf16_f32(128, 128, 0, 0), k > 0);
         }
         mma_commit(bar_mma);
     };
@@ -631,7 +639,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         {
             const int j0 = 16 * cg;
             float ws[16], ui[16];
-            tmem_ld16(tb + lo + TC_WS + j0, ws);
+            tmem_ld16(tb + lo + TC_WQS + 128 * b + j0, ws);
             const uint8_t* urow = st + SG_UT;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
@@ -716,7 +724,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         {
             tc_fence_after();
             float qs[16], po[16];
-            tmem_ld16(tb + lo + TC_QS + 64 * b + i0, qs);
+            tmem_ld16(tb + lo + TC_WQS + 128 * b + 64 + i0, qs);
             tmem_ld16(tb + lo + TC_O + 64 * b + i0, po);
             tmem_wait_ld();
             if (n == C) {
@@ -822,7 +830,7 @@ cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_by
     CUtensorMap qmap, omap, wtmap, utmap, pmap;
     if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) ||
         !encode2d(&omap, a.o, (uint64_t)a.H_v * D, (uint64_t)a.T, 64, 64) ||
-        !encode2d(&wtmap, w.wt, 64, U * 128, 64, 128) || !encode2d(&utmap, w.ut, 64, U * 128, 64, 128) ||
+        !encode2d(&wtmap, w.wt, 128, U * 64, 64, 64) || !encode2d(&utmap, w.ut, 64, U * 128, 64, 128) ||
         !encode2d(&pmap, w.p, 64, U * 64, 64, 64))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
@@ -833,7 +841,7 @@ cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_by
     chunk_offsets_kernel<<<1, 1024, 0, s>>>(a.cu, a.n_seq, a.T, w.coff);
     for (int64_t seg = 0; seg < Ly.n_seg; ++seg) {
         const int64_t C0 = seg * Ly.segc;
-        chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, s>>>(qmap, a, w, C0);
+        chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, s>>>(qmap, wtmap, a, w, C0);
         chunk_chain_kernel<<<(unsigned)(a.n_seq * a.H_v), NT_C, CSMEM, s>>>(qmap, omap, wtmap, utmap,
                                                                           pmap, a, w, C0, Ly.segc);
     }
@@ -921,7 +929,7 @@ cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s) {
     CUtensorMap qmap, omap, wtmap, utmap, pmap;
     if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) ||
         !encode2d(&omap, a.o, (uint64_t)a.H_v * D, (uint64_t)a.T, 64, 64) ||
-        !encode2d(&wtmap, w.wt, 64, U * 128, 64, 128) || !encode2d(&utmap, w.ut, 64, U * 128, 64, 128) ||
+        !encode2d(&wtmap, w.wt, 128, U * 64, 64, 64) || !encode2d(&utmap, w.ut, 64, U * 128, 64, 128) ||
         !encode2d(&pmap, w.p, 64, U * 64, 64, 64))
         return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
@@ -931,7 +939,7 @@ cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s) {
     chunk_offsets_kernel<<<1, 1024, 0, s>>>(a.cu, a.n_seq, a.T, w.coff);
     for (int64_t seg = 0; seg < n_seg; ++seg) {
         const int64_t C0 = seg * segc;
-        chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)segc), NT_I, ISMEM, s>>>(qmap, a, w, C0);
+        chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)segc), NT_I, ISMEM, s>>>(qmap, wtmap, a, w, C0);
         chunk_chain_kernel<<<(unsigned)(a.n_seq * a.H_v), NT_C, CSMEM, s>>>(qmap, omap, wtmap, utmap,
                                                                           pmap, a, w, C0, segc);
     }
