@@ -488,8 +488,10 @@ constexpr int CS_BAR = CS_UTD + 16384;
 constexpr int CS_TOTAL = CS_BAR + 64;
 constexpr int CSMEM = CS_TOTAL + 1024;
 static_assert(CSMEM <= 232448, "chain kernel shared memory");
-// TMEM: state, two buffers of [(W S)^T | (Q S)^T] and two of U'^T P^T
-constexpr uint32_t TC_S = 0, TC_WQS = 128, TC_O = 384, TC_COLS = 512;
+// TMEM: the chunk's state increment, two buffers of [(W S)^T | (Q S)^T] and two
+// of U'^T P^T.  The f32 state itself lives in registers: thread (v, cg) holds
+// S[d][v] for d in [32 cg, 32 cg + 32).
+constexpr uint32_t TC_DS = 0, TC_WQS = 128, TC_O = 384, TC_COLS = 512;
 
 // Per chunk: MMA(S^T W^T, S^T Q^T) -> U' -> MMA(state update, U'^T P^T) -> state
 // read-back (bf16 operand for the next chunk, the next chunk's decay applied in
@@ -592,24 +594,15 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 
     // initial state of this segment: the sequence's initial state at its first
     // chunk, else what the previous segment left in the carry
-    bool ok;
+    float sv[32];
     {
         const float* src = (c_lo == cs) ? a.S0 : w.carry;
-        float sv[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             sv[j] = src != nullptr ? src[sbase + (int64_t)(32 * cg + j) * D + row] : 0.f;
         store_row_bf16(sm + CS_ST + (cg >> 1) * 16384, row, (cg & 1) * 32, sv, 32);
-        ok = __syncthreads_and(wait_stage(c_lo));
-        if (ok) {
-            // TMEM holds e^{G_n} S for the coming state update
-            const float eGn = reinterpret_cast<const float*>(sm + CS_STAGE + SG_VEC)[128];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sv[j] *= eGn;
-            tmem_st32(tb + lo + TC_S + 32 * cg, sv);
-            tmem_wait_st();
-        }
     }
+    bool ok = __syncthreads_and(wait_stage(c_lo));
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -636,6 +629,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 
         // U'^T = U^T - (W S)^T (bf16, and scaled by e^{G_n-G_j} rk_j)
         float erq[16];  // e^{G_i} rq_i of this thread's O rows (the stage is reloaded below)
+        const float eGn = vs[128];
         {
             const int j0 = 16 * cg;
             float ws[16], ui[16];
@@ -662,15 +656,15 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         tc_fence_before();
         __syncthreads();
 
-        // S^T += U'^T_dec K  (M = v, N = d, K = j);  O_P^T = U'^T P^T  (N = i)
+        // dS^T = U'^T_dec K  (M = v, N = d, K = j);  O_P^T = U'^T P^T  (N = i)
         if (tid == 0) {
             tc_fence_after();
             const uint32_t autd = smem_u32(sm + CS_UTD), aut = smem_u32(sm + CS_UTC);
             const uint32_t bk = smem_u32(st + SG_K), bp = smem_u32(st + SG_P);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                mma_bf16(tb + TC_S, sdesc_sw128(autd + k * 32, 16, 1024),
-                         sdesc_sw128(bk + k * 2048, 8192, 1024), idesc_bf16_f32(128, 128, 0, 1), 1);
+                mma_bf16(tb + TC_DS, sdesc_sw128(autd + k * 32, 16, 1024),
+                         sdesc_sw128(bk + k * 2048, 8192, 1024), idesc_bf16_f32(128, 128, 0, 1), k > 0);
                 mma_bf16(tb + TC_O + 64 * b, sdesc_sw128(aut + k * 32, 16, 1024),
                          sdesc_sw128(bp + k * 32, 16, 1024), idesc_bf16_f32(128, 64, 0, 0), k > 0);
             }
@@ -684,7 +678,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         tc_fence_after();
         if (tid == 0 && gcc + 2 < c_hi) issue(gcc + 2);  // this chunk's stage is consumed
 
-        // new state -> bf16 S^T operand (and checkpoint); TMEM <- e^{G_n'} S for the next chunk
+        // S <- e^{G_n} S + dS (registers) -> bf16 S^T operand (and checkpoint)
         const bool more = gcc + 1 < c_hi;
         bool landed = true;
         {
@@ -694,24 +688,16 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 const int64_t crow = ck_row0 + done / a.ckpt_every - 1;
                 if (crow < a.ckpt_rows) ck = a.ckpt + (crow * a.H_v + h) * D * D;
             }
-            float sv[32];
-            tmem_ld32(tb + lo + TC_S + 32 * cg, sv);
+            float ds[32];
+            tmem_ld32(tb + lo + TC_DS + 32 * cg, ds);
             tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sv[j] = fmaf(eGn, sv[j], ds[j]);
             store_row_bf16(sm + CS_ST + (cg >> 1) * 16384, row, (cg & 1) * 32, sv, 32);
             if (ck != nullptr)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ck[(int64_t)(32 * cg + j) * D + row] = sv[j];
-            if (more) {
-                landed = wait_stage(gcc + 1);
-                if (landed) {
-                    const float eGn = reinterpret_cast<const float*>(sm + CS_STAGE + (b ^ 1) * STAGE +
-                                                                     SG_VEC)[128];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) sv[j] *= eGn;
-                    tmem_st32(tb + lo + TC_S + 32 * cg, sv);
-                    tmem_wait_st();
-                }
-            }
+            if (more) landed = wait_stage(gcc + 1);
         }
         fence_async_smem();
         tc_fence_before();
@@ -755,14 +741,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 
     if (ok) {
         float* dst = a.S_final != nullptr ? a.S_final : w.carry;
-        if (dst != nullptr) {
-            tc_fence_after();
-            float sv[32];
-            tmem_ld32(tb + lo + TC_S + 32 * cg, sv);
-            tmem_wait_ld();
+        if (dst != nullptr)
 #pragma unroll
             for (int j = 0; j < 32; ++j) dst[sbase + (int64_t)(32 * cg + j) * D + row] = sv[j];
-        }
     } else if (tid == 0) {
         atomicOr(&g_device_error, 1);
         if (mma_pending) mbar_wait(bar_mma, mma_phase, kWaitNs);
