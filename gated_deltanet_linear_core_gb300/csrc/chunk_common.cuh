@@ -22,12 +22,6 @@ __device__ __forceinline__ void store_row_bf16(uint8_t* blk, int row, int c0, co
     }
 }
 
-// Element (i, j) of a 64 x 64 f32 table whose float4 groups are XOR-swizzled
-// by row, so that a warp reading one float4 per row hits distinct banks.
-__device__ __forceinline__ int ftab(int i, int j) {
-    return i * 64 + ((((j >> 2) ^ (i & 15)) & 15) << 2) + (j & 3);
-}
-
 // Sum of squares of 32 elements (four 16-byte chunks) of a 128-element bf16
 // row stored as two 128-byte swizzled rows; part p (0..3) covers chunks
 // 4(p&1)..4(p&1)+3 of block p>>1, visited in a bank-conflict-free order.

@@ -43,44 +43,69 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr size_t kSegBytes = 128ull << 20;  // workspace intermediates per segment
 
 // per (chunk, value head) unit in the workspace
-constexpr size_t U_WT = 16384, U_UT = 16384, U_P = 8192, U_VEC = 1024;
-constexpr size_t UNIT_BYTES = U_WT + U_UT + U_P + U_VEC;
-
-struct Layout {
-    int64_t segc;    // chunks per segment
-    int64_t n_seg;
-    size_t off_wt, off_ut, off_p, off_vec, off_coff, off_carry, carry_bytes, total;
-};
-
-Layout layout_of(int n_seq, int64_t T, int H_v) {
-    Layout L;
-    const int64_t max_chunks = T / C + n_seq;
-    int64_t segc = (int64_t)(kSegBytes / ((size_t)H_v * UNIT_BYTES));
-    if (segc < 1) segc = 1;
-    if (segc > max_chunks) segc = max_chunks;
-    if (segc > 65535) segc = 65535;  // grid.y of the intra kernel
-    L.segc = segc;
-    L.n_seg = (max_chunks + segc - 1) / segc;
-    const size_t U = (size_t)segc * H_v;
-    L.off_wt = 0;
-    L.off_ut = L.off_wt + U * U_WT;
-    L.off_p = L.off_ut + U * U_UT;
-    L.off_vec = L.off_p + U * U_P;
-    L.off_coff = L.off_vec + U * U_VEC;
-    L.off_carry = (L.off_coff + 4 * ((size_t)n_seq + 1) + 255) & ~(size_t)255;
-    L.carry_bytes = L.n_seg > 1 ? (size_t)n_seq * H_v * D * D * 4 : 0;
-    L.total = L.off_carry + L.carry_bytes;
-    return L;
-}
+constexpr size_t U_WT = 16384, U_UT = 16384, U_P = 8192, U_VEC = 1024, U_GB = 512;
+constexpr size_t UNIT_BYTES = U_WT + U_UT + U_P + U_VEC + U_GB;
+constexpr size_t CMETA_BYTES = 16;  // per chunk of a segment
 
 struct Work {
     bf16* wt;       // W, [U][64][128] (row i of W = 128 d-values)
     bf16* ut;       // [U][128][64]
     bf16* p;        // [U][64][64]
     float* vec;     // [U][256]: e^G rq (0..63), e^{G_n-G_j} rk (64..127), e^{G_n} (128)
+    float* gb;      // [U][128]: G (log2 domain, 0..63), beta (64..127)
+    int4* cmeta;    // [segc]: first token (lo, hi), length (0: no such chunk)
     int32_t* coff;  // [n_seq + 1] chunk offsets
     float* carry;   // state between segments (final_state or workspace), may be null
 };
+
+// Segment size and the places of the intermediates inside one scratch area:
+// chunk offsets, chunk metadata, then the per-unit arrays, then the carry.
+struct Layout {
+    int64_t segc;    // chunks per segment
+    int64_t n_seg;
+    size_t off_coff, off_cmeta, off_units, off_carry, carry_bytes, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// seg_bytes bounds the per-segment intermediates; coff_slots is the number of
+// chunk-offset entries reserved (at least n_seq + 1).
+Layout layout_for(int n_seq, int64_t T, int H_v, size_t seg_bytes, size_t coff_slots, bool carry) {
+    Layout L;
+    const int64_t max_chunks = T / C + n_seq;
+    int64_t segc = (int64_t)(seg_bytes / ((size_t)H_v * UNIT_BYTES + CMETA_BYTES));
+    if (segc < 1) segc = 1;
+    if (segc > max_chunks) segc = max_chunks;
+    if (segc > 65535) segc = 65535;  // grid.y of the intra kernel
+    L.segc = segc;
+    L.n_seg = (max_chunks + segc - 1) / segc;
+    L.off_coff = 0;
+    L.off_cmeta = align256(4 * coff_slots);
+    L.off_units = align256(L.off_cmeta + CMETA_BYTES * (size_t)segc);
+    L.off_carry = L.off_units + (size_t)segc * H_v * UNIT_BYTES;
+    L.carry_bytes = carry && L.n_seg > 1 ? (size_t)n_seq * H_v * D * D * 4 : 0;
+    L.total = L.off_carry + L.carry_bytes;
+    return L;
+}
+
+Layout layout_of(int n_seq, int64_t T, int H_v) {
+    return layout_for(n_seq, T, H_v, kSegBytes, (size_t)n_seq + 1, true);
+}
+
+Work work_at(uint8_t* base, const Layout& L, int H_v) {
+    const size_t U = (size_t)L.segc * H_v;
+    uint8_t* un = base + L.off_units;
+    Work w;
+    w.coff = reinterpret_cast<int32_t*>(base + L.off_coff);
+    w.cmeta = reinterpret_cast<int4*>(base + L.off_cmeta);
+    w.wt = reinterpret_cast<bf16*>(un);
+    w.ut = reinterpret_cast<bf16*>(un + U * U_WT);
+    w.p = reinterpret_cast<bf16*>(un + U * (U_WT + U_UT));
+    w.vec = reinterpret_cast<float*>(un + U * (U_WT + U_UT + U_P));
+    w.gb = reinterpret_cast<float*>(un + U * (U_WT + U_UT + U_P + U_VEC));
+    w.carry = L.carry_bytes ? reinterpret_cast<float*>(base + L.off_carry) : nullptr;
+    return w;
+}
 
 // coff[i] = number of chunks of sequences 0..i-1 (one block, any n_seq)
 __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, int n_seq, int64_t T,
@@ -127,55 +152,157 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, 
     }
 }
 
+// ============================================================== gates kernel
+// Gates of every (chunk, value head) unit of a segment: beta = sigmoid(b) and
+// G = the chunk-local cumulative sum of g = -exp(A_log) softplus(a + dt_bias)
+// in the log2 domain, both zero past the chunk's last token; and each chunk's
+// first token and length.  One CTA per (chunk, 32 value heads): coalesced
+// reads of a token's heads, then one warp-wide scan per head.
+constexpr int NT_G = 256;
+
+__global__ void __launch_bounds__(NT_G) chunk_gates_kernel(DeltaArgs a, Work w, int64_t C0) {
+    __shared__ float sg[64][33], sb[64][33];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t gc = C0 + blockIdx.x;
+    const int h0 = blockIdx.y * 32;
+    constexpr float kLog2e = 1.4426950408889634f;
+    // first token and length of chunk gc (every thread; a single sequence
+    // without offsets needs no loads)
+    int64_t t0 = 0;
+    int n = 0;
+    if (a.cu == nullptr) {
+        t0 = gc * C;
+        if (t0 < a.T) n = (int)(a.T - t0 < C ? a.T - t0 : C);
+    } else if (gc < w.coff[a.n_seq]) {
+        int lo_s = 0, hi_s = a.n_seq - 1;  // sequence of chunk gc
+        while (lo_s < hi_s) {
+            const int mid = (lo_s + hi_s + 1) >> 1;
+            if ((int64_t)w.coff[mid] <= gc) lo_s = mid; else hi_s = mid - 1;
+        }
+        int64_t s0, s1;
+        seq_bounds(a.cu, lo_s, a.T, s0, s1);
+        t0 = s0 + (gc - w.coff[lo_s]) * C;
+        n = (int)(s1 - t0 < C ? s1 - t0 : C);
+    }
+    if (tid == 0 && blockIdx.y == 0)
+        w.cmeta[blockIdx.x] = make_int4((int)(uint32_t)(uint64_t)t0, (int)((uint64_t)t0 >> 32), n, 0);
+    if (n == 0) return;
+    {   // thread (token warp + 8k, head h0 + lane): all loads issued before any use
+        const int h = h0 + lane;
+        const bool hv = h < a.H_v;
+        float gv[8], bv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int t = warp + 8 * k;
+            const int64_t gi = (t < n && hv) ? (t0 + t) * a.H_v + h : 0;  // index 0 exists: T > 0
+            if (a.g != nullptr) {
+                gv[k] = a.g[gi];
+                bv[k] = a.beta[gi];
+            } else {
+                gv[k] = to_f(static_cast<const bf16*>(a.a)[gi]);
+                bv[k] = to_f(static_cast<const bf16*>(a.b)[gi]);
+            }
+        }
+        const float Al = hv && a.g == nullptr ? a.A_log[h] : 0.f;
+        const float dtb = hv && a.g == nullptr ? a.dt_bias[h] : 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int t = warp + 8 * k;
+            const bool live = t < n && hv;
+            float g = gv[k], bt = bv[k];
+            if (a.g == nullptr) {
+                g = gate_g(g, Al, dtb);
+                bt = sigmoid_f(bt);
+            }
+            sg[t][lane] = live ? g * kLog2e : 0.f;
+            sb[t][lane] = live ? bt : 0.f;
+        }
+    }
+    __syncthreads();
+    for (int hl = warp; hl < 32 && h0 + hl < a.H_v; hl += 8) {
+        float x0 = sg[lane][hl], x1 = sg[lane + 32][hl];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
+            const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
+            if (lane >= o) {
+                x0 += y0;
+                x1 += y1;
+            }
+        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        float* dst = w.gb + ((gc - C0) * a.H_v + h0 + hl) * 128;
+        dst[lane] = x0;
+        dst[lane + 32] = x1;
+        dst[64 + lane] = sb[lane][hl];
+        dst[96 + lane] = sb[lane + 32][hl];
+    }
+}
+
 // ============================================================== intra kernel
+// One CTA per (chunk, value head); 256 threads, three CTAs per SM (72 KB of
+// shared memory and 128 TMEM columns each), so that the latency-bound phases
+// of one CTA overlap the copies and MMAs of the others.
 constexpr int NT_I = 256;
-constexpr int IS_KQ = 0;                       // [cb0: K | Q][cb1: K | Q]; Q halves reused for B_W, B_U
-constexpr int IS_V = IS_KQ + 32768;
-constexpr int IS_A = IS_V + 16384;             // A, f32 [64][68]
+constexpr int IS_KQ = 0;                          // [cb0: K | Q][cb1: K | Q]; the Q halves then hold T'
+constexpr int IS_V = IS_KQ + 32768;               // V, then the W staging tile
+constexpr int IS_A = IS_V + 16384;                // A, f32 [64][68]; then B_W | B_U (bf16)
 constexpr int A_PITCH = 68;
-constexpr int IS_F = IS_A + 64 * A_PITCH * 4;  // factor tables, then T' and block temporaries
-constexpr int IS_VEC = IS_F + 32768;           // G, e^G, beta, dec, rk, rq, misc, fw
-constexpr int IS_BAR = IS_VEC + 8 * 64 * 4;
+constexpr int IS_X = IS_A + 64 * A_PITCH * 4;     // solve temporaries, f32 [32][36]
+constexpr int X_PITCH = 36;
+constexpr int IS_VEC = IS_X + 32 * X_PITCH * 4;   // G (log2), beta (one bulk copy), beta e^G rk, rk, rq,
+                                                  // G - log2 rk
+constexpr int IS_BAR = IS_VEC + 6 * 64 * 4;
 constexpr int IS_TOTAL = IS_BAR + 64;
 constexpr int ISMEM = IS_TOTAL + 1024;
-constexpr uint32_t TI_D1 = 0, TI_DW = 64, TI_DU = 128, TI_COLS = 256;
+constexpr uint32_t TI_D1 = 0, TI_DW = 0, TI_DU = 64, TI_COLS = 128;  // D1 (128 columns) is dead before W, U
 
-__global__ void __launch_bounds__(NT_I, 2)
+// Element (r, c) of T' = (I + A)^-1, f32, in the two Q halves of the [K | Q]
+// tile (rows 0-31 in the first, 32-63 in the second); float4 groups of a row
+// are XOR-swizzled by the row so that column-wise reads spread over banks.
+__device__ __forceinline__ float* tp_at(uint8_t* kq, int r, int c) {
+    return reinterpret_cast<float*>(kq + (r < 32 ? 8192 : 24576) + (r & 31) * 256) +
+           ((((c >> 2) ^ (r & 15)) & 15) << 2) + (c & 3);
+}
+
+// v[lane] without dynamic register indexing (a tree of selects on lane's bits).
+__device__ __forceinline__ float select_lane(const float (&v)[32], int lane) {
+    float a[16], b[8], c[4], d[2];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) a[k] = (lane & 16) ? v[k + 16] : v[k];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b[k] = (lane & 8) ? a[k + 8] : a[k];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c[k] = (lane & 4) ? b[k + 4] : b[k];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) d[k] = (lane & 2) ? c[k + 2] : c[k];
+    return (lane & 1) ? d[1] : d[0];
+}
+
+__global__ void __launch_bounds__(NT_I, 3)
 chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
                    DeltaArgs a, Work w, int64_t C0) {
     const int h = blockIdx.x;
-    const int64_t gc = C0 + blockIdx.y;
-    const int n_seq = a.n_seq;
-    if (gc >= w.coff[n_seq]) return;  // past the last chunk of the call
-    int lo_s = 0, hi_s = n_seq - 1;   // sequence of chunk gc
-    while (lo_s < hi_s) {
-        const int mid = (lo_s + hi_s + 1) >> 1;
-        if ((int64_t)w.coff[mid] <= gc) lo_s = mid; else hi_s = mid - 1;
-    }
-    const int seq = lo_s;
-    const int64_t lc = gc - w.coff[seq];
-    int64_t s0, s1;
-    seq_bounds(a.cu, seq, a.T, s0, s1);
-    const int64_t L = s1 - s0;
-    const int64_t t0 = s0 + lc * C;
-    const int n = (int)(L - lc * C < C ? L - lc * C : C);
+    const int4 cm = w.cmeta[blockIdx.y];
+    const int n = cm.z;
+    if (n == 0) return;  // past the last chunk of the call
+    const int64_t t0 = (int64_t)((uint64_t)(uint32_t)cm.x | ((uint64_t)(uint32_t)cm.y << 32));
     const int kh = h / (a.H_v / a.H_k);
     const int xq = kh * D, xk = a.H_k * D + kh * D, xv = 2 * a.H_k * D + h * D;
-    const int64_t u = (gc - C0) * a.H_v + h;
+    const int64_t u = (int64_t)blockIdx.y * a.H_v + h;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* kq = sm + IS_KQ;
     uint8_t* vv = sm + IS_V;
-    float* Gs = reinterpret_cast<float*>(sm + IS_VEC);
-    float* eGs = Gs + 64;
-    float* Bs = Gs + 128;
-    float* DECs = Gs + 192;
-    float* RKs = Gs + 256;
-    float* RQs = Gs + 320;
-    float* misc = Gs + 384;
-    float* FWs = Gs + 448;
     float* Am = reinterpret_cast<float*>(sm + IS_A);
+    float* Xs = reinterpret_cast<float*>(sm + IS_X);
+    float* Gs = reinterpret_cast<float*>(sm + IS_VEC);
+    float* Bs = Gs + 64;
+    float* FWs = Gs + 128;
+    float* RKs = Gs + 192;
+    float* RQs = Gs + 256;
+    float* Ms = Gs + 320;
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + IS_BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 2);
@@ -184,13 +311,13 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     const int quarter = warp & 3, half = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lo = (uint32_t)(quarter * 32) << 16;
-    constexpr float kLog2e = 1.4426950408889634f;
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar_tma, 6 * 8192);
+        mbar_arrive_expect_tx(bar_tma, 6 * 8192 + (uint32_t)U_GB);
+        bulk_load(Gs, w.gb + u * (int64_t)(U_GB / 4), (uint32_t)U_GB, bar_tma);  // G | beta
         const int y = (int)t0;
         tma_load_2d(kq, &qmap, bar_tma, xk, y);
         tma_load_2d(kq + 16384, &qmap, bar_tma, xk + 64, y);
@@ -203,28 +330,6 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         tmem_alloc(tslot, TI_COLS);
         tmem_relinquish();
     }
-    // gates (log2 domain) and in-warp cumulative sums
-    if (tid < 64) {
-        float g = 0.f, bt = 0.f;
-        if (tid < n) {
-            const int64_t gi = (t0 + tid) * a.H_v + h;
-            if (a.g != nullptr) {
-                g = a.g[gi];
-                bt = a.beta[gi];
-            } else {
-                g = gate_g(to_f(static_cast<const bf16*>(a.a)[gi]), a.A_log[h], a.dt_bias[h]);
-                bt = sigmoid_f(to_f(static_cast<const bf16*>(a.b)[gi]));
-            }
-        }
-        float x = g * kLog2e;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        Gs[tid] = x;
-        Bs[tid] = bt;
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -233,54 +338,8 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     bool mma_pending = false;
     uint32_t mma_phase = 0;
     if (ok) {
-        if (tid >= 32 && tid < 64) Gs[tid] += Gs[31];
-        {   // l2-norm factors: 128 rows (k then q) x 2 halves of 64 elements
-            const int r = tid >> 1, hh = tid & 1, rr = r & 63;
-            const bool isk = r < 64;
-            const uint8_t* b0 = isk ? kq : kq + 8192;
-            const uint8_t* b1 = isk ? kq + 16384 : kq + 24576;
-            float ss = row_sumsq_part(b0, b1, rr, 2 * hh) + row_sumsq_part(b0, b1, rr, 2 * hh + 1);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            if (hh == 0) {
-                float f = isk ? 1.f : a.scale;
-                if (a.l2norm) f = f / sqrtf(ss + 1e-6f);
-                (isk ? RKs : RQs)[rr] = f;
-            }
-        }
-        __syncthreads();
-        if (tid < 64) {
-            const float Gn = Gs[n - 1];
-            const float eg = exp2f(Gs[tid]);
-            eGs[tid] = eg;
-            FWs[tid] = Bs[tid] * eg * RKs[tid];
-            DECs[tid] = tid < n ? exp2f(Gn - Gs[tid]) : 0.f;
-            if (tid == 0) misc[0] = exp2f(Gn);
-        }
-        {   // decay-and-norm factor tables: thread t fills 16 entries of row t/4
-            float* FA = reinterpret_cast<float*>(sm + IS_F);
-            float* FP = FA + 64 * 64;
-            const int i = tid >> 2, j0 = (tid & 3) * 16;
-            const float Gi = Gs[i], fa = Bs[i] * RKs[i], fq = RQs[i];
-            const bool live = i < n;
-#pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4) {
-                const int j = j0 + 4 * g4;
-                const float4 G4 = *reinterpret_cast<const float4*>(Gs + j);
-                const float4 R4 = *reinterpret_cast<const float4*>(RKs + j);
-                const float gj[4] = {G4.x, G4.y, G4.z, G4.w}, rj[4] = {R4.x, R4.y, R4.z, R4.w};
-                float va[4], vp[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float e = (live && j + q <= i) ? exp2f(fminf(Gi - gj[q], 0.f)) : 0.f;
-                    vp[q] = fq * rj[q] * e;
-                    va[q] = (j + q < i) ? fa * rj[q] * e : 0.f;
-                }
-                *reinterpret_cast<float4*>(FA + ftab(i, j)) = make_float4(va[0], va[1], va[2], va[3]);
-                *reinterpret_cast<float4*>(FP + ftab(i, j)) = make_float4(vp[0], vp[1], vp[2], vp[3]);
-            }
-        }
-        __syncthreads();
-        // D1 = [K; Q] K^T
+        // D1 = [K; Q] [K; Q]^T: the k.k and q.k products of A and P, and on its
+        // diagonal the squared norms of the k and q rows
         if (tid == 0) {
             tc_fence_after();
             const uint32_t akq = smem_u32(kq);
@@ -288,7 +347,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             for (int k = 0; k < 8; ++k) {
                 const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
                 mma_bf16(tb + TI_D1, sdesc_sw128(akq + off, 16, 1024),
-                         sdesc_sw128(akq + off, 16, 1024), idesc_bf16_f32(128, 64, 0, 0), k > 0);
+                         sdesc_sw128(akq + off, 16, 1024), idesc_bf16_f32(128, 128, 0, 0), k > 0);
             }
             mma_commit(bar_mma);
         }
@@ -299,129 +358,184 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         mma_phase ^= 1;
         mma_pending = false;
         tc_fence_after();
-        {   // A (rows 0-63 -> shared, f32) and P (rows 64-127 -> workspace, bf16)
-            float d1[32];
-            tmem_ld32(tb + lo + TI_D1 + 32 * half, d1);
-            tmem_wait_ld();
-            const int i = row & 63;
-            const float* F = reinterpret_cast<const float*>(sm + IS_F) + (row < 64 ? 0 : 64 * 64);
-#pragma unroll
-            for (int g4 = 0; g4 < 8; ++g4) {
-                const float4 f = *reinterpret_cast<const float4*>(F + ftab(i, 32 * half + 4 * g4));
-                d1[4 * g4 + 0] *= f.x;
-                d1[4 * g4 + 1] *= f.y;
-                d1[4 * g4 + 2] *= f.z;
-                d1[4 * g4 + 3] *= f.w;
+        const bool isk = row < 64;
+        const int i = row & 63, j0 = 32 * half;
+        float d1[32];
+        tmem_ld32(tb + lo + TI_D1 + 32 * half, d1);
+        // the warp whose 32 columns hold its rows' diagonal: l2-norm factors,
+        // the row factors of W and the workspace vectors
+        if (isk ? quarter == half : quarter - 2 == half) {
+            float ss;
+            if (isk) {
+                tmem_wait_ld();
+                ss = select_lane(d1, lane);
+            } else {
+                float dq[32];
+                tmem_ld32(tb + lo + TI_D1 + 64 + 32 * half, dq);
+                tmem_wait_ld();
+                ss = select_lane(dq, lane);
             }
-            if (row < 64) {
+            float f = isk ? 1.f : a.scale;
+            if (a.l2norm) f = f / sqrtf(ss + 1e-6f);
+            const float Gn = Gs[n - 1];
+            const float eg = exp2f(Gs[i]);
+            float* vec = w.vec + u * (U_VEC / 4);
+            if (isk) {
+                RKs[i] = f;
+                FWs[i] = Bs[i] * eg * f;
+                Ms[i] = Gs[i] - lg2_approx(f);
+                vec[64 + i] = i < n ? exp2f(Gn - Gs[i]) * f : 0.f;
+                if (i == 0) vec[128] = exp2f(Gn);
+            } else {
+                RQs[i] = f;
+                vec[i] = eg * f;
+            }
+        } else {
+            tmem_wait_ld();
+        }
+        __syncthreads();
+        {   // A (k rows -> shared, f32) and P (q rows -> workspace, bf16):
+            //   A_ij = beta_i rk_i rk_j e^{G_i-G_j} k_i.k_j (j<i), P_ij = rq_i rk_j e^{G_i-G_j} q_i.k_j (j<=i)
+            // with the row and column factors folded into the exponent:
+            //   f_i rk_j 2^{G_i-G_j} = 2^{(G_i + log2 f_i) - (G_j - log2 rk_j)}
+            if (j0 <= (i | 31)) {  // else every (i, j) of this warp has j > i
+                float fi = i < n ? (isk ? Bs[i] * RKs[i] : RQs[i]) : 0.f;
+                if (fi < 0.f) {  // a negative q scale (or beta): its sign stays outside the exponent
+                    fi = -fi;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) d1[q] = -d1[q];
+                }
+                const float Li = Gs[i] + lg2_approx(fi);  // -inf when f_i = 0
+                const int jmax = isk ? i - 1 : i;
+#pragma unroll
+                for (int g4 = 0; g4 < 8; ++g4) {
+                    const float4 M4 = *reinterpret_cast<const float4*>(Ms + j0 + 4 * g4);
+                    const float mj[4] = {M4.x, M4.y, M4.z, M4.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        d1[4 * g4 + q] = j0 + 4 * g4 + q <= jmax ? d1[4 * g4 + q] * ex2_approx(Li - mj[q]) : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) d1[q] = 0.f;
+            }
+            if (isk) {
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4)
-                    *reinterpret_cast<float4*>(&Am[i * A_PITCH + 32 * half + 4 * g4]) =
+                    *reinterpret_cast<float4*>(&Am[i * A_PITCH + j0 + 4 * g4]) =
                         make_float4(d1[4 * g4], d1[4 * g4 + 1], d1[4 * g4 + 2], d1[4 * g4 + 3]);
             } else {
-                bf16* pp = w.p + u * (U_P / 2) + i * 64 + 32 * half;
+                bf16* pp = w.p + u * (U_P / 2) + i * 64 + j0;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) store16(pp + 8 * g, d1 + 8 * g);
             }
         }
         __syncthreads();
-        {   // T' = (I + A)^-1 blocked by 16 (see the fused kernel's derivation)
-            float* Tm = reinterpret_cast<float*>(sm + IS_F);
-            float* Mt = Tm + 64 * A_PITCH;
-            if (tid < 64) {
-                const int r0 = (tid >> 4) * 16, cl = tid & 15;
-                float x[16];
+        // T' = (I + A)^-1 (unit lower triangular): the four diagonal 16-blocks
+        // by forward substitution (f32), then the off-diagonal blocks by
+        // doubling on warp-level tf32 MMAs (T' is rounded to bf16 right after),
+        //   T'_{10} = -D_1 A_{10} D_0 (and T'_{32}),  T'_{[23][01]} = -T'_{[23][23]} A_{[23][01]} T'_{[01][01]}
+        if (tid < 64) {
+            const int r0 = (tid >> 4) * 16, cl = tid & 15;
+            float x[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const float* Ar = &Am[(r0 + r) * A_PITCH + r0];
-                    float acc = (r == cl) ? 1.f : 0.f;
+            for (int r = 0; r < 16; ++r) x[r] = r == cl ? 1.f : 0.f;
 #pragma unroll
-                    for (int q = 0; q < r; ++q) acc = fmaf(-Ar[q], x[q], acc);
-                    x[r] = acc;
-                }
+            for (int q = 0; q < 15; ++q)
 #pragma unroll
-                for (int r = 0; r < 16; ++r) Tm[(r0 + r) * A_PITCH + r0 + cl] = x[r];
-            } else {
-                for (int e = tid - 64; e < 6 * 256; e += NT_I - 64) {
-                    const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-                    const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                    const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                    Tm[(br * 16 + r) * A_PITCH + bc * 16 + cc] = 0.f;
-                }
+                for (int r = q + 1; r < 16; ++r) x[r] = fmaf(-Am[(r0 + r) * A_PITCH + r0 + q], x[q], x[r]);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) *tp_at(kq, r0 + r, r0 + cl) = x[r];
+        }
+        __syncthreads();
+        const int fg = lane >> 2, ft = lane & 3;  // MMA fragment row group, thread in group
+        if (warp < 4) {  // level 1, X = A_{b+1,b} D_b for b = 0, 2; warp = (block pair, 8 columns)
+            const int blk = warp >> 1, c0 = 32 * blk + 8 * (warp & 1), r0 = 32 * blk + 16;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int k0 = 32 * blk + 8 * ks;
+                const float af[4] = {Am[(r0 + fg) * A_PITCH + k0 + ft], Am[(r0 + fg + 8) * A_PITCH + k0 + ft],
+                                     Am[(r0 + fg) * A_PITCH + k0 + ft + 4], Am[(r0 + fg + 8) * A_PITCH + k0 + ft + 4]};
+                const float bfr[2] = {*tp_at(kq, k0 + ft, c0 + fg), *tp_at(kq, k0 + ft + 4, c0 + fg)};
+                mma_tf32_16x8x8(c, af, bfr);
             }
-            __syncthreads();
-            for (int dd = 1; dd < 4; ++dd) {
-                const int nstrip = (4 - dd) * 64;
-                if (tid < nstrip) {
-                    const int bl = tid >> 6, r = (tid >> 2) & 15, q4 = (tid & 3) * 4;
-                    const float* Ar = &Am[((bl + dd) * 16 + r) * A_PITCH];
-                    const float* Tc = &Tm[bl * 16 + q4];
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int k = bl * 16; k < (bl + dd) * 16; k += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(Ar + k);
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+            float* xr = Xs + (16 * blk + fg) * X_PITCH + 8 * (warp & 1) + 2 * ft;
+            *reinterpret_cast<float2*>(xr) = make_float2(c[0], c[1]);
+            *reinterpret_cast<float2*>(xr + 8 * X_PITCH) = make_float2(c[2], c[3]);
+        }
+        __syncthreads();
+        if (warp < 4) {  // T'_{b+1,b} = -D_{b+1} X
+            const int blk = warp >> 1, n0 = 8 * (warp & 1), r0 = 32 * blk + 16;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float4 t4 = *reinterpret_cast<const float4*>(Tc + (k + q) * A_PITCH);
-                            acc.x = fmaf(av[q], t4.x, acc.x);
-                            acc.y = fmaf(av[q], t4.y, acc.y);
-                            acc.z = fmaf(av[q], t4.z, acc.z);
-                            acc.w = fmaf(av[q], t4.w, acc.w);
-                        }
-                    }
-                    *reinterpret_cast<float4*>(&Mt[(bl << 8) + r * 16 + q4]) = acc;
-                }
-                __syncthreads();
-                if (tid < nstrip) {
-                    const int bl = tid >> 6, r = (tid >> 2) & 15, q4 = (tid & 3) * 4;
-                    const int a0 = (bl + dd) * 16;
-                    const float* Ta = &Tm[(a0 + r) * A_PITCH + a0];
-                    const float* Mb = &Mt[(bl << 8) + q4];
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int k = 0; k < 16; k += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(Ta + k);
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float4 m4 = *reinterpret_cast<const float4*>(Mb + (k + q) * 16);
-                            acc.x = fmaf(av[q], m4.x, acc.x);
-                            acc.y = fmaf(av[q], m4.y, acc.y);
-                            acc.z = fmaf(av[q], m4.z, acc.z);
-                            acc.w = fmaf(av[q], m4.w, acc.w);
-                        }
-                    }
-                    *reinterpret_cast<float4*>(&Tm[(a0 + r) * A_PITCH + bl * 16 + q4]) =
-                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-                }
-                __syncthreads();
+            for (int ks = 0; ks < 2; ++ks) {
+                const int k0 = 8 * ks;
+                const float af[4] = {*tp_at(kq, r0 + fg, r0 + k0 + ft), *tp_at(kq, r0 + fg + 8, r0 + k0 + ft),
+                                     *tp_at(kq, r0 + fg, r0 + k0 + ft + 4), *tp_at(kq, r0 + fg + 8, r0 + k0 + ft + 4)};
+                const float bfr[2] = {Xs[(16 * blk + k0 + ft) * X_PITCH + n0 + fg],
+                                      Xs[(16 * blk + k0 + ft + 4) * X_PITCH + n0 + fg]};
+                mma_tf32_16x8x8(c, af, bfr);
             }
-            // B_W = T' diag(beta e^G rk), B_U = T' diag(beta) into the (consumed) Q halves
-            {
-                const int which = tid >> 7, i = (tid >> 1) & 63, c0 = (tid & 1) * 32;
-                const float* Ti = &Tm[i * A_PITCH + c0];
-                const float* Fc = (which == 0 ? FWs : Bs) + c0;
-                float vals[32];
-#pragma unroll
-                for (int g4 = 0; g4 < 8; ++g4) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(Ti + 4 * g4);
-                    const float4 f4 = *reinterpret_cast<const float4*>(Fc + 4 * g4);
-                    vals[4 * g4 + 0] = t4.x * f4.x;
-                    vals[4 * g4 + 1] = t4.y * f4.y;
-                    vals[4 * g4 + 2] = t4.z * f4.z;
-                    vals[4 * g4 + 3] = t4.w * f4.w;
-                }
-                store_row_bf16(kq + (which == 0 ? 8192 : 24576), i, c0, vals, 32);
+            const int cc = 32 * blk + n0 + 2 * ft;
+            *reinterpret_cast<float2*>(tp_at(kq, r0 + fg, cc)) = make_float2(-c[0], -c[1]);
+            *reinterpret_cast<float2*>(tp_at(kq, r0 + fg + 8, cc)) = make_float2(-c[2], -c[3]);
+        }
+        __syncthreads();
+        {   // level 2, X = A_{[23][01]} T'_{[01][01]} (32 x 32); warp = (16 rows, 8 columns)
+            const int mt = warp >> 2, nt = warp & 3, r0 = 32 + 16 * mt;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int ks = nt; ks < 4; ++ks) {  // T'(k, c) = 0 for k < c
+                const int k0 = 8 * ks;
+                const float af[4] = {Am[(r0 + fg) * A_PITCH + k0 + ft], Am[(r0 + fg + 8) * A_PITCH + k0 + ft],
+                                     Am[(r0 + fg) * A_PITCH + k0 + ft + 4], Am[(r0 + fg + 8) * A_PITCH + k0 + ft + 4]};
+                const float bfr[2] = {*tp_at(kq, k0 + ft, 8 * nt + fg), *tp_at(kq, k0 + ft + 4, 8 * nt + fg)};
+                mma_tf32_16x8x8(c, af, bfr);
             }
+            float* xr = Xs + (16 * mt + fg) * X_PITCH + 8 * nt + 2 * ft;
+            *reinterpret_cast<float2*>(xr) = make_float2(c[0], c[1]);
+            *reinterpret_cast<float2*>(xr + 8 * X_PITCH) = make_float2(c[2], c[3]);
+        }
+        __syncthreads();
+        {   // T'_{[23][01]} = -T'_{[23][23]} X
+            const int mt = warp >> 2, nt = warp & 3, r0 = 32 + 16 * mt;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int ks = 0; ks < 2 * mt + 2; ++ks) {  // T'(r, 32 + k) = 0 for k > r - 32
+                const int k0 = 8 * ks;
+                const float af[4] = {*tp_at(kq, r0 + fg, 32 + k0 + ft), *tp_at(kq, r0 + fg + 8, 32 + k0 + ft),
+                                     *tp_at(kq, r0 + fg, 32 + k0 + ft + 4),
+                                     *tp_at(kq, r0 + fg + 8, 32 + k0 + ft + 4)};
+                const float bfr[2] = {Xs[(k0 + ft) * X_PITCH + 8 * nt + fg], Xs[(k0 + ft + 4) * X_PITCH + 8 * nt + fg]};
+                mma_tf32_16x8x8(c, af, bfr);
+            }
+            *reinterpret_cast<float2*>(tp_at(kq, r0 + fg, 8 * nt + 2 * ft)) = make_float2(-c[0], -c[1]);
+            *reinterpret_cast<float2*>(tp_at(kq, r0 + fg + 8, 8 * nt + 2 * ft)) = make_float2(-c[2], -c[3]);
+        }
+        __syncthreads();
+        {   // B_W = T' diag(beta e^G rk), B_U = T' diag(beta) (bf16) into the A region
+            const int which = tid >> 7, i = (tid >> 1) & 63, c0 = (tid & 1) * 32;
+            const float* Fc = (which == 0 ? FWs : Bs) + c0;
+            float vals[32];
+#pragma unroll
+            for (int g4 = 0; g4 < 8; ++g4) {
+                const int c = c0 + 4 * g4;
+                const float4 t4 = *reinterpret_cast<const float4*>(tp_at(kq, i, c));
+                const float4 f4 = *reinterpret_cast<const float4*>(Fc + 4 * g4);
+                vals[4 * g4 + 0] = c + 0 <= i ? t4.x * f4.x : 0.f;
+                vals[4 * g4 + 1] = c + 1 <= i ? t4.y * f4.y : 0.f;
+                vals[4 * g4 + 2] = c + 2 <= i ? t4.z * f4.z : 0.f;
+                vals[4 * g4 + 3] = c + 3 <= i ? t4.w * f4.w : 0.f;
+            }
+            store_row_bf16(sm + IS_A + which * 8192, i, c0, vals, 32);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // W^T = K^T B_W^T,  U^T = V^T B_U^T
+        // W^T = K^T B_W^T,  U^T = V^T B_U^T  (M = d, N = i, K = j)
         if (tid == 0) {
             tc_fence_after();
             const uint32_t akq = smem_u32(kq), av = smem_u32(vv);
-            const uint32_t bw = smem_u32(kq + 8192), bu = smem_u32(kq + 24576);
+            const uint32_t bw = smem_u32(sm + IS_A), bu = bw + 8192;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 mma_bf16(tb + TI_DW, sdesc_sw128(akq + k * 2048, 16384, 1024),
@@ -437,29 +551,22 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     if (ok) {
         mma_pending = false;
         tc_fence_after();
-        {   // W (row-major, staged 128B-swizzled in the consumed V tile, stored by TMA)
-            // and U^T rows (bf16, 32 columns per thread)
-            float v32[32];
-            tmem_ld32(tb + lo + TI_DW + 32 * half, v32);
-            tmem_wait_ld();
-            uint8_t* stg = vv + (row >> 6) * 8192;
-            const int dc = row & 63;
+        // W (row-major, staged 128B-swizzled in the consumed V tile, stored by
+        // TMA) and U^T rows (bf16, 32 columns per thread)
+        float v32[32];
+        tmem_ld32(tb + lo + TI_DW + 32 * half, v32);
+        tmem_wait_ld();
+        uint8_t* stg = vv + (row >> 6) * 8192;
+        const int dc = row & 63;
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-                *reinterpret_cast<bf16*>(stg + sw128_off(32 * half + q, dc)) = __float2bfloat16_rn(v32[q]);
-            tmem_ld32(tb + lo + TI_DU + 32 * half, v32);
-            tmem_wait_ld();
-            bf16* dst = w.ut + u * (U_UT / 2) + row * 64 + 32 * half;
+        for (int q = 0; q < 32; ++q)
+            *reinterpret_cast<bf16*>(stg + sw128_off(32 * half + q, dc)) = __float2bfloat16_rn(v32[q]);
+        tmem_ld32(tb + lo + TI_DU + 32 * half, v32);
+        tmem_wait_ld();
+        bf16* dst = w.ut + u * (U_UT / 2) + row * 64 + 32 * half;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) store16(dst + 8 * g, v32 + 8 * g);
-            fence_async_smem();
-        }
-        if (tid < 64) {
-            float* vec = w.vec + u * (U_VEC / 4);
-            vec[tid] = eGs[tid] * RQs[tid];
-            vec[64 + tid] = DECs[tid] * RKs[tid];
-            if (tid == 0) vec[128] = misc[0];
-        }
+        for (int g = 0; g < 4; ++g) store16(dst + 8 * g, v32 + 8 * g);
+        fence_async_smem();
     } else if (tid == 0) {
         atomicOr(&g_device_error, 1);
         if (mma_pending) mbar_wait(bar_mma, mma_phase, kWaitNs);
@@ -471,7 +578,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         tma_store_2d(&wmap, vv, 0, (int)(u * 64));
         tma_store_2d(&wmap, vv + 8192, 64, (int)(u * 64));
         bulk_commit();
-        bulk_wait_all();
+        bulk_wait_read_all();  // the staging tile must outlive the copy's reads
     }
     if (warp == 0) tmem_dealloc(tb, TI_COLS);
 }
@@ -787,25 +894,8 @@ bool encode2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-size_t chunk_split_workspace_bytes(int n_seq, int64_t T, int H_v) {
-    return layout_of(n_seq, T, H_v).total;
-}
-
-cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s) {
-    const Layout Ly = layout_of(a.n_seq, a.T, a.H_v);
-    if (workspace == nullptr || ws_bytes < Ly.total) return cudaErrorInvalidValue;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    Work w;
-    w.wt = reinterpret_cast<bf16*>(ws + Ly.off_wt);
-    w.ut = reinterpret_cast<bf16*>(ws + Ly.off_ut);
-    w.p = reinterpret_cast<bf16*>(ws + Ly.off_p);
-    w.vec = reinterpret_cast<float*>(ws + Ly.off_vec);
-    w.coff = reinterpret_cast<int32_t*>(ws + Ly.off_coff);
-    w.carry = Ly.carry_bytes ? reinterpret_cast<float*>(ws + Ly.off_carry) : nullptr;
-    if (a.S_final != nullptr) w.carry = a.S_final;
-
+// Chunk offsets, then per segment: gates, intra, chain.
+cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cudaStream_t s) {
     const uint64_t conv_dim = 2ull * a.H_k * D + (uint64_t)a.H_v * D;
     const uint64_t U = (uint64_t)Ly.segc * a.H_v;
     CUtensorMap qmap, omap, wtmap, utmap, pmap;
@@ -822,11 +912,26 @@ cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_by
     chunk_offsets_kernel<<<1, 1024, 0, s>>>(a.cu, a.n_seq, a.T, w.coff);
     for (int64_t seg = 0; seg < Ly.n_seg; ++seg) {
         const int64_t C0 = seg * Ly.segc;
+        chunk_gates_kernel<<<dim3((unsigned)Ly.segc, (unsigned)((a.H_v + 31) / 32)), NT_G, 0, s>>>(a, w, C0);
         chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, s>>>(qmap, wtmap, a, w, C0);
         chunk_chain_kernel<<<(unsigned)(a.n_seq * a.H_v), NT_C, CSMEM, s>>>(qmap, omap, wtmap, utmap,
                                                                           pmap, a, w, C0, Ly.segc);
     }
     return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t chunk_split_workspace_bytes(int n_seq, int64_t T, int H_v) {
+    return layout_of(n_seq, T, H_v).total;
+}
+
+cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s) {
+    const Layout Ly = layout_of(a.n_seq, a.T, a.H_v);
+    if (workspace == nullptr || ws_bytes < Ly.total) return cudaErrorInvalidValue;
+    Work w = work_at(static_cast<uint8_t*>(workspace), Ly, a.H_v);
+    if (a.S_final != nullptr) w.carry = a.S_final;
+    return run_segments(a, w, Ly, s);
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t s, int* flags) {
@@ -862,12 +967,18 @@ static __device__ __align__(256) uint8_t g_prefill_scratch[kStaticScratchBytes];
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[128];  // device address of g_prefill_scratch, per device ordinal
 
+Layout static_layout(int n_seq, int64_t T, int H_v) {
+    return layout_for(n_seq, T, H_v, kStaticScratchBytes - align256(4 * ((size_t)kStaticMaxSeq + 1)) - 256,
+                      (size_t)kStaticMaxSeq + 1, false);
+}
+
 }  // namespace
 
 bool chunk_split_static_fits(int n_seq, int H_v) {
-    const size_t coff_bytes = ((size_t)4 * (kStaticMaxSeq + 1) + 255) & ~(size_t)255;
-    return n_seq >= 1 && n_seq <= kStaticMaxSeq &&
-           (size_t)H_v * UNIT_BYTES <= kStaticScratchBytes - coff_bytes;
+    if (n_seq < 1 || n_seq > kStaticMaxSeq) return false;
+    // one chunk per segment must fit
+    const Layout L = layout_for(n_seq, 0, H_v, 0, (size_t)kStaticMaxSeq + 1, false);
+    return L.off_units + (size_t)H_v * UNIT_BYTES <= kStaticScratchBytes;
 }
 
 cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s) {
@@ -889,42 +1000,14 @@ cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s) {
         }
         base = static_cast<uint8_t*>(g_scratch_ptr[dev]);
     }
-    // layout inside the fixed array: chunk offsets, then as many chunks per
-    // segment as fit; final_state carries the state between segments
-    const size_t coff_bytes = ((size_t)4 * (kStaticMaxSeq + 1) + 255) & ~(size_t)255;
-    const int64_t max_chunks = a.T / C + a.n_seq;
-    int64_t segc = (int64_t)((kStaticScratchBytes - coff_bytes) / ((size_t)a.H_v * UNIT_BYTES));
-    if (segc > max_chunks) segc = max_chunks;
-    if (segc > 65535) segc = 65535;
-    const int64_t n_seg = (max_chunks + segc - 1) / segc;
-    const size_t U = (size_t)segc * a.H_v;
-    Work w;
-    w.coff = reinterpret_cast<int32_t*>(base);
-    w.wt = reinterpret_cast<bf16*>(base + coff_bytes);
-    w.ut = reinterpret_cast<bf16*>(base + coff_bytes + U * U_WT);
-    w.p = reinterpret_cast<bf16*>(base + coff_bytes + U * (U_WT + U_UT));
-    w.vec = reinterpret_cast<float*>(base + coff_bytes + U * (U_WT + U_UT + U_P));
+    // layout inside the fixed array: chunk offsets, chunk metadata, then as
+    // many chunks per segment as fit; final_state carries the state between
+    // segments
+    const Layout Ly = static_layout(a.n_seq, a.T, a.H_v);
+    if (Ly.total > kStaticScratchBytes) return cudaErrorInvalidValue;
+    Work w = work_at(base, Ly, a.H_v);
     w.carry = a.S_final;
-
-    const uint64_t conv_dim = 2ull * a.H_k * D + (uint64_t)a.H_v * D;
-    CUtensorMap qmap, omap, wtmap, utmap, pmap;
-    if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) ||
-        !encode2d(&omap, a.o, (uint64_t)a.H_v * D, (uint64_t)a.T, 64, 64) ||
-        !encode2d(&wtmap, w.wt, 128, U * 64, 64, 64) || !encode2d(&utmap, w.ut, 64, U * 128, 64, 128) ||
-        !encode2d(&pmap, w.p, 64, U * 64, 64, 64))
-        return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CSMEM);
-    if (e != cudaSuccess) return e;
-    chunk_offsets_kernel<<<1, 1024, 0, s>>>(a.cu, a.n_seq, a.T, w.coff);
-    for (int64_t seg = 0; seg < n_seg; ++seg) {
-        const int64_t C0 = seg * segc;
-        chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)segc), NT_I, ISMEM, s>>>(qmap, wtmap, a, w, C0);
-        chunk_chain_kernel<<<(unsigned)(a.n_seq * a.H_v), NT_C, CSMEM, s>>>(qmap, omap, wtmap, utmap,
-                                                                          pmap, a, w, C0, segc);
-    }
-    return cudaGetLastError();
+    return run_segments(a, w, Ly, s);
 }
 
 }  // namespace gdn

@@ -9,17 +9,19 @@
 //
 // The conv is HBM-bound (about 4 bytes of traffic per bf16 channel-token and
 // 4 FMAs).  Each thread owns one 16-byte channel vector (8 bf16 or 4 f32
-// channels) and walks a run of TOK tokens, keeping the three previous inputs
-// in registers, so x is read ~once (3/TOK re-read at run edges) and y written
-// once, both with coalesced 128-bit accesses (a warp covers 512 contiguous
-// bytes of a token row).
+// channels) of a run of kTok tokens.  A run inside one sequence issues all of
+// its kTok + 3 row loads at once (the 3 halo rows are the previous run's last
+// rows, mostly L2 hits) and then writes kTok outputs, so every thread has one
+// memory round trip; coalesced 128-bit accesses (a warp covers 512 contiguous
+// bytes of a token row).  Runs that touch a sequence start take the general
+// path, which walks the tokens with the three previous inputs in registers.
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
 
 namespace gdn {
 namespace {
 
-constexpr int kTok = 32;      // tokens per thread
+constexpr int kTok = 8;       // tokens per thread
 constexpr int kThreads = 128;
 
 template <typename T>
@@ -42,7 +44,7 @@ __device__ __forceinline__ void conv_out(const float (&w)[Vec16<T>::N][4], const
         acc = fmaf(w[e][1], w1[e], acc);
         acc = fmaf(w[e][2], w2[e], acc);
         acc = fmaf(w[e][3], cur[e], acc);
-        out[e] = silu ? silu_f(acc) : acc;
+        out[e] = silu ? silu_fast(acc) : acc;
     }
     store16(dst, out);
 }
@@ -76,6 +78,30 @@ __global__ void __launch_bounds__(kThreads) conv1d_fwd_kernel(ConvArgs a) {
     int seq = seq_of_token(a.cu, a.n_seq, t0);
     int64_t s, e;
     seq_bounds(a.cu, seq, a.T, s, e);
+
+    if (t0 - 3 >= s && t0 + kTok <= e) {
+        // the run and its halo lie inside one sequence: one round trip
+        uint4 raw[kTok + 3];
+#pragma unroll
+        for (int j = 0; j < kTok + 3; ++j)
+            raw[j] = __ldg(reinterpret_cast<const uint4*>(x + (t0 - 3 + j) * C + c0));
+        float r0[V], r1[V], r2[V], r3[V];
+        unpack16<T>(raw[0], r0);
+        unpack16<T>(raw[1], r1);
+        unpack16<T>(raw[2], r2);
+#pragma unroll
+        for (int j = 0; j < kTok; ++j) {
+            unpack16<T>(raw[j + 3], r3);
+            conv_out<T>(w, r0, r1, r2, r3, a.silu, y + (t0 + j) * C + c0);
+#pragma unroll
+            for (int q = 0; q < V; ++q) {
+                r0[q] = r1[q];
+                r1[q] = r2[q];
+                r2[q] = r3[q];
+            }
+        }
+        return;
+    }
 
     float win[3][V];  // inputs at t-3, t-2, t-1
     bool need_init = true;

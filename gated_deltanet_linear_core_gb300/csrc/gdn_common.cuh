@@ -21,9 +21,9 @@ template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __flo
 // VecN<T>::N elements of T fill one 16-byte (128-bit) access.
 template <typename T> struct Vec16 { static constexpr int N = 16 / sizeof(T); };
 
+// The Vec16<T>::N values of one 16-byte vector as f32 (bf16 -> f32 is exact).
 template <typename T>
-__device__ __forceinline__ void load16(const T* __restrict__ p, float* out) {
-    uint4 u = *reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ void unpack16(uint4 u, float* out) {
     if constexpr (sizeof(T) == 4) {
         out[0] = __uint_as_float(u.x); out[1] = __uint_as_float(u.y);
         out[2] = __uint_as_float(u.z); out[3] = __uint_as_float(u.w);
@@ -37,21 +37,15 @@ __device__ __forceinline__ void load16(const T* __restrict__ p, float* out) {
     }
 }
 
+template <typename T>
+__device__ __forceinline__ void load16(const T* __restrict__ p, float* out) {
+    unpack16<T>(*reinterpret_cast<const uint4*>(p), out);
+}
+
 // Streaming variant: no L1 allocation (data read once).
 template <typename T>
 __device__ __forceinline__ void load16_stream(const T* __restrict__ p, float* out) {
-    uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
-    if constexpr (sizeof(T) == 4) {
-        out[0] = __uint_as_float(u.x); out[1] = __uint_as_float(u.y);
-        out[2] = __uint_as_float(u.z); out[3] = __uint_as_float(u.w);
-    } else {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            out[2 * i] = __uint_as_float(w[i] << 16);
-            out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
-    }
+    unpack16<T>(__ldcs(reinterpret_cast<const uint4*>(p)), out);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -75,6 +69,11 @@ __device__ __forceinline__ void store16(T* __restrict__ p, const float* in) {
 // ---------------------------------------------------------------- math
 // Full-precision CUDA math functions only (no hand-written approximations).
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+// SiLU with the hardware exponential and an approximate divide (a few ulp of
+// f32; the exponent is clamped so the divisor stays finite and below 2^126).
+__device__ __forceinline__ float silu_fast(float x) {
+    return __fdividef(x, 1.0f + __expf(fminf(-x, 80.0f)));
+}
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 // softplus with the identity branch above 20 (cortex unit test "softplus small/large branches")
 __device__ __forceinline__ float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }

@@ -42,10 +42,10 @@ __global__ void __launch_bounds__(256) rmsnorm_gated_kernel(const T* o,  // may 
     for (int i = 0; i < V; ++i) ss = fmaf(ov[i], ov[i], ss);
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float rs = 1.0f / sqrtf(ss / (float)D + eps);
+    const float rs = rsqrtf(ss / (float)D + eps);
     float res[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) res[i] = wv[i] * (ov[i] * rs) * silu_f(zv[i]);
+    for (int i = 0; i < V; ++i) res[i] = wv[i] * (ov[i] * rs) * silu_fast(zv[i]);
     if (valid) store16(out + row * D + c0, res);
 }
 

@@ -217,6 +217,34 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
         : "memory");
 }
 
+// Warp-level D (16x8, f32) += A (16x8) * B (8x8) with tf32 operands (the
+// f32 bit patterns are passed as they are; the tensor core reads their tf32
+// part).  Fragments, g = lane / 4, t = lane % 4:
+//   A: a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4)
+//   B: b0 (t, g), b1 (t + 4, g)
+//   D: d0 (g, 2t), d1 (g, 2t + 1), d2 (g + 8, 2t), d3 (g + 8, 2t + 1)
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(__float_as_uint(a[0])), "r"(__float_as_uint(a[1])), "r"(__float_as_uint(a[2])),
+          "r"(__float_as_uint(a[3])), "r"(__float_as_uint(b[0])), "r"(__float_as_uint(b[1])));
+}
+
+// 2^x and log2(x) on the special-function unit (approximate, subnormal
+// results flushed to zero; ex2(-inf) = 0, lg2(0) = -inf).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Byte offset of bf16 element (r, c), c < 64, in a block of 128-byte rows
 // under the 128-byte swizzle (the 16-byte chunk index is XORed with r mod 8).
 __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) {
