@@ -584,47 +584,74 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 }
 
 // ============================================================== chain kernel
+// One CTA per (sequence, value head, slice of VS value columns).  The columns
+// of the state are independent under the delta rule, so a head's state can be
+// split across CTAs when there are few (sequence, head) pairs.  Per chunk,
+// with the chunk's rows on TMEM lanes and the slice's columns as the MMA N:
+//   MMA1  [Q S; W S]      M = 128 (q rows | w rows), N = VS, K = d   (A = [Q; W], B = S, MN-major)
+//   U' = U - W S          (w-row lanes; bf16 operands U' and U' diag(e^{G_n-G_j} rk))
+//   MMA2  dS = K^T U'_dec M = d, N = VS, K = j                        (the state's critical path)
+//   MMA3  P U'            M = 128 (P and 64 rows of padding), N = VS, K = j
+//   S <- e^{G_n} S + dS   (f32 in registers; bf16 operand for the next MMA1)
+//   O = (Q S) diag(e^G rq) + P U'  (q-row lanes; rows stored straight to global
+//                                   while the next chunk's MMA1 runs)
 constexpr int NT_C = 512;
-constexpr int CS_ST = 0;                           // S^T bf16 [v][d], 2 blocks of 16 KB
-constexpr int STAGE = 74752;  // [W|Q] 32K (per 64-column block: W rows, Q rows) | UT 16K | P 8K | K 16K | vec 1K
-constexpr int CS_STAGE = CS_ST + 32768;
-constexpr int SG_WQ = 0, SG_UT = 32768, SG_P = 49152, SG_K = 57344, SG_VEC = 73728;
-constexpr int CS_UTC = CS_STAGE + 2 * STAGE;       // U'^T bf16 (then the O staging tile)
-constexpr int CS_UTD = CS_UTC + 16384;             // U'^T diag(e^{G_n-G_j} rk)
-constexpr int CS_BAR = CS_UTD + 16384;
-constexpr int CS_TOTAL = CS_BAR + 64;
-constexpr int CSMEM = CS_TOTAL + 1024;
-static_assert(CSMEM <= 232448, "chain kernel shared memory");
-// TMEM: the chunk's state increment, two buffers of [(W S)^T | (Q S)^T] and two
-// of U'^T P^T.  The f32 state itself lives in registers: thread (v, cg) holds
-// S[d][v] for d in [32 cg, 32 cg + 32).
-constexpr uint32_t TC_DS = 0, TC_WQS = 128, TC_O = 384, TC_COLS = 512;
 
-// Per chunk: MMA(S^T W^T, S^T Q^T) -> U' -> MMA(state update, U'^T P^T) -> state
-// read-back (bf16 operand for the next chunk, the next chunk's decay applied in
-// TMEM) -> the next chunk's first MMAs are issued -> this chunk's O epilogue
-// runs while they execute.
+template <int VS>
+struct ChainLayout {
+    static constexpr int NB = VS / 64;                  // 64-column blocks of the slice
+    static constexpr int SG_QW = 0;                     // per 64-wide d block: Q rows | W rows (16 KB)
+    static constexpr int SG_P = 32768;                  // P; K follows, as the padded P operand's rows 64-127
+    static constexpr int SG_K = SG_P + 8192;
+    static constexpr int SG_UT = SG_K + 16384;          // U^T rows of the slice, [VS][64]
+    static constexpr int SG_VEC = SG_UT + VS * 128;
+    static constexpr int STAGE = SG_VEC + 1024;
+    static constexpr int CS_S = 0;                      // S [d][v] bf16, NB blocks of 16 KB
+    static constexpr int CS_STAGE = CS_S + NB * 16384;
+    static constexpr int CS_UP = CS_STAGE + 2 * STAGE;  // U' [j][v] bf16, NB blocks of 8 KB
+    static constexpr int CS_UD = CS_UP + NB * 8192;     // U' diag(e^{G_n-G_j} rk)
+    static constexpr int CS_BAR = CS_UD + NB * 8192;
+    static constexpr int SMEM = CS_BAR + 64 + 1024;
+    // TMEM: two buffers of [Q S; W S], then dS, then P U'
+    static constexpr uint32_t T_QW = 0, T_DS = 2 * VS, T_OP = 3 * VS, T_COLS = 4 * VS;
+    static_assert(SMEM <= 232448, "chain kernel shared memory");
+};
+
+template <int N>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, float* v) {
+    if constexpr (N == 16) tmem_ld16(taddr, v); else tmem_ld32(taddr, v);
+}
+
+template <int VS>
 __global__ void __launch_bounds__(NT_C, 1)
-chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-                   const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap utmap,
-                   const __grid_constant__ CUtensorMap pmap, DeltaArgs a, Work w, int64_t C0,
-                   int64_t segc) {
-    const int h = blockIdx.x % a.H_v;
-    const int seq = blockIdx.x / a.H_v;
+chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
+                   const __grid_constant__ CUtensorMap utmap, const __grid_constant__ CUtensorMap pmap,
+                   DeltaArgs a, Work w, int64_t C0, int64_t segc) {
+    using Ly = ChainLayout<VS>;
+    constexpr int NV = D / VS, CV = VS / 4;
+    const int vp = blockIdx.x % NV;
+    const int h = (blockIdx.x / NV) % a.H_v;
+    const int seq = blockIdx.x / (NV * a.H_v);
+    const int v0 = vp * VS;
     const int64_t cs = w.coff[seq], ce = w.coff[seq + 1];
     const int64_t c_lo = cs > C0 ? cs : C0, c_hi = ce < C0 + segc ? ce : C0 + segc;
     const int64_t sbase = ((int64_t)seq * a.H_v + h) * D * D;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (c_lo >= c_hi) {
         // no chunk of this sequence in this segment; an empty sequence's final
         // state is its initial state (written once, by the first segment)
         if (cs == ce && C0 == 0 && a.S_final != nullptr && a.S_final != a.S0)
-            for (int e = tid; e < D * D; e += NT_C)
-                a.S_final[sbase + e] = a.S0 != nullptr ? a.S0[sbase + e] : 0.f;
+            for (int e = tid; e < D * VS; e += NT_C) {
+                const int64_t off = sbase + (int64_t)(e / VS) * D + v0 + e % VS;
+                a.S_final[off] = a.S0 != nullptr ? a.S0[off] : 0.f;
+            }
         return;
     }
+    // warp (quarter, cg): TMEM lanes 32 quarter + lane -- q rows 0-63, w rows
+    // 64-127, state rows d -- and the slice's columns [c0, c0 + CV)
     const int quarter = warp & 3, cg = warp >> 2;
-    const int row = quarter * 32 + (tid & 31);
+    const int lrow = quarter * 32 + lane;
+    const int c0 = cg * CV;
     const uint32_t lo = (uint32_t)(quarter * 32) << 16;
     const int kh = h / (a.H_v / a.H_k);
     const int xq = kh * D, xk = a.H_k * D + kh * D;
@@ -636,18 +663,26 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + CS_BAR);  // [0], [1]
-    uint64_t* bar_mma = bar_tma + 2;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 3);
+    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + Ly::CS_BAR);  // [0], [1]
+    uint64_t* bar_m1 = bar_tma + 2;
+    uint64_t* bar_m2 = bar_tma + 3;
+    uint64_t* bar_m3 = bar_tma + 4;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 5);
+    uint8_t* s_op = sm + Ly::CS_S + (c0 >> 6) * 16384;    // this thread's block of the S operand
+    uint8_t* up_op = sm + Ly::CS_UP + (c0 >> 6) * 8192;   // ... of U'
+    uint8_t* ud_op = sm + Ly::CS_UD + (c0 >> 6) * 8192;   // ... of U'_dec
+    const int cb = c0 & 63;                              // column inside the block
 
     if (tid == 0) {
         mbar_init(&bar_tma[0], 1);
         mbar_init(&bar_tma[1], 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_m1, 1);
+        mbar_init(bar_m2, 1);
+        mbar_init(bar_m3, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tslot, TC_COLS);
+        tmem_alloc(tslot, Ly::T_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -656,21 +691,21 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     const uint32_t tb = *tslot;
 
     int issued0 = 0, issued1 = 0, consumed0 = 0, consumed1 = 0;
-    auto issue = [&](int64_t gcc) {
+    auto issue = [&](int64_t gcc) {  // thread 0: the stage of chunk gcc
         const int b = (int)((gcc - c_lo) & 1);
-        uint8_t* st = sm + CS_STAGE + b * STAGE;
+        uint8_t* st = sm + Ly::CS_STAGE + b * Ly::STAGE;
         const int y = (int)(s0 + (gcc - cs) * C);
         const int64_t uu = (gcc - C0) * a.H_v + h;
-        mbar_arrive_expect_tx(&bar_tma[b], STAGE);
-        tma_load_2d(st + SG_WQ, &wmap, &bar_tma[b], 0, (int)(uu * 64));
-        tma_load_2d(st + SG_WQ + 16384, &wmap, &bar_tma[b], 64, (int)(uu * 64));
-        tma_load_2d(st + SG_WQ + 8192, &qmap, &bar_tma[b], xq, y);
-        tma_load_2d(st + SG_WQ + 24576, &qmap, &bar_tma[b], xq + 64, y);
-        tma_load_2d(st + SG_UT, &utmap, &bar_tma[b], 0, (int)(uu * 128));
-        tma_load_2d(st + SG_P, &pmap, &bar_tma[b], 0, (int)(uu * 64));
-        tma_load_2d(st + SG_K, &qmap, &bar_tma[b], xk, y);
-        tma_load_2d(st + SG_K + 8192, &qmap, &bar_tma[b], xk + 64, y);
-        bulk_load(st + SG_VEC, w.vec + uu * (int64_t)(U_VEC / 4), (uint32_t)U_VEC, &bar_tma[b]);
+        mbar_arrive_expect_tx(&bar_tma[b], Ly::STAGE);
+        tma_load_2d(st + Ly::SG_QW, &qmap, &bar_tma[b], xq, y);
+        tma_load_2d(st + Ly::SG_QW + 8192, &wmap, &bar_tma[b], 0, (int)(uu * 64));
+        tma_load_2d(st + Ly::SG_QW + 16384, &qmap, &bar_tma[b], xq + 64, y);
+        tma_load_2d(st + Ly::SG_QW + 24576, &wmap, &bar_tma[b], 64, (int)(uu * 64));
+        tma_load_2d(st + Ly::SG_P, &pmap, &bar_tma[b], 0, (int)(uu * 64));
+        tma_load_2d(st + Ly::SG_K, &qmap, &bar_tma[b], xk, y);
+        tma_load_2d(st + Ly::SG_K + 8192, &qmap, &bar_tma[b], xk + 64, y);
+        tma_load_2d(st + Ly::SG_UT, &utmap, &bar_tma[b], 0, (int)(uu * 128 + v0));
+        bulk_load(st + Ly::SG_VEC, w.vec + uu * (int64_t)(U_VEC / 4), (uint32_t)U_VEC, &bar_tma[b]);
         if (b) ++issued1; else ++issued0;
     };
     auto wait_stage = [&](int64_t gcc) -> bool {  // every thread, in chunk order
@@ -681,18 +716,16 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         }
         return r;
     };
-    auto issue_mma45 = [&](int64_t gcc) {  // thread 0: [(W S)^T | (Q S)^T] of chunk gcc, one N=128 MMA
+    auto issue_m1 = [&](int64_t gcc) {  // thread 0: [Q S; W S] of chunk gcc
         const int b = (int)((gcc - c_lo) & 1);
-        uint8_t* st = sm + CS_STAGE + b * STAGE;
+        const uint32_t aqw = smem_u32(sm + Ly::CS_STAGE + b * Ly::STAGE + Ly::SG_QW);
+        const uint32_t bs = smem_u32(sm + Ly::CS_S);
         tc_fence_after();
-        const uint32_t ast = smem_u32(sm + CS_ST), bwq = smem_u32(st + SG_WQ);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-            mma_bf16(tb + TC_WQS + 128 * b, sdesc_sw128(ast + off, 16, 1024),
-                     sdesc_sw128(bwq + off, 16, 1024), idesc_bf16_f32(128, 128, 0, 0), k > 0);
-        }
-        mma_commit(bar_mma);
+        for (int k = 0; k < 8; ++k)
+            mma_bf16(tb + Ly::T_QW + VS * b, sdesc_sw128(aqw + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                     sdesc_sw128(bs + k * 2048, 16384, 1024), idesc_bf16_f32(128, VS, 0, 1), k > 0);
+        mma_commit(bar_m1);
     };
     if (tid == 0) {
         issue(c_lo);
@@ -700,92 +733,100 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     }
 
     // initial state of this segment: the sequence's initial state at its first
-    // chunk, else what the previous segment left in the carry
-    float sv[32];
+    // chunk, else what the previous segment left in the carry.  Thread
+    // (lrow = d, cg) holds S[d][v0 + c0 .. v0 + c0 + CV).
+    float sv[CV];
     {
         const float* src = (c_lo == cs) ? a.S0 : w.carry;
+        const float* p = src != nullptr ? src + sbase + (int64_t)lrow * D + v0 + c0 : nullptr;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            sv[j] = src != nullptr ? src[sbase + (int64_t)(32 * cg + j) * D + row] : 0.f;
-        store_row_bf16(sm + CS_ST + (cg >> 1) * 16384, row, (cg & 1) * 32, sv, 32);
+        for (int q = 0; q < CV; q += 4) {
+            const float4 f = p != nullptr ? *reinterpret_cast<const float4*>(p + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            sv[q] = f.x;
+            sv[q + 1] = f.y;
+            sv[q + 2] = f.z;
+            sv[q + 3] = f.w;
+        }
+        store_row_bf16(s_op, lrow, cb, sv, CV);
     }
     bool ok = __syncthreads_and(wait_stage(c_lo));
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    uint32_t mma_phase = 0;
-    bool mma_pending = false;
-    if (ok && tid == 0) issue_mma45(c_lo);
-    mma_pending = ok;
+    uint32_t m1_phase = 0, m2_phase = 0, m3_phase = 0;
+    bool m1_pending = false, m3_pending = false;
+    uint32_t m3_parity = 0;  // phase of the P U' commit in flight
+    if (ok && tid == 0) issue_m1(c_lo);
+    m1_pending = ok;
+    bool ok_local = true;  // a thread's own wait results, folded into the next barrier
 
     for (int64_t gcc = c_lo; ok && gcc < c_hi; ++gcc) {
         const int b = (int)((gcc - c_lo) & 1);
-        uint8_t* st = sm + CS_STAGE + b * STAGE;
-        const float* vs = reinterpret_cast<const float*>(st + SG_VEC);
+        const uint8_t* st = sm + Ly::CS_STAGE + b * Ly::STAGE;
+        const float* vs = reinterpret_cast<const float*>(st + Ly::SG_VEC);
         const int64_t lc = gcc - cs;
         const int64_t t0 = s0 + lc * C;
         const int n = (int)(L - lc * C < C ? L - lc * C : C);
-        const int i0 = 16 * cg;
 
-        if (tid == 0) bulk_wait_read_all();  // the previous O tile store has left U'^T's buffer
-        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase, kWaitNs));
+        ok = __syncthreads_and(ok_local && mbar_wait(bar_m1, m1_phase, kWaitNs));
         if (!ok) break;
-        mma_phase ^= 1;
-        mma_pending = false;
+        m1_phase ^= 1;
+        m1_pending = false;
         tc_fence_after();
 
-        // U'^T = U^T - (W S)^T (bf16, and scaled by e^{G_n-G_j} rk_j)
-        float erq[16];  // e^{G_i} rq_i of this thread's O rows (the stage is reloaded below)
         const float eGn = vs[128];
-        {
-            const int j0 = 16 * cg;
-            float ws[16], ui[16];
-            tmem_ld16(tb + lo + TC_WQS + 128 * b + j0, ws);
-            const uint8_t* urow = st + SG_UT;
+        float erq = 0.f;
+        if (quarter >= 2) {
+            // U' = U - W S for w row j (U read from the U^T tile), and its
+            // copy scaled by e^{G_n-G_j} rk_j
+            const int j = lrow - 64;
+            const float dj = vs[64 + j];
+            const uint8_t* ut = st + Ly::SG_UT;
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                float t8[8];
-                load16(reinterpret_cast<const bf16*>(urow + sw128_off(row, j0 + 8 * g)), t8);
+            for (int h16 = 0; h16 < CV; h16 += 16) {
+                float ws[16], up[16];
+                tmem_ld16(tb + lo + Ly::T_QW + VS * b + c0 + h16, ws);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ui[8 * g + e] = t8[e];
+                for (int q = 0; q < 16; ++q)
+                    up[q] = __bfloat162float(*reinterpret_cast<const bf16*>(ut + sw128_off(c0 + h16 + q, j)));
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 16; ++q) up[q] -= ws[q];
+                store_row_bf16(up_op, j, cb + h16, up, 16);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) ws[q] = up[q] * dj;
+                store_row_bf16(ud_op, j, cb + h16, ws, 16);
             }
-#pragma unroll
-            for (int q = 0; q < 16; ++q) erq[q] = vs[i0 + q];
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) ui[j] -= ws[j];
-            store_row_bf16(sm + CS_UTC, row, j0, ui, 16);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) ws[j] = ui[j] * vs[64 + j0 + j];
-            store_row_bf16(sm + CS_UTD, row, j0, ws, 16);
+        } else {
+            erq = vs[lrow];  // e^{G_i} rq_i of q row i
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // dS^T = U'^T_dec K  (M = v, N = d, K = j);  O_P^T = U'^T P^T  (N = i)
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t autd = smem_u32(sm + CS_UTD), aut = smem_u32(sm + CS_UTC);
-            const uint32_t bk = smem_u32(st + SG_K), bp = smem_u32(st + SG_P);
+            const uint32_t ak = smem_u32(st + Ly::SG_K), ap = smem_u32(st + Ly::SG_P);
+            const uint32_t bud = smem_u32(sm + Ly::CS_UD), bup = smem_u32(sm + Ly::CS_UP);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                mma_bf16(tb + TC_DS, sdesc_sw128(autd + k * 32, 16, 1024),
-                         sdesc_sw128(bk + k * 2048, 8192, 1024), idesc_bf16_f32(128, 128, 0, 1), k > 0);
-                mma_bf16(tb + TC_O + 64 * b, sdesc_sw128(aut + k * 32, 16, 1024),
-                         sdesc_sw128(bp + k * 32, 16, 1024), idesc_bf16_f32(128, 64, 0, 0), k > 0);
-            }
-            mma_commit(bar_mma);
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tb + Ly::T_DS, sdesc_sw128(ak + k * 2048, 8192, 1024),
+                         sdesc_sw128(bud + k * 2048, 8192, 1024), idesc_bf16_f32(128, VS, 1, 1), k > 0);
+            mma_commit(bar_m2);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(tb + Ly::T_OP, sdesc_sw128(ap + k * 32, 16, 1024),
+                         sdesc_sw128(bup + k * 2048, 8192, 1024), idesc_bf16_f32(128, VS, 0, 1), k > 0);
+            mma_commit(bar_m3);
         }
-        mma_pending = true;
-        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase, kWaitNs));
-        if (!ok) break;
-        mma_phase ^= 1;
-        mma_pending = false;
-        tc_fence_after();
-        if (tid == 0 && gcc + 2 < c_hi) issue(gcc + 2);  // this chunk's stage is consumed
+        m3_pending = true;
+        m3_parity = m3_phase;
 
-        // S <- e^{G_n} S + dS (registers) -> bf16 S^T operand (and checkpoint)
+        // S <- e^{G_n} S + dS -> bf16 S operand (and checkpoint)
+        ok = __syncthreads_and(mbar_wait(bar_m2, m2_phase, kWaitNs));
+        if (!ok) break;
+        m2_phase ^= 1;
+        tc_fence_after();
         const bool more = gcc + 1 < c_hi;
         bool landed = true;
         {
@@ -793,77 +834,82 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             float* ck = nullptr;
             if (a.ckpt_every > 0 && a.ckpt != nullptr && done % a.ckpt_every == 0) {
                 const int64_t crow = ck_row0 + done / a.ckpt_every - 1;
-                if (crow < a.ckpt_rows) ck = a.ckpt + (crow * a.H_v + h) * D * D;
+                if (crow < a.ckpt_rows) ck = a.ckpt + (crow * a.H_v + h) * D * D + (int64_t)lrow * D + v0 + c0;
             }
-            float ds[32];
-            tmem_ld32(tb + lo + TC_DS + 32 * cg, ds);
+            float ds[CV];
+            tmem_ldn<CV>(tb + lo + Ly::T_DS + c0, ds);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sv[j] = fmaf(eGn, sv[j], ds[j]);
-            store_row_bf16(sm + CS_ST + (cg >> 1) * 16384, row, (cg & 1) * 32, sv, 32);
+            for (int q = 0; q < CV; ++q) sv[q] = fmaf(eGn, sv[q], ds[q]);
+            store_row_bf16(s_op, lrow, cb, sv, CV);
             if (ck != nullptr)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) ck[(int64_t)(32 * cg + j) * D + row] = sv[j];
+                for (int q = 0; q < CV; q += 4)
+                    *reinterpret_cast<float4*>(ck + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
             if (more) landed = wait_stage(gcc + 1);
         }
         fence_async_smem();
         tc_fence_before();
         ok = __syncthreads_and(landed);
         if (!ok) break;
-        if (more && tid == 0) issue_mma45(gcc + 1);
-        mma_pending = more;
+        if (more && tid == 0) issue_m1(gcc + 1);
+        m1_pending = more;
 
-        // O = (Q S) diag(e^G rq) + P U' of this chunk, while the next chunk's MMAs run
-        {
-            tc_fence_after();
-            float qs[16], po[16];
-            tmem_ld16(tb + lo + TC_WQS + 128 * b + 64 + i0, qs);
-            tmem_ld16(tb + lo + TC_O + 64 * b + i0, po);
-            tmem_wait_ld();
-            if (n == C) {
-                uint8_t* stg = sm + CS_UTC + (row >> 6) * 8192;
-                const int cc = row & 63;
+        // O = (Q S) diag(e^G rq) + P U' of this chunk (q-row lanes), while the
+        // next chunk's MMA1 runs; then this chunk's stage takes chunk gcc + 2
+        bool m3ok = true;
+        if (quarter < 2) {
+            m3ok = mbar_wait(bar_m3, m3_phase, kWaitNs);
+            if (m3ok) {
+                tc_fence_after();
+                bf16* o = static_cast<bf16*>(a.o) + ((t0 + lrow) * a.H_v + h) * D + v0 + c0;
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    *reinterpret_cast<bf16*>(stg + sw128_off(i0 + q, cc)) =
-                        __float2bfloat16_rn(erq[q] * qs[q] + po[q]);
-                fence_async_smem();
-                __syncthreads();
-                if (tid == 0) {
-                    tma_store_2d(&omap, sm + CS_UTC, h * D, (int)t0);
-                    tma_store_2d(&omap, sm + CS_UTC + 8192, h * D + 64, (int)t0);
-                    bulk_commit();
+                for (int h16 = 0; h16 < CV; h16 += 16) {
+                    float qs[16], po[16];
+                    tmem_ld16(tb + lo + Ly::T_QW + VS * b + c0 + h16, qs);
+                    tmem_ld16(tb + lo + Ly::T_OP + c0 + h16, po);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) po[q] = fmaf(erq, qs[q], po[q]);
+                    if (lrow < n) {
+                        store16(o + h16, po);
+                        store16(o + h16 + 8, po + 8);
+                    }
                 }
-            } else {
-                bf16* o = static_cast<bf16*>(a.o) + (t0 * a.H_v + h) * D + row;
-                const int64_t ostride = (int64_t)a.H_v * D;
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    if (i0 + q < n) o[(i0 + q) * ostride] = __float2bfloat16_rn(erq[q] * qs[q] + po[q]);
             }
         }
+        m3_phase ^= 1;
+        if (tid == 0 && m3ok) {
+            m3_pending = false;
+            if (gcc + 2 < c_hi) issue(gcc + 2);
+        }
         tc_fence_before();
-        __syncthreads();
+        ok_local = m3ok;
     }
+    ok = __syncthreads_and(ok && ok_local);
 
     if (ok) {
         float* dst = a.S_final != nullptr ? a.S_final : w.carry;
-        if (dst != nullptr)
+        if (dst != nullptr) {
+            float* p = dst + sbase + (int64_t)lrow * D + v0 + c0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) dst[sbase + (int64_t)(32 * cg + j) * D + row] = sv[j];
+            for (int q = 0; q < CV; q += 4)
+                *reinterpret_cast<float4*>(p + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
+        }
     } else if (tid == 0) {
         atomicOr(&g_device_error, 1);
-        if (mma_pending) mbar_wait(bar_mma, mma_phase, kWaitNs);
+        if (m1_pending) mbar_wait(bar_m1, m1_phase, kWaitNs);
+        if (m3_pending) mbar_wait(bar_m3, m3_parity, kWaitNs);
         for (int k = consumed0; k < issued0; ++k) mbar_wait(&bar_tma[0], (uint32_t)(k & 1), kWaitNs);
         for (int k = consumed1; k < issued1; ++k) mbar_wait(&bar_tma[1], (uint32_t)(k & 1), kWaitNs);
     }
-    if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, TC_COLS);
+    if (warp == 0) tmem_dealloc(tb, Ly::T_COLS);
 }
 
 }  // namespace
+
 
 PFN_cuTensorMapEncodeTiled_v12000 tensormap_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -894,19 +940,37 @@ bool encode2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Chunk offsets, then per segment: gates, intra, chain.
+int sm_count() {
+    static int count[128];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 1;
+    if (count[dev] == 0) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1) c = 1;
+        count[dev] = c;
+    }
+    return count[dev];
+}
+
+// Chunk offsets, then per segment: gates, intra, chain.  The chain splits each
+// head's state into two 64-column slices when that still leaves at most one
+// CTA per SM.
 cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cudaStream_t s) {
     const uint64_t conv_dim = 2ull * a.H_k * D + (uint64_t)a.H_v * D;
     const uint64_t U = (uint64_t)Ly.segc * a.H_v;
-    CUtensorMap qmap, omap, wtmap, utmap, pmap;
-    if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) ||
-        !encode2d(&omap, a.o, (uint64_t)a.H_v * D, (uint64_t)a.T, 64, 64) ||
-        !encode2d(&wtmap, w.wt, 128, U * 64, 64, 64) || !encode2d(&utmap, w.ut, 64, U * 128, 64, 128) ||
-        !encode2d(&pmap, w.p, 64, U * 64, 64, 64))
+    const bool split = (int64_t)a.n_seq * a.H_v * 2 <= sm_count();
+    const uint32_t vs = split ? 64 : 128;
+    CUtensorMap qmap, wtmap, utmap, pmap;
+    if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) || !encode2d(&wtmap, w.wt, 128, U * 64, 64, 64) ||
+        !encode2d(&utmap, w.ut, 64, U * 128, 64, vs) || !encode2d(&pmap, w.p, 64, U * 64, 64, 64))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CSMEM);
+        e = cudaFuncSetAttribute(chunk_chain_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ChainLayout<64>::SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chunk_chain_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ChainLayout<128>::SMEM);
     if (e != cudaSuccess) return e;
 
     chunk_offsets_kernel<<<1, 1024, 0, s>>>(a.cu, a.n_seq, a.T, w.coff);
@@ -914,8 +978,12 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
         const int64_t C0 = seg * Ly.segc;
         chunk_gates_kernel<<<dim3((unsigned)Ly.segc, (unsigned)((a.H_v + 31) / 32)), NT_G, 0, s>>>(a, w, C0);
         chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, s>>>(qmap, wtmap, a, w, C0);
-        chunk_chain_kernel<<<(unsigned)(a.n_seq * a.H_v), NT_C, CSMEM, s>>>(qmap, omap, wtmap, utmap,
-                                                                          pmap, a, w, C0, Ly.segc);
+        if (split)
+            chunk_chain_kernel<64><<<(unsigned)(a.n_seq * a.H_v * 2), NT_C, ChainLayout<64>::SMEM, s>>>(
+                qmap, wtmap, utmap, pmap, a, w, C0, Ly.segc);
+        else
+            chunk_chain_kernel<128><<<(unsigned)(a.n_seq * a.H_v), NT_C, ChainLayout<128>::SMEM, s>>>(
+                qmap, wtmap, utmap, pmap, a, w, C0, Ly.segc);
     }
     return cudaGetLastError();
 }
