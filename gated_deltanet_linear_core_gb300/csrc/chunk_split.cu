@@ -590,12 +590,17 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 // with the chunk's rows on TMEM lanes and the slice's columns as the MMA N:
 //   MMA1  [Q S; W S]      M = 128 (q rows | w rows), N = VS, K = d   (A = [Q; W], B = S, MN-major)
 //   U' = U - W S          (w-row lanes; bf16 operands U' and U' diag(e^{G_n-G_j} rk))
-//   MMA2  dS = K^T U'_dec M = d, N = VS, K = j                        (the state's critical path)
-//   MMA3  P U'            M = 128 (P and 64 rows of padding), N = VS, K = j
+//   MMA2  dS = K^T U'_dec M = d, N = VS, K = j
 //   S <- e^{G_n} S + dS   (f32 in registers; bf16 operand for the next MMA1)
-//   O = (Q S) diag(e^G rq) + P U'  (q-row lanes; rows stored straight to global
-//                                   while the next chunk's MMA1 runs)
-constexpr int NT_C = 512;
+//   MMA3  P U'            M = 128 (P and 64 rows of padding), N = VS, K = j
+//   O = (Q S) diag(e^G rq) + P U'  (q-row lanes, stored straight to global)
+// Warp roles: 16 compute warps, one warp that issues the MMAs and one that
+// issues the TMA copies; they hand work to each other through mbarriers, so
+// the copies, the O epilogue and the P U' product run off the state's
+// critical path (MMA1 -> U' -> MMA2 -> S update -> next MMA1).
+constexpr int NT_COMP = 512;
+constexpr int NT_C = NT_COMP + 64;
+constexpr int W_MMA = NT_COMP / 32, W_TMA = W_MMA + 1;
 
 template <int VS>
 struct ChainLayout {
@@ -611,7 +616,7 @@ struct ChainLayout {
     static constexpr int CS_UP = CS_STAGE + 2 * STAGE;  // U' [j][v] bf16, NB blocks of 8 KB
     static constexpr int CS_UD = CS_UP + NB * 8192;     // U' diag(e^{G_n-G_j} rk)
     static constexpr int CS_BAR = CS_UD + NB * 8192;
-    static constexpr int SMEM = CS_BAR + 64 + 1024;
+    static constexpr int SMEM = CS_BAR + 128 + 1024;
     // TMEM: two buffers of [Q S; W S], then dS, then P U'
     static constexpr uint32_t T_QW = 0, T_DS = 2 * VS, T_OP = 3 * VS, T_COLS = 4 * VS;
     static_assert(SMEM <= 232448, "chain kernel shared memory");
@@ -620,6 +625,30 @@ struct ChainLayout {
 template <int N>
 __device__ __forceinline__ void tmem_ldn(uint32_t taddr, float* v) {
     if constexpr (N == 16) tmem_ld16(taddr, v); else tmem_ld32(taddr, v);
+}
+
+// Bounded wait that also gives up once another role has given up.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_test(bar, parity)) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitNs) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+// every lane of the warp waits; the warp proceeds only if all lanes saw the phase
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, mbar_wait_or_abort(bar, parity, abort_flag));
+}
+// after the warp's shared-memory writes and TMEM reads: one arrival per warp
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
 }
 
 template <int VS>
@@ -647,38 +676,34 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             }
         return;
     }
-    // warp (quarter, cg): TMEM lanes 32 quarter + lane -- q rows 0-63, w rows
-    // 64-127, state rows d -- and the slice's columns [c0, c0 + CV)
-    const int quarter = warp & 3, cg = warp >> 2;
-    const int lrow = quarter * 32 + lane;
-    const int c0 = cg * CV;
-    const uint32_t lo = (uint32_t)(quarter * 32) << 16;
     const int kh = h / (a.H_v / a.H_k);
     const int xq = kh * D, xk = a.H_k * D + kh * D;
     int64_t s0, s1;
     seq_bounds(a.cu, seq, a.T, s0, s1);
     const int64_t L = s1 - s0;
-    int64_t ck_row0 = 0;
-    if (a.ckpt_every > 0 && a.ckpt != nullptr) ck_row0 = ckpt_row0(a.cu, seq, a.T, a.ckpt_every);
+    const int nch = (int)(c_hi - c_lo);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + Ly::CS_BAR);  // [0], [1]
-    uint64_t* bar_m1 = bar_tma + 2;
-    uint64_t* bar_m2 = bar_tma + 3;
-    uint64_t* bar_m3 = bar_tma + 4;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 5);
-    uint8_t* s_op = sm + Ly::CS_S + (c0 >> 6) * 16384;    // this thread's block of the S operand
-    uint8_t* up_op = sm + Ly::CS_UP + (c0 >> 6) * 8192;   // ... of U'
-    uint8_t* ud_op = sm + Ly::CS_UD + (c0 >> 6) * 8192;   // ... of U'_dec
-    const int cb = c0 & 63;                              // column inside the block
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::CS_BAR);
+    uint64_t* full = bars;       // [2] stage landed (TMA)
+    uint64_t* empty = bars + 2;  // [2] stage consumed (tcgen05.commit after P U')
+    uint64_t* m1 = bars + 4;     // [Q S; W S] done
+    uint64_t* m2 = bars + 5;     // dS done
+    uint64_t* m3 = bars + 6;     // P U' done
+    uint64_t* s_rdy = bars + 7;  // S operand written (16 compute warps)
+    uint64_t* u_rdy = bars + 8;  // U' operands written, stage reads done (16 compute warps)
+    uint64_t* o_done = bars + 9; // O epilogue's TMEM reads done (8 q-row warps)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 11);
 
     if (tid == 0) {
-        mbar_init(&bar_tma[0], 1);
-        mbar_init(&bar_tma[1], 1);
-        mbar_init(bar_m1, 1);
-        mbar_init(bar_m2, 1);
-        mbar_init(bar_m3, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        for (int i = 4; i < 7; ++i) mbar_init(&bars[i], 1);
+        mbar_init(s_rdy, NT_COMP / 32);
+        mbar_init(u_rdy, NT_COMP / 32);
+        mbar_init(o_done, NT_COMP / 64);
+        *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -690,177 +715,185 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     tc_fence_after();
     const uint32_t tb = *tslot;
 
-    int issued0 = 0, issued1 = 0, consumed0 = 0, consumed1 = 0;
-    auto issue = [&](int64_t gcc) {  // thread 0: the stage of chunk gcc
-        const int b = (int)((gcc - c_lo) & 1);
-        uint8_t* st = sm + Ly::CS_STAGE + b * Ly::STAGE;
-        const int y = (int)(s0 + (gcc - cs) * C);
-        const int64_t uu = (gcc - C0) * a.H_v + h;
-        mbar_arrive_expect_tx(&bar_tma[b], Ly::STAGE);
-        tma_load_2d(st + Ly::SG_QW, &qmap, &bar_tma[b], xq, y);
-        tma_load_2d(st + Ly::SG_QW + 8192, &wmap, &bar_tma[b], 0, (int)(uu * 64));
-        tma_load_2d(st + Ly::SG_QW + 16384, &qmap, &bar_tma[b], xq + 64, y);
-        tma_load_2d(st + Ly::SG_QW + 24576, &wmap, &bar_tma[b], 64, (int)(uu * 64));
-        tma_load_2d(st + Ly::SG_P, &pmap, &bar_tma[b], 0, (int)(uu * 64));
-        tma_load_2d(st + Ly::SG_K, &qmap, &bar_tma[b], xk, y);
-        tma_load_2d(st + Ly::SG_K + 8192, &qmap, &bar_tma[b], xk + 64, y);
-        tma_load_2d(st + Ly::SG_UT, &utmap, &bar_tma[b], 0, (int)(uu * 128 + v0));
-        bulk_load(st + Ly::SG_VEC, w.vec + uu * (int64_t)(U_VEC / 4), (uint32_t)U_VEC, &bar_tma[b]);
-        if (b) ++issued1; else ++issued0;
-    };
-    auto wait_stage = [&](int64_t gcc) -> bool {  // every thread, in chunk order
-        const int b = (int)((gcc - c_lo) & 1);
-        const bool r = mbar_wait(&bar_tma[b], (uint32_t)((b ? consumed1 : consumed0) & 1), kWaitNs);
-        if (r) {
-            if (b) ++consumed1; else ++consumed0;
+    if (warp == W_TMA) {
+        // ------------------------------------------------ TMA producer (lane 0)
+        if (lane == 0) {
+            int issued = 0;  // stages issued
+            for (int k = 0; k < nch; ++k) {
+                const int b = k & 1;
+                if (k >= 2 && !mbar_wait_or_abort(&empty[b], (uint32_t)(((k >> 1) - 1) & 1), abort_flag)) break;
+                const int64_t gcc = c_lo + k;
+                uint8_t* st = sm + Ly::CS_STAGE + b * Ly::STAGE;
+                const int y = (int)(s0 + (gcc - cs) * C);
+                const int64_t uu = (gcc - C0) * a.H_v + h;
+                mbar_arrive_expect_tx(&full[b], Ly::STAGE);
+                tma_load_2d(st + Ly::SG_QW, &qmap, &full[b], xq, y);
+                tma_load_2d(st + Ly::SG_QW + 8192, &wmap, &full[b], 0, (int)(uu * 64));
+                tma_load_2d(st + Ly::SG_QW + 16384, &qmap, &full[b], xq + 64, y);
+                tma_load_2d(st + Ly::SG_QW + 24576, &wmap, &full[b], 64, (int)(uu * 64));
+                tma_load_2d(st + Ly::SG_P, &pmap, &full[b], 0, (int)(uu * 64));
+                tma_load_2d(st + Ly::SG_K, &qmap, &full[b], xk, y);
+                tma_load_2d(st + Ly::SG_K + 8192, &qmap, &full[b], xk + 64, y);
+                tma_load_2d(st + Ly::SG_UT, &utmap, &full[b], 0, (int)(uu * 128 + v0));
+                bulk_load(st + Ly::SG_VEC, w.vec + uu * (int64_t)(U_VEC / 4), (uint32_t)U_VEC, &full[b]);
+                issued = k + 1;
+            }
+            // on abort: let the copies in flight land before the CTA exits
+            if (*abort_flag)
+                for (int k = issued - 2 > 0 ? issued - 2 : 0; k < issued; ++k)
+                    mbar_wait(&full[k & 1], (uint32_t)((k >> 1) & 1), kWaitNs);
         }
-        return r;
-    };
-    auto issue_m1 = [&](int64_t gcc) {  // thread 0: [Q S; W S] of chunk gcc
-        const int b = (int)((gcc - c_lo) & 1);
-        const uint32_t aqw = smem_u32(sm + Ly::CS_STAGE + b * Ly::STAGE + Ly::SG_QW);
-        const uint32_t bs = smem_u32(sm + Ly::CS_S);
-        tc_fence_after();
+    } else if (warp == W_MMA) {
+        // ------------------------------------------------ MMA issuer (lane 0)
+        if (lane == 0) {
+            const uint32_t bs = smem_u32(sm + Ly::CS_S);
+            const uint32_t bud = smem_u32(sm + Ly::CS_UD), bup = smem_u32(sm + Ly::CS_UP);
+            uint64_t* last = nullptr;  // the last commit, for the drain on abort
+            uint32_t last_parity = 0;
+            for (int k = 0; k < nch; ++k) {
+                const int b = k & 1;
+                const uint32_t par = (uint32_t)(k & 1);
+                const uint32_t st = smem_u32(sm + Ly::CS_STAGE + b * Ly::STAGE);
+                if (!mbar_wait_or_abort(&full[b], (uint32_t)((k >> 1) & 1), abort_flag)) break;
+                if (!mbar_wait_or_abort(s_rdy, par, abort_flag)) break;
+                tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            mma_bf16(tb + Ly::T_QW + VS * b, sdesc_sw128(aqw + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                     sdesc_sw128(bs + k * 2048, 16384, 1024), idesc_bf16_f32(128, VS, 0, 1), k > 0);
-        mma_commit(bar_m1);
-    };
-    if (tid == 0) {
-        issue(c_lo);
-        if (c_lo + 1 < c_hi) issue(c_lo + 1);
-    }
-
-    // initial state of this segment: the sequence's initial state at its first
-    // chunk, else what the previous segment left in the carry.  Thread
-    // (lrow = d, cg) holds S[d][v0 + c0 .. v0 + c0 + CV).
-    float sv[CV];
-    {
-        const float* src = (c_lo == cs) ? a.S0 : w.carry;
-        const float* p = src != nullptr ? src + sbase + (int64_t)lrow * D + v0 + c0 : nullptr;
+                for (int q = 0; q < 8; ++q)
+                    mma_bf16(tb + Ly::T_QW + VS * b,
+                             sdesc_sw128(st + Ly::SG_QW + (q >> 2) * 16384 + (q & 3) * 32, 16, 1024),
+                             sdesc_sw128(bs + q * 2048, 16384, 1024), idesc_bf16_f32(128, VS, 0, 1), q > 0);
+                mma_commit(m1);
+                last = m1;
+                last_parity = par;
+                if (!mbar_wait_or_abort(u_rdy, par, abort_flag)) break;
+                tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < CV; q += 4) {
-            const float4 f = p != nullptr ? *reinterpret_cast<const float4*>(p + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-            sv[q] = f.x;
-            sv[q + 1] = f.y;
-            sv[q + 2] = f.z;
-            sv[q + 3] = f.w;
+                for (int q = 0; q < 4; ++q)
+                    mma_bf16(tb + Ly::T_DS, sdesc_sw128(st + Ly::SG_K + q * 2048, 8192, 1024),
+                             sdesc_sw128(bud + q * 2048, 8192, 1024), idesc_bf16_f32(128, VS, 1, 1), q > 0);
+                mma_commit(m2);
+                last = m2;
+                if (k > 0 && !mbar_wait_or_abort(o_done, par ^ 1u, abort_flag)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    mma_bf16(tb + Ly::T_OP, sdesc_sw128(st + Ly::SG_P + q * 32, 16, 1024),
+                             sdesc_sw128(bup + q * 2048, 8192, 1024), idesc_bf16_f32(128, VS, 0, 1), q > 0);
+                mma_commit(m3);
+                mma_commit(&empty[b]);
+                last = m3;
+            }
+            if (*abort_flag && last != nullptr) mbar_wait(last, last_parity, kWaitNs);
         }
-        store_row_bf16(s_op, lrow, cb, sv, CV);
-    }
-    bool ok = __syncthreads_and(wait_stage(c_lo));
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    uint32_t m1_phase = 0, m2_phase = 0, m3_phase = 0;
-    bool m1_pending = false, m3_pending = false;
-    uint32_t m3_parity = 0;  // phase of the P U' commit in flight
-    if (ok && tid == 0) issue_m1(c_lo);
-    m1_pending = ok;
-    bool ok_local = true;  // a thread's own wait results, folded into the next barrier
+    } else {
+        // ------------------------------------------------ compute warps
+        // warp (quarter, cg): TMEM lanes 32 quarter + lane -- q rows 0-63, w rows
+        // 64-127, state rows d -- and the slice's columns [c0, c0 + CV)
+        const int quarter = warp & 3, cg = warp >> 2;
+        const int lrow = quarter * 32 + lane;
+        const int c0 = cg * CV;
+        const uint32_t lo = (uint32_t)(quarter * 32) << 16;
+        const bool qrow = quarter < 2;
+        uint8_t* s_op = sm + Ly::CS_S + (c0 >> 6) * 16384;    // this thread's block of the S operand
+        uint8_t* up_op = sm + Ly::CS_UP + (c0 >> 6) * 8192;   // ... of U'
+        uint8_t* ud_op = sm + Ly::CS_UD + (c0 >> 6) * 8192;   // ... of U'_dec
+        const int cb = c0 & 63;
+        int64_t ck_row0 = 0;
+        if (a.ckpt_every > 0 && a.ckpt != nullptr) ck_row0 = ckpt_row0(a.cu, seq, a.T, a.ckpt_every);
 
-    for (int64_t gcc = c_lo; ok && gcc < c_hi; ++gcc) {
-        const int b = (int)((gcc - c_lo) & 1);
-        const uint8_t* st = sm + Ly::CS_STAGE + b * Ly::STAGE;
-        const float* vs = reinterpret_cast<const float*>(st + Ly::SG_VEC);
-        const int64_t lc = gcc - cs;
-        const int64_t t0 = s0 + lc * C;
-        const int n = (int)(L - lc * C < C ? L - lc * C : C);
-
-        ok = __syncthreads_and(ok_local && mbar_wait(bar_m1, m1_phase, kWaitNs));
-        if (!ok) break;
-        m1_phase ^= 1;
-        m1_pending = false;
-        tc_fence_after();
-
-        const float eGn = vs[128];
-        float erq = 0.f;
-        if (quarter >= 2) {
-            // U' = U - W S for w row j (U read from the U^T tile), and its
-            // copy scaled by e^{G_n-G_j} rk_j
-            const int j = lrow - 64;
-            const float dj = vs[64 + j];
-            const uint8_t* ut = st + Ly::SG_UT;
+        // initial state of this segment: the sequence's initial state at its
+        // first chunk, else what the previous segment left in the carry.
+        // Thread (lrow = d, cg) holds S[d][v0 + c0 .. v0 + c0 + CV).
+        float sv[CV];
+        {
+            const float* src = (c_lo == cs) ? a.S0 : w.carry;
+            const float* p = src != nullptr ? src + sbase + (int64_t)lrow * D + v0 + c0 : nullptr;
 #pragma unroll
-            for (int h16 = 0; h16 < CV; h16 += 16) {
-                float ws[16], up[16];
-                tmem_ld16(tb + lo + Ly::T_QW + VS * b + c0 + h16, ws);
+            for (int q = 0; q < CV; q += 4) {
+                const float4 f = p != nullptr ? *reinterpret_cast<const float4*>(p + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                sv[q] = f.x;
+                sv[q + 1] = f.y;
+                sv[q + 2] = f.z;
+                sv[q + 3] = f.w;
+            }
+            store_row_bf16(s_op, lrow, cb, sv, CV);
+            fence_async_smem();
+            warp_arrive(s_rdy, lane);
+        }
+
+        for (int k = 0; k < nch; ++k) {
+            const int b = k & 1;
+            const uint32_t par = (uint32_t)(k & 1);
+            const uint8_t* st = sm + Ly::CS_STAGE + b * Ly::STAGE;
+            const float* vs = reinterpret_cast<const float*>(st + Ly::SG_VEC);
+            const int64_t gcc = c_lo + k;
+            const int64_t lc = gcc - cs;
+            const int64_t t0 = s0 + lc * C;
+            const int n = (int)(L - lc * C < C ? L - lc * C : C);
+
+            if (!warp_wait(&full[b], (uint32_t)((k >> 1) & 1), abort_flag)) break;
+            if (!warp_wait(m1, par, abort_flag)) break;
+            tc_fence_after();
+            // everything this chunk needs from its stage is read before u_rdy:
+            // the stage is reloaded once P U' has completed
+            const float eGn = vs[128];
+            float erq = 0.f;
+            if (!qrow) {
+                // U' = U - W S for w row j (U from the U^T tile), and its copy
+                // scaled by e^{G_n-G_j} rk_j
+                const int j = lrow - 64;
+                const float dj = vs[64 + j];
+                const uint8_t* ut = st + Ly::SG_UT;
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    up[q] = __bfloat162float(*reinterpret_cast<const bf16*>(ut + sw128_off(c0 + h16 + q, j)));
+                for (int h16 = 0; h16 < CV; h16 += 16) {
+                    float ws[16], up[16];
+                    tmem_ld16(tb + lo + Ly::T_QW + VS * b + c0 + h16, ws);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        up[q] = __bfloat162float(*reinterpret_cast<const bf16*>(ut + sw128_off(c0 + h16 + q, j)));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) up[q] -= ws[q];
+                    store_row_bf16(up_op, j, cb + h16, up, 16);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) ws[q] = up[q] * dj;
+                    store_row_bf16(ud_op, j, cb + h16, ws, 16);
+                }
+                fence_async_smem();
+            } else {
+                erq = vs[lrow];  // e^{G_i} rq_i of q row i
+            }
+            warp_arrive(u_rdy, lane);
+
+            // S <- e^{G_n} S + dS -> bf16 S operand (and checkpoint)
+            if (!warp_wait(m2, par, abort_flag)) break;
+            tc_fence_after();
+            {
+                const int64_t done = lc * C + n;
+                float* ck = nullptr;
+                if (a.ckpt_every > 0 && a.ckpt != nullptr && done % a.ckpt_every == 0) {
+                    const int64_t crow = ck_row0 + done / a.ckpt_every - 1;
+                    if (crow < a.ckpt_rows)
+                        ck = a.ckpt + (crow * a.H_v + h) * D * D + (int64_t)lrow * D + v0 + c0;
+                }
+                float ds[CV];
+                tmem_ldn<CV>(tb + lo + Ly::T_DS + c0, ds);
                 tmem_wait_ld();
 #pragma unroll
-                for (int q = 0; q < 16; ++q) up[q] -= ws[q];
-                store_row_bf16(up_op, j, cb + h16, up, 16);
+                for (int q = 0; q < CV; ++q) sv[q] = fmaf(eGn, sv[q], ds[q]);
+                store_row_bf16(s_op, lrow, cb, sv, CV);
+                fence_async_smem();
+                if (ck != nullptr)
 #pragma unroll
-                for (int q = 0; q < 16; ++q) ws[q] = up[q] * dj;
-                store_row_bf16(ud_op, j, cb + h16, ws, 16);
+                    for (int q = 0; q < CV; q += 4)
+                        *reinterpret_cast<float4*>(ck + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
             }
-        } else {
-            erq = vs[lrow];  // e^{G_i} rq_i of q row i
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
+            warp_arrive(s_rdy, lane);
 
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t ak = smem_u32(st + Ly::SG_K), ap = smem_u32(st + Ly::SG_P);
-            const uint32_t bud = smem_u32(sm + Ly::CS_UD), bup = smem_u32(sm + Ly::CS_UP);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(tb + Ly::T_DS, sdesc_sw128(ak + k * 2048, 8192, 1024),
-                         sdesc_sw128(bud + k * 2048, 8192, 1024), idesc_bf16_f32(128, VS, 1, 1), k > 0);
-            mma_commit(bar_m2);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(tb + Ly::T_OP, sdesc_sw128(ap + k * 32, 16, 1024),
-                         sdesc_sw128(bup + k * 2048, 8192, 1024), idesc_bf16_f32(128, VS, 0, 1), k > 0);
-            mma_commit(bar_m3);
-        }
-        m3_pending = true;
-        m3_parity = m3_phase;
-
-        // S <- e^{G_n} S + dS -> bf16 S operand (and checkpoint)
-        ok = __syncthreads_and(mbar_wait(bar_m2, m2_phase, kWaitNs));
-        if (!ok) break;
-        m2_phase ^= 1;
-        tc_fence_after();
-        const bool more = gcc + 1 < c_hi;
-        bool landed = true;
-        {
-            const int64_t done = lc * C + n;
-            float* ck = nullptr;
-            if (a.ckpt_every > 0 && a.ckpt != nullptr && done % a.ckpt_every == 0) {
-                const int64_t crow = ck_row0 + done / a.ckpt_every - 1;
-                if (crow < a.ckpt_rows) ck = a.ckpt + (crow * a.H_v + h) * D * D + (int64_t)lrow * D + v0 + c0;
-            }
-            float ds[CV];
-            tmem_ldn<CV>(tb + lo + Ly::T_DS + c0, ds);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < CV; ++q) sv[q] = fmaf(eGn, sv[q], ds[q]);
-            store_row_bf16(s_op, lrow, cb, sv, CV);
-            if (ck != nullptr)
-#pragma unroll
-                for (int q = 0; q < CV; q += 4)
-                    *reinterpret_cast<float4*>(ck + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
-            if (more) landed = wait_stage(gcc + 1);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        ok = __syncthreads_and(landed);
-        if (!ok) break;
-        if (more && tid == 0) issue_m1(gcc + 1);
-        m1_pending = more;
-
-        // O = (Q S) diag(e^G rq) + P U' of this chunk (q-row lanes), while the
-        // next chunk's MMA1 runs; then this chunk's stage takes chunk gcc + 2
-        bool m3ok = true;
-        if (quarter < 2) {
-            m3ok = mbar_wait(bar_m3, m3_phase, kWaitNs);
-            if (m3ok) {
+            // O = (Q S) diag(e^G rq) + P U' of this chunk (q-row lanes), while
+            // the next chunk's MMA1 runs
+            if (qrow) {
+                if (!warp_wait(m3, par, abort_flag)) break;
                 tc_fence_after();
                 bf16* o = static_cast<bf16*>(a.o) + ((t0 + lrow) * a.H_v + h) * D + v0 + c0;
 #pragma unroll
@@ -876,35 +909,22 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                         store16(o + h16 + 8, po + 8);
                     }
                 }
+                warp_arrive(o_done, lane);
             }
         }
-        m3_phase ^= 1;
-        if (tid == 0 && m3ok) {
-            m3_pending = false;
-            if (gcc + 2 < c_hi) issue(gcc + 2);
-        }
-        tc_fence_before();
-        ok_local = m3ok;
-    }
-    ok = __syncthreads_and(ok && ok_local);
-
-    if (ok) {
-        float* dst = a.S_final != nullptr ? a.S_final : w.carry;
-        if (dst != nullptr) {
-            float* p = dst + sbase + (int64_t)lrow * D + v0 + c0;
+        if (!*abort_flag) {
+            float* dst = a.S_final != nullptr ? a.S_final : w.carry;
+            if (dst != nullptr) {
+                float* p = dst + sbase + (int64_t)lrow * D + v0 + c0;
 #pragma unroll
-            for (int q = 0; q < CV; q += 4)
-                *reinterpret_cast<float4*>(p + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
+                for (int q = 0; q < CV; q += 4)
+                    *reinterpret_cast<float4*>(p + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
+            }
         }
-    } else if (tid == 0) {
-        atomicOr(&g_device_error, 1);
-        if (m1_pending) mbar_wait(bar_m1, m1_phase, kWaitNs);
-        if (m3_pending) mbar_wait(bar_m3, m3_parity, kWaitNs);
-        for (int k = consumed0; k < issued0; ++k) mbar_wait(&bar_tma[0], (uint32_t)(k & 1), kWaitNs);
-        for (int k = consumed1; k < issued1; ++k) mbar_wait(&bar_tma[1], (uint32_t)(k & 1), kWaitNs);
     }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && *abort_flag) atomicOr(&g_device_error, 1);
     if (warp == 0) tmem_dealloc(tb, Ly::T_COLS);
 }
 
