@@ -609,16 +609,21 @@ struct ChainLayout {
     static constexpr int SG_P = 32768;                  // P; K follows, as the padded P operand's rows 64-127
     static constexpr int SG_K = SG_P + 8192;
     static constexpr int SG_UT = SG_K + 16384;          // U^T rows of the slice, [VS][64]
-    static constexpr int SG_VEC = SG_UT + VS * 128;
-    static constexpr int STAGE = SG_VEC + 1024;
+    static constexpr int STAGE = SG_UT + VS * 128;
+    static constexpr int NST = VS == 64 ? 3 : 2;        // stages in the ring
+    static constexpr int VEC = 528;                     // bytes of a chunk's vectors copied (129 floats used)
     static constexpr int CS_S = 0;                      // S [d][v] bf16, NB blocks of 16 KB
     static constexpr int CS_STAGE = CS_S + NB * 16384;
-    static constexpr int CS_UP = CS_STAGE + 2 * STAGE;  // U' [j][v] bf16, NB blocks of 8 KB
+    static constexpr int CS_UP = CS_STAGE + NST * STAGE;  // U' [j][v] bf16, NB blocks of 8 KB
     static constexpr int CS_UD = CS_UP + NB * 8192;     // U' diag(e^{G_n-G_j} rk)
-    static constexpr int CS_BAR = CS_UD + NB * 8192;
-    static constexpr int SMEM = CS_BAR + 128 + 1024;
-    // TMEM: two buffers of [Q S; W S], then dS, then P U'
-    static constexpr uint32_t T_QW = 0, T_DS = 2 * VS, T_OP = 3 * VS, T_COLS = 4 * VS;
+    static constexpr int CS_VEC = CS_UD + NB * 8192;    // the stages' vectors, NST x VEC
+    static constexpr int CS_BAR = CS_VEC + NST * VEC;
+    static constexpr int SMEM = CS_BAR + 128 + 1024;    // 15 barrier / flag words
+    // TMEM: two buffers of [Q S; W S], dS, and OPB buffers of P U' (two when they
+    // fit: the next chunk's P U' then needs no wait for this chunk's O epilogue)
+    static constexpr int OPB = 5 * VS <= 512 ? 2 : 1;
+    static constexpr uint32_t T_QW = 0, T_DS = 2 * VS, T_OP = 3 * VS;
+    static constexpr uint32_t T_COLS = (3 + OPB) * VS <= 256 ? 256 : 512;
     static_assert(SMEM <= 232448, "chain kernel shared memory");
 };
 
@@ -627,18 +632,21 @@ __device__ __forceinline__ void tmem_ldn(uint32_t taddr, float* v) {
     if constexpr (N == 16) tmem_ld16(taddr, v); else tmem_ld32(taddr, v);
 }
 
-// Bounded wait that also gives up once another role has given up.
+// Bounded wait that also gives up once another role has given up (the clock
+// and the flag are read every 32 polls).
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_test(bar, parity)) {
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitNs) {
-            *abort_flag = 1;
-            return false;
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test(bar, parity)) return true;
+        if ((it & 31) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitNs) {
+                *abort_flag = 1;
+                return false;
+            }
         }
     }
-    return true;
 }
 // every lane of the warp waits; the warp proceeds only if all lanes saw the phase
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -655,7 +663,7 @@ template <int VS>
 __global__ void __launch_bounds__(NT_C, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
                    const __grid_constant__ CUtensorMap utmap, const __grid_constant__ CUtensorMap pmap,
-                   DeltaArgs a, Work w, int64_t C0, int64_t segc) {
+                   const __grid_constant__ CUtensorMap omap, DeltaArgs a, Work w, int64_t C0, int64_t segc) {
     using Ly = ChainLayout<VS>;
     constexpr int NV = D / VS, CV = VS / 4;
     const int vp = blockIdx.x % NV;
@@ -685,24 +693,31 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    constexpr int NST = Ly::NST;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::CS_BAR);
-    uint64_t* full = bars;       // [2] stage landed (TMA)
-    uint64_t* empty = bars + 2;  // [2] stage consumed (tcgen05.commit after P U')
-    uint64_t* m1 = bars + 4;     // [Q S; W S] done
-    uint64_t* m2 = bars + 5;     // dS done
-    uint64_t* m3 = bars + 6;     // P U' done
-    uint64_t* s_rdy = bars + 7;  // S operand written (16 compute warps)
-    uint64_t* u_rdy = bars + 8;  // U' operands written, stage reads done (16 compute warps)
-    uint64_t* o_done = bars + 9; // O epilogue's TMEM reads done (8 q-row warps)
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 11);
+    uint64_t* full = bars;        // [NST] stage landed (TMA)
+    uint64_t* empty = bars + 3;   // [NST] stage consumed: tcgen05.commit after P U', and the O store has read it
+    uint64_t* m1 = bars + 6;      // [Q S; W S] done
+    uint64_t* m2 = bars + 7;      // dS done
+    uint64_t* m3 = bars + 8;      // P U' done
+    uint64_t* s_rdy = bars + 9;   // S operand written (16 compute warps)
+    uint64_t* u_rdy = bars + 10;  // U' operands written, stage reads done (16 compute warps)
+    uint64_t* o_done = bars + 11; // [2] O epilogue's TMEM reads of a P U' buffer done (8 q-row warps)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 13);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14);
+    auto stage_of = [&](int k) { return sm + Ly::CS_STAGE + (k % NST) * Ly::STAGE; };
+    auto vec_of = [&](int k) { return sm + Ly::CS_VEC + (k % NST) * Ly::VEC; };
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
-        for (int i = 4; i < 7; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 2);
+        }
+        for (int i = 6; i < 9; ++i) mbar_init(&bars[i], 1);
         mbar_init(s_rdy, NT_COMP / 32);
         mbar_init(u_rdy, NT_COMP / 32);
-        mbar_init(o_done, NT_COMP / 64);
+        mbar_init(&o_done[0], NT_COMP / 64);
+        mbar_init(&o_done[1], NT_COMP / 64);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -720,13 +735,13 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         if (lane == 0) {
             int issued = 0;  // stages issued
             for (int k = 0; k < nch; ++k) {
-                const int b = k & 1;
-                if (k >= 2 && !mbar_wait_or_abort(&empty[b], (uint32_t)(((k >> 1) - 1) & 1), abort_flag)) break;
+                const int b = k % NST;
+                if (k >= NST && !mbar_wait_or_abort(&empty[b], (uint32_t)((k / NST - 1) & 1), abort_flag)) break;
                 const int64_t gcc = c_lo + k;
-                uint8_t* st = sm + Ly::CS_STAGE + b * Ly::STAGE;
+                uint8_t* st = stage_of(k);
                 const int y = (int)(s0 + (gcc - cs) * C);
                 const int64_t uu = (gcc - C0) * a.H_v + h;
-                mbar_arrive_expect_tx(&full[b], Ly::STAGE);
+                mbar_arrive_expect_tx(&full[b], Ly::STAGE + Ly::VEC);
                 tma_load_2d(st + Ly::SG_QW, &qmap, &full[b], xq, y);
                 tma_load_2d(st + Ly::SG_QW + 8192, &wmap, &full[b], 0, (int)(uu * 64));
                 tma_load_2d(st + Ly::SG_QW + 16384, &qmap, &full[b], xq + 64, y);
@@ -735,13 +750,13 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 tma_load_2d(st + Ly::SG_K, &qmap, &full[b], xk, y);
                 tma_load_2d(st + Ly::SG_K + 8192, &qmap, &full[b], xk + 64, y);
                 tma_load_2d(st + Ly::SG_UT, &utmap, &full[b], 0, (int)(uu * 128 + v0));
-                bulk_load(st + Ly::SG_VEC, w.vec + uu * (int64_t)(U_VEC / 4), (uint32_t)U_VEC, &full[b]);
+                bulk_load(vec_of(k), w.vec + uu * (int64_t)(U_VEC / 4), (uint32_t)Ly::VEC, &full[b]);
                 issued = k + 1;
             }
             // on abort: let the copies in flight land before the CTA exits
             if (*abort_flag)
-                for (int k = issued - 2 > 0 ? issued - 2 : 0; k < issued; ++k)
-                    mbar_wait(&full[k & 1], (uint32_t)((k >> 1) & 1), kWaitNs);
+                for (int k = issued - NST > 0 ? issued - NST : 0; k < issued; ++k)
+                    mbar_wait(&full[k % NST], (uint32_t)((k / NST) & 1), kWaitNs);
         }
     } else if (warp == W_MMA) {
         // ------------------------------------------------ MMA issuer (lane 0)
@@ -751,10 +766,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             uint64_t* last = nullptr;  // the last commit, for the drain on abort
             uint32_t last_parity = 0;
             for (int k = 0; k < nch; ++k) {
-                const int b = k & 1;
+                const int b = k & 1;  // TMEM buffers
                 const uint32_t par = (uint32_t)(k & 1);
-                const uint32_t st = smem_u32(sm + Ly::CS_STAGE + b * Ly::STAGE);
-                if (!mbar_wait_or_abort(&full[b], (uint32_t)((k >> 1) & 1), abort_flag)) break;
+                const uint32_t st = smem_u32(stage_of(k));
+                if (!mbar_wait_or_abort(&full[k % NST], (uint32_t)((k / NST) & 1), abort_flag)) break;
                 if (!mbar_wait_or_abort(s_rdy, par, abort_flag)) break;
                 tc_fence_after();
 #pragma unroll
@@ -773,14 +788,18 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                              sdesc_sw128(bud + q * 2048, 8192, 1024), idesc_bf16_f32(128, VS, 1, 1), q > 0);
                 mma_commit(m2);
                 last = m2;
-                if (k > 0 && !mbar_wait_or_abort(o_done, par ^ 1u, abort_flag)) break;
+                // P U' into buffer ob once the O epilogue of its previous use is done
+                const int ob = Ly::OPB == 2 ? b : 0;
+                if (k >= Ly::OPB &&
+                    !mbar_wait_or_abort(&o_done[ob], (uint32_t)(((k / Ly::OPB) - 1) & 1), abort_flag))
+                    break;
                 tc_fence_after();
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    mma_bf16(tb + Ly::T_OP, sdesc_sw128(st + Ly::SG_P + q * 32, 16, 1024),
+                    mma_bf16(tb + Ly::T_OP + VS * ob, sdesc_sw128(st + Ly::SG_P + q * 32, 16, 1024),
                              sdesc_sw128(bup + q * 2048, 8192, 1024), idesc_bf16_f32(128, VS, 0, 1), q > 0);
                 mma_commit(m3);
-                mma_commit(&empty[b]);
+                mma_commit(&empty[k % NST]);
                 last = m3;
             }
             if (*abort_flag && last != nullptr) mbar_wait(last, last_parity, kWaitNs);
@@ -822,16 +841,16 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         }
 
         for (int k = 0; k < nch; ++k) {
-            const int b = k & 1;
+            const int b = k & 1;  // TMEM buffers
             const uint32_t par = (uint32_t)(k & 1);
-            const uint8_t* st = sm + Ly::CS_STAGE + b * Ly::STAGE;
-            const float* vs = reinterpret_cast<const float*>(st + Ly::SG_VEC);
+            uint8_t* st = stage_of(k);
+            const float* vs = reinterpret_cast<const float*>(vec_of(k));
             const int64_t gcc = c_lo + k;
             const int64_t lc = gcc - cs;
             const int64_t t0 = s0 + lc * C;
             const int n = (int)(L - lc * C < C ? L - lc * C : C);
 
-            if (!warp_wait(&full[b], (uint32_t)((k >> 1) & 1), abort_flag)) break;
+            if (!warp_wait(&full[k % NST], (uint32_t)((k / NST) & 1), abort_flag)) break;
             if (!warp_wait(m1, par, abort_flag)) break;
             tc_fence_after();
             // everything this chunk needs from its stage is read before u_rdy:
@@ -891,25 +910,44 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             warp_arrive(s_rdy, lane);
 
             // O = (Q S) diag(e^G rq) + P U' of this chunk (q-row lanes), while
-            // the next chunk's MMA1 runs
+            // the next chunk's MMA1 runs.  A full chunk's O tile is staged in
+            // the stage's consumed P | K region and written by TMA stores;
+            // the last, partial chunk of a sequence is stored row by row.
             if (qrow) {
                 if (!warp_wait(m3, par, abort_flag)) break;
                 tc_fence_after();
+                uint8_t* ostg = st + Ly::SG_P + (c0 >> 6) * 8192;
                 bf16* o = static_cast<bf16*>(a.o) + ((t0 + lrow) * a.H_v + h) * D + v0 + c0;
 #pragma unroll
                 for (int h16 = 0; h16 < CV; h16 += 16) {
                     float qs[16], po[16];
                     tmem_ld16(tb + lo + Ly::T_QW + VS * b + c0 + h16, qs);
-                    tmem_ld16(tb + lo + Ly::T_OP + c0 + h16, po);
+                    tmem_ld16(tb + lo + Ly::T_OP + VS * (Ly::OPB == 2 ? b : 0) + c0 + h16, po);
                     tmem_wait_ld();
 #pragma unroll
                     for (int q = 0; q < 16; ++q) po[q] = fmaf(erq, qs[q], po[q]);
-                    if (lrow < n) {
+                    if (n == C) {
+                        store_row_bf16(ostg, lrow, cb + h16, po, 16);
+                    } else if (lrow < n) {
                         store16(o + h16, po);
                         store16(o + h16 + 8, po + 8);
                     }
                 }
-                warp_arrive(o_done, lane);
+                fence_async_smem();
+                const int ob = Ly::OPB == 2 ? b : 0;
+                warp_arrive(&o_done[ob], lane);
+                // thread 0 stores the tile once all 8 q-row warps have staged it
+                if (tid == 0 && mbar_wait_or_abort(&o_done[ob], (uint32_t)((k / Ly::OPB) & 1), abort_flag)) {
+                    if (n == C) {
+                        uint8_t* otile = st + Ly::SG_P;
+#pragma unroll
+                        for (int nb = 0; nb < Ly::NB; ++nb)
+                            tma_store_2d(&omap, otile + nb * 8192, h * D + v0 + 64 * nb, (int)t0);
+                        bulk_commit();
+                        bulk_wait_read_all();
+                    }
+                    mbar_arrive(&empty[k % NST]);
+                }
             }
         }
         if (!*abort_flag) {
@@ -922,6 +960,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             }
         }
     }
+    if (tid == 0) bulk_wait_all();  // O stores complete before the CTA exits
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && *abort_flag) atomicOr(&g_device_error, 1);
@@ -980,9 +1019,10 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
     const uint64_t U = (uint64_t)Ly.segc * a.H_v;
     const bool split = (int64_t)a.n_seq * a.H_v * 2 <= sm_count();
     const uint32_t vs = split ? 64 : 128;
-    CUtensorMap qmap, wtmap, utmap, pmap;
+    CUtensorMap qmap, wtmap, utmap, pmap, omap;
     if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) || !encode2d(&wtmap, w.wt, 128, U * 64, 64, 64) ||
-        !encode2d(&utmap, w.ut, 64, U * 128, 64, vs) || !encode2d(&pmap, w.p, 64, U * 64, 64, 64))
+        !encode2d(&utmap, w.ut, 64, U * 128, 64, vs) || !encode2d(&pmap, w.p, 64, U * 64, 64, 64) ||
+        !encode2d(&omap, a.o, (uint64_t)a.H_v * D, (uint64_t)a.T, 64, 64))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
     if (e == cudaSuccess)
@@ -1000,10 +1040,10 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
         chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, s>>>(qmap, wtmap, a, w, C0);
         if (split)
             chunk_chain_kernel<64><<<(unsigned)(a.n_seq * a.H_v * 2), NT_C, ChainLayout<64>::SMEM, s>>>(
-                qmap, wtmap, utmap, pmap, a, w, C0, Ly.segc);
+                qmap, wtmap, utmap, pmap, omap, a, w, C0, Ly.segc);
         else
             chunk_chain_kernel<128><<<(unsigned)(a.n_seq * a.H_v), NT_C, ChainLayout<128>::SMEM, s>>>(
-                qmap, wtmap, utmap, pmap, a, w, C0, Ly.segc);
+                qmap, wtmap, utmap, pmap, omap, a, w, C0, Ly.segc);
     }
     return cudaGetLastError();
 }
