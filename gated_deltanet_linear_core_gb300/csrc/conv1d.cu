@@ -8,21 +8,28 @@
 // Summary: convolution state checkpoints for hybrid prefix caching.
 //
 // The conv is HBM-bound (about 4 bytes of traffic per bf16 channel-token and
-// 4 FMAs).  Each thread owns one 16-byte channel vector (8 bf16 or 4 f32
-// channels) of a run of kTok tokens.  A run inside one sequence issues all of
-// its kTok + 3 row loads at once (the 3 halo rows are the previous run's last
-// rows, mostly L2 hits) and then writes kTok outputs, so every thread has one
-// memory round trip; coalesced 128-bit accesses (a warp covers 512 contiguous
-// bytes of a token row).  Runs that touch a sequence start take the general
-// path, which walks the tokens with the three previous inputs in registers.
+// 4 FMAs).  A CTA takes a tile of 64 tokens x 512 bytes of channels: one TMA
+// copy brings the tile and its 3-token halo (negative rows read as zeros)
+// into shared memory, so x is read 67/64 times; each thread then owns one
+// 16-byte channel vector (8 bf16 or 4 f32 channels) of 8 tokens and writes
+// them with coalesced 128-bit stores (a warp covers a 512-byte token row).
+// Inputs before a sequence's first token come from its conv state (or are
+// zero), not from the tile.
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
+#include "tc_ptx.cuh"
 
 namespace gdn {
+
+__device__ int g_conv_error;  // bit 0: a bounded wait gave up
+
 namespace {
 
-constexpr int kTok = 8;       // tokens per thread
-constexpr int kThreads = 128;
+constexpr int kThreads = 128;  // decode and state kernels
+constexpr int kTT = 64;        // tokens per tile
+constexpr int kRowBytes = 512;  // bytes of channels per tile row
+constexpr int kTileThreads = 256;
+constexpr uint64_t kConvWaitNs = 1000000000ull;
 
 template <typename T>
 __device__ __forceinline__ void load_state_col(const T* __restrict__ st, int64_t seq, int C, int c0,
@@ -30,6 +37,27 @@ __device__ __forceinline__ void load_state_col(const T* __restrict__ st, int64_t
     constexpr int V = Vec16<T>::N;
 #pragma unroll
     for (int e = 0; e < V; ++e) dst[e] = to_f(st[((int64_t)seq * C + c0 + e) * 3 + col]);
+}
+
+// One 16-byte vector of outputs from the inputs at t-3..t, channel pairs in
+// packed f32x2 arithmetic (same products and order as the scalar form).
+template <typename T>
+__device__ __forceinline__ void conv_out2(const float2 (&w)[Vec16<T>::N / 2][4], const float* x0,
+                                          const float* x1, const float* x2, const float* x3, int silu,
+                                          T* __restrict__ dst) {
+    constexpr int P = Vec16<T>::N / 2;
+    float out[2 * P];
+#pragma unroll
+    for (int k = 0; k < P; ++k) {
+        float2 acc = __fmul2_rn(w[k][0], make_float2(x0[2 * k], x0[2 * k + 1]));
+        acc = __ffma2_rn(w[k][1], make_float2(x1[2 * k], x1[2 * k + 1]), acc);
+        acc = __ffma2_rn(w[k][2], make_float2(x2[2 * k], x2[2 * k + 1]), acc);
+        acc = __ffma2_rn(w[k][3], make_float2(x3[2 * k], x3[2 * k + 1]), acc);
+        if (silu) acc = silu2<T>(acc);
+        out[2 * k] = acc.x;
+        out[2 * k + 1] = acc.y;
+    }
+    store16(dst, out);
 }
 
 template <typename T>
@@ -50,49 +78,67 @@ __device__ __forceinline__ void conv_out(const float (&w)[Vec16<T>::N][4], const
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads) conv1d_fwd_kernel(ConvArgs a) {
+__global__ void __launch_bounds__(kTileThreads, 3) conv1d_fwd_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                  ConvArgs a) {
     constexpr int V = Vec16<T>::N;
-    const int nvec = a.C / V;
-    const int cv = blockIdx.y * blockDim.x + threadIdx.x;
-    if (cv >= nvec) return;
+    constexpr int TC = kRowBytes / (int)sizeof(T);  // channels per tile
+    __shared__ alignas(128) uint8_t tile[(kTT + 3) * kRowBytes];
+    __shared__ alignas(8) uint64_t bar;
+    const int tid = threadIdx.x, cg = tid & 31, tg = tid >> 5;
+    const int64_t t0 = (int64_t)blockIdx.x * kTT;
+    const int cbase = blockIdx.y * TC;
+    if (tid == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+        tc::mbar_arrive_expect_tx(&bar, (kTT + 3) * kRowBytes);
+        tc::tma_load_2d(tile, &xmap, &bar, cbase, (int)(t0 - 3));  // row r of the tile = token t0 - 3 + r
+    }
+    __syncthreads();
+    // while the copy is in flight: weights and the sequence of the first token
     const int C = a.C;
-    const int c0 = cv * V;
-    const T* __restrict__ x = static_cast<const T*>(a.x);
-    const T* __restrict__ st = static_cast<const T*>(a.state_in);
-    T* __restrict__ y = static_cast<T*>(a.y);
-
-    float w[V][4];
-    {
+    const int c0 = cbase + cg * V;
+    const bool cv = c0 < C;
+    float2 w[V / 2][4];  // (channel 2k, channel 2k + 1) x tap
+    if (cv) {
         const T* wp = static_cast<const T*>(a.w) + (int64_t)c0 * 4;
         float tmp[4 * V];
 #pragma unroll
         for (int i = 0; i < 4; ++i) load16(wp + i * V, tmp + i * V);
 #pragma unroll
-        for (int e = 0; e < V; ++e)
+        for (int k = 0; k < V / 2; ++k)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) w[e][j] = tmp[e * 4 + j];
+            for (int j = 0; j < 4; ++j) w[k][j] = make_float2(tmp[(2 * k) * 4 + j], tmp[(2 * k + 1) * 4 + j]);
     }
-
-    const int64_t t0 = (int64_t)blockIdx.x * kTok;
-    const int64_t t1 = t0 + kTok < a.T ? t0 + kTok : a.T;
-    int seq = seq_of_token(a.cu, a.n_seq, t0);
-    int64_t s, e;
-    seq_bounds(a.cu, seq, a.T, s, e);
-
-    if (t0 - 3 >= s && t0 + kTok <= e) {
-        // the run and its halo lie inside one sequence: one round trip
-        uint4 raw[kTok + 3];
-#pragma unroll
-        for (int j = 0; j < kTok + 3; ++j)
-            raw[j] = __ldg(reinterpret_cast<const uint4*>(x + (t0 - 3 + j) * C + c0));
+    const int64_t tb = t0 + 8 * tg;
+    const int64_t te = tb + 8 < a.T ? tb + 8 : a.T;
+    int seq = 0;
+    int64_t s = 0, e = a.T;
+    if (tb < a.T) {
+        seq = seq_of_token(a.cu, a.n_seq, tb);
+        seq_bounds(a.cu, seq, a.T, s, e);
+    }
+    const bool landed = tc::mbar_wait(&bar, 0, kConvWaitNs);
+    if (!landed) {
+        if (tid == 0) atomicOr(&g_conv_error, 1);
+        return;
+    }
+    if (!cv || tb >= a.T) return;
+    const T* st = static_cast<const T*>(a.state_in);
+    T* __restrict__ y = static_cast<T*>(a.y);
+    auto row = [&](int64_t p, float* dst) {  // input of token p (p >= t0 - 3) from the tile
+        unpack16<T>(*reinterpret_cast<const uint4*>(tile + (p - t0 + 3) * kRowBytes + cg * 16), dst);
+    };
+    if (tb - 3 >= s && te <= e) {
+        // the run and its halo lie inside one sequence
         float r0[V], r1[V], r2[V], r3[V];
-        unpack16<T>(raw[0], r0);
-        unpack16<T>(raw[1], r1);
-        unpack16<T>(raw[2], r2);
+        row(tb - 3, r0);
+        row(tb - 2, r1);
+        row(tb - 1, r2);
 #pragma unroll
-        for (int j = 0; j < kTok; ++j) {
-            unpack16<T>(raw[j + 3], r3);
-            conv_out<T>(w, r0, r1, r2, r3, a.silu, y + (t0 + j) * C + c0);
+        for (int j = 0; j < 8; ++j) {
+            if (tb + j >= te) break;
+            row(tb + j, r3);
+            conv_out2<T>(w, r0, r1, r2, r3, a.silu, y + (tb + j) * C + c0);
 #pragma unroll
             for (int q = 0; q < V; ++q) {
                 r0[q] = r1[q];
@@ -102,62 +148,26 @@ __global__ void __launch_bounds__(kThreads) conv1d_fwd_kernel(ConvArgs a) {
         }
         return;
     }
-
-    float win[3][V];  // inputs at t-3, t-2, t-1
-    bool need_init = true;
-    int64_t t = t0;
-    while (t < t1) {
+    // a sequence starts inside the run or its halo
+    for (int64_t t = tb; t < te; ++t) {
         while (t >= e && seq + 1 < a.n_seq) {
             ++seq;
             seq_bounds(a.cu, seq, a.T, s, e);
-            need_init = true;
         }
-        if (need_init) {
-            const int64_t ss = s < t ? s : t;  // clamp (only differs for invalid offsets)
+        float in[4][V];
 #pragma unroll
-            for (int j = 1; j <= 3; ++j) {
-                float* dst = win[3 - j];
-                const int64_t p = t - j;
-                if (p >= ss) {
-                    load16(x + p * C + c0, dst);
-                } else if (st != nullptr) {
-                    load_state_col(st, seq, C, c0, (int)(3 - (ss - p)), dst);
-                } else {
+        for (int m = 0; m < 4; ++m) {
+            const int64_t p = t - 3 + m;
+            if (p >= s) {
+                row(p, in[m]);
+            } else if (st != nullptr) {
+                load_state_col(st, seq, C, c0, (int)(3 - (s - p)), in[m]);
+            } else {
 #pragma unroll
-                    for (int q = 0; q < V; ++q) dst[q] = 0.f;
-                }
+                for (int q = 0; q < V; ++q) in[m][q] = 0.f;
             }
-            need_init = false;
         }
-        const int64_t lim = e < t1 ? e : t1;
-        if (t + 4 <= lim) {
-            // four tokens inside one sequence: issue the loads together
-            float c[4][V];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) load16_stream(x + (t + u) * C + c0, c[u]);
-            conv_out<T>(w, win[0], win[1], win[2], c[0], a.silu, y + t * C + c0);
-            conv_out<T>(w, win[1], win[2], c[0], c[1], a.silu, y + (t + 1) * C + c0);
-            conv_out<T>(w, win[2], c[0], c[1], c[2], a.silu, y + (t + 2) * C + c0);
-            conv_out<T>(w, c[0], c[1], c[2], c[3], a.silu, y + (t + 3) * C + c0);
-#pragma unroll
-            for (int q = 0; q < V; ++q) {
-                win[0][q] = c[1][q];
-                win[1][q] = c[2][q];
-                win[2][q] = c[3][q];
-            }
-            t += 4;
-        } else {
-            float c[V];
-            load16_stream(x + t * C + c0, c);
-            conv_out<T>(w, win[0], win[1], win[2], c, a.silu, y + t * C + c0);
-#pragma unroll
-            for (int q = 0; q < V; ++q) {
-                win[0][q] = win[1][q];
-                win[1][q] = win[2][q];
-                win[2][q] = c[q];
-            }
-            t += 1;
-        }
+        conv_out2<T>(w, in[0], in[1], in[2], in[3], a.silu, y + t * C + c0);
     }
 }
 
@@ -263,11 +273,25 @@ __global__ void __launch_bounds__(kThreads) conv1d_update_kernel(const T* __rest
 template <typename T>
 cudaError_t conv_fwd_t(const ConvArgs& a, cudaStream_t s) {
     constexpr int V = Vec16<T>::N;
+    constexpr int TC = kRowBytes / (int)sizeof(T);
     const int nvec = a.C / V;
     const dim3 blk(kThreads);
     if (a.T > 0) {
-        const dim3 grid((unsigned)((a.T + kTok - 1) / kTok), (nvec + kThreads - 1) / kThreads);
-        conv1d_fwd_kernel<T><<<grid, blk, 0, s>>>(a);
+        // x as a [T][C] tensor; a box is one tile with its halo
+        const PFN_cuTensorMapEncodeTiled_v12000 enc = tensormap_encoder();
+        if (enc == nullptr) return cudaErrorNotSupported;
+        CUtensorMap xmap;
+        cuuint64_t gdim[2] = {(cuuint64_t)a.C, (cuuint64_t)a.T};
+        cuuint64_t gstr[1] = {(cuuint64_t)a.C * sizeof(T)};
+        cuuint32_t box[2] = {(cuuint32_t)TC, (cuuint32_t)(kTT + 3)};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&xmap, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                const_cast<void*>(a.x), gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        const dim3 grid((unsigned)((a.T + kTT - 1) / kTT), (unsigned)((a.C + TC - 1) / TC));
+        conv1d_fwd_kernel<T><<<grid, kTileThreads, 0, s>>>(xmap, a);
     }
     if (a.state_out != nullptr || (a.ckpt_every > 0 && a.ckpt != nullptr)) {
         const dim3 grid2((unsigned)a.n_seq, (nvec + kThreads - 1) / kThreads);
@@ -277,6 +301,20 @@ cudaError_t conv_fwd_t(const ConvArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t read_and_clear_conv_error(cudaStream_t s, int* flags) {
+    int hf = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&hf, g_conv_error, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    *flags = hf;
+    if (hf != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_conv_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
+}
 
 cudaError_t launch_conv1d_fwd(const ConvArgs& a, gdn_dtype_t dt, cudaStream_t s) {
     return dt == GDN_BF16 ? conv_fwd_t<bf16>(a, s) : conv_fwd_t<float>(a, s);

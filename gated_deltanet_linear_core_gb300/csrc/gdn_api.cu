@@ -118,10 +118,11 @@ gdn_status_t gdn_check_cu_seqlens(const int32_t* cu, int32_t n_seq, int64_t T, v
 }
 
 gdn_status_t gdn_sync_status(void* stream) {
-    int flags = 0;
+    int flags = 0, cflags = 0;
     cudaError_t e = gdn::read_and_clear_device_error((cudaStream_t)stream, &flags);
+    if (e == cudaSuccess) e = gdn::read_and_clear_conv_error((cudaStream_t)stream, &cflags);
     if (e != cudaSuccess) return cuda_status(e);
-    return (flags & 1) ? GDN_ERR_TIMEOUT : GDN_OK;
+    return ((flags | cflags) & 1) ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
 gdn_status_t gdn_conv1d_fwd(const void* x, const void* w, const int32_t* cu_seqlens, int32_t n_seq,

@@ -74,6 +74,24 @@ __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x));
 __device__ __forceinline__ float silu_fast(float x) {
     return __fdividef(x, 1.0f + __expf(fminf(-x, 80.0f)));
 }
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// SiLU of a pair as x sigma(x) = h (1 + tanh h), h = x / 2, with the hardware
+// tanh (one special-function op per element; its relative error, a few 1e-4 at
+// most, is below bf16 rounding, so this is used where the result is bf16).
+__device__ __forceinline__ float2 silu2_tanh(float2 x) {
+    const float2 h = __fmul2_rn(x, make_float2(0.5f, 0.5f));
+    return __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
+}
+// SiLU of a pair: the tanh form for bf16 results, the exponential form for f32.
+template <typename T>
+__device__ __forceinline__ float2 silu2(float2 x) {
+    if constexpr (sizeof(T) == 2) return silu2_tanh(x);
+    else return make_float2(silu_fast(x.x), silu_fast(x.y));
+}
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 // softplus with the identity branch above 20 (cortex unit test "softplus small/large branches")
 __device__ __forceinline__ float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }

@@ -73,6 +73,8 @@ cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s);
 
 // Reads (synchronising `s`) and clears the library's device error word.
 cudaError_t read_and_clear_device_error(cudaStream_t s, int* flags);
+// The same for the conv kernels' own error word.
+cudaError_t read_and_clear_conv_error(cudaStream_t s, int* flags);
 
 cudaError_t launch_rmsnorm_gated(const void* o, const void* z, const void* w, float eps, int64_t T,
                                  int H, int D, void* out, gdn_dtype_t dt, cudaStream_t s);

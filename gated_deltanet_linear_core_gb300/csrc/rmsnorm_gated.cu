@@ -37,15 +37,27 @@ __global__ void __launch_bounds__(256) rmsnorm_gated_kernel(const T* o,  // may 
         for (int i = 0; i < V; ++i) ov[i] = zv[i] = 0.f;
     }
     load16(w + c0, wv);
-    float ss = 0.f;
+    // channel pairs in packed f32x2 arithmetic
+    float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < V; ++i) ss = fmaf(ov[i], ov[i], ss);
+    for (int i = 0; i < V; i += 2) {
+        const float2 o2 = make_float2(ov[i], ov[i + 1]);
+        ss2 = __ffma2_rn(o2, o2, ss2);
+    }
+    float ss = ss2.x + ss2.y;
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float rs = rsqrtf(ss / (float)D + eps);
     float res[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) res[i] = wv[i] * (ov[i] * rs) * silu_fast(zv[i]);
+    for (int i = 0; i < V; i += 2) {
+        const float2 g = silu2<T>(make_float2(zv[i], zv[i + 1]));
+        const float2 r = __fmul2_rn(__fmul2_rn(make_float2(wv[i], wv[i + 1]),
+                                               __fmul2_rn(make_float2(ov[i], ov[i + 1]), make_float2(rs, rs))),
+                                    g);
+        res[i] = r.x;
+        res[i + 1] = r.y;
+    }
     if (valid) store16(out + row * D + c0, res);
 }
 
