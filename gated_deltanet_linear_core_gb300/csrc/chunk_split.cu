@@ -49,7 +49,7 @@ constexpr size_t CMETA_BYTES = 16;  // per chunk of a segment
 
 struct Work {
     bf16* wt;       // W, [U][64][128] (row i of W = 128 d-values)
-    bf16* ut;       // [U][128][64]
+    bf16* ut;       // U, [U][64][128] (row i of U = 128 v-values)
     bf16* p;        // [U][64][64]
     float* vec;     // [U][256]: e^G rq (0..63), e^{G_n-G_j} rk (64..127), e^{G_n} (128)
     float* gb;      // [U][128]: G (log2 domain, 0..63), beta (64..127)
@@ -281,7 +281,7 @@ __device__ __forceinline__ float select_lane(const float (&v)[32], int lane) {
 
 __global__ void __launch_bounds__(NT_I, 3)
 chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
-                   DeltaArgs a, Work w, int64_t C0) {
+                   const __grid_constant__ CUtensorMap umap, DeltaArgs a, Work w, int64_t C0) {
     const int h = blockIdx.x;
     const int4 cm = w.cmeta[blockIdx.y];
     const int n = cm.z;
@@ -551,21 +551,30 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     if (ok) {
         mma_pending = false;
         tc_fence_after();
-        // W (row-major, staged 128B-swizzled in the consumed V tile, stored by
-        // TMA) and U^T rows (bf16, 32 columns per thread)
-        float v32[32];
-        tmem_ld32(tb + lo + TI_DW + 32 * half, v32);
-        tmem_wait_ld();
-        uint8_t* stg = vv + (row >> 6) * 8192;
-        const int dc = row & 63;
+        // W and U as row-major bf16 tiles for TMA stores: the accumulators
+        // (lanes = d, columns = i) are read in the 16x256b shape, whose
+        // fragments stmatrix.trans writes transposed -- 16 bytes of a row at a
+        // time -- into 128-byte-swizzled staging tiles (W in the consumed V
+        // tile, U in the consumed B_W | B_U region).  Warp (quarter, half):
+        // d in [32 quarter, +32), i in [32 half, +32).
+        const int mk = lane >> 3, mr = lane & 7;  // this thread's row address: matrix mk, row mr
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-            *reinterpret_cast<bf16*>(stg + sw128_off(32 * half + q, dc)) = __float2bfloat16_rn(v32[q]);
-        tmem_ld32(tb + lo + TI_DU + 32 * half, v32);
-        tmem_wait_ld();
-        bf16* dst = w.ut + u * (U_UT / 2) + row * 64 + 32 * half;
+        for (int acc = 0; acc < 2; ++acc) {
+            uint8_t* stg = acc == 0 ? vv : sm + IS_A;
+            const uint32_t col = (acc == 0 ? TI_DW : TI_DU) + 32 * half;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) store16(dst + 8 * g, v32 + 8 * g);
+            for (int q = 0; q < 4; ++q) {
+                const int d0 = 32 * quarter + 16 * (q & 1), i0 = 32 * half + 16 * (q >> 1);
+                uint32_t r[8], p[4];
+                tmem_ld16x256b_x2(tb + ((uint32_t)d0 << 16) + col + 16 * (q >> 1), r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) p[k] = pack_bf16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+                // matrices: 0 (d0.., i0..), 1 (d0+8.., i0..), 2 (d0.., i0+8..), 3 (d0+8.., i0+8..)
+                const int ri = i0 + 8 * (mk >> 1) + mr, rd = d0 + 8 * (mk & 1);
+                stmatrix_x4_trans(stg + (rd >> 6) * 8192 + sw128_off(ri, rd & 63), p);
+            }
+        }
         fence_async_smem();
     } else if (tid == 0) {
         atomicOr(&g_device_error, 1);
@@ -577,8 +586,10 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     if (ok && tid == 0) {
         tma_store_2d(&wmap, vv, 0, (int)(u * 64));
         tma_store_2d(&wmap, vv + 8192, 64, (int)(u * 64));
+        tma_store_2d(&umap, sm + IS_A, 0, (int)(u * 64));
+        tma_store_2d(&umap, sm + IS_A + 8192, 64, (int)(u * 64));
         bulk_commit();
-        bulk_wait_read_all();  // the staging tile must outlive the copy's reads
+        bulk_wait_read_all();  // the staging tiles must outlive the copies' reads
     }
     if (warp == 0) tmem_dealloc(tb, TI_COLS);
 }
@@ -608,7 +619,7 @@ struct ChainLayout {
     static constexpr int SG_QW = 0;                     // per 64-wide d block: Q rows | W rows (16 KB)
     static constexpr int SG_P = 32768;                  // P; K follows, as the padded P operand's rows 64-127
     static constexpr int SG_K = SG_P + 8192;
-    static constexpr int SG_UT = SG_K + 16384;          // U^T rows of the slice, [VS][64]
+    static constexpr int SG_UT = SG_K + 16384;          // U rows of the slice, NB blocks of [64][64]
     static constexpr int STAGE = SG_UT + VS * 128;
     static constexpr int NST = VS == 64 ? 3 : 2;        // stages in the ring
     static constexpr int VEC = 528;                     // bytes of a chunk's vectors copied (129 floats used)
@@ -749,7 +760,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 tma_load_2d(st + Ly::SG_P, &pmap, &full[b], 0, (int)(uu * 64));
                 tma_load_2d(st + Ly::SG_K, &qmap, &full[b], xk, y);
                 tma_load_2d(st + Ly::SG_K + 8192, &qmap, &full[b], xk + 64, y);
-                tma_load_2d(st + Ly::SG_UT, &utmap, &full[b], 0, (int)(uu * 128 + v0));
+#pragma unroll
+                for (int nb = 0; nb < Ly::NB; ++nb)
+                    tma_load_2d(st + Ly::SG_UT + nb * 8192, &utmap, &full[b], v0 + 64 * nb, (int)(uu * 64));
                 bulk_load(vec_of(k), w.vec + uu * (int64_t)(U_VEC / 4), (uint32_t)Ly::VEC, &full[b]);
                 issued = k + 1;
             }
@@ -858,18 +871,16 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             const float eGn = vs[128];
             float erq = 0.f;
             if (!qrow) {
-                // U' = U - W S for w row j (U from the U^T tile), and its copy
-                // scaled by e^{G_n-G_j} rk_j
+                // U' = U - W S for w row j, and its copy scaled by e^{G_n-G_j} rk_j
                 const int j = lrow - 64;
                 const float dj = vs[64 + j];
-                const uint8_t* ut = st + Ly::SG_UT;
+                const uint8_t* ut = st + Ly::SG_UT + (c0 >> 6) * 8192;
 #pragma unroll
                 for (int h16 = 0; h16 < CV; h16 += 16) {
                     float ws[16], up[16];
                     tmem_ld16(tb + lo + Ly::T_QW + VS * b + c0 + h16, ws);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        up[q] = __bfloat162float(*reinterpret_cast<const bf16*>(ut + sw128_off(c0 + h16 + q, j)));
+                    unpack16<bf16>(*reinterpret_cast<const uint4*>(ut + sw128_off(j, cb + h16)), up);
+                    unpack16<bf16>(*reinterpret_cast<const uint4*>(ut + sw128_off(j, cb + h16 + 8)), up + 8);
                     tmem_wait_ld();
 #pragma unroll
                     for (int q = 0; q < 16; ++q) up[q] -= ws[q];
@@ -1018,10 +1029,9 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
     const uint64_t conv_dim = 2ull * a.H_k * D + (uint64_t)a.H_v * D;
     const uint64_t U = (uint64_t)Ly.segc * a.H_v;
     const bool split = (int64_t)a.n_seq * a.H_v * 2 <= sm_count();
-    const uint32_t vs = split ? 64 : 128;
     CUtensorMap qmap, wtmap, utmap, pmap, omap;
     if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) || !encode2d(&wtmap, w.wt, 128, U * 64, 64, 64) ||
-        !encode2d(&utmap, w.ut, 64, U * 128, 64, vs) || !encode2d(&pmap, w.p, 64, U * 64, 64, 64) ||
+        !encode2d(&utmap, w.ut, 128, U * 64, 64, 64) || !encode2d(&pmap, w.p, 64, U * 64, 64, 64) ||
         !encode2d(&omap, a.o, (uint64_t)a.H_v * D, (uint64_t)a.T, 64, 64))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
@@ -1037,7 +1047,7 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
     for (int64_t seg = 0; seg < Ly.n_seg; ++seg) {
         const int64_t C0 = seg * Ly.segc;
         chunk_gates_kernel<<<dim3((unsigned)Ly.segc, (unsigned)((a.H_v + 31) / 32)), NT_G, 0, s>>>(a, w, C0);
-        chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, s>>>(qmap, wtmap, a, w, C0);
+        chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, s>>>(qmap, wtmap, utmap, a, w, C0);
         if (split)
             chunk_chain_kernel<64><<<(unsigned)(a.n_seq * a.H_v * 2), NT_C, ChainLayout<64>::SMEM, s>>>(
                 qmap, wtmap, utmap, pmap, omap, a, w, C0, Ly.segc);

@@ -169,6 +169,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 16 lanes x 256 bits, twice along the columns: thread t receives lane
+// (lane_base + t/4) at columns col + 2(t%4) + {0, 1} in v[0..1], lane
+// (lane_base + 8 + t/4) there in v[2..3], and the same 8 columns further in
+// v[4..7] -- the fragment layout of an 8x8-matrix store (stmatrix).
+__device__ __forceinline__ void tmem_ld16x256b_x2(uint32_t taddr, uint32_t* v) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                   "=r"(v[7])
+                 : "r"(taddr));
+}
+// Four 8x8 b16 matrices stored transposed: register k holds row t/4, columns
+// 2(t%4) and 2(t%4)+1 of matrix k; thread 8k + c gives the shared address of
+// row c of the transposed matrix k (16 contiguous bytes).
+__device__ __forceinline__ void stmatrix_x4_trans(void* row_addr, const uint32_t* r) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(row_addr)),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
