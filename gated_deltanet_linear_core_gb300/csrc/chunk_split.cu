@@ -43,27 +43,24 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr size_t kSegBytes = 128ull << 20;  // workspace intermediates per segment
 
 // per (chunk, value head) unit in the workspace
-constexpr size_t U_WT = 16384, U_UT = 16384, U_P = 8192, U_VEC = 1024, U_GB = 512;
-constexpr size_t UNIT_BYTES = U_WT + U_UT + U_P + U_VEC + U_GB;
-constexpr size_t CMETA_BYTES = 16;  // per chunk of a segment
+constexpr size_t U_WT = 16384, U_UT = 16384, U_P = 8192, U_VEC = 1024;
+constexpr size_t UNIT_BYTES = U_WT + U_UT + U_P + U_VEC;
 
 struct Work {
     bf16* wt;       // W, [U][64][128] (row i of W = 128 d-values)
     bf16* ut;       // U, [U][64][128] (row i of U = 128 v-values)
     bf16* p;        // [U][64][64]
     float* vec;     // [U][256]: e^G rq (0..63), e^{G_n-G_j} rk (64..127), e^{G_n} (128)
-    float* gb;      // [U][128]: G (log2 domain, 0..63), beta (64..127)
-    int4* cmeta;    // [segc]: first token (lo, hi), length (0: no such chunk)
     int32_t* coff;  // [n_seq + 1] chunk offsets
     float* carry;   // state between segments (final_state or workspace), may be null
 };
 
 // Segment size and the places of the intermediates inside one scratch area:
-// chunk offsets, chunk metadata, then the per-unit arrays, then the carry.
+// chunk offsets, then the per-unit arrays, then the carry.
 struct Layout {
     int64_t segc;    // chunks per segment
     int64_t n_seg;
-    size_t off_coff, off_cmeta, off_units, off_carry, carry_bytes, total;
+    size_t off_coff, off_units, off_carry, carry_bytes, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -73,15 +70,14 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 Layout layout_for(int n_seq, int64_t T, int H_v, size_t seg_bytes, size_t coff_slots, bool carry) {
     Layout L;
     const int64_t max_chunks = T / C + n_seq;
-    int64_t segc = (int64_t)(seg_bytes / ((size_t)H_v * UNIT_BYTES + CMETA_BYTES));
+    int64_t segc = (int64_t)(seg_bytes / ((size_t)H_v * UNIT_BYTES));
     if (segc < 1) segc = 1;
     if (segc > max_chunks) segc = max_chunks;
     if (segc > 65535) segc = 65535;  // grid.y of the intra kernel
     L.segc = segc;
     L.n_seg = (max_chunks + segc - 1) / segc;
     L.off_coff = 0;
-    L.off_cmeta = align256(4 * coff_slots);
-    L.off_units = align256(L.off_cmeta + CMETA_BYTES * (size_t)segc);
+    L.off_units = align256(4 * coff_slots);
     L.off_carry = L.off_units + (size_t)segc * H_v * UNIT_BYTES;
     L.carry_bytes = carry && L.n_seg > 1 ? (size_t)n_seq * H_v * D * D * 4 : 0;
     L.total = L.off_carry + L.carry_bytes;
@@ -97,12 +93,10 @@ Work work_at(uint8_t* base, const Layout& L, int H_v) {
     uint8_t* un = base + L.off_units;
     Work w;
     w.coff = reinterpret_cast<int32_t*>(base + L.off_coff);
-    w.cmeta = reinterpret_cast<int4*>(base + L.off_cmeta);
     w.wt = reinterpret_cast<bf16*>(un);
     w.ut = reinterpret_cast<bf16*>(un + U * U_WT);
     w.p = reinterpret_cast<bf16*>(un + U * (U_WT + U_UT));
     w.vec = reinterpret_cast<float*>(un + U * (U_WT + U_UT + U_P));
-    w.gb = reinterpret_cast<float*>(un + U * (U_WT + U_UT + U_P + U_VEC));
     w.carry = L.carry_bytes ? reinterpret_cast<float*>(base + L.off_carry) : nullptr;
     return w;
 }
@@ -152,93 +146,6 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, 
     }
 }
 
-// ============================================================== gates kernel
-// Gates of every (chunk, value head) unit of a segment: beta = sigmoid(b) and
-// G = the chunk-local cumulative sum of g = -exp(A_log) softplus(a + dt_bias)
-// in the log2 domain, both zero past the chunk's last token; and each chunk's
-// first token and length.  One CTA per (chunk, 32 value heads): coalesced
-// reads of a token's heads, then one warp-wide scan per head.
-constexpr int NT_G = 256;
-
-__global__ void __launch_bounds__(NT_G) chunk_gates_kernel(DeltaArgs a, Work w, int64_t C0) {
-    __shared__ float sg[64][33], sb[64][33];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t gc = C0 + blockIdx.x;
-    const int h0 = blockIdx.y * 32;
-    constexpr float kLog2e = 1.4426950408889634f;
-    // first token and length of chunk gc (every thread; a single sequence
-    // without offsets needs no loads)
-    int64_t t0 = 0;
-    int n = 0;
-    if (a.cu == nullptr) {
-        t0 = gc * C;
-        if (t0 < a.T) n = (int)(a.T - t0 < C ? a.T - t0 : C);
-    } else if (gc < w.coff[a.n_seq]) {
-        int lo_s = 0, hi_s = a.n_seq - 1;  // sequence of chunk gc
-        while (lo_s < hi_s) {
-            const int mid = (lo_s + hi_s + 1) >> 1;
-            if ((int64_t)w.coff[mid] <= gc) lo_s = mid; else hi_s = mid - 1;
-        }
-        int64_t s0, s1;
-        seq_bounds(a.cu, lo_s, a.T, s0, s1);
-        t0 = s0 + (gc - w.coff[lo_s]) * C;
-        n = (int)(s1 - t0 < C ? s1 - t0 : C);
-    }
-    if (tid == 0 && blockIdx.y == 0)
-        w.cmeta[blockIdx.x] = make_int4((int)(uint32_t)(uint64_t)t0, (int)((uint64_t)t0 >> 32), n, 0);
-    if (n == 0) return;
-    {   // thread (token warp + 8k, head h0 + lane): all loads issued before any use
-        const int h = h0 + lane;
-        const bool hv = h < a.H_v;
-        float gv[8], bv[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int t = warp + 8 * k;
-            const int64_t gi = (t < n && hv) ? (t0 + t) * a.H_v + h : 0;  // index 0 exists: T > 0
-            if (a.g != nullptr) {
-                gv[k] = a.g[gi];
-                bv[k] = a.beta[gi];
-            } else {
-                gv[k] = to_f(static_cast<const bf16*>(a.a)[gi]);
-                bv[k] = to_f(static_cast<const bf16*>(a.b)[gi]);
-            }
-        }
-        const float Al = hv && a.g == nullptr ? a.A_log[h] : 0.f;
-        const float dtb = hv && a.g == nullptr ? a.dt_bias[h] : 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int t = warp + 8 * k;
-            const bool live = t < n && hv;
-            float g = gv[k], bt = bv[k];
-            if (a.g == nullptr) {
-                g = gate_g(g, Al, dtb);
-                bt = sigmoid_f(bt);
-            }
-            sg[t][lane] = live ? g * kLog2e : 0.f;
-            sb[t][lane] = live ? bt : 0.f;
-        }
-    }
-    __syncthreads();
-    for (int hl = warp; hl < 32 && h0 + hl < a.H_v; hl += 8) {
-        float x0 = sg[lane][hl], x1 = sg[lane + 32][hl];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
-            const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
-            if (lane >= o) {
-                x0 += y0;
-                x1 += y1;
-            }
-        }
-        x1 += __shfl_sync(0xffffffffu, x0, 31);
-        float* dst = w.gb + ((gc - C0) * a.H_v + h0 + hl) * 128;
-        dst[lane] = x0;
-        dst[lane + 32] = x1;
-        dst[64 + lane] = sb[lane][hl];
-        dst[96 + lane] = sb[lane + 32][hl];
-    }
-}
-
 // ============================================================== intra kernel
 // One CTA per (chunk, value head); 256 threads, three CTAs per SM (72 KB of
 // shared memory and 128 TMEM columns each), so that the latency-bound phases
@@ -250,7 +157,7 @@ constexpr int IS_A = IS_V + 16384;                // A, f32 [64][68]; then B_W |
 constexpr int A_PITCH = 68;
 constexpr int IS_X = IS_A + 64 * A_PITCH * 4;     // solve temporaries, f32 [32][36]
 constexpr int X_PITCH = 36;
-constexpr int IS_VEC = IS_X + 32 * X_PITCH * 4;   // G (log2), beta (one bulk copy), beta e^G rk, rk, rq,
+constexpr int IS_VEC = IS_X + 32 * X_PITCH * 4;   // G (log2), beta, beta e^G rk, rk, rq,
                                                   // G - log2 rk
 constexpr int IS_BAR = IS_VEC + 6 * 64 * 4;
 constexpr int IS_TOTAL = IS_BAR + 64;
@@ -283,10 +190,26 @@ __global__ void __launch_bounds__(NT_I, 3)
 chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
                    const __grid_constant__ CUtensorMap umap, DeltaArgs a, Work w, int64_t C0) {
     const int h = blockIdx.x;
-    const int4 cm = w.cmeta[blockIdx.y];
-    const int n = cm.z;
-    if (n == 0) return;  // past the last chunk of the call
-    const int64_t t0 = (int64_t)((uint64_t)(uint32_t)cm.x | ((uint64_t)(uint32_t)cm.y << 32));
+    const int64_t gc = C0 + blockIdx.y;
+    // first token and length of chunk gc (no loads for one sequence without offsets)
+    int64_t t0;
+    int n;
+    if (a.cu == nullptr) {
+        t0 = gc * C;
+        if (t0 >= a.T) return;  // past the last chunk of the call
+        n = (int)(a.T - t0 < C ? a.T - t0 : C);
+    } else {
+        if (gc >= w.coff[a.n_seq]) return;
+        int lo_s = 0, hi_s = a.n_seq - 1;  // sequence of chunk gc
+        while (lo_s < hi_s) {
+            const int mid = (lo_s + hi_s + 1) >> 1;
+            if ((int64_t)w.coff[mid] <= gc) lo_s = mid; else hi_s = mid - 1;
+        }
+        int64_t s0, s1;
+        seq_bounds(a.cu, lo_s, a.T, s0, s1);
+        t0 = s0 + (gc - w.coff[lo_s]) * C;
+        n = (int)(s1 - t0 < C ? s1 - t0 : C);
+    }
     const int kh = h / (a.H_v / a.H_k);
     const int xq = kh * D, xk = a.H_k * D + kh * D, xv = 2 * a.H_k * D + h * D;
     const int64_t u = (int64_t)blockIdx.y * a.H_v + h;
@@ -311,13 +234,13 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     const int quarter = warp & 3, half = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lo = (uint32_t)(quarter * 32) << 16;
+    constexpr float kLog2e = 1.4426950408889634f;
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar_tma, 6 * 8192 + (uint32_t)U_GB);
-        bulk_load(Gs, w.gb + u * (int64_t)(U_GB / 4), (uint32_t)U_GB, bar_tma);  // G | beta
+        mbar_arrive_expect_tx(bar_tma, 6 * 8192);
         const int y = (int)t0;
         tma_load_2d(kq, &qmap, bar_tma, xk, y);
         tma_load_2d(kq + 16384, &qmap, bar_tma, xk + 64, y);
@@ -329,6 +252,50 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     if (warp == 0) {
         tmem_alloc(tslot, TI_COLS);
         tmem_relinquish();
+    }
+    if (warp == 1) {
+        // beta = sigmoid(b) and g = -exp(A_log) softplus(a + dt_bias) of tokens
+        // lane and lane + 32 (every load issued before any use), then the
+        // chunk-local cumulative decay G in the log2 domain; zero past token n
+        int64_t gi[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) gi[e] = lane + 32 * e < n ? (t0 + lane + 32 * e) * a.H_v + h : 0;
+        const bool raw = a.g == nullptr;
+        float gv[2], bv[2];
+        if (raw) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                gv[e] = to_f(static_cast<const bf16*>(a.a)[gi[e]]);
+                bv[e] = to_f(static_cast<const bf16*>(a.b)[gi[e]]);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                gv[e] = a.g[gi[e]];
+                bv[e] = a.beta[gi[e]];
+            }
+        }
+        const float Al = raw ? a.A_log[h] : 0.f, dtb = raw ? a.dt_bias[h] : 0.f;
+        float x[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const bool live = lane + 32 * e < n;
+            const float g = raw ? gate_g(gv[e], Al, dtb) : gv[e];
+            const float bt = raw ? sigmoid_f(bv[e]) : bv[e];
+            x[e] = live ? g * kLog2e : 0.f;
+            Bs[lane + 32 * e] = live ? bt : 0.f;
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y0 = __shfl_up_sync(0xffffffffu, x[0], o);
+            const float y1 = __shfl_up_sync(0xffffffffu, x[1], o);
+            if (lane >= o) {
+                x[0] += y0;
+                x[1] += y1;
+            }
+        }
+        Gs[lane] = x[0];
+        Gs[lane + 32] = x[1] + __shfl_sync(0xffffffffu, x[0], 31);
     }
     tc_fence_before();
     __syncthreads();
@@ -410,10 +377,17 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4) {
                     const float4 M4 = *reinterpret_cast<const float4*>(Ms + j0 + 4 * g4);
-                    const float mj[4] = {M4.x, M4.y, M4.z, M4.w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        d1[4 * g4 + q] = j0 + 4 * g4 + q <= jmax ? d1[4 * g4 + q] * ex2_approx(Li - mj[q]) : 0.f;
+                    const float2 x01 = __fadd2_rn(make_float2(Li, Li), make_float2(-M4.x, -M4.y));
+                    const float2 x23 = __fadd2_rn(make_float2(Li, Li), make_float2(-M4.z, -M4.w));
+                    const float2 p01 = __fmul2_rn(make_float2(d1[4 * g4], d1[4 * g4 + 1]),
+                                                  make_float2(ex2_approx(x01.x), ex2_approx(x01.y)));
+                    const float2 p23 = __fmul2_rn(make_float2(d1[4 * g4 + 2], d1[4 * g4 + 3]),
+                                                  make_float2(ex2_approx(x23.x), ex2_approx(x23.y)));
+                    const int j = j0 + 4 * g4;
+                    d1[4 * g4 + 0] = j + 0 <= jmax ? p01.x : 0.f;
+                    d1[4 * g4 + 1] = j + 1 <= jmax ? p01.y : 0.f;
+                    d1[4 * g4 + 2] = j + 2 <= jmax ? p23.x : 0.f;
+                    d1[4 * g4 + 3] = j + 3 <= jmax ? p23.y : 0.f;
                 }
             } else {
 #pragma unroll
@@ -446,6 +420,16 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 for (int r = q + 1; r < 16; ++r) x[r] = fmaf(-Am[(r0 + r) * A_PITCH + r0 + q], x[q], x[r]);
 #pragma unroll
             for (int r = 0; r < 16; ++r) *tp_at(kq, r0 + r, r0 + cl) = x[r];
+        } else {
+            // meanwhile the other threads zero T' above its diagonal blocks
+            // (blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)), 2 float4 each
+#pragma unroll
+            for (int e = tid - 64; e < 384; e += NT_I - 64) {
+                const int blk = e >> 6, br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                *reinterpret_cast<float4*>(tp_at(kq, 16 * br + ((e >> 2) & 15), 16 * bc + (e & 3) * 4)) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
         __syncthreads();
         const int fg = lane >> 2, ft = lane & 3;  // MMA fragment row group, thread in group
@@ -515,16 +499,17 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         {   // B_W = T' diag(beta e^G rk), B_U = T' diag(beta) (bf16) into the A region
             const int which = tid >> 7, i = (tid >> 1) & 63, c0 = (tid & 1) * 32;
             const float* Fc = (which == 0 ? FWs : Bs) + c0;
-            float vals[32];
+            float vals[32];  // T' is zero above its diagonal (all of it is written)
 #pragma unroll
             for (int g4 = 0; g4 < 8; ++g4) {
-                const int c = c0 + 4 * g4;
-                const float4 t4 = *reinterpret_cast<const float4*>(tp_at(kq, i, c));
+                const float4 t4 = *reinterpret_cast<const float4*>(tp_at(kq, i, c0 + 4 * g4));
                 const float4 f4 = *reinterpret_cast<const float4*>(Fc + 4 * g4);
-                vals[4 * g4 + 0] = c + 0 <= i ? t4.x * f4.x : 0.f;
-                vals[4 * g4 + 1] = c + 1 <= i ? t4.y * f4.y : 0.f;
-                vals[4 * g4 + 2] = c + 2 <= i ? t4.z * f4.z : 0.f;
-                vals[4 * g4 + 3] = c + 3 <= i ? t4.w * f4.w : 0.f;
+                const float2 lo = __fmul2_rn(make_float2(t4.x, t4.y), make_float2(f4.x, f4.y));
+                const float2 hi = __fmul2_rn(make_float2(t4.z, t4.w), make_float2(f4.z, f4.w));
+                vals[4 * g4 + 0] = lo.x;
+                vals[4 * g4 + 1] = lo.y;
+                vals[4 * g4 + 2] = hi.x;
+                vals[4 * g4 + 3] = hi.y;
             }
             store_row_bf16(sm + IS_A + which * 8192, i, c0, vals, 32);
         }
@@ -1022,7 +1007,7 @@ int sm_count() {
     return count[dev];
 }
 
-// Chunk offsets, then per segment: gates, intra, chain.  The chain splits each
+// Chunk offsets, then per segment: intra, chain.  The chain splits each
 // head's state into two 64-column slices when that still leaves at most one
 // CTA per SM.
 cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cudaStream_t s) {
@@ -1046,7 +1031,6 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
     chunk_offsets_kernel<<<1, 1024, 0, s>>>(a.cu, a.n_seq, a.T, w.coff);
     for (int64_t seg = 0; seg < Ly.n_seg; ++seg) {
         const int64_t C0 = seg * Ly.segc;
-        chunk_gates_kernel<<<dim3((unsigned)Ly.segc, (unsigned)((a.H_v + 31) / 32)), NT_G, 0, s>>>(a, w, C0);
         chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, s>>>(qmap, wtmap, utmap, a, w, C0);
         if (split)
             chunk_chain_kernel<64><<<(unsigned)(a.n_seq * a.H_v * 2), NT_C, ChainLayout<64>::SMEM, s>>>(

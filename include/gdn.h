@@ -207,8 +207,8 @@ gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, co
  *     the other shapes);
  *   - final_state is required (it carries the state between the call's
  *     segments); it may alias initial_state;
- *   - limits: n_seq <= 16384 and H_v * 42,496 bytes must fit in the array
- *     (H_v <= 590); calls beyond them return GDN_ERR_WORKSPACE;
+ *   - limits: n_seq <= 16384 and H_v * 41,984 bytes must fit in the array
+ *     (H_v <= 597); calls beyond them return GDN_ERR_WORKSPACE;
  *   - the first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any
  *     stream capture;
