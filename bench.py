@@ -237,7 +237,9 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     clocks.mark(False)
     barrier(dist, dev)
-    launches += args.steps * 4  # conv (2 kernels), chunk, norm
+    chunk_launches = gdn.gdn_chunk_prefill_launches(1, T, dims, wp.dtype)
+    step_launches = 2 + chunk_launches + 1  # conv (tile kernel + state kernel), chunk, norm
+    launches += args.steps * step_launches
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
     conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
     chunk_ms = [e[1].elapsed_time(e[2]) for e in evs]
@@ -347,7 +349,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     clocks.mark(False)
     barrier(dist, dev)
-    launches += args.steps * 4
+    launches += args.steps * step_launches
     e_total = max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in eev) / 1e3, dev)
     e2e = {"value": round(world * T * args.steps / e_total, 1), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

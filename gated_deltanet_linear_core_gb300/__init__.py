@@ -22,7 +22,7 @@ from ._lib import GDNError, GDN_QK_L2NORM  # noqa: F401
 
 __all__ = [
     "GDNDims", "GDNError", "gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
-    "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode", "gdn_rmsnorm_gated",
+    "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_launches", "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode", "gdn_rmsnorm_gated",
     "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_sync_status", "gdn_layer_prefill", "gdn_layer_decode",
     "library_path",
 ]
@@ -157,6 +157,11 @@ def gdn_chunk_prefill_workspace_size(n_seq: int, T_tot: int, dims, dtype) -> int
     code = _lib.GDN_BF16 if dtype == torch.bfloat16 else _lib.GDN_F32
     return int(_lib.load().gdn_chunk_prefill_workspace_size(int(n_seq), int(T_tot), _dims(dims),
                                                             code))
+
+
+def gdn_chunk_prefill_launches(n_seq: int, T_tot: int, dims, dtype) -> int:
+    code = _lib.GDN_BF16 if dtype == torch.bfloat16 else _lib.GDN_F32
+    return int(_lib.load().gdn_chunk_prefill_launches(int(n_seq), int(T_tot), _dims(dims), code))
 
 
 def _gate_ptrs(a, b, A_log, dt_bias, g, beta, dt):

@@ -1048,6 +1048,10 @@ size_t chunk_split_workspace_bytes(int n_seq, int64_t T, int H_v) {
     return layout_of(n_seq, T, H_v).total;
 }
 
+int chunk_split_launches(int n_seq, int64_t T, int H_v) {
+    return 1 + 2 * (int)layout_of(n_seq, T, H_v).n_seg;
+}
+
 cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s) {
     const Layout Ly = layout_of(a.n_seq, a.T, a.H_v);
     if (workspace == nullptr || ws_bytes < Ly.total) return cudaErrorInvalidValue;

@@ -65,6 +65,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensormap_encoder();
 size_t chunk_split_workspace_bytes(int n_seq, int64_t T, int H_v);
 cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes,
                                cudaStream_t s);
+// Kernel launches launch_chunk_split issues: chunk offsets, then intra + chain per segment.
+int chunk_split_launches(int n_seq, int64_t T, int H_v);
 
 // The same chunked prefill with its scratch in a fixed device array of the
 // library (gdn_chunk_prefill_noalloc): no allocation; final_state required.

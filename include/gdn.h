@@ -156,6 +156,13 @@ size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t
                                         gdn_dtype_t dtype);
 
 /*
+ * Number of kernel launches one gdn_chunk_prefill call with these sizes
+ * issues (for profiling and launch accounting; the library has no paper
+ * counterpart for it).  0 for T_tot == 0 or invalid dims.
+ */
+int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, gdn_dims_t dims, gdn_dtype_t dtype);
+
+/*
  * Chunked gated delta rule (chunk size 64, WY/UT form) over packed sequences.
  * Defined by: cortex GatedDeltaNet commit, "Discretisation" (g, beta in f32),
  * "Block" (L2norm on q,k), "Delta rule (recurrent, per-token)" (the result is
