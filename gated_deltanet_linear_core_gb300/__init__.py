@@ -23,7 +23,7 @@ from ._lib import GDNError, GDN_QK_L2NORM  # noqa: F401
 __all__ = [
     "GDNDims", "GDNError", "gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_launches", "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode", "gdn_rmsnorm_gated",
-    "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_sync_status", "gdn_layer_prefill", "gdn_layer_decode",
+    "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_sync_status", "gdn_selftest_bounded_wait", "gdn_layer_prefill", "gdn_layer_decode",
     "library_path",
 ]
 
@@ -115,6 +115,15 @@ def gdn_sync_status(device=None, stream=None) -> None:
         stream = torch.cuda.current_stream(device)
     s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     _lib.check(_lib.load().gdn_sync_status(s), "gdn_sync_status")
+
+
+def gdn_selftest_bounded_wait(limit_ns: int = 1_000_000, device=None, stream=None) -> None:
+    """Enqueues one kernel whose bounded wait runs out after limit_ns (nothing
+    arrives at its barrier); the next gdn_sync_status raises GDN_ERR_TIMEOUT."""
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _lib.check(_lib.load().gdn_selftest_bounded_wait(int(limit_ns), s), "gdn_selftest_bounded_wait")
 
 
 def gdn_conv1d_fwd(x, w, dims, cu_seqlens=None, conv_state_in=None, conv_state_out=None,

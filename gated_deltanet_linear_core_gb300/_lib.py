@@ -44,6 +44,7 @@ SIGNATURES = {
     "gdn_ckpt_count": (I64, [P, I32, I32]),
     "gdn_check_cu_seqlens": (ST, [P, I32, I64, P]),
     "gdn_sync_status": (ST, [P]),
+    "gdn_selftest_bounded_wait": (ST, [I64, P]),
     "gdn_conv1d_fwd": (ST, [P, P, P, I32, I64, P, P, I32, P, I64, I32, P, Dims, ST, P]),
     "gdn_conv1d_update": (ST, [P, P, P, I32, I32, P, Dims, ST, P]),
     "gdn_chunk_prefill_workspace_size": (SZ, [I32, I64, Dims, ST]),

@@ -1060,6 +1060,23 @@ cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_by
     return run_segments(a, w, Ly, s);
 }
 
+namespace {
+// One bounded wait that runs out: nothing arrives at the barrier.
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ alignas(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        if (!mbar_wait(&bar, 0, limit_ns)) atomicOr(&g_device_error, 1);
+    }
+}
+}  // namespace
+
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, cudaStream_t s) {
+    bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_device_error(cudaStream_t s, int* flags) {
     int hf = 0;
     cudaError_t e = cudaMemcpyFromSymbolAsync(&hf, g_device_error, sizeof(int), 0, cudaMemcpyDeviceToHost, s);

@@ -125,6 +125,12 @@ gdn_status_t gdn_sync_status(void* stream) {
     return ((flags | cflags) & 1) ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
+gdn_status_t gdn_selftest_bounded_wait(int64_t limit_ns, void* stream) {
+    if (limit_ns < 1000) limit_ns = 1000;
+    if (limit_ns > 1000000000) limit_ns = 1000000000;
+    return cuda_status(gdn::launch_bounded_wait_selftest((uint64_t)limit_ns, (cudaStream_t)stream));
+}
+
 gdn_status_t gdn_conv1d_fwd(const void* x, const void* w, const int32_t* cu_seqlens, int32_t n_seq,
                             int64_t T_tot, const void* conv_state_in, void* conv_state_out,
                             int32_t ckpt_every, void* conv_ckpt_out, int64_t ckpt_rows,

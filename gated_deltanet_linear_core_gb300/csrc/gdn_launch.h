@@ -75,6 +75,8 @@ cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s);
 
 // Reads (synchronising `s`) and clears the library's device error word.
 cudaError_t read_and_clear_device_error(cudaStream_t s, int* flags);
+// One CTA whose bounded wait runs out after limit_ns and sets the error word.
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, cudaStream_t s);
 // The same for the conv kernels' own error word.
 cudaError_t read_and_clear_conv_error(cudaStream_t s, int* flags);
 

@@ -156,6 +156,16 @@ size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t
                                         gdn_dtype_t dtype);
 
 /*
+ * Self-test of the failure-detection path (the pages have no counterpart):
+ * launches one CTA whose bounded wait on an mbarrier that nothing arrives at
+ * gives up after limit_ns nanoseconds (clamped to [1 us, 1 s]) and sets the
+ * device error word, as a kernel's timed-out wait does.  gdn_sync_status then
+ * returns GDN_ERR_TIMEOUT and clears the word.  Nothing faults or traps; the
+ * context stays usable.  Asynchronous on `stream`.
+ */
+gdn_status_t gdn_selftest_bounded_wait(int64_t limit_ns, void* stream);
+
+/*
  * Number of kernel launches one gdn_chunk_prefill call with these sizes
  * issues (for profiling and launch accounting; the library has no paper
  * counterpart for it).  0 for T_tot == 0 or invalid dims.

@@ -263,3 +263,26 @@ def test_no_kernel_gave_up_a_bounded_wait():
     """Every chunked-prefill launch above completed its waits: the library's
     device error word is clear (gdn_sync_status raises on GDN_ERR_TIMEOUT)."""
     gdn.gdn_sync_status()
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_context_survives():
+    """Failure detection on the GPU without a fault: a kernel whose bounded wait
+    runs out (nothing arrives at its barrier) sets the device error word;
+    gdn_sync_status reports GDN_ERR_TIMEOUT once and clears it; the next
+    tensor-core prefill on the same context still matches the oracle."""
+    gdn.gdn_sync_status()  # nothing pending before
+    gdn.gdn_selftest_bounded_wait(2_000_000)
+    with pytest.raises(gdn.GDNError, match="TIMEOUT"):
+        gdn.gdn_sync_status()
+    gdn.gdn_sync_status()  # cleared
+    shape = SMALL_128
+    inp = _delta_inputs(shape, torch.bfloat16, [130, 64], seed=77)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    Sf = torch.empty((2, shape.H_v, shape.d_k, shape.d_v), device="cuda")
+    o = gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(shape), d["a"], d["b"], d["A_log"],
+                              d["dt_bias"], cu_seqlens=d["cu_seqlens"], initial_state=d["S0"],
+                              final_state=Sf)
+    gdn.gdn_sync_status()
+    o_ref, S_ref, _ = _oracle_delta(inp, shape)
+    assert_close("o", host(o), o_ref, TOL[torch.bfloat16], per_head_axis=1)
+    assert_close("S_final", host(Sf), S_ref, TOL[torch.bfloat16], per_head_axis=1)
