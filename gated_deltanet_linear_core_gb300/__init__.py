@@ -23,7 +23,8 @@ from ._lib import GDNError, GDN_QK_L2NORM  # noqa: F401
 __all__ = [
     "GDNDims", "GDNError", "gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_launches", "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode", "gdn_rmsnorm_gated",
-    "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_sync_status", "gdn_selftest_bounded_wait", "gdn_layer_prefill", "gdn_layer_decode",
+    "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_sync_status", "gdn_selftest_bounded_wait",
+    "gdn_layer_prefill_host", "gdn_layer_prefill", "gdn_layer_decode",
     "library_path",
 ]
 
@@ -296,6 +297,60 @@ def gdn_layer_prefill(mixed_qkv, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, 
     if return_intermediates:
         r.update({"y": y, "o": o})
     return r
+
+
+def _hptr(t, name, dtype=None, shape=None):
+    """Address of a contiguous page-locked CPU tensor."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.device.type != "cpu" or not t.is_pinned():
+        raise ValueError(f"{name}: must be a page-locked (pinned) CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr() if t.numel() else None
+
+
+def gdn_layer_prefill_host(h_qkv, h_z, h_a, h_b, conv_w, A_log, dt_bias, norm_w, dims,
+                           initial_state=None, conv_state_in=None, scale=0.0, l2norm=True,
+                           norm_eps=1e-6, h_out=None, final_state=None, conv_state_out=None,
+                           workspace=None, stream=None):
+    """The layer core for one sequence whose activations (h_qkv [T, conv_dim],
+    h_z [T, H_v*d_v], h_a, h_b [T, H_v]) and output h_out are pinned CPU tensors;
+    parameters and states are CUDA tensors.  Copies in, kernels and copies out
+    overlap piece by piece inside the library.  Returns a dict with out (the
+    pinned host tensor; complete once the stream reaches this point),
+    final_state [1, H_v, d_k, d_v] f32 and conv_state [1, conv_dim, 3]."""
+    dt = h_qkv.dtype
+    dev = conv_w.device
+    T = int(h_qkv.shape[0])
+    C, O = _conv_dim(dims), int(dims.H_v) * int(dims.d_v)
+    code = _dtype_code(h_qkv)
+    if h_out is None:
+        h_out = torch.empty((T, O), dtype=dt).pin_memory()
+    if final_state is None:
+        final_state = torch.empty((1, dims.H_v, dims.d_k, dims.d_v), dtype=torch.float32, device=dev)
+    if conv_state_out is None:
+        conv_state_out = torch.empty((1, C, 3), dtype=dt, device=dev)
+    lib = _lib.load()
+    need = lib.gdn_layer_prefill_host_workspace_size(T, _dims(dims), code)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    st = lib.gdn_layer_prefill_host(
+        _hptr(h_qkv, "h_qkv", dt, (T, C)), _hptr(h_z, "h_z", dt, (T, O)),
+        _hptr(h_a, "h_a", dt, (T, dims.H_v)), _hptr(h_b, "h_b", dt, (T, dims.H_v)),
+        _ptr(conv_w, "conv_w", dt, (C, 4)), _ptr(A_log, "A_log", torch.float32),
+        _ptr(dt_bias, "dt_bias", torch.float32), _ptr(norm_w, "norm_w", dt), T,
+        _ptr(initial_state, "initial_state", torch.float32), _ptr(final_state, "final_state", torch.float32),
+        _ptr(conv_state_in, "conv_state_in", dt), _ptr(conv_state_out, "conv_state_out", dt),
+        float(scale), _lib.GDN_QK_L2NORM if l2norm else 0, float(norm_eps),
+        _hptr(h_out, "h_out", dt, (T, O)), _ptr(workspace, "workspace", torch.uint8),
+        workspace.numel() if workspace is not None else 0, _dims(dims), code, _stream(conv_w, stream))
+    _lib.check(st, "gdn_layer_prefill_host")
+    return {"out": h_out, "final_state": final_state, "conv_state": conv_state_out}
 
 
 def gdn_layer_decode(x, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, state, conv_state,

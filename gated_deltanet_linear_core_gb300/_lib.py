@@ -45,6 +45,10 @@ SIGNATURES = {
     "gdn_check_cu_seqlens": (ST, [P, I32, I64, P]),
     "gdn_sync_status": (ST, [P]),
     "gdn_selftest_bounded_wait": (ST, [I64, P]),
+    "gdn_layer_prefill_host_workspace_size": (SZ, [I64, Dims, ST]),
+    "gdn_layer_prefill_host_piece": (I64, [I64, Dims, ST]),
+    "gdn_layer_prefill_host": (ST, [P, P, P, P, P, P, P, P, I64, P, P, P, P, F32, U32, F32, P, P, SZ,
+                                    Dims, ST, P]),
     "gdn_conv1d_fwd": (ST, [P, P, P, I32, I64, P, P, I32, P, I64, I32, P, Dims, ST, P]),
     "gdn_conv1d_update": (ST, [P, P, P, I32, I32, P, Dims, ST, P]),
     "gdn_chunk_prefill_workspace_size": (SZ, [I32, I64, Dims, ST]),

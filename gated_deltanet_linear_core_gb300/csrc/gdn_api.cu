@@ -125,6 +125,85 @@ gdn_status_t gdn_sync_status(void* stream) {
     return ((flags | cflags) & 1) ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
+size_t gdn_layer_prefill_host_workspace_size(int64_t T, gdn_dims_t dims, gdn_dtype_t dtype) {
+    if (check_dims(dims, dtype) != GDN_OK || T <= 0 || T > (int64_t)INT32_MAX) return 0;
+    return gdn::layer_prefill_host_workspace_bytes(T, dims.H_k, dims.H_v, dims.d_k, (int)elem_size(dtype),
+                                                   dtype == GDN_BF16 && dims.d_k == 128);
+}
+
+int64_t gdn_layer_prefill_host_piece(int64_t T, gdn_dims_t dims, gdn_dtype_t dtype) {
+    if (check_dims(dims, dtype) != GDN_OK || T <= 0 || T > (int64_t)INT32_MAX) return 0;
+    return gdn::layer_prefill_host_piece(T, dims.H_k, dims.H_v, dims.d_k, (int)elem_size(dtype),
+                                         dtype == GDN_BF16 && dims.d_k == 128);
+}
+
+namespace {
+bool page_locked(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost;
+}
+}  // namespace
+
+gdn_status_t gdn_layer_prefill_host(const void* h_qkv, const void* h_z, const void* h_a,
+                                    const void* h_b, const void* conv_w, const float* A_log,
+                                    const float* dt_bias, const void* norm_w, int64_t T,
+                                    const float* initial_state, float* final_state,
+                                    const void* conv_state_in, void* conv_state_out, float scale,
+                                    uint32_t flags, float norm_eps, void* h_out, void* workspace,
+                                    size_t ws_bytes, gdn_dims_t dims, gdn_dtype_t dtype,
+                                    void* stream) {
+    gdn_status_t st = check_dims(dims, dtype);
+    if (st != GDN_OK) return st;
+    if (T < 0 || T > (int64_t)INT32_MAX) return GDN_ERR_INVALID_ARG;
+    if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if (!isfinite(scale) || !isfinite(norm_eps) || norm_eps < 0.f) return GDN_ERR_INVALID_ARG;
+    if (conv_w == nullptr || A_log == nullptr || dt_bias == nullptr || norm_w == nullptr ||
+        final_state == nullptr || conv_state_out == nullptr)
+        return GDN_ERR_INVALID_ARG;
+    if (T > 0 && (h_qkv == nullptr || h_z == nullptr || h_a == nullptr || h_b == nullptr || h_out == nullptr))
+        return GDN_ERR_INVALID_ARG;
+    if (!aligned16(conv_w) || !aligned16(norm_w) || !aligned_n(A_log, 4) || !aligned_n(dt_bias, 4) ||
+        !aligned16(initial_state) || !aligned16(final_state) || !aligned16(conv_state_in) ||
+        !aligned16(conv_state_out) || !aligned16(workspace))
+        return GDN_ERR_ALIGN;
+    if (T > 0 && !(page_locked(h_qkv) && page_locked(h_z) && page_locked(h_a) && page_locked(h_b) &&
+                   page_locked(h_out)))
+        return GDN_ERR_INVALID_ARG;
+    const size_t need = gdn_layer_prefill_host_workspace_size(T, dims, dtype);
+    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return GDN_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {
+        // no tokens: the states pass through (conv state pass, then the empty prefill)
+        gdn::ConvArgs c;
+        memset(&c, 0, sizeof(c));
+        c.w = conv_w; c.n_seq = 1; c.C = (int)conv_dim_of(dims);
+        c.state_in = conv_state_in; c.state_out = conv_state_out; c.silu = 1;
+        cudaError_t e = gdn::launch_conv1d_fwd(c, dtype, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        gdn::DeltaArgs d;
+        memset(&d, 0, sizeof(d));
+        d.A_log = A_log; d.dt_bias = dt_bias; d.n_seq = 1;
+        d.H_k = dims.H_k; d.H_v = dims.H_v; d.D = dims.d_k;
+        d.S0 = initial_state; d.S_final = final_state; d.scale = 1.f;
+        return cuda_status(gdn::launch_chunk_ffma(d, dtype, s));
+    }
+    gdn::HostLayerArgs h;
+    h.h_qkv = h_qkv; h.h_z = h_z; h.h_a = h_a; h.h_b = h_b;
+    h.conv_w = conv_w; h.A_log = A_log; h.dt_bias = dt_bias; h.norm_w = norm_w;
+    h.T = T; h.H_k = dims.H_k; h.H_v = dims.H_v; h.D = dims.d_k;
+    h.initial_state = initial_state; h.final_state = final_state;
+    h.conv_state_in = conv_state_in; h.conv_state_out = conv_state_out;
+    h.scale = scale == 0.f ? 1.0f / sqrtf((float)dims.d_k) : scale;
+    h.eps = norm_eps;
+    h.l2norm = (flags & GDN_QK_L2NORM) != 0;
+    h.h_out = h_out;
+    return cuda_status(gdn::launch_layer_prefill_host(h, dtype, workspace, s));
+}
+
 gdn_status_t gdn_selftest_bounded_wait(int64_t limit_ns, void* stream) {
     if (limit_ns < 1000) limit_ns = 1000;
     if (limit_ns > 1000000000) limit_ns = 1000000000;

@@ -83,4 +83,25 @@ cudaError_t read_and_clear_conv_error(cudaStream_t s, int* flags);
 cudaError_t launch_rmsnorm_gated(const void* o, const void* z, const void* w, float eps, int64_t T,
                                  int H, int D, void* out, gdn_dtype_t dt, cudaStream_t s);
 
+// The layer core for one sequence streamed from page-locked host memory
+// (gdn_layer_prefill_host).
+struct HostLayerArgs {
+    const void *h_qkv, *h_z, *h_a, *h_b;  // host, page-locked
+    const void* conv_w;
+    const float *A_log, *dt_bias;
+    const void* norm_w;
+    int64_t T;
+    int H_k, H_v, D;
+    const float* initial_state;
+    float* final_state;
+    const void* conv_state_in;
+    void* conv_state_out;
+    float scale, eps;
+    int l2norm;
+    void* h_out;  // host, page-locked
+};
+size_t layer_prefill_host_workspace_bytes(int64_t T, int H_k, int H_v, int D, int es, bool tensor_core);
+int64_t layer_prefill_host_piece(int64_t T, int H_k, int H_v, int D, int es, bool tensor_core);
+cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, void* workspace, cudaStream_t s);
+
 }  // namespace gdn

@@ -1,0 +1,170 @@
+// gdn_layer_prefill_host: the layer core (conv1d + SiLU -> chunked delta rule
+// -> RMSNormGated) for one sequence whose activations live in page-locked host
+// memory.  The tokens run in pieces: piece p's inputs are copied in on one
+// stream while piece p-1 computes on the caller's stream, and piece p-1's
+// output is copied out on a third stream while piece p computes, so the
+// host<->device copies overlap the kernels.  The conv state and the recurrent
+// state carry from piece to piece in place on the device.
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "gdn_launch.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kMaxDev = 128;
+std::mutex g_host_mu;
+cudaStream_t g_copy_in[kMaxDev], g_copy_out[kMaxDev];
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Slot {
+    size_t qkv, z, y, o, out;  // byte offsets in the workspace
+};
+
+struct HostLayout {
+    int64_t piece;  // tokens per piece (a multiple of 64 unless the whole sequence is one piece)
+    size_t a, b;    // the whole sequence's gate inputs (copied once)
+    Slot slot[2];
+    size_t chunk_ws, chunk_ws_bytes, total;
+};
+
+HostLayout host_layout(int64_t T, int H_k, int H_v, int D, int es, bool tensor_core) {
+    HostLayout L;
+    // about 16 pieces of a multiple of 64 tokens, at least 512 (a short
+    // sequence is one piece)
+    int64_t p = T;
+    if (T > 1024) {
+        p = (T + 15) / 16;
+        p = ((p + 63) / 64) * 64;
+        if (p < 512) p = 512;
+    }
+    L.piece = p;
+    const size_t C = (size_t)(2 * H_k + H_v) * D, O = (size_t)H_v * D;
+    size_t off = 0;
+    L.a = off; off = align256(off + (size_t)T * H_v * es);
+    L.b = off; off = align256(off + (size_t)T * H_v * es);
+    for (int s = 0; s < 2; ++s) {
+        Slot& q = L.slot[s];
+        q.qkv = off; off = align256(off + (size_t)p * C * es);
+        q.z = off;   off = align256(off + (size_t)p * O * es);
+        q.y = off;   off = align256(off + (size_t)p * C * es);
+        q.o = off;   off = align256(off + (size_t)p * O * es);
+        q.out = off; off = align256(off + (size_t)p * O * es);
+    }
+    L.chunk_ws = off;
+    L.chunk_ws_bytes = tensor_core ? chunk_split_workspace_bytes(1, p, H_v) : 0;
+    L.total = off + L.chunk_ws_bytes;
+    return L;
+}
+
+cudaError_t copy_streams(cudaStream_t* in, cudaStream_t* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    if (g_copy_in[dev] == nullptr) {
+        e = cudaStreamCreateWithFlags(&g_copy_in[dev], cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g_copy_out[dev], cudaStreamNonBlocking);
+        if (e != cudaSuccess) return e;
+    }
+    *in = g_copy_in[dev];
+    *out = g_copy_out[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t layer_prefill_host_workspace_bytes(int64_t T, int H_k, int H_v, int D, int es, bool tensor_core) {
+    return T > 0 ? host_layout(T, H_k, H_v, D, es, tensor_core).total : 0;
+}
+
+int64_t layer_prefill_host_piece(int64_t T, int H_k, int H_v, int D, int es, bool tensor_core) {
+    return host_layout(T, H_k, H_v, D, es, tensor_core).piece;
+}
+
+cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, void* workspace,
+                                      cudaStream_t s) {
+    const int es = dt == GDN_BF16 ? 2 : 4;
+    const bool tc = dt == GDN_BF16 && h.D == 128;
+    const HostLayout L = host_layout(h.T, h.H_k, h.H_v, h.D, es, tc);
+    const size_t C = (size_t)(2 * h.H_k + h.H_v) * h.D, O = (size_t)h.H_v * h.D;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t cin, cout;
+    cudaError_t e = copy_streams(&cin, &cout);
+    if (e != cudaSuccess) return e;
+    cudaEvent_t ev[7];  // in[2], comp[2], out[2], start
+    int made = 0;
+    for (; made < 7 && e == cudaSuccess; ++made)
+        e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
+    cudaEvent_t* ev_in = ev;
+    cudaEvent_t* ev_comp = ev + 2;
+    cudaEvent_t* ev_out = ev + 4;
+    // the copy streams start after whatever the caller queued on `s`
+    if (e == cudaSuccess) e = cudaEventRecord(ev[6], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cin, ev[6], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cout, ev[6], 0);
+    // the gate inputs of the whole sequence (small) in two copies
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ws + L.a, h.h_a, (size_t)h.T * h.H_v * es, cudaMemcpyHostToDevice, cin);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ws + L.b, h.h_b, (size_t)h.T * h.H_v * es, cudaMemcpyHostToDevice, cin);
+    const int64_t n_piece = (h.T + L.piece - 1) / L.piece;
+    for (int64_t p = 0; p < n_piece && e == cudaSuccess; ++p) {
+        const int sl = (int)(p & 1);
+        const Slot& q = L.slot[sl];
+        const int64_t t0 = p * L.piece;
+        const int64_t tp = h.T - t0 < L.piece ? h.T - t0 : L.piece;
+        const uint8_t* hq = static_cast<const uint8_t*>(h.h_qkv);
+        // inputs of piece p (the slot's previous piece has finished reading them)
+        if (p >= 2) e = cudaStreamWaitEvent(cin, ev_comp[sl], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(ws + q.qkv, hq + (size_t)t0 * C * es, (size_t)tp * C * es, cudaMemcpyHostToDevice, cin);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(ws + q.z, static_cast<const uint8_t*>(h.h_z) + (size_t)t0 * O * es,
+                                (size_t)tp * O * es, cudaMemcpyHostToDevice, cin);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_in[sl], cin);
+        // compute on the caller's stream once the inputs are in and the output
+        // slot has been copied out
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_in[sl], 0);
+        if (e == cudaSuccess && p >= 2) e = cudaStreamWaitEvent(s, ev_out[sl], 0);
+        if (e == cudaSuccess) {
+            ConvArgs c;
+            c.x = ws + q.qkv; c.w = h.conv_w; c.cu = nullptr; c.n_seq = 1; c.T = tp; c.C = (int)C;
+            c.state_in = p == 0 ? h.conv_state_in : h.conv_state_out;
+            c.state_out = h.conv_state_out;
+            c.ckpt_every = 0; c.ckpt = nullptr; c.ckpt_rows = 0; c.silu = 1; c.y = ws + q.y;
+            e = launch_conv1d_fwd(c, dt, s);
+        }
+        if (e == cudaSuccess) {
+            DeltaArgs d = {};
+            d.qkv = ws + q.y; d.a = ws + L.a + (size_t)t0 * h.H_v * es;
+            d.b = ws + L.b + (size_t)t0 * h.H_v * es; d.A_log = h.A_log; d.dt_bias = h.dt_bias;
+            d.cu = nullptr; d.n_seq = 1; d.T = tp; d.H_k = h.H_k; d.H_v = h.H_v; d.D = h.D;
+            d.S0 = p == 0 ? h.initial_state : h.final_state;
+            d.S_final = h.final_state;
+            d.scale = h.scale; d.l2norm = h.l2norm; d.o = ws + q.o;
+            e = tc ? launch_chunk_split(d, ws + L.chunk_ws, L.chunk_ws_bytes, s) : launch_chunk_ffma(d, dt, s);
+        }
+        if (e == cudaSuccess)
+            e = launch_rmsnorm_gated(ws + q.o, ws + q.z, h.norm_w, h.eps, tp, h.H_v, h.D, ws + q.out, dt, s);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_comp[sl], s);
+        // output of piece p
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cout, ev_comp[sl], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<uint8_t*>(h.h_out) + (size_t)t0 * O * es, ws + q.out,
+                                (size_t)tp * O * es, cudaMemcpyDeviceToHost, cout);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_out[sl], cout);
+    }
+    // join: the caller's stream waits for the last copies out
+    for (int sl = 0; sl < 2 && e == cudaSuccess; ++sl)
+        if (n_piece > sl) e = cudaStreamWaitEvent(s, ev_out[(n_piece - 1 - sl) & 1], 0);
+    for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);  // released once complete
+    return e;
+}
+
+}  // namespace gdn

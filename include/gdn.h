@@ -156,6 +156,43 @@ size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t
                                         gdn_dtype_t dtype);
 
 /*
+ * The layer core -- conv1d + SiLU, chunked delta rule, RMSNormGated, as in
+ * gdn_conv1d_fwd, gdn_chunk_prefill and gdn_rmsnorm_gated -- for ONE sequence
+ * whose activations and output are in page-locked host memory (the pages have
+ * no counterpart; this is the host-buffer form of the three calls).  The tokens
+ * run in pieces (gdn_layer_prefill_host_piece): a piece's inputs are copied to
+ * the device while the previous piece computes, and its output is copied back
+ * while the next computes, on two internal streams of the library that start
+ * after the work already queued on `stream` and are joined back to it.  The
+ * conv state and the recurrent state carry from piece to piece on the device.
+ *   h_qkv      (host, page-locked) [T, conv_dim]    dtype
+ *   h_z        (host, page-locked) [T, H_v*d_v]     dtype
+ *   h_a, h_b   (host, page-locked) [T, H_v]         dtype
+ *   conv_w     (device) [conv_dim, 4] dtype;  norm_w (device) [d_v] dtype
+ *   A_log, dt_bias (device) [H_v] f32
+ *   initial_state  (device) [1, H_v, d_k, d_v] f32, or NULL (zeros)
+ *   final_state    (device) [1, H_v, d_k, d_v] f32, required; may alias initial_state
+ *   conv_state_in  (device) [1, conv_dim, 3] dtype, or NULL (zeros)
+ *   conv_state_out (device) [1, conv_dim, 3] dtype, required; may alias conv_state_in
+ *   scale      0 -> d_k^-1/2;  flags: GDN_QK_L2NORM;  norm_eps: RMSNormGated epsilon
+ *   h_out      (host, page-locked) [T, H_v*d_v] dtype
+ *   workspace  (device) >= gdn_layer_prefill_host_workspace_size(T, dims, dtype) bytes
+ * Host buffers that are not page-locked: GDN_ERR_INVALID_ARG.  No checkpoints.
+ * Make the first call on a device before any stream capture (it creates the
+ * two copy streams).  h_out is complete once `stream` reaches this point.
+ */
+size_t gdn_layer_prefill_host_workspace_size(int64_t T, gdn_dims_t dims, gdn_dtype_t dtype);
+int64_t gdn_layer_prefill_host_piece(int64_t T, gdn_dims_t dims, gdn_dtype_t dtype);
+gdn_status_t gdn_layer_prefill_host(const void* h_qkv, const void* h_z, const void* h_a,
+                                    const void* h_b, const void* conv_w, const float* A_log,
+                                    const float* dt_bias, const void* norm_w, int64_t T,
+                                    const float* initial_state, float* final_state,
+                                    const void* conv_state_in, void* conv_state_out, float scale,
+                                    uint32_t flags, float norm_eps, void* h_out, void* workspace,
+                                    size_t ws_bytes, gdn_dims_t dims, gdn_dtype_t dtype,
+                                    void* stream);
+
+/*
  * Self-test of the failure-detection path (the pages have no counterpart):
  * launches one CTA whose bounded wait on an mbarrier that nothing arrives at
  * gives up after limit_ns nanoseconds (clamped to [1 us, 1 s]) and sets the
