@@ -24,7 +24,7 @@ __all__ = [
     "GDNDims", "GDNError", "gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_launches", "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode", "gdn_rmsnorm_gated",
     "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_sync_status", "gdn_selftest_bounded_wait",
-    "gdn_layer_prefill_host", "gdn_layer_prefill", "gdn_layer_decode",
+    "gdn_layer_prefill_host", "gdn_decode_step", "gdn_layer_prefill", "gdn_layer_decode",
     "library_path",
 ]
 
@@ -351,6 +351,36 @@ def gdn_layer_prefill_host(h_qkv, h_z, h_a, h_b, conv_w, A_log, dt_bias, norm_w,
         workspace.numel() if workspace is not None else 0, _dims(dims), code, _stream(conv_w, stream))
     _lib.check(st, "gdn_layer_prefill_host")
     return {"out": h_out, "final_state": final_state, "conv_state": conv_state_out}
+
+
+def gdn_decode_step(x, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, state, conv_state,
+                    slots=None, scale=0.0, l2norm=True, norm_eps=1e-6, out=None, stream=None):
+    """One fused decode step (conv update, gates, recurrence, RMSNormGated) in
+    one kernel for B sequences; x [B, conv_dim], z [B, H_v*d_v], a, b [B, H_v];
+    state [n_slots, H_v, d_k, d_v] f32 and conv_state [n_slots, conv_dim, 3]
+    are updated in place at slots[b] (int32 [B], distinct) or at b.  Returns
+    out [B, H_v*d_v]."""
+    dt = x.dtype
+    B = int(x.shape[0])
+    C, O = _conv_dim(dims), int(dims.H_v) * int(dims.d_v)
+    if out is None:
+        out = torch.empty((B, O), dtype=dt, device=x.device)
+    if state.dim() != 4 or tuple(state.shape[1:]) != (dims.H_v, dims.d_k, dims.d_v):
+        raise ValueError("state: expected [n_slots, H_v, d_k, d_v]")
+    if conv_state.dim() != 3 or tuple(conv_state.shape[1:]) != (C, 3):
+        raise ValueError("conv_state: expected [n_slots, conv_dim, 3]")
+    if slots is None and (state.shape[0] < B or conv_state.shape[0] < B):
+        raise ValueError("state/conv_state: fewer slots than sequences")
+    st = _lib.load().gdn_decode_step(
+        _ptr(x, "x", dt, (B, C)), _ptr(conv_w, "conv_w", dt, (C, 4)), _ptr(conv_state, "conv_state", dt),
+        _ptr(z, "z", dt, (B, O)), _ptr(a, "a", dt, (B, dims.H_v)), _ptr(b, "b", dt, (B, dims.H_v)),
+        _ptr(A_log, "A_log", torch.float32), _ptr(dt_bias, "dt_bias", torch.float32),
+        _ptr(state, "state", torch.float32), _ptr(norm_w, "norm_w", dt), float(norm_eps),
+        _ptr(slots, "slots", torch.int32, (B,)) if slots is not None else None, B, float(scale),
+        _lib.GDN_QK_L2NORM if l2norm else 0, _ptr(out, "out", dt, (B, O)), _dims(dims),
+        _dtype_code(x), _stream(x, stream))
+    _lib.check(st, "gdn_decode_step")
+    return out
 
 
 def gdn_layer_decode(x, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, state, conv_state,

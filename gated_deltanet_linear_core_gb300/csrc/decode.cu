@@ -146,7 +146,200 @@ cudaError_t decode_t(const DeltaArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- fused decode step
+// conv update + SiLU -> gates, l2 norms -> recurrence -> RMSNormGated for one
+// token per sequence.  One CTA per (sequence, key head): it owns every conv
+// channel of that key head (q, k and the r = H_v / H_k value heads' v), so it
+// reads their old conv state and writes the shifted state in place with no
+// other CTA touching them; it then runs the recurrence of its r value heads
+// one after the other, each streaming its state once through registers as
+// above, with the RMSNormGated of the head's output row as the epilogue.
+// The conv output is rounded to the activation dtype before the rule, as the
+// separate calls round y.
+template <typename T, int D, int NW, int RMAX>
+__global__ void __launch_bounds__(NW * 32, (D >= 128 ? 2 : 1))
+decode_step_kernel(DecodeStepArgs a) {
+    constexpr int NT = NW * 32;
+    constexpr int TPR = D / 4;
+    constexpr int RPP = NT / TPR;
+    constexpr int PASSES = D / RPP;
+    static_assert(NT % TPR == 0 && D % RPP == 0 && NT >= D, "layout");
+
+    const int b = blockIdx.x / a.H_k;
+    const int kh = blockIdx.x - b * a.H_k;
+    const int r = a.H_v / a.H_k;
+    const int64_t slot = a.slots != nullptr ? a.slots[b] : b;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cq = tid % TPR;
+    const int r0 = tid / TPR;
+    const int C = 2 * a.H_k * D + a.H_v * D;
+
+    __shared__ __align__(16) float qs[D], ks[D], vs[RMAX][D], ds[D], os[D];
+    __shared__ __align__(16) float red[2][RPP][D];
+    __shared__ float gb[RMAX][2];
+    __shared__ float wsum[NW];
+
+    // the first head's state streams in while the conv runs
+    float4 s[PASSES];
+    auto load_state = [&](int j) {
+        const float* S = a.state + (slot * a.H_v + kh * r + j) * D * D;
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p)
+            s[p] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(r0 + p * RPP) * D) + cq);
+    };
+    load_state(0);
+
+    // 1. conv update of the group's channels: q, k, then the r heads' v, one
+    //    16-byte vector of channels per thread (x, 3 state and 4 weight
+    //    vectors loaded together; [c][3] and [c][4] keep V channels contiguous)
+    {
+        constexpr int V = Vec16<T>::N;
+        const T* x = static_cast<const T*>(a.x) + (int64_t)b * C;
+        const T* w = static_cast<const T*>(a.conv_w);
+        T* cs = static_cast<T*>(a.conv_state) + slot * C * 3;
+        const int nvec = (2 + r) * D / V;
+        for (int e = tid; e < nvec; e += NT) {
+            const int grp = (e * V) / D, i0 = e * V - grp * D;
+            const int c0 = grp == 0 ? kh * D + i0
+                         : grp == 1 ? a.H_k * D + kh * D + i0
+                                    : 2 * a.H_k * D + (kh * r + grp - 2) * D + i0;
+            float xv[V], st[3 * V], wt[4 * V];
+            load16(x + c0, xv);
+#pragma unroll
+            for (int k = 0; k < 3; ++k) load16(cs + (int64_t)c0 * 3 + k * V, st + k * V);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) load16(w + (int64_t)c0 * 4 + k * V, wt + k * V);
+            float* dst = grp == 0 ? qs + i0 : grp == 1 ? ks + i0 : vs[grp - 2] + i0;
+            float nst[3 * V];
+#pragma unroll
+            for (int q = 0; q < V; ++q) {
+                float acc = wt[q * 4] * st[q * 3];
+                acc = fmaf(wt[q * 4 + 1], st[q * 3 + 1], acc);
+                acc = fmaf(wt[q * 4 + 2], st[q * 3 + 2], acc);
+                acc = fmaf(wt[q * 4 + 3], xv[q], acc);
+                dst[q] = to_f(from_f<T>(silu_f(acc)));
+                nst[q * 3] = st[q * 3 + 1];
+                nst[q * 3 + 1] = st[q * 3 + 2];
+                nst[q * 3 + 2] = xv[q];
+            }
+#pragma unroll
+            for (int k = 0; k < 3; ++k) store16(cs + (int64_t)c0 * 3 + k * V, nst + k * V);
+        }
+        if (tid < r) {
+            const int h = kh * r + tid;
+            const int64_t gi = (int64_t)b * a.H_v + h;
+            gb[tid][0] = gate_g(to_f(static_cast<const T*>(a.a)[gi]), a.A_log[h], a.dt_bias[h]);
+            gb[tid][1] = sigmoid_f(to_f(static_cast<const T*>(a.b)[gi]));
+        }
+    }
+    __syncthreads();
+    float sq = 0.f, sk = 0.f, sqk = 0.f;
+    for (int i = lane; i < D; i += 32) {
+        sq = fmaf(qs[i], qs[i], sq);
+        sk = fmaf(ks[i], ks[i], sk);
+        sqk = fmaf(qs[i], ks[i], sqk);
+    }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    sqk = warp_sum(sqk);
+    float rq = a.scale, rk = 1.f;
+    if (a.l2norm) {
+        rq = a.scale / sqrtf(sq + 1e-6f);
+        rk = 1.f / sqrtf(sk + 1e-6f);
+    }
+    const float kq = sqk * rq * rk;
+
+    // 2. the r value heads in turn
+    for (int j = 0; j < r; ++j) {
+        const int h = kh * r + j;
+        float* __restrict__ S = a.state + (slot * a.H_v + h) * D * D;
+        if (j > 0) load_state(j);
+        float mk[4] = {0.f, 0.f, 0.f, 0.f}, mq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p) {
+            const int i = r0 + p * RPP;
+            const float kv = ks[i] * rk, qv = qs[i] * rq;
+            mk[0] = fmaf(s[p].x, kv, mk[0]); mk[1] = fmaf(s[p].y, kv, mk[1]);
+            mk[2] = fmaf(s[p].z, kv, mk[2]); mk[3] = fmaf(s[p].w, kv, mk[3]);
+            mq[0] = fmaf(s[p].x, qv, mq[0]); mq[1] = fmaf(s[p].y, qv, mq[1]);
+            mq[2] = fmaf(s[p].z, qv, mq[2]); mq[3] = fmaf(s[p].w, qv, mq[3]);
+        }
+        *reinterpret_cast<float4*>(&red[0][r0][cq * 4]) = make_float4(mk[0], mk[1], mk[2], mk[3]);
+        *reinterpret_cast<float4*>(&red[1][r0][cq * 4]) = make_float4(mq[0], mq[1], mq[2], mq[3]);
+        __syncthreads();
+        const float eg = expf(gb[j][0]);
+        const float bt = gb[j][1];
+        float o2 = 0.f;
+        for (int c = tid; c < D; c += NT) {
+            float m = 0.f, pq = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < RPP; ++rr) {
+                m += red[0][rr][c];
+                pq += red[1][rr][c];
+            }
+            const float delta = bt * (vs[j][c] - eg * m);
+            ds[c] = delta;
+            const float o = to_f(from_f<T>(eg * pq + kq * delta));  // o as the separate call stores it
+            os[c] = o;
+            o2 = fmaf(o, o, o2);
+        }
+        o2 = warp_sum(o2);
+        if (lane == 0) wsum[warp] = o2;
+        __syncthreads();
+        // S <- e^g S + k^ delta^T, written from registers
+        const float4 d4 = *reinterpret_cast<const float4*>(&ds[cq * 4]);
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p) {
+            const int i = r0 + p * RPP;
+            const float kv = ks[i] * rk;
+            float4 n;
+            n.x = fmaf(kv, d4.x, eg * s[p].x);
+            n.y = fmaf(kv, d4.y, eg * s[p].y);
+            n.z = fmaf(kv, d4.z, eg * s[p].z);
+            n.w = fmaf(kv, d4.w, eg * s[p].w);
+            __stcs(reinterpret_cast<float4*>(S + (int64_t)i * D) + cq, n);
+        }
+        // RMSNormGated of the head's output row
+        float tot = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < NW; ++ww) tot += wsum[ww];
+        const float rs = rsqrtf(tot / (float)D + a.eps);
+        const T* z = static_cast<const T*>(a.z) + ((int64_t)b * a.H_v + h) * D;
+        T* out = static_cast<T*>(a.out) + ((int64_t)b * a.H_v + h) * D;
+        const T* nw = static_cast<const T*>(a.norm_w);
+        for (int c = 2 * tid; c < D; c += 2 * NT) {
+            const float2 g = silu2<T>(make_float2(to_f(z[c]), to_f(z[c + 1])));
+            const float2 res = __fmul2_rn(__fmul2_rn(make_float2(to_f(nw[c]), to_f(nw[c + 1])),
+                                                     __fmul2_rn(make_float2(os[c], os[c + 1]), make_float2(rs, rs))),
+                                          g);
+            out[c] = from_f<T>(res.x);
+            out[c + 1] = from_f<T>(res.y);
+        }
+        __syncthreads();  // red, ds, os and wsum are reused by the next head
+    }
+}
+
+template <typename T>
+cudaError_t decode_step_t(const DecodeStepArgs& a, cudaStream_t s) {
+    const unsigned units = (unsigned)(a.B * a.H_k);
+    if (units == 0) return cudaSuccess;
+    const int r = a.H_v / a.H_k;
+    if (r > 8) return cudaErrorNotSupported;
+    // same thread layout (and so the same summation order of S^T k and S^T q)
+    // as the recurrent decode kernel: the fused step's state is bit-identical
+    // to the separate calls'
+    if (a.D == 128)
+        decode_step_kernel<T, 128, 8, 8><<<units, 256, 0, s>>>(a);
+    else
+        decode_step_kernel<T, 16, 1, 8><<<units, 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_decode_step(const DecodeStepArgs& a, gdn_dtype_t dt, cudaStream_t s) {
+    return dt == GDN_BF16 ? decode_step_t<bf16>(a, s) : decode_step_t<float>(a, s);
+}
 
 cudaError_t launch_recurrent_decode(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s) {
     return dt == GDN_BF16 ? decode_t<bf16>(a, s) : decode_t<float>(a, s);

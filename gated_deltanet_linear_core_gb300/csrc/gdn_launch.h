@@ -56,6 +56,24 @@ cudaError_t launch_chunk_ffma(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s
 // Recurrent decode: T = B tokens, sequence i = token i, state in place (S0 == S_final).
 cudaError_t launch_recurrent_decode(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s);
 
+// Fused decode step: conv update, gates, recurrence and RMSNormGated for one
+// token per sequence; conv state and state in place at slots[b] (or b).
+struct DecodeStepArgs {
+    const void* x;         // [B, conv_dim]
+    const void* conv_w;    // [conv_dim, 4]
+    void* conv_state;      // [slots, conv_dim, 3]
+    const void *z, *a, *b; // [B, H_v*D], [B, H_v], [B, H_v]
+    const float *A_log, *dt_bias;
+    float* state;          // [slots, H_v, D, D]
+    const void* norm_w;    // [D]
+    const int32_t* slots;  // [B] or null
+    int B, H_k, H_v, D;
+    float scale, eps;
+    int l2norm;
+    void* out;             // [B, H_v*D]
+};
+cudaError_t launch_decode_step(const DecodeStepArgs& a, gdn_dtype_t dt, cudaStream_t s);
+
 // cuTensorMapEncodeTiled from the driver (nullptr if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensormap_encoder();
 

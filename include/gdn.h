@@ -301,6 +301,36 @@ gdn_status_t gdn_recurrent_decode(const void* qkv, const void* a, const void* b,
                                   void* stream);
 
 /*
+ * One fused decode step of the layer core: conv update + SiLU (as
+ * gdn_conv1d_update), gates and l2 norms, the recurrent rule (as
+ * gdn_recurrent_decode) and RMSNormGated (as gdn_rmsnorm_gated) for one token
+ * of each of B sequences, in one kernel (one CTA per sequence and key head).
+ * Defined by the passages of those three calls; the fusion has no counterpart
+ * on the pages beyond the hybrid cache they describe (NxD-Inference PR "Add
+ * Qwen3.6-27B hybrid DeltaNet/GQA contrib model and vLLM serving path",
+ * Summary: GDN recurrent and convolution state per cache slot).
+ *   x          (device) [B, conv_dim]      dtype (pre-conv mixed_qkv of the token)
+ *   conv_w     (device) [conv_dim, 4]      dtype
+ *   conv_state (device) [n_slots, conv_dim, 3] dtype, updated in place
+ *   z          (device) [B, H_v*d_v]       dtype
+ *   a, b       (device) [B, H_v]           dtype;  A_log, dt_bias (device) [H_v] f32
+ *   state      (device) [n_slots, H_v, d_k, d_v] f32, updated in place
+ *   norm_w     (device) [d_v] dtype;  norm_eps > 0 (the layer uses 1e-6)
+ *   slots      (device) [B] int32 cache slot of each sequence, or NULL (slot b);
+ *              the slots of one call must be distinct and < n_slots (not checked
+ *              on the device: an out-of-range slot is out of bounds)
+ *   scale, flags as gdn_recurrent_decode;  out (device) [B, H_v*d_v] dtype
+ * H_v / H_k <= 8.  Results equal the three separate calls up to the rounding
+ * order of the norm's sum of squares.
+ */
+gdn_status_t gdn_decode_step(const void* x, const void* conv_w, void* conv_state, const void* z,
+                             const void* a, const void* b, const float* A_log,
+                             const float* dt_bias, float* state, const void* norm_w,
+                             float norm_eps, const int32_t* slots, int32_t B, float scale,
+                             uint32_t flags, void* out, gdn_dims_t dims, gdn_dtype_t dtype,
+                             void* stream);
+
+/*
  * RMSNormGated over each value head.
  * Defined by: cortex GatedDeltaNet commit, "Output": RMSNormGated(core_attn_out, z).
  *   out[t, h*d_v + j] = w[j] * o[t,h,j] / sqrt(mean_j o[t,h,j]^2 + eps) * silu(z[t, h*d_v + j])

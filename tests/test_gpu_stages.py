@@ -286,3 +286,53 @@ def test_a_wait_that_runs_out_is_reported_and_the_context_survives():
     o_ref, S_ref, _ = _oracle_delta(inp, shape)
     assert_close("o", host(o), o_ref, TOL[torch.bfloat16], per_head_axis=1)
     assert_close("S_final", host(Sf), S_ref, TOL[torch.bfloat16], per_head_axis=1)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [W.TINY, SMALL_128], ids=["d16", "d128"])
+def test_fused_decode_step_with_slots(dtype, shape):
+    """gdn_decode_step (conv update + gates + recurrence + RMSNormGated in one
+    kernel) on cache slots: the outputs of all steps and the final states match
+    the oracle (one decode step of B sequences = a layer prefill of B one-token
+    sequences from their states), and after every step the states equal the
+    three separate calls' bit for bit."""
+    B, n_slots, steps = 5, 9, 3
+    d = W.decode_inputs(shape, dtype, B, steps, seed=41)
+    p = W.layer_params(shape, dtype, seed=41)
+    S_all = W.draw((n_slots, shape.H_v, shape.d_k, shape.d_v), seed=41, stream=60,
+                   dtype=torch.float32, p1=0.02)
+    cs_all = W.draw((n_slots, shape.conv_dim, 3), seed=41, stream=61, dtype=dtype)
+    slots = torch.tensor([7, 2, 0, 5, 3], dtype=torch.int32)
+    pd = {k: v.cuda() for k, v in p.items()}
+    S_f, cs_f = S_all.clone().cuda(), cs_all.clone().cuda()  # fused, on slots
+    S_u = S_all[slots.long()].clone().cuda()                  # separate calls, dense
+    cs_u = cs_all[slots.long()].clone().cuda()
+    S_ref = W.to_f64(S_all[slots.long()])
+    cs_ref = W.to_f64(cs_all[slots.long()])
+    f = W.to_f64
+    outs, refs = [], []
+    for t in range(steps):
+        x, z, a, b = (d[k][t].cuda() for k in ("qkv", "z", "a", "b"))
+        out = gdn.gdn_decode_step(x, z, a, b, pd["conv_w"], pd["A_log"], pd["dt_bias"],
+                                  pd["norm_w"], _dims(shape), S_f, cs_f, slots=slots.cuda())
+        y = gdn.gdn_conv1d_update(x, pd["conv_w"], cs_u, _dims(shape), True)
+        o = gdn.gdn_recurrent_decode(y, S_u, _dims(shape), a, b, pd["A_log"], pd["dt_bias"])
+        out_u = gdn.gdn_rmsnorm_gated(o, z, pd["norm_w"], _dims(shape))
+        gdn.gdn_sync_status()
+        ref = oracle.layer_prefill(f(d["qkv"][t]), f(d["z"][t]), f(d["a"][t]), f(d["b"][t]),
+                                   f(p["conv_w"]), f(p["A_log"]), f(p["dt_bias"]), f(p["norm_w"]),
+                                   shape.H_k, shape.H_v, shape.d_k, shape.d_v,
+                                   cu_seqlens=np.arange(B + 1), S0=S_ref, conv_state0=cs_ref)
+        S_ref, cs_ref = ref["S"], ref["conv_state"]
+        outs.append(host(out))
+        refs.append(ref["out"])
+        assert torch.equal(S_f[slots.long()].cpu(), S_u.cpu()), f"state step {t}"
+        assert torch.equal(cs_f[slots.long()].cpu(), cs_u.cpu()), f"conv state step {t}"
+        assert rel_l2(host(out), host(out_u)) <= 1e-5
+    # the decode outputs as one tensor [steps, B, H_v*d_v] (rel-L2 per output tensor)
+    assert_close("out", np.stack(outs), np.stack(refs), TOL[dtype])
+    assert_close("S", host(S_f[slots.long()]), S_ref, TOL[dtype], per_head_axis=1)
+    # slots not named by the call are untouched
+    others = [i for i in range(n_slots) if i not in slots.tolist()]
+    assert torch.equal(S_f[others].cpu(), S_all[others])
+    assert torch.equal(cs_f[others].cpu(), cs_all[others])
