@@ -350,7 +350,8 @@ def run_ours(args):
         "call": "gdn_decode_step (one fused kernel per step)",
         "roofline": {"kernel": "gdn_decode_step", "bound": "hbm", "achieved": round(f_gbs, 1),
                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(f_gbs / pk["hbm_gbs"], 4),
-                     "peak_source": pk["source"] + " (HBM copy)", "traffic": None,
+                     "peak_source": pk["source"] + " (HBM copy)",
+                     "traffic": traffic_record("decode_step"),
                      "algorithmic_bytes_per_launch": fbytes},
         "separate_calls": {
             "value": round(world * B * nd / max_over_ranks(dist, sum(dstep_ms) / 1e3, dev), 1),
