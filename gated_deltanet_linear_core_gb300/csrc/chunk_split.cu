@@ -1009,8 +1009,11 @@ int sm_count() {
 
 // Chunk offsets, then per segment: intra, chain.  The chain splits each
 // head's state into two 64-column slices when that still leaves at most one
-// CTA per SM.
-cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cudaStream_t s) {
+// CTA per SM.  With a second stream s_pre and an event (one segment only), the
+// offsets and intra kernels run on s_pre and the chain on s after the event,
+// so the caller can overlap them with other work.
+cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cudaStream_t s,
+                         cudaStream_t s_pre = nullptr, cudaEvent_t ev_pre = nullptr) {
     const uint64_t conv_dim = 2ull * a.H_k * D + (uint64_t)a.H_v * D;
     const uint64_t U = (uint64_t)Ly.segc * a.H_v;
     const bool split = (int64_t)a.n_seq * a.H_v * 2 <= sm_count();
@@ -1028,10 +1031,22 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
                                  ChainLayout<128>::SMEM);
     if (e != cudaSuccess) return e;
 
-    chunk_offsets_kernel<<<1, 1024, 0, s>>>(a.cu, a.n_seq, a.T, w.coff);
+    const bool two = ev_pre != nullptr && Ly.n_seg == 1;
+    cudaStream_t si = two ? s_pre : s;
+    if (ev_pre != nullptr && !two) {
+        // more than one segment: everything in order on s, after s_pre's work
+        if ((e = cudaEventRecord(ev_pre, s_pre)) != cudaSuccess || (e = cudaStreamWaitEvent(s, ev_pre, 0)) != cudaSuccess)
+            return e;
+    }
+    chunk_offsets_kernel<<<1, 1024, 0, si>>>(a.cu, a.n_seq, a.T, w.coff);
     for (int64_t seg = 0; seg < Ly.n_seg; ++seg) {
         const int64_t C0 = seg * Ly.segc;
-        chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, s>>>(qmap, wtmap, utmap, a, w, C0);
+        chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, si>>>(qmap, wtmap, utmap, a, w, C0);
+        if (two) {
+            if ((e = cudaGetLastError()) != cudaSuccess || (e = cudaEventRecord(ev_pre, si)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(s, ev_pre, 0)) != cudaSuccess)
+                return e;
+        }
         if (split)
             chunk_chain_kernel<64><<<(unsigned)(a.n_seq * a.H_v * 2), NT_C, ChainLayout<64>::SMEM, s>>>(
                 qmap, wtmap, utmap, pmap, omap, a, w, C0, Ly.segc);
@@ -1058,6 +1073,15 @@ cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_by
     Work w = work_at(static_cast<uint8_t*>(workspace), Ly, a.H_v);
     if (a.S_final != nullptr) w.carry = a.S_final;
     return run_segments(a, w, Ly, s);
+}
+
+cudaError_t launch_chunk_split_two(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s_pre,
+                                   cudaStream_t s_chain, cudaEvent_t ev_pre) {
+    const Layout Ly = layout_of(a.n_seq, a.T, a.H_v);
+    if (workspace == nullptr || ws_bytes < Ly.total || ev_pre == nullptr) return cudaErrorInvalidValue;
+    Work w = work_at(static_cast<uint8_t*>(workspace), Ly, a.H_v);
+    if (a.S_final != nullptr) w.carry = a.S_final;
+    return run_segments(a, w, Ly, s_chain, s_pre, ev_pre);
 }
 
 namespace {

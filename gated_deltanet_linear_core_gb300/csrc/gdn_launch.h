@@ -83,6 +83,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensormap_encoder();
 size_t chunk_split_workspace_bytes(int n_seq, int64_t T, int H_v);
 cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes,
                                cudaStream_t s);
+// The same with the chunk offsets and intra kernels on s_pre and the chain on
+// s_chain after ev_pre (recorded on s_pre, waited on s_chain); with more than
+// one workspace segment everything runs on s_chain after ev_pre.
+cudaError_t launch_chunk_split_two(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s_pre,
+                                   cudaStream_t s_chain, cudaEvent_t ev_pre);
 // Kernel launches launch_chunk_split issues: chunk offsets, then intra + chain per segment.
 int chunk_split_launches(int n_seq, int64_t T, int H_v);
 

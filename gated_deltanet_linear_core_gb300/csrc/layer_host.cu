@@ -1,10 +1,14 @@
 // gdn_layer_prefill_host: the layer core (conv1d + SiLU -> chunked delta rule
 // -> RMSNormGated) for one sequence whose activations live in page-locked host
-// memory.  The tokens run in pieces: piece p's inputs are copied in on one
-// stream while piece p-1 computes on the caller's stream, and piece p-1's
-// output is copied out on a third stream while piece p computes, so the
-// host<->device copies overlap the kernels.  The conv state and the recurrent
-// state carry from piece to piece in place on the device.
+// memory.  The tokens run in pieces, each through four streams:
+//   copy-in:   piece p's inputs
+//   pre:       conv1d of piece p, then the chunk-local (intra) kernels
+//   caller's:  the state chain of piece p (in order, carrying the state), RMSNormGated
+//   copy-out:  piece p's output
+// so the copies, the chunk-parallel work of piece p + 1 and the sequential
+// chain of piece p overlap; only the chain and the norm are serial per piece.
+// The conv state and the recurrent state carry from piece to piece in place on
+// the device.
 #include <math.h>
 #include <stdint.h>
 
@@ -17,7 +21,7 @@ namespace {
 
 constexpr int kMaxDev = 128;
 std::mutex g_host_mu;
-cudaStream_t g_copy_in[kMaxDev], g_copy_out[kMaxDev];
+cudaStream_t g_copy_in[kMaxDev], g_copy_out[kMaxDev], g_pre[kMaxDev];
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -29,7 +33,7 @@ struct HostLayout {
     int64_t piece;  // tokens per piece (a multiple of 64 unless the whole sequence is one piece)
     size_t a, b;    // the whole sequence's gate inputs (copied once)
     Slot slot[2];
-    size_t chunk_ws, chunk_ws_bytes, total;
+    size_t chunk_ws[2], chunk_ws_bytes, total;
 };
 
 HostLayout host_layout(int64_t T, int H_k, int H_v, int D, int es, bool tensor_core) {
@@ -55,13 +59,14 @@ HostLayout host_layout(int64_t T, int H_k, int H_v, int D, int es, bool tensor_c
         q.o = off;   off = align256(off + (size_t)p * O * es);
         q.out = off; off = align256(off + (size_t)p * O * es);
     }
-    L.chunk_ws = off;
-    L.chunk_ws_bytes = tensor_core ? chunk_split_workspace_bytes(1, p, H_v) : 0;
-    L.total = off + L.chunk_ws_bytes;
+    L.chunk_ws_bytes = tensor_core ? align256(chunk_split_workspace_bytes(1, p, H_v)) : 0;
+    L.chunk_ws[0] = off; off += L.chunk_ws_bytes;
+    L.chunk_ws[1] = off; off += L.chunk_ws_bytes;
+    L.total = off;
     return L;
 }
 
-cudaError_t copy_streams(cudaStream_t* in, cudaStream_t* out) {
+cudaError_t copy_streams(cudaStream_t* in, cudaStream_t* out, cudaStream_t* pre) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -70,10 +75,12 @@ cudaError_t copy_streams(cudaStream_t* in, cudaStream_t* out) {
     if (g_copy_in[dev] == nullptr) {
         e = cudaStreamCreateWithFlags(&g_copy_in[dev], cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g_copy_out[dev], cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g_pre[dev], cudaStreamNonBlocking);
         if (e != cudaSuccess) return e;
     }
     *in = g_copy_in[dev];
     *out = g_copy_out[dev];
+    *pre = g_pre[dev];
     return cudaSuccess;
 }
 
@@ -94,20 +101,22 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
     const HostLayout L = host_layout(h.T, h.H_k, h.H_v, h.D, es, tc);
     const size_t C = (size_t)(2 * h.H_k + h.H_v) * h.D, O = (size_t)h.H_v * h.D;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    cudaStream_t cin, cout;
-    cudaError_t e = copy_streams(&cin, &cout);
+    cudaStream_t cin, cout, pre;
+    cudaError_t e = copy_streams(&cin, &cout, &pre);
     if (e != cudaSuccess) return e;
-    cudaEvent_t ev[7];  // in[2], comp[2], out[2], start
+    cudaEvent_t ev[9];  // in[2], comp[2], out[2], pre[2], start
     int made = 0;
-    for (; made < 7 && e == cudaSuccess; ++made)
+    for (; made < 9 && e == cudaSuccess; ++made)
         e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
     cudaEvent_t* ev_in = ev;
     cudaEvent_t* ev_comp = ev + 2;
     cudaEvent_t* ev_out = ev + 4;
-    // the copy streams start after whatever the caller queued on `s`
-    if (e == cudaSuccess) e = cudaEventRecord(ev[6], s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cin, ev[6], 0);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cout, ev[6], 0);
+    cudaEvent_t* ev_pre = ev + 6;
+    // the other streams start after whatever the caller queued on `s`
+    if (e == cudaSuccess) e = cudaEventRecord(ev[8], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cin, ev[8], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cout, ev[8], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(pre, ev[8], 0);
     // the gate inputs of the whole sequence (small) in two copies
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(ws + L.a, h.h_a, (size_t)h.T * h.H_v * es, cudaMemcpyHostToDevice, cin);
@@ -120,7 +129,8 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
         const int64_t t0 = p * L.piece;
         const int64_t tp = h.T - t0 < L.piece ? h.T - t0 : L.piece;
         const uint8_t* hq = static_cast<const uint8_t*>(h.h_qkv);
-        // inputs of piece p (the slot's previous piece has finished reading them)
+        // inputs of piece p, once piece p - 2 (same slot) has finished with the
+        // slot's buffers and chunk workspace
         if (p >= 2) e = cudaStreamWaitEvent(cin, ev_comp[sl], 0);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(ws + q.qkv, hq + (size_t)t0 * C * es, (size_t)tp * C * es, cudaMemcpyHostToDevice, cin);
@@ -128,17 +138,15 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
             e = cudaMemcpyAsync(ws + q.z, static_cast<const uint8_t*>(h.h_z) + (size_t)t0 * O * es,
                                 (size_t)tp * O * es, cudaMemcpyHostToDevice, cin);
         if (e == cudaSuccess) e = cudaEventRecord(ev_in[sl], cin);
-        // compute on the caller's stream once the inputs are in and the output
-        // slot has been copied out
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_in[sl], 0);
-        if (e == cudaSuccess && p >= 2) e = cudaStreamWaitEvent(s, ev_out[sl], 0);
+        // conv and the chunk-local kernels on the pre stream once the inputs are in
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(pre, ev_in[sl], 0);
         if (e == cudaSuccess) {
             ConvArgs c;
             c.x = ws + q.qkv; c.w = h.conv_w; c.cu = nullptr; c.n_seq = 1; c.T = tp; c.C = (int)C;
             c.state_in = p == 0 ? h.conv_state_in : h.conv_state_out;
             c.state_out = h.conv_state_out;
             c.ckpt_every = 0; c.ckpt = nullptr; c.ckpt_rows = 0; c.silu = 1; c.y = ws + q.y;
-            e = launch_conv1d_fwd(c, dt, s);
+            e = launch_conv1d_fwd(c, dt, pre);
         }
         if (e == cudaSuccess) {
             DeltaArgs d = {};
@@ -148,7 +156,18 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
             d.S0 = p == 0 ? h.initial_state : h.final_state;
             d.S_final = h.final_state;
             d.scale = h.scale; d.l2norm = h.l2norm; d.o = ws + q.o;
-            e = tc ? launch_chunk_split(d, ws + L.chunk_ws, L.chunk_ws_bytes, s) : launch_chunk_ffma(d, dt, s);
+            // the chain (and the norm after it) on the caller's stream, once the
+            // output slot has been copied out
+            if (e == cudaSuccess && p >= 2) e = cudaStreamWaitEvent(s, ev_out[sl], 0);
+            if (e == cudaSuccess) {
+                if (tc) {
+                    e = launch_chunk_split_two(d, ws + L.chunk_ws[sl], L.chunk_ws_bytes, pre, s, ev_pre[sl]);
+                } else {
+                    e = cudaEventRecord(ev_pre[sl], pre);
+                    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_pre[sl], 0);
+                    if (e == cudaSuccess) e = launch_chunk_ffma(d, dt, s);
+                }
+            }
         }
         if (e == cudaSuccess)
             e = launch_rmsnorm_gated(ws + q.o, ws + q.z, h.norm_w, h.eps, tp, h.H_v, h.D, ws + q.out, dt, s);
