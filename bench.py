@@ -382,8 +382,7 @@ def run_ours(args):
     cst_h = torch.empty((1, s.conv_dim, 3), dtype=wp.dtype, device=dev)
     ws_h = torch.empty(gdn._lib.load().gdn_layer_prefill_host_workspace_size(
         T, gdn._dims(dims), gdn._lib.GDN_BF16), dtype=torch.uint8, device=dev)
-    host_pieces = -(-T // gdn._lib.load().gdn_layer_prefill_host_piece(
-        T, gdn._dims(dims), gdn._lib.GDN_BF16))
+    host_pieces = gdn._lib.load().gdn_layer_prefill_host_pieces(T, gdn._dims(dims), gdn._lib.GDN_BF16)
 
     def e2e_step():
         gdn.gdn_layer_prefill_host(hin["mixed_qkv"], hin["z"], hin["a"], hin["b"], d["conv_w"],
@@ -406,7 +405,8 @@ def run_ours(args):
     clocks.mark(False)
     barrier(dist, dev)
     piece_launches = 2 + gdn.gdn_chunk_prefill_launches(
-        1, -(-T // host_pieces), dims, wp.dtype) + 1
+        1, gdn._lib.load().gdn_layer_prefill_host_piece(T, gdn._dims(dims), gdn._lib.GDN_BF16),
+        dims, wp.dtype) + 1
     launches += args.steps * host_pieces * piece_launches
     e_total = max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in eev) / 1e3, dev)
     e2e = {"value": round(world * T * args.steps / e_total, 1), "unit": "tokens/s",

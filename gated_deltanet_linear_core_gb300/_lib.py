@@ -47,6 +47,7 @@ SIGNATURES = {
     "gdn_selftest_bounded_wait": (ST, [I64, P]),
     "gdn_layer_prefill_host_workspace_size": (SZ, [I64, Dims, ST]),
     "gdn_layer_prefill_host_piece": (I64, [I64, Dims, ST]),
+    "gdn_layer_prefill_host_pieces": (I64, [I64, Dims, ST]),
     "gdn_layer_prefill_host": (ST, [P, P, P, P, P, P, P, P, I64, P, P, P, P, F32, U32, F32, P, P, SZ,
                                     Dims, ST, P]),
     "gdn_conv1d_fwd": (ST, [P, P, P, I32, I64, P, P, I32, P, I64, I32, P, Dims, ST, P]),

@@ -137,6 +137,12 @@ int64_t gdn_layer_prefill_host_piece(int64_t T, gdn_dims_t dims, gdn_dtype_t dty
                                          dtype == GDN_BF16 && dims.d_k == 128);
 }
 
+int64_t gdn_layer_prefill_host_pieces(int64_t T, gdn_dims_t dims, gdn_dtype_t dtype) {
+    if (check_dims(dims, dtype) != GDN_OK || T <= 0 || T > (int64_t)INT32_MAX) return 0;
+    return gdn::layer_prefill_host_pieces(T, dims.H_k, dims.H_v, dims.d_k, (int)elem_size(dtype),
+                                          dtype == GDN_BF16 && dims.d_k == 128);
+}
+
 namespace {
 bool page_locked(const void* p) {
     cudaPointerAttributes at;

@@ -125,6 +125,7 @@ struct HostLayerArgs {
 };
 size_t layer_prefill_host_workspace_bytes(int64_t T, int H_k, int H_v, int D, int es, bool tensor_core);
 int64_t layer_prefill_host_piece(int64_t T, int H_k, int H_v, int D, int es, bool tensor_core);
+int64_t layer_prefill_host_pieces(int64_t T, int H_k, int H_v, int D, int es, bool tensor_core);
 cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, void* workspace, cudaStream_t s);
 
 }  // namespace gdn

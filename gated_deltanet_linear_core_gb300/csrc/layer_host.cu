@@ -25,6 +25,9 @@ cudaStream_t g_copy_in[kMaxDev], g_copy_out[kMaxDev], g_pre[kMaxDev];
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// pieces in flight: piece p reuses the buffers of piece p - kSlots
+constexpr int kSlots = 3;
+
 struct Slot {
     size_t qkv, z, y, o, out;  // byte offsets in the workspace
 };
@@ -32,8 +35,8 @@ struct Slot {
 struct HostLayout {
     int64_t piece;  // tokens per piece (a multiple of 64 unless the whole sequence is one piece)
     size_t a, b;    // the whole sequence's gate inputs (copied once)
-    Slot slot[2];
-    size_t chunk_ws[2], chunk_ws_bytes, total;
+    Slot slot[kSlots];
+    size_t chunk_ws[kSlots], chunk_ws_bytes, total;
 };
 
 HostLayout host_layout(int64_t T, int H_k, int H_v, int D, int es, bool tensor_core) {
@@ -51,7 +54,7 @@ HostLayout host_layout(int64_t T, int H_k, int H_v, int D, int es, bool tensor_c
     size_t off = 0;
     L.a = off; off = align256(off + (size_t)T * H_v * es);
     L.b = off; off = align256(off + (size_t)T * H_v * es);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
         Slot& q = L.slot[s];
         q.qkv = off; off = align256(off + (size_t)p * C * es);
         q.z = off;   off = align256(off + (size_t)p * O * es);
@@ -60,10 +63,50 @@ HostLayout host_layout(int64_t T, int H_k, int H_v, int D, int es, bool tensor_c
         q.out = off; off = align256(off + (size_t)p * O * es);
     }
     L.chunk_ws_bytes = tensor_core ? align256(chunk_split_workspace_bytes(1, p, H_v)) : 0;
-    L.chunk_ws[0] = off; off += L.chunk_ws_bytes;
-    L.chunk_ws[1] = off; off += L.chunk_ws_bytes;
+    for (int s = 0; s < kSlots; ++s) {
+        L.chunk_ws[s] = off;
+        off += L.chunk_ws_bytes;
+    }
     L.total = off;
     return L;
+}
+
+// Piece plan: pieces of L.piece tokens, except that when the sequence is a
+// whole number (>= 2) of full pieces the last one is cut into 3/4 and 1/4
+// (multiples of 64): after the last copy in, only the small last piece's
+// kernels and copy out remain.
+struct PiecePlan {
+    int64_t full;  // leading pieces of L.piece tokens
+    int64_t tail[2];
+    int n_tail;
+};
+
+PiecePlan piece_plan(int64_t T, int64_t P) {
+    PiecePlan q;
+    q.n_tail = 0;
+    q.full = (T + P - 1) / P;
+    const int64_t quarter = (P / 4) & ~(int64_t)63;
+    if (T > P && T % P == 0 && quarter >= 64) {
+        q.full = T / P - 1;
+        q.tail[0] = P - quarter;
+        q.tail[1] = quarter;
+        q.n_tail = 2;
+    }
+    return q;
+}
+
+int64_t plan_count(const PiecePlan& q) { return q.full + q.n_tail; }
+
+// tokens [t0, t0 + tp) of piece p
+void plan_span(const PiecePlan& q, int64_t T, int64_t P, int64_t p, int64_t& t0, int64_t& tp) {
+    if (p < q.full) {
+        t0 = p * P;
+        tp = T - t0 < P ? T - t0 : P;
+        return;
+    }
+    t0 = q.full * P;
+    for (int64_t i = 0; i < p - q.full; ++i) t0 += q.tail[i];
+    tp = q.tail[p - q.full];
 }
 
 cudaError_t copy_streams(cudaStream_t* in, cudaStream_t* out, cudaStream_t* pre) {
@@ -94,6 +137,10 @@ int64_t layer_prefill_host_piece(int64_t T, int H_k, int H_v, int D, int es, boo
     return host_layout(T, H_k, H_v, D, es, tensor_core).piece;
 }
 
+int64_t layer_prefill_host_pieces(int64_t T, int H_k, int H_v, int D, int es, bool tensor_core) {
+    return T > 0 ? plan_count(piece_plan(T, host_layout(T, H_k, H_v, D, es, tensor_core).piece)) : 0;
+}
+
 cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, void* workspace,
                                       cudaStream_t s) {
     const int es = dt == GDN_BF16 ? 2 : 4;
@@ -104,34 +151,37 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
     cudaStream_t cin, cout, pre;
     cudaError_t e = copy_streams(&cin, &cout, &pre);
     if (e != cudaSuccess) return e;
-    cudaEvent_t ev[9];  // in[2], comp[2], out[2], pre[2], start
+    constexpr int NEV = 4 * kSlots + 1;
+    cudaEvent_t ev[NEV];  // in, comp, out, pre per slot; start
     int made = 0;
-    for (; made < 9 && e == cudaSuccess; ++made)
+    for (; made < NEV && e == cudaSuccess; ++made)
         e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
     cudaEvent_t* ev_in = ev;
-    cudaEvent_t* ev_comp = ev + 2;
-    cudaEvent_t* ev_out = ev + 4;
-    cudaEvent_t* ev_pre = ev + 6;
+    cudaEvent_t* ev_comp = ev + kSlots;
+    cudaEvent_t* ev_out = ev + 2 * kSlots;
+    cudaEvent_t* ev_pre = ev + 3 * kSlots;
+    cudaEvent_t ev_start = ev[4 * kSlots];
     // the other streams start after whatever the caller queued on `s`
-    if (e == cudaSuccess) e = cudaEventRecord(ev[8], s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cin, ev[8], 0);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cout, ev[8], 0);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(pre, ev[8], 0);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cin, ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cout, ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(pre, ev_start, 0);
     // the gate inputs of the whole sequence (small) in two copies
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(ws + L.a, h.h_a, (size_t)h.T * h.H_v * es, cudaMemcpyHostToDevice, cin);
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(ws + L.b, h.h_b, (size_t)h.T * h.H_v * es, cudaMemcpyHostToDevice, cin);
-    const int64_t n_piece = (h.T + L.piece - 1) / L.piece;
+    const PiecePlan plan = piece_plan(h.T, L.piece);
+    const int64_t n_piece = plan_count(plan);
     for (int64_t p = 0; p < n_piece && e == cudaSuccess; ++p) {
-        const int sl = (int)(p & 1);
+        const int sl = (int)(p % kSlots);
         const Slot& q = L.slot[sl];
-        const int64_t t0 = p * L.piece;
-        const int64_t tp = h.T - t0 < L.piece ? h.T - t0 : L.piece;
+        int64_t t0, tp;
+        plan_span(plan, h.T, L.piece, p, t0, tp);
         const uint8_t* hq = static_cast<const uint8_t*>(h.h_qkv);
-        // inputs of piece p, once piece p - 2 (same slot) has finished with the
+        // inputs of piece p, once piece p - kSlots (same slot) has finished with the
         // slot's buffers and chunk workspace
-        if (p >= 2) e = cudaStreamWaitEvent(cin, ev_comp[sl], 0);
+        if (p >= kSlots) e = cudaStreamWaitEvent(cin, ev_comp[sl], 0);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(ws + q.qkv, hq + (size_t)t0 * C * es, (size_t)tp * C * es, cudaMemcpyHostToDevice, cin);
         if (e == cudaSuccess)
@@ -158,7 +208,7 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
             d.scale = h.scale; d.l2norm = h.l2norm; d.o = ws + q.o;
             // the chain (and the norm after it) on the caller's stream, once the
             // output slot has been copied out
-            if (e == cudaSuccess && p >= 2) e = cudaStreamWaitEvent(s, ev_out[sl], 0);
+            if (e == cudaSuccess && p >= kSlots) e = cudaStreamWaitEvent(s, ev_out[sl], 0);
             if (e == cudaSuccess) {
                 if (tc) {
                     e = launch_chunk_split_two(d, ws + L.chunk_ws[sl], L.chunk_ws_bytes, pre, s, ev_pre[sl]);
@@ -180,8 +230,8 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
         if (e == cudaSuccess) e = cudaEventRecord(ev_out[sl], cout);
     }
     // join: the caller's stream waits for the last copies out
-    for (int sl = 0; sl < 2 && e == cudaSuccess; ++sl)
-        if (n_piece > sl) e = cudaStreamWaitEvent(s, ev_out[(n_piece - 1 - sl) & 1], 0);
+    for (int sl = 0; sl < kSlots && e == cudaSuccess; ++sl)
+        if (n_piece > sl) e = cudaStreamWaitEvent(s, ev_out[(n_piece - 1 - sl) % kSlots], 0);
     for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);  // released once complete
     return e;
 }

@@ -160,11 +160,16 @@ size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t
  * gdn_conv1d_fwd, gdn_chunk_prefill and gdn_rmsnorm_gated -- for ONE sequence
  * whose activations and output are in page-locked host memory (the pages have
  * no counterpart; this is the host-buffer form of the three calls).  The tokens
- * run in pieces (gdn_layer_prefill_host_piece): a piece's inputs are copied to
- * the device while the previous piece computes, and its output is copied back
- * while the next computes, on two internal streams of the library that start
- * after the work already queued on `stream` and are joined back to it.  The
- * conv state and the recurrent state carry from piece to piece on the device.
+ * run in gdn_layer_prefill_host_pieces pieces of at most
+ * gdn_layer_prefill_host_piece tokens, cut at multiples of 64 (when T is a
+ * whole number of full pieces the last is cut into 3/4 and 1/4, so little work
+ * remains after the last copy in).  A piece's inputs are copied to the device
+ * while earlier pieces compute and its output is copied back while later ones
+ * do; the copies, each piece's conv and chunk-local kernels, and the state
+ * chain + RMSNormGated run on three internal streams of the library and
+ * `stream`, starting after the work already queued on `stream` and joined back
+ * to it.  The conv state and the recurrent state carry from piece to piece on
+ * the device, so the result equals the three device calls bit for bit.
  *   h_qkv      (host, page-locked) [T, conv_dim]    dtype
  *   h_z        (host, page-locked) [T, H_v*d_v]     dtype
  *   h_a, h_b   (host, page-locked) [T, H_v]         dtype
@@ -179,10 +184,11 @@ size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t
  *   workspace  (device) >= gdn_layer_prefill_host_workspace_size(T, dims, dtype) bytes
  * Host buffers that are not page-locked: GDN_ERR_INVALID_ARG.  No checkpoints.
  * Make the first call on a device before any stream capture (it creates the
- * two copy streams).  h_out is complete once `stream` reaches this point.
+ * three internal streams).  h_out is complete once `stream` reaches this point.
  */
 size_t gdn_layer_prefill_host_workspace_size(int64_t T, gdn_dims_t dims, gdn_dtype_t dtype);
 int64_t gdn_layer_prefill_host_piece(int64_t T, gdn_dims_t dims, gdn_dtype_t dtype);
+int64_t gdn_layer_prefill_host_pieces(int64_t T, gdn_dims_t dims, gdn_dtype_t dtype);
 gdn_status_t gdn_layer_prefill_host(const void* h_qkv, const void* h_z, const void* h_a,
                                     const void* h_b, const void* conv_w, const float* A_log,
                                     const float* dt_bias, const void* norm_w, int64_t T,

@@ -199,6 +199,22 @@ def test_prefill_launch_count(lib):
     assert gdn.gdn_chunk_prefill_launches(1, 0, dims, torch.bfloat16) == 0
 
 
+def test_host_prefill_piece_plan(lib):
+    # pieces of at most `piece` tokens, multiples of 64; a whole number (>= 2) of
+    # full pieces has its last piece cut into 3/4 and 1/4; a short sequence is
+    # one piece
+    d = gdn._dims(gdn.GDNDims(16, 48, 128, 128))
+    bf = gdn._lib.GDN_BF16
+    piece = lib.gdn_layer_prefill_host_piece
+    pieces = lib.gdn_layer_prefill_host_pieces
+    assert piece(4096, d, bf) == 512 and pieces(4096, d, bf) == 7 + 2
+    assert piece(3000, d, bf) == 512 and pieces(3000, d, bf) == 6
+    assert piece(1024, d, bf) == 1024 and pieces(1024, d, bf) == 1
+    assert piece(64, d, bf) == 64 and pieces(64, d, bf) == 1
+    assert piece(65536, d, bf) == 4096 and pieces(65536, d, bf) == 15 + 2
+    assert pieces(0, d, bf) == 0
+
+
 def test_binding_rejects_host_tensors_before_the_library():
     x = torch.zeros(4, 128)
     with pytest.raises(ValueError, match="CUDA"):
