@@ -238,3 +238,57 @@ def test_host_streamed_prefill_equals_device_prefill(T):
     for h in heads:
         sl = slice(h * shape.d_v, (h + 1) * shape.d_v)
         assert rel_l2(host(r_h["out"])[:, sl], ref[h]["out"]) <= TOL[torch.bfloat16]
+
+
+def _resume_inputs(inp, r, lengths, N, m):
+    """Inputs of the run resumed from checkpoint m[i] (token m[i] * N) of each
+    sequence of an uninterrupted run r with checkpoints every N tokens: the
+    remaining tokens, the state checkpoint as initial state and the conv
+    checkpoint (the 3 raw inputs before the resume point) as conv state."""
+    cu = [0] + list(np.cumsum(lengths))
+    rows0 = [0] + list(np.cumsum([L // N for L in lengths]))
+    keep, rest, rows = [], [], []
+    for i, L in enumerate(lengths):
+        assert 1 <= m[i] <= L // N
+        keep.append(torch.arange(cu[i] + m[i] * N, cu[i + 1]))
+        rest.append(L - m[i] * N)
+        rows.append(rows0[i] + m[i] - 1)
+    idx = torch.cat(keep)
+    res = {k: inp[k][idx] for k in ("mixed_qkv", "z", "a", "b")}
+    for k in ("conv_w", "A_log", "dt_bias", "norm_w"):
+        res[k] = inp[k]
+    res["cu_seqlens"] = W.cu_seqlens_of(rest)
+    res["S0"] = r["state_ckpt"][rows].cpu()
+    res["conv_state0"] = r["conv_ckpt"][rows].cpu()
+    return res, idx, rest, rows0
+
+
+@pytest.mark.parametrize("lengths,N,m", [
+    ([3000], 64, [1]),
+    ([3000], 192, [7]),
+    ([4096], 1024, [3]),
+    ([1000, 2500, 640], 128, [2, 19, 5]),  # the last sequence resumes at its end
+], ids=["N64-first", "N192-mid", "N1024-last", "varlen-N128"])
+def test_resume_from_checkpoint_is_bit_identical(lengths, N, m):
+    """Prefix reuse: resuming each sequence from its mid-sequence checkpoint (state
+    and conv checkpoints of an uninterrupted run) gives the uninterrupted run's
+    remaining outputs, final states, conv states and later checkpoints bit for
+    bit, whatever the alignment of the checkpoint cadence with the chunks."""
+    shape = W.QWEN36_27B
+    inp = W.layer_inputs(shape, torch.bfloat16, lengths, seed=41, init_state=True)
+    r = _run_prefill(inp, shape, ckpt_every=N)
+    res, idx, rest, rows0 = _resume_inputs(inp, r, lengths, N, m)
+    r2 = _run_prefill(res, shape, ckpt_every=N)
+    assert torch.equal(r2["out"], r["out"][idx.cuda()])
+    assert torch.equal(r2["final_state"], r["final_state"])
+    assert torch.equal(r2["conv_state"], r["conv_state"])
+    row = 0
+    for i, L in enumerate(lengths):
+        later = L // N - m[i]
+        assert later == rest[i] // N
+        if later:
+            a0 = rows0[i] + m[i]
+            assert torch.equal(r2["state_ckpt"][row:row + later], r["state_ckpt"][a0:a0 + later])
+            assert torch.equal(r2["conv_ckpt"][row:row + later], r["conv_ckpt"][a0:a0 + later])
+        row += later
+    assert torch.isfinite(r["out"]).all()
