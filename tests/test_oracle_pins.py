@@ -226,13 +226,13 @@ def test_tiny_bruteforce_householder_form(oracle_mod, d_k, d_v, T):
     np.testing.assert_allclose(S[0, 0], S2, rtol=1e-13, atol=1e-13)
 
 
-def chunked_dense(q, k, v, g, beta, S0, C):
+def chunked_dense(q, k, v, g, beta, S0, C, inverse=None):
     """Dense chunked (WY/UT) restatement of the delta rule for one head with
     pre-normalised q, k: per chunk, G = cumsum(g); A_ij = beta_i e^{G_i-G_j}
     k_i.k_j (j < i); T = (I + A)^-1 diag(beta); W = T diag(e^G) K; U = T V;
     U' = U - W S; O = diag(e^G) Q S + [(Q K^T) o e^{G_i-G_j} 1(j<=i)] U';
     S <- e^{G_n} S + (diag(e^{G_n - G_j}) K)^T U'.  numpy.linalg.solve does the
-    triangular system."""
+    triangular system, or `inverse(A)` = (I + A)^-1 when given."""
     L = len(g)
     S = S0.copy()
     O = np.zeros((L, v.shape[1]))
@@ -244,7 +244,8 @@ def chunked_dense(q, k, v, g, beta, S0, C):
         low = np.tril(np.ones((n, n), dtype=bool))
         Dm = np.exp(np.where(low, G[:, None] - G[None, :], -np.inf))
         A = np.tril(bb[:, None] * Dm * (K @ K.T), -1)
-        Tm = np.linalg.solve(np.eye(n) + A, np.diag(bb))
+        Tm = (np.linalg.solve(np.eye(n) + A, np.diag(bb)) if inverse is None
+              else inverse(A) @ np.diag(bb))
         W = Tm @ (np.exp(G)[:, None] * K)
         Up = Tm @ V - W @ S
         O[sl] = np.exp(G)[:, None] * (Q @ S) + ((Q @ K.T) * Dm) @ Up
