@@ -257,6 +257,31 @@ def run_ours(args):
     total_s = max_over_ranks(dist, sum(step_ms) / 1e3, dev)
     value = world * T * args.steps / total_s
     chunk_avg = sum(chunk_ms) / len(chunk_ms) / 1e3
+
+    # the same chunk stage with each chunk's (I + A)^-1 formed as the
+    # Neumann-style product instead of the direct solve (GDN_SOLVE_NEUMANN)
+    def neumann_chunk():
+        gdn.gdn_chunk_prefill(y, dims, d["a"], d["b"], d["A_log"], d["dt_bias"], final_state=S,
+                              o=o, solve="neumann")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        neumann_chunk()
+    nev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    clocks.mark(True)
+    for k in range(args.steps):
+        flush.zero_()
+        nev[k][0].record(stream)
+        neumann_chunk()
+        nev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark(False)
+    launches += args.steps * chunk_launches
+    neumann_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in nev)
+    chunk_solve = {"direct_ms": round(chunk_avg * 1e3, 4), "neumann_ms": round(neumann_ms, 4),
+                   "call": "gdn_chunk_prefill, flags GDN_QK_L2NORM vs | GDN_SOLVE_NEUMANN"}
     flops = FLOP_PER_TOKEN_HEAD * T * s.H_v
     achieved_tf = flops / chunk_avg / 1e12
     ncu_bytes = traffic_record("chunk_prefill")
@@ -430,6 +455,7 @@ def run_ours(args):
                        "d_k": s.d_k, "d_v": s.d_v, "chunk": 64, "state": "f32",
                        "l2": "flushed (512 MiB write) between timed steps",
                        "parallelism": f"replicas x{world}"},
+            "chunk_solve": chunk_solve,
             "per_kernel_ms": {"conv1d_fwd": round(statistics.mean(conv_ms), 4),
                               "chunk_prefill": round(statistics.mean(chunk_ms), 4),
                               "rmsnorm_gated": round(statistics.mean(norm_ms), 4)},

@@ -18,7 +18,7 @@ from dataclasses import dataclass
 import torch
 
 from . import _lib
-from ._lib import GDNError, GDN_QK_L2NORM  # noqa: F401
+from ._lib import GDNError, GDN_QK_L2NORM, GDN_SOLVE_NEUMANN  # noqa: F401
 
 __all__ = [
     "GDNDims", "GDNError", "gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
@@ -183,9 +183,13 @@ def _gate_ptrs(a, b, A_log, dt_bias, g, beta, dt):
 def gdn_chunk_prefill(qkv, dims, a=None, b=None, A_log=None, dt_bias=None, g=None, beta=None,
                       cu_seqlens=None, initial_state=None, final_state=None, ckpt_every=0,
                       state_ckpt_out=None, scale=0.0, l2norm_qk=True, o=None, workspace=None,
-                      stream=None):
+                      stream=None, solve="direct"):
     """Chunked gated delta rule over packed sequences.  qkv [T, conv_dim]
-    (post-conv); states [n_seq, H_v, d_k, d_v] f32; returns o [T, H_v, d_v]."""
+    (post-conv); states [n_seq, H_v, d_k, d_v] f32; returns o [T, H_v, d_v].
+    solve="neumann" forms each chunk's (I + A)^-1 as the Neumann-style product
+    (GDN_SOLVE_NEUMANN; tensor-core path only)."""
+    if solve not in ("direct", "neumann"):
+        raise ValueError(f"solve must be 'direct' or 'neumann', not {solve!r}")
     dt = qkv.dtype
     T = int(qkv.shape[0])
     if o is None:
@@ -204,7 +208,8 @@ def gdn_chunk_prefill(qkv, dims, a=None, b=None, A_log=None, dt_bias=None, g=Non
         _ptr(initial_state, "initial_state", torch.float32),
         _ptr(final_state, "final_state", torch.float32), int(ckpt_every),
         _ptr(state_ckpt_out, "state_ckpt_out", torch.float32), rows, float(scale),
-        _lib.GDN_QK_L2NORM if l2norm_qk else 0, _ptr(o, "o", dt), _ptr(workspace, "workspace"),
+        (_lib.GDN_QK_L2NORM if l2norm_qk else 0) | (_lib.GDN_SOLVE_NEUMANN if solve == "neumann" else 0),
+        _ptr(o, "o", dt), _ptr(workspace, "workspace"),
         ws, _dims(dims), _dtype_code(qkv), _stream(qkv, stream))
     _lib.check(st, "gdn_chunk_prefill")
     return o

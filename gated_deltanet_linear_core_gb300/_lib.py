@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_ALIGN",
 GDN_F32 = 0
 GDN_BF16 = 1
 GDN_QK_L2NORM = 1
+GDN_SOLVE_NEUMANN = 2
 
 
 class Dims(ctypes.Structure):

@@ -186,6 +186,7 @@ __device__ __forceinline__ float select_lane(const float (&v)[32], int lane) {
     return (lane & 1) ? d[1] : d[0];
 }
 
+template <bool NEUMANN>
 __global__ void __launch_bounds__(NT_I, 3)
 chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
                    const __grid_constant__ CUtensorMap umap, DeltaArgs a, Work w, int64_t C0) {
@@ -405,97 +406,166 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             }
         }
         __syncthreads();
-        // T' = (I + A)^-1 (unit lower triangular): the four diagonal 16-blocks
-        // by forward substitution (f32), then the off-diagonal blocks by
-        // doubling on warp-level tf32 MMAs (T' is rounded to bf16 right after),
-        //   T'_{10} = -D_1 A_{10} D_0 (and T'_{32}),  T'_{[23][01]} = -T'_{[23][23]} A_{[23][01]} T'_{[01][01]}
-        if (tid < 64) {
-            const int r0 = (tid >> 4) * 16, cl = tid & 15;
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) x[r] = r == cl ? 1.f : 0.f;
-#pragma unroll
-            for (int q = 0; q < 15; ++q)
-#pragma unroll
-                for (int r = q + 1; r < 16; ++r) x[r] = fmaf(-Am[(r0 + r) * A_PITCH + r0 + q], x[q], x[r]);
-#pragma unroll
-            for (int r = 0; r < 16; ++r) *tp_at(kq, r0 + r, r0 + cl) = x[r];
+        if constexpr (!NEUMANN) {
+            // T' = (I + A)^-1 (unit lower triangular): the four diagonal 16-blocks
+            // by forward substitution (f32), then the off-diagonal blocks by
+            // doubling on warp-level tf32 MMAs (T' is rounded to bf16 right after),
+            //   T'_{10} = -D_1 A_{10} D_0 (and T'_{32}),  T'_{[23][01]} = -T'_{[23][23]} A_{[23][01]} T'_{[01][01]}
+            if (tid < 64) {
+                const int r0 = (tid >> 4) * 16, cl = tid & 15;
+                float x[16];
+    #pragma unroll
+                for (int r = 0; r < 16; ++r) x[r] = r == cl ? 1.f : 0.f;
+    #pragma unroll
+                for (int q = 0; q < 15; ++q)
+    #pragma unroll
+                    for (int r = q + 1; r < 16; ++r) x[r] = fmaf(-Am[(r0 + r) * A_PITCH + r0 + q], x[q], x[r]);
+    #pragma unroll
+                for (int r = 0; r < 16; ++r) *tp_at(kq, r0 + r, r0 + cl) = x[r];
+            } else {
+                // meanwhile the other threads zero T' above its diagonal blocks
+                // (blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)), 2 float4 each
+    #pragma unroll
+                for (int e = tid - 64; e < 384; e += NT_I - 64) {
+                    const int blk = e >> 6, br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                    const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                    *reinterpret_cast<float4*>(tp_at(kq, 16 * br + ((e >> 2) & 15), 16 * bc + (e & 3) * 4)) =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            __syncthreads();
+            const int fg = lane >> 2, ft = lane & 3;  // MMA fragment row group, thread in group
+            if (warp < 4) {  // level 1, X = A_{b+1,b} D_b for b = 0, 2; warp = (block pair, 8 columns)
+                const int blk = warp >> 1, c0 = 32 * blk + 8 * (warp & 1), r0 = 32 * blk + 16;
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+    #pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int k0 = 32 * blk + 8 * ks;
+                    const float af[4] = {Am[(r0 + fg) * A_PITCH + k0 + ft], Am[(r0 + fg + 8) * A_PITCH + k0 + ft],
+                                         Am[(r0 + fg) * A_PITCH + k0 + ft + 4], Am[(r0 + fg + 8) * A_PITCH + k0 + ft + 4]};
+                    const float bfr[2] = {*tp_at(kq, k0 + ft, c0 + fg), *tp_at(kq, k0 + ft + 4, c0 + fg)};
+                    mma_tf32_16x8x8(c, af, bfr);
+                }
+                float* xr = Xs + (16 * blk + fg) * X_PITCH + 8 * (warp & 1) + 2 * ft;
+                *reinterpret_cast<float2*>(xr) = make_float2(c[0], c[1]);
+                *reinterpret_cast<float2*>(xr + 8 * X_PITCH) = make_float2(c[2], c[3]);
+            }
+            __syncthreads();
+            if (warp < 4) {  // T'_{b+1,b} = -D_{b+1} X
+                const int blk = warp >> 1, n0 = 8 * (warp & 1), r0 = 32 * blk + 16;
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+    #pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int k0 = 8 * ks;
+                    const float af[4] = {*tp_at(kq, r0 + fg, r0 + k0 + ft), *tp_at(kq, r0 + fg + 8, r0 + k0 + ft),
+                                         *tp_at(kq, r0 + fg, r0 + k0 + ft + 4), *tp_at(kq, r0 + fg + 8, r0 + k0 + ft + 4)};
+                    const float bfr[2] = {Xs[(16 * blk + k0 + ft) * X_PITCH + n0 + fg],
+                                          Xs[(16 * blk + k0 + ft + 4) * X_PITCH + n0 + fg]};
+                    mma_tf32_16x8x8(c, af, bfr);
+                }
+                const int cc = 32 * blk + n0 + 2 * ft;
+                *reinterpret_cast<float2*>(tp_at(kq, r0 + fg, cc)) = make_float2(-c[0], -c[1]);
+                *reinterpret_cast<float2*>(tp_at(kq, r0 + fg + 8, cc)) = make_float2(-c[2], -c[3]);
+            }
+            __syncthreads();
+            {   // level 2, X = A_{[23][01]} T'_{[01][01]} (32 x 32); warp = (16 rows, 8 columns)
+                const int mt = warp >> 2, nt = warp & 3, r0 = 32 + 16 * mt;
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int ks = nt; ks < 4; ++ks) {  // T'(k, c) = 0 for k < c
+                    const int k0 = 8 * ks;
+                    const float af[4] = {Am[(r0 + fg) * A_PITCH + k0 + ft], Am[(r0 + fg + 8) * A_PITCH + k0 + ft],
+                                         Am[(r0 + fg) * A_PITCH + k0 + ft + 4], Am[(r0 + fg + 8) * A_PITCH + k0 + ft + 4]};
+                    const float bfr[2] = {*tp_at(kq, k0 + ft, 8 * nt + fg), *tp_at(kq, k0 + ft + 4, 8 * nt + fg)};
+                    mma_tf32_16x8x8(c, af, bfr);
+                }
+                float* xr = Xs + (16 * mt + fg) * X_PITCH + 8 * nt + 2 * ft;
+                *reinterpret_cast<float2*>(xr) = make_float2(c[0], c[1]);
+                *reinterpret_cast<float2*>(xr + 8 * X_PITCH) = make_float2(c[2], c[3]);
+            }
+            __syncthreads();
+            {   // T'_{[23][01]} = -T'_{[23][23]} X
+                const int mt = warp >> 2, nt = warp & 3, r0 = 32 + 16 * mt;
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int ks = 0; ks < 2 * mt + 2; ++ks) {  // T'(r, 32 + k) = 0 for k > r - 32
+                    const int k0 = 8 * ks;
+                    const float af[4] = {*tp_at(kq, r0 + fg, 32 + k0 + ft), *tp_at(kq, r0 + fg + 8, 32 + k0 + ft),
+                                         *tp_at(kq, r0 + fg, 32 + k0 + ft + 4),
+                                         *tp_at(kq, r0 + fg + 8, 32 + k0 + ft + 4)};
+                    const float bfr[2] = {Xs[(k0 + ft) * X_PITCH + 8 * nt + fg], Xs[(k0 + ft + 4) * X_PITCH + 8 * nt + fg]};
+                    mma_tf32_16x8x8(c, af, bfr);
+                }
+                *reinterpret_cast<float2*>(tp_at(kq, r0 + fg, 8 * nt + 2 * ft)) = make_float2(-c[0], -c[1]);
+                *reinterpret_cast<float2*>(tp_at(kq, r0 + fg + 8, 8 * nt + 2 * ft)) = make_float2(-c[2], -c[3]);
+            }
+            __syncthreads();
         } else {
-            // meanwhile the other threads zero T' above its diagonal blocks
-            // (blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)), 2 float4 each
+            // T' = (I + A)^-1 as the Neumann-style product (I + N)(I + N^2)...(I + N^32),
+            // N = -A (nilpotent, so six factors are exact for 64 rows): P = N,
+            // T' = I + N, then five times P <- P P and T' <- T' + T' P.  Each
+            // product is a full 64 x 64 x 64 tf32 MMA, a 16 x 32 tile per warp,
+            // accumulated in registers and written back in place after a barrier.
+            for (int e = tid; e < 64 * 64; e += NT_I) {
+                const int r = e >> 6, c = e & 63;
+                const float nv = c < r ? -Am[r * A_PITCH + c] : 0.f;
+                Am[r * A_PITCH + c] = nv;
+                *tp_at(kq, r, c) = r == c ? 1.f : nv;
+            }
+            __syncthreads();
+            const int fg = lane >> 2, ft = lane & 3;
+            const int r0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
+            for (int lev = 0; lev < 5; ++lev) {
+                float c[4][4];
 #pragma unroll
-            for (int e = tid - 64; e < 384; e += NT_I - 64) {
-                const int blk = e >> 6, br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                *reinterpret_cast<float4*>(tp_at(kq, 16 * br + ((e >> 2) & 15), 16 * bc + (e & 3) * 4)) =
-                    make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        __syncthreads();
-        const int fg = lane >> 2, ft = lane & 3;  // MMA fragment row group, thread in group
-        if (warp < 4) {  // level 1, X = A_{b+1,b} D_b for b = 0, 2; warp = (block pair, 8 columns)
-            const int blk = warp >> 1, c0 = 32 * blk + 8 * (warp & 1), r0 = 32 * blk + 16;
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int nt = 0; nt < 4; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int k0 = 32 * blk + 8 * ks;
-                const float af[4] = {Am[(r0 + fg) * A_PITCH + k0 + ft], Am[(r0 + fg + 8) * A_PITCH + k0 + ft],
-                                     Am[(r0 + fg) * A_PITCH + k0 + ft + 4], Am[(r0 + fg + 8) * A_PITCH + k0 + ft + 4]};
-                const float bfr[2] = {*tp_at(kq, k0 + ft, c0 + fg), *tp_at(kq, k0 + ft + 4, c0 + fg)};
-                mma_tf32_16x8x8(c, af, bfr);
-            }
-            float* xr = Xs + (16 * blk + fg) * X_PITCH + 8 * (warp & 1) + 2 * ft;
-            *reinterpret_cast<float2*>(xr) = make_float2(c[0], c[1]);
-            *reinterpret_cast<float2*>(xr + 8 * X_PITCH) = make_float2(c[2], c[3]);
-        }
-        __syncthreads();
-        if (warp < 4) {  // T'_{b+1,b} = -D_{b+1} X
-            const int blk = warp >> 1, n0 = 8 * (warp & 1), r0 = 32 * blk + 16;
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int ks = 0; ks < 8; ++ks) {  // P P
+                    const int k0 = 8 * ks;
+                    const float af[4] = {Am[(r0 + fg) * A_PITCH + k0 + ft], Am[(r0 + fg + 8) * A_PITCH + k0 + ft],
+                                         Am[(r0 + fg) * A_PITCH + k0 + ft + 4],
+                                         Am[(r0 + fg + 8) * A_PITCH + k0 + ft + 4]};
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int k0 = 8 * ks;
-                const float af[4] = {*tp_at(kq, r0 + fg, r0 + k0 + ft), *tp_at(kq, r0 + fg + 8, r0 + k0 + ft),
-                                     *tp_at(kq, r0 + fg, r0 + k0 + ft + 4), *tp_at(kq, r0 + fg + 8, r0 + k0 + ft + 4)};
-                const float bfr[2] = {Xs[(16 * blk + k0 + ft) * X_PITCH + n0 + fg],
-                                      Xs[(16 * blk + k0 + ft + 4) * X_PITCH + n0 + fg]};
-                mma_tf32_16x8x8(c, af, bfr);
+                    for (int nt = 0; nt < 4; ++nt) {
+                        const float bfr[2] = {Am[(k0 + ft) * A_PITCH + n0 + 8 * nt + fg],
+                                              Am[(k0 + ft + 4) * A_PITCH + n0 + 8 * nt + fg]};
+                        mma_tf32_16x8x8(c[nt], af, bfr);
+                    }
+                }
+                __syncthreads();
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    float* pr = Am + (r0 + fg) * A_PITCH + n0 + 8 * nt + 2 * ft;
+                    pr[0] = c[nt][0];
+                    pr[1] = c[nt][1];
+                    pr[8 * A_PITCH] = c[nt][2];
+                    pr[8 * A_PITCH + 1] = c[nt][3];
+                }
+                __syncthreads();
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {  // T' P
+                    const int k0 = 8 * ks;
+                    const float af[4] = {*tp_at(kq, r0 + fg, k0 + ft), *tp_at(kq, r0 + fg + 8, k0 + ft),
+                                         *tp_at(kq, r0 + fg, k0 + ft + 4), *tp_at(kq, r0 + fg + 8, k0 + ft + 4)};
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        const float bfr[2] = {Am[(k0 + ft) * A_PITCH + n0 + 8 * nt + fg],
+                                              Am[(k0 + ft + 4) * A_PITCH + n0 + 8 * nt + fg]};
+                        mma_tf32_16x8x8(c[nt], af, bfr);
+                    }
+                }
+                __syncthreads();
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int cc = n0 + 8 * nt + 2 * ft;
+                    *tp_at(kq, r0 + fg, cc) += c[nt][0];
+                    *tp_at(kq, r0 + fg, cc + 1) += c[nt][1];
+                    *tp_at(kq, r0 + fg + 8, cc) += c[nt][2];
+                    *tp_at(kq, r0 + fg + 8, cc + 1) += c[nt][3];
+                }
+                __syncthreads();
             }
-            const int cc = 32 * blk + n0 + 2 * ft;
-            *reinterpret_cast<float2*>(tp_at(kq, r0 + fg, cc)) = make_float2(-c[0], -c[1]);
-            *reinterpret_cast<float2*>(tp_at(kq, r0 + fg + 8, cc)) = make_float2(-c[2], -c[3]);
         }
-        __syncthreads();
-        {   // level 2, X = A_{[23][01]} T'_{[01][01]} (32 x 32); warp = (16 rows, 8 columns)
-            const int mt = warp >> 2, nt = warp & 3, r0 = 32 + 16 * mt;
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int ks = nt; ks < 4; ++ks) {  // T'(k, c) = 0 for k < c
-                const int k0 = 8 * ks;
-                const float af[4] = {Am[(r0 + fg) * A_PITCH + k0 + ft], Am[(r0 + fg + 8) * A_PITCH + k0 + ft],
-                                     Am[(r0 + fg) * A_PITCH + k0 + ft + 4], Am[(r0 + fg + 8) * A_PITCH + k0 + ft + 4]};
-                const float bfr[2] = {*tp_at(kq, k0 + ft, 8 * nt + fg), *tp_at(kq, k0 + ft + 4, 8 * nt + fg)};
-                mma_tf32_16x8x8(c, af, bfr);
-            }
-            float* xr = Xs + (16 * mt + fg) * X_PITCH + 8 * nt + 2 * ft;
-            *reinterpret_cast<float2*>(xr) = make_float2(c[0], c[1]);
-            *reinterpret_cast<float2*>(xr + 8 * X_PITCH) = make_float2(c[2], c[3]);
-        }
-        __syncthreads();
-        {   // T'_{[23][01]} = -T'_{[23][23]} X
-            const int mt = warp >> 2, nt = warp & 3, r0 = 32 + 16 * mt;
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int ks = 0; ks < 2 * mt + 2; ++ks) {  // T'(r, 32 + k) = 0 for k > r - 32
-                const int k0 = 8 * ks;
-                const float af[4] = {*tp_at(kq, r0 + fg, 32 + k0 + ft), *tp_at(kq, r0 + fg + 8, 32 + k0 + ft),
-                                     *tp_at(kq, r0 + fg, 32 + k0 + ft + 4),
-                                     *tp_at(kq, r0 + fg + 8, 32 + k0 + ft + 4)};
-                const float bfr[2] = {Xs[(k0 + ft) * X_PITCH + 8 * nt + fg], Xs[(k0 + ft + 4) * X_PITCH + 8 * nt + fg]};
-                mma_tf32_16x8x8(c, af, bfr);
-            }
-            *reinterpret_cast<float2*>(tp_at(kq, r0 + fg, 8 * nt + 2 * ft)) = make_float2(-c[0], -c[1]);
-            *reinterpret_cast<float2*>(tp_at(kq, r0 + fg + 8, 8 * nt + 2 * ft)) = make_float2(-c[2], -c[3]);
-        }
-        __syncthreads();
         {   // B_W = T' diag(beta e^G rk), B_U = T' diag(beta) (bf16) into the A region
             const int which = tid >> 7, i = (tid >> 1) & 63, c0 = (tid & 1) * 32;
             const float* Fc = (which == 0 ? FWs : Bs) + c0;
@@ -1022,7 +1092,9 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
         !encode2d(&utmap, w.ut, 128, U * 64, 64, 64) || !encode2d(&pmap, w.p, 64, U * 64, 64, 64) ||
         !encode2d(&omap, a.o, (uint64_t)a.H_v * D, (uint64_t)a.T, 64, 64))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
+    cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chunk_intra_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(chunk_chain_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  ChainLayout<64>::SMEM);
@@ -1041,7 +1113,10 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
     chunk_offsets_kernel<<<1, 1024, 0, si>>>(a.cu, a.n_seq, a.T, w.coff);
     for (int64_t seg = 0; seg < Ly.n_seg; ++seg) {
         const int64_t C0 = seg * Ly.segc;
-        chunk_intra_kernel<<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, si>>>(qmap, wtmap, utmap, a, w, C0);
+        if (a.neumann)
+            chunk_intra_kernel<true><<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, si>>>(qmap, wtmap, utmap, a, w, C0);
+        else
+            chunk_intra_kernel<false><<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, si>>>(qmap, wtmap, utmap, a, w, C0);
         if (two) {
             if ((e = cudaGetLastError()) != cudaSuccess || (e = cudaEventRecord(ev_pre, si)) != cudaSuccess ||
                 (e = cudaStreamWaitEvent(s, ev_pre, 0)) != cudaSuccess)

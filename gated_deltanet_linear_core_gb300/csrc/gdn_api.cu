@@ -312,7 +312,8 @@ gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, co
     if ((st = check_seqs(cu_seqlens, n_seq, T_tot)) != GDN_OK) return st;
     if ((st = check_ckpt(ckpt_every, state_ckpt_out, ckpt_rows)) != GDN_OK) return st;
     if (T_tot > 0 && (st = check_gates(a, b, A_log, dt_bias, g, beta, dtype)) != GDN_OK) return st;
-    if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(GDN_QK_L2NORM | GDN_SOLVE_NEUMANN)) return GDN_ERR_INVALID_ARG;
+    if ((flags & GDN_SOLVE_NEUMANN) && !(dtype == GDN_BF16 && dims.d_k == 128)) return GDN_ERR_UNSUPPORTED;
     if (!isfinite(scale)) return GDN_ERR_INVALID_ARG;
     if (T_tot > 0 && (qkv == nullptr || o == nullptr)) return GDN_ERR_INVALID_ARG;
     if (!aligned16(qkv) || !aligned16(o) || !aligned16(initial_state) || !aligned16(final_state) ||
@@ -334,6 +335,7 @@ gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, co
     d.ckpt_rows = ckpt_rows;
     d.scale = scale == 0.f ? 1.0f / sqrtf((float)dims.d_k) : scale;
     d.l2norm = (flags & GDN_QK_L2NORM) != 0;
+    d.neumann = (flags & GDN_SOLVE_NEUMANN) != 0;
     d.o = o;
     cudaStream_t s = (cudaStream_t)stream;
     if (need > 0) return cuda_status(gdn::launch_chunk_split(d, workspace, ws_bytes, s));

@@ -50,6 +50,7 @@ struct DeltaArgs {
     float scale;
     int l2norm;
     void* o;  // [T, H_v, D]
+    int neumann;  // chunk inverse by the Neumann-style product (tensor-core path)
 };
 // Chunked prefill on CUDA cores (f32 arithmetic; any supported D and dtype).
 cudaError_t launch_chunk_ffma(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s);

@@ -68,6 +68,14 @@ typedef struct {
 
 /* flags of gdn_chunk_prefill / gdn_recurrent_decode */
 #define GDN_QK_L2NORM 1u /* l2-normalise q and k per head (eps 1e-6 inside the sqrt) */
+/* gdn_chunk_prefill only, tensor-core path (bf16, d = 128): form each chunk's
+ * (I + A)^-1 as the Neumann-style product (I + N)(I + N^2)...(I + N^32),
+ * N = -A, instead of the direct solve.  NxD-Inference Qwen3.6-27B PR, "Known
+ * limitations" (a faster Neumann-style path against the stable direct solve).
+ * Exact in exact arithmetic (A is nilpotent) but unstable when the chunk's
+ * inverse is far from the identity (slow decay, correlated keys); shipped to
+ * compare the two.  Other paths: GDN_ERR_UNSUPPORTED. */
+#define GDN_SOLVE_NEUMANN 2u
 
 /* Text for a status code (static storage, never NULL). */
 const char* gdn_status_string(gdn_status_t status);
@@ -239,7 +247,7 @@ int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, gdn_dims_t dims
  *               [gdn_ckpt_count rows, H_v, d_k, d_v] f32: state after m*ckpt_every tokens
  *   ckpt_rows   rows allocated in state_ckpt_out; rows past it are never written
  *   scale       query scale; 0 means d_k^-1/2
- *   flags       GDN_QK_L2NORM or 0
+ *   flags       GDN_QK_L2NORM, optionally | GDN_SOLVE_NEUMANN, or 0
  *   o          (device) [T_tot, H_v, d_v]   (dtype)
  *   workspace  (device) >= gdn_chunk_prefill_workspace_size bytes, or NULL if that is 0
  */

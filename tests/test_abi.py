@@ -133,7 +133,12 @@ def test_chunk_prefill_validation(lib):
     assert chunk(lib, a=None, g=A + 0x5000) == E.GDN_ERR_INVALID_ARG  # ... nor g AND beta
     assert chunk(lib, A_log=A + 0x3002) == E.GDN_ERR_ALIGN
     assert chunk(lib, a=A + 0x1001) == E.GDN_ERR_ALIGN       # bf16 needs 2-byte alignment
-    assert chunk(lib, flags=2) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, flags=4) == E.GDN_ERR_INVALID_ARG
+    # the Neumann-style solve: tensor-core path only (bf16, d = 128); here the
+    # flags pass and the missing workspace is what is reported
+    neu = E.GDN_QK_L2NORM | E.GDN_SOLVE_NEUMANN
+    assert chunk(lib, flags=neu) == E.GDN_ERR_WORKSPACE
+    assert chunk(lib, flags=neu, dt=E.GDN_F32, a=A + 0x1000, b=A + 0x2000) == E.GDN_ERR_UNSUPPORTED
     assert chunk(lib, scale=float("nan")) == E.GDN_ERR_INVALID_ARG
     assert chunk(lib, scale=float("inf")) == E.GDN_ERR_INVALID_ARG
     assert chunk(lib, o=None) == E.GDN_ERR_INVALID_ARG

@@ -193,6 +193,53 @@ def test_chunk_prefill_slow_decay(dtype, keys):
     print(f"GPU o {eo:.2e}, S {es:.2e}")
 
 
+def test_chunk_prefill_neumann_solve():
+    """GDN_SOLVE_NEUMANN (tensor-core path): within the bf16 tolerance of the
+    oracle on N(0,1) activations with the configs' gate distributions, where
+    each chunk's (I + A)^-1 is close to the identity; with slow decay and
+    correlated keys its intermediate powers grow and the result is useless,
+    while the direct solve holds (the CPU error study predicts both)."""
+    shape = SMALL_128
+    inp = _delta_inputs(shape, torch.bfloat16, LENGTHS, seed=15)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    args = (d["mixed_qkv"], _dims(shape), d["a"], d["b"], d["A_log"], d["dt_bias"])
+    Sf = torch.empty_like(d["S0"])
+    o = gdn.gdn_chunk_prefill(*args, cu_seqlens=d["cu_seqlens"], initial_state=d["S0"],
+                              final_state=Sf, solve="neumann")
+    o_direct = gdn.gdn_chunk_prefill(*args, cu_seqlens=d["cu_seqlens"], initial_state=d["S0"])
+    torch.cuda.synchronize()
+    o_ref, S_ref, _ = _oracle_delta(inp, shape)
+    e_n = assert_close("o (Neumann)", host(o), o_ref, TOL[torch.bfloat16], per_head_axis=1)
+    assert_close("S (Neumann)", host(Sf), S_ref, TOL[torch.bfloat16], per_head_axis=1)
+    e_d = rel_l2(host(o_direct), o_ref)
+    print(f"\nN(0,1) inputs: Neumann o {e_n:.2e}, direct o {e_d:.2e}")
+
+    # slow decay, correlated keys (as in test_chunk_prefill_slow_decay)
+    inp = _delta_inputs(shape, torch.bfloat16, [1000, 300], seed=18)
+    gen = torch.Generator().manual_seed(18)
+    inp["A_log"] = torch.log(1e-3 + 9e-3 * torch.rand(shape.H_v, generator=gen))
+    D, T = shape.d_k, inp["mixed_qkv"].shape[0]
+    x = inp["mixed_qkv"].float()
+    for kh in range(shape.H_k):
+        c0 = shape.H_k * D + kh * D
+        u = torch.randn(D, generator=gen)
+        x[:, c0:c0 + D] = u[None, :] + 0.5 * torch.randn((T, D), generator=gen)
+    inp["mixed_qkv"] = x.to(torch.bfloat16)
+    inp["b"] = (inp["b"].float() + 2.2).to(torch.bfloat16)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    args = (d["mixed_qkv"], _dims(shape), d["a"], d["b"], d["A_log"], d["dt_bias"])
+    o_n = gdn.gdn_chunk_prefill(*args, cu_seqlens=d["cu_seqlens"], initial_state=d["S0"],
+                                solve="neumann")
+    o_d = gdn.gdn_chunk_prefill(*args, cu_seqlens=d["cu_seqlens"], initial_state=d["S0"])
+    torch.cuda.synchronize()
+    o_ref, _, _ = _oracle_delta(inp, shape)
+    got = host(o_n)
+    e_n = rel_l2(got, o_ref) if np.all(np.isfinite(got)) else float("inf")
+    e_d = rel_l2(host(o_d), o_ref)
+    print(f"slow decay, correlated keys: Neumann o {e_n:.2e}, direct o {e_d:.2e}")
+    assert e_d < 1e-2 and e_n > 0.1
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_chunk_prefill_in_place_state_and_zero_init(dtype):
     shape = SMALL_128
