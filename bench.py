@@ -62,6 +62,15 @@ def decode_step_bytes_per_seq(s: W.GDNShape) -> int:
     return state + conv_state + (s.conv_dim + s.z_dim + 2 * s.H_v + s.H_v * s.d_v) * 2
 
 
+def verify_bytes_per_seq(s: W.GDNShape, K: int) -> int:
+    """Algorithmic bytes of one K-token verification per sequence: the f32
+    state and the bf16 conv state read once and written after every draft
+    token, the tokens' qkv, z, a, b read and their outputs written."""
+    state = s.H_v * s.d_k * s.d_v * 4
+    conv_state = s.conv_dim * 3 * 2
+    return (1 + K) * (state + conv_state) + K * (s.conv_dim + s.z_dim + 2 * s.H_v + s.H_v * s.d_v) * 2
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -369,6 +378,52 @@ def run_ours(args):
     ftotal = max_over_ranks(dist, sum(fstep_ms) / 1e3, dev)
     fbytes = B * decode_step_bytes_per_seq(s)
     f_gbs = fbytes / (sum(fstep_ms) / nd / 1e3) / 1e9
+    # speculative-decoding verification: K draft tokens per sequence per call,
+    # states read from one cache slot and written to K others
+    KV = 4
+    nv = nd // KV
+    S_pool = torch.empty(((KV + 1) * B,) + tuple(Sd.shape[1:]), dtype=torch.float32, device=dev)
+    cs_pool = torch.empty(((KV + 1) * B,) + tuple(csd.shape[1:]), dtype=csd.dtype, device=dev)
+    S_pool[:B].copy_(dd["S0"])
+    cs_pool[:B].copy_(dd["conv_state0"])
+    vslots = (torch.arange(KV + 1, device=dev, dtype=torch.int32)[None, :] * B +
+              torch.arange(B, device=dev, dtype=torch.int32)[:, None]).contiguous()
+    vin = [{k: dd[k][KV * i:KV * (i + 1)].transpose(0, 1).contiguous() for k in ("qkv", "z", "a", "b")}
+           for i in range(nv)]
+    vout = torch.empty((B, KV, s.H_v * s.d_v), dtype=wd.dtype, device=dev)
+
+    def verify_call(i):
+        v = vin[i]
+        gdn.gdn_decode_verify(v["qkv"], v["z"], v["a"], v["b"], dd["conv_w"], dd["A_log"],
+                              dd["dt_bias"], dd["norm_w"], dims, S_pool, cs_pool, vslots, out=vout)
+
+    for i in range(min(args.warmup, nv)):
+        flush.zero_()
+        verify_call(i)
+    vevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(nv)]
+    torch.cuda.synchronize(dev)
+    clocks.mark(True)
+    for i in range(nv):
+        flush.zero_()
+        vevs[i][0].record(stream)
+        verify_call(i)
+        vevs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark(False)
+    launches += nv
+    vms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in vevs)
+    vbytes = B * verify_bytes_per_seq(s, KV)
+    v_gbs = vbytes / (vms / 1e3) / 1e9
+    verify = {
+        "draft_tokens": KV, "value": round(world * B * KV / (vms / 1e3), 1), "unit": "tokens/s",
+        "ms_per_call": round(vms, 4), "calls": nv, "call": "gdn_decode_verify (one kernel per call)",
+        "roofline": {"kernel": "gdn_decode_verify", "bound": "hbm", "achieved": round(v_gbs, 1),
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(v_gbs / pk["hbm_gbs"], 4),
+                     "peak_source": pk["source"] + " (HBM copy)", "traffic": None,
+                     "algorithmic_bytes_per_launch": vbytes},
+    }
+
     decode = {
         "workload": DECODE, "value": round(world * B * nd / ftotal, 1), "unit": "tokens/s",
         "ms_per_step": round(sum(fstep_ms) / nd, 4), "steps": nd, "batch": B,
@@ -392,6 +447,7 @@ def run_ours(args):
                          "traffic": traffic_record("recurrent_decode"),
                          "algorithmic_bytes_per_launch": dbytes},
         },
+        "verify": verify,
         "l2": "flushed between steps",
     }
 

@@ -24,7 +24,8 @@ __all__ = [
     "GDNDims", "GDNError", "gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_launches", "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode", "gdn_rmsnorm_gated",
     "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_sync_status", "gdn_selftest_bounded_wait",
-    "gdn_layer_prefill_host", "gdn_decode_step", "gdn_layer_prefill", "gdn_layer_decode",
+    "gdn_layer_prefill_host", "gdn_decode_step", "gdn_decode_verify", "gdn_layer_prefill",
+    "gdn_layer_decode",
     "library_path",
 ]
 
@@ -385,6 +386,38 @@ def gdn_decode_step(x, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, state, con
         _lib.GDN_QK_L2NORM if l2norm else 0, _ptr(out, "out", dt, (B, O)), _dims(dims),
         _dtype_code(x), _stream(x, stream))
     _lib.check(st, "gdn_decode_step")
+    return out
+
+
+def gdn_decode_verify(x, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, state, conv_state,
+                      slots, scale=0.0, l2norm=True, norm_eps=1e-6, out=None, stream=None):
+    """Speculative-decoding verification: K draft tokens of B sequences
+    (x [B, K, conv_dim], z [B, K, H_v*d_v], a, b [B, K, H_v]) through the fused
+    decode step in one kernel.  States are read from slot slots[b, 0] of
+    state [n_slots, H_v, d_k, d_v] f32 / conv_state [n_slots, conv_dim, 3]; the
+    states after draft token t are written to slot slots[b, t + 1] (slots int32
+    [B, K + 1]).  Returns out [B, K, H_v*d_v]."""
+    dt = x.dtype
+    if x.dim() != 3:
+        raise ValueError("x: expected [B, K, conv_dim]")
+    B, K = int(x.shape[0]), int(x.shape[1])
+    C, O = _conv_dim(dims), int(dims.H_v) * int(dims.d_v)
+    if out is None:
+        out = torch.empty((B, K, O), dtype=dt, device=x.device)
+    if state.dim() != 4 or tuple(state.shape[1:]) != (dims.H_v, dims.d_k, dims.d_v):
+        raise ValueError("state: expected [n_slots, H_v, d_k, d_v]")
+    if conv_state.dim() != 3 or tuple(conv_state.shape[1:]) != (C, 3):
+        raise ValueError("conv_state: expected [n_slots, conv_dim, 3]")
+    st = _lib.load().gdn_decode_verify(
+        _ptr(x, "x", dt, (B, K, C)), _ptr(conv_w, "conv_w", dt, (C, 4)),
+        _ptr(conv_state, "conv_state", dt), _ptr(z, "z", dt, (B, K, O)),
+        _ptr(a, "a", dt, (B, K, dims.H_v)), _ptr(b, "b", dt, (B, K, dims.H_v)),
+        _ptr(A_log, "A_log", torch.float32), _ptr(dt_bias, "dt_bias", torch.float32),
+        _ptr(state, "state", torch.float32), _ptr(norm_w, "norm_w", dt), float(norm_eps),
+        _ptr(slots, "slots", torch.int32, (B, K + 1)), B, K, float(scale),
+        _lib.GDN_QK_L2NORM if l2norm else 0, _ptr(out, "out", dt, (B, K, O)), _dims(dims),
+        _dtype_code(x), _stream(x, stream))
+    _lib.check(st, "gdn_decode_verify")
     return out
 
 

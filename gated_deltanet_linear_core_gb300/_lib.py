@@ -62,6 +62,8 @@ SIGNATURES = {
     "gdn_recurrent_decode": (ST, [P, P, P, P, P, P, P, P, I32, F32, U32, P, Dims, ST, P]),
     "gdn_rmsnorm_gated": (ST, [P, P, P, F32, I64, P, Dims, ST, P]),
     "gdn_decode_step": (ST, [P, P, P, P, P, P, P, P, P, P, F32, P, I32, F32, U32, P, Dims, ST, P]),
+    "gdn_decode_verify": (ST, [P, P, P, P, P, P, P, P, P, P, F32, P, I32, I32, F32, U32, P, Dims, ST,
+                               P]),
 }
 
 _lock = threading.Lock()

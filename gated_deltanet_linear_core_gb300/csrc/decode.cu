@@ -335,10 +335,241 @@ cudaError_t decode_step_t(const DecodeStepArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// K draft tokens of speculative decoding checked in one pass: per sequence,
+// the conv update, gates, l2 norms, recurrence and RMSNormGated of tokens
+// 0..K-1 in order, from the states in slot slots[b][0], writing the conv state
+// and the recurrent state after token t to slot slots[b][t + 1] (so that
+// accepting j draft tokens is choosing slot slots[b][j], with no copy).  One
+// CTA per (sequence, key head) as in the fused step, with its thread layout and
+// arithmetic order, so every state and output equals that of K fused steps;
+// the state of each value head is read once and written K times.
+template <typename T, int D, int NW>
+__global__ void __launch_bounds__(NW * 32, (D >= 128 ? 2 : 1))
+decode_verify_kernel(DecodeVerifyArgs a) {
+    constexpr int NT = NW * 32;
+    constexpr int TPR = D / 4;
+    constexpr int RPP = NT / TPR;
+    constexpr int PASSES = D / RPP;
+    constexpr int V = Vec16<T>::N;
+    static_assert(NT % TPR == 0 && D % RPP == 0 && NT >= D, "layout");
+
+    const int b = blockIdx.x / a.H_k;
+    const int kh = blockIdx.x - b * a.H_k;
+    const int r = a.H_v / a.H_k, K = a.K;
+    const int32_t* sl = a.slots + (int64_t)b * (K + 1);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cq = tid % TPR;
+    const int r0 = tid / TPR;
+    const int C = 2 * a.H_k * D + a.H_v * D;
+
+    extern __shared__ __align__(16) float vsm[];
+    float* qs = vsm;                  // [K][D]
+    float* ks = qs + K * D;           // [K][D]
+    float* vs = ks + K * D;           // [K][r][D]
+    float* ds = vs + K * r * D;       // [D]
+    float* os = ds + D;               // [D]
+    float* red = os + D;              // [2][RPP][D]
+    float* gb = red + 2 * RPP * D;    // [K][r][2]: g, beta
+    float* nrm = gb + 2 * K * r;      // [K][3]: rq, rk, k.q rq rk
+    float* wsum = nrm + 3 * K;        // [NW]
+
+    const int64_t s_in = sl[0];
+    float4 s[PASSES];
+    auto load_state = [&](int j) {
+        const float* S = a.state + (s_in * a.H_v + kh * r + j) * D * D;
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p)
+            s[p] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(r0 + p * RPP) * D) + cq);
+    };
+
+    // 1. conv over the K tokens: q, k, then the r heads' v, one 16-byte vector
+    //    of channels per thread; the window slides over [state | x_0 .. x_{K-1}]
+    {
+        const T* x = static_cast<const T*>(a.x) + (int64_t)b * K * C;
+        const T* w = static_cast<const T*>(a.conv_w);
+        T* cs = static_cast<T*>(a.conv_state);
+        const int nvec = (2 + r) * D / V;
+        for (int e = tid; e < nvec; e += NT) {
+            const int grp = (e * V) / D, i0 = e * V - grp * D;
+            const int c0 = grp == 0 ? kh * D + i0
+                         : grp == 1 ? a.H_k * D + kh * D + i0
+                                    : 2 * a.H_k * D + (kh * r + grp - 2) * D + i0;
+            float st[3 * V], wt[4 * V];
+#pragma unroll
+            for (int k = 0; k < 3; ++k) load16(cs + (s_in * C + c0) * 3 + k * V, st + k * V);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) load16(w + (int64_t)c0 * 4 + k * V, wt + k * V);
+            float* dst = grp == 0 ? qs + i0 : grp == 1 ? ks + i0 : vs + (grp - 2) * D + i0;
+            const int tstride = grp < 2 ? D : r * D;
+            for (int t = 0; t < K; ++t) {
+                float xv[V];
+                load16(x + (int64_t)t * C + c0, xv);
+#pragma unroll
+                for (int q = 0; q < V; ++q) {
+                    float acc = wt[q * 4] * st[q * 3];
+                    acc = fmaf(wt[q * 4 + 1], st[q * 3 + 1], acc);
+                    acc = fmaf(wt[q * 4 + 2], st[q * 3 + 2], acc);
+                    acc = fmaf(wt[q * 4 + 3], xv[q], acc);
+                    dst[t * tstride + q] = to_f(from_f<T>(silu_f(acc)));
+                    st[q * 3] = st[q * 3 + 1];  // the window moves one token
+                    st[q * 3 + 1] = st[q * 3 + 2];
+                    st[q * 3 + 2] = xv[q];
+                }
+                T* out_cs = cs + ((int64_t)sl[t + 1] * C + c0) * 3;
+#pragma unroll
+                for (int k = 0; k < 3; ++k) store16(out_cs + k * V, st + k * V);
+            }
+        }
+        for (int e = tid; e < K * r; e += NT) {
+            const int t = e / r, j = e - t * r;
+            const int h = kh * r + j;
+            const int64_t gi = ((int64_t)b * K + t) * a.H_v + h;
+            gb[2 * e] = gate_g(to_f(static_cast<const T*>(a.a)[gi]), a.A_log[h], a.dt_bias[h]);
+            gb[2 * e + 1] = sigmoid_f(to_f(static_cast<const T*>(a.b)[gi]));
+        }
+    }
+    __syncthreads();
+    // the first value head's state streams in while the norms are formed (the
+    // conv's K-token window needs the registers before)
+    load_state(0);
+    // l2 norms of each token's q and k (each warp sums the whole row, lanes
+    // strided, as the fused step does)
+    for (int t = warp; t < K; t += NW) {
+        float sq = 0.f, sk = 0.f, sqk = 0.f;
+        for (int i = lane; i < D; i += 32) {
+            sq = fmaf(qs[t * D + i], qs[t * D + i], sq);
+            sk = fmaf(ks[t * D + i], ks[t * D + i], sk);
+            sqk = fmaf(qs[t * D + i], ks[t * D + i], sqk);
+        }
+        sq = warp_sum(sq);
+        sk = warp_sum(sk);
+        sqk = warp_sum(sqk);
+        float rq = a.scale, rk = 1.f;
+        if (a.l2norm) {
+            rq = a.scale / sqrtf(sq + 1e-6f);
+            rk = 1.f / sqrtf(sk + 1e-6f);
+        }
+        if (lane == 0) {
+            nrm[3 * t] = rq;
+            nrm[3 * t + 1] = rk;
+            nrm[3 * t + 2] = sqk * rq * rk;
+        }
+    }
+    __syncthreads();
+
+    // 2. the r value heads in turn, each through the K tokens in registers
+    for (int j = 0; j < r; ++j) {
+        const int h = kh * r + j;
+        if (j > 0) load_state(j);
+        for (int t = 0; t < K; ++t) {
+            const float rq = nrm[3 * t], rk = nrm[3 * t + 1], kq = nrm[3 * t + 2];
+            const float* kt = ks + t * D;
+            const float* qt = qs + t * D;
+            float mk[4] = {0.f, 0.f, 0.f, 0.f}, mq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int p = 0; p < PASSES; ++p) {
+                const int i = r0 + p * RPP;
+                const float kv = kt[i] * rk, qv = qt[i] * rq;
+                mk[0] = fmaf(s[p].x, kv, mk[0]); mk[1] = fmaf(s[p].y, kv, mk[1]);
+                mk[2] = fmaf(s[p].z, kv, mk[2]); mk[3] = fmaf(s[p].w, kv, mk[3]);
+                mq[0] = fmaf(s[p].x, qv, mq[0]); mq[1] = fmaf(s[p].y, qv, mq[1]);
+                mq[2] = fmaf(s[p].z, qv, mq[2]); mq[3] = fmaf(s[p].w, qv, mq[3]);
+            }
+            *reinterpret_cast<float4*>(&red[r0 * D + cq * 4]) = make_float4(mk[0], mk[1], mk[2], mk[3]);
+            *reinterpret_cast<float4*>(&red[(RPP + r0) * D + cq * 4]) = make_float4(mq[0], mq[1], mq[2], mq[3]);
+            __syncthreads();
+            const float eg = expf(gb[2 * (t * r + j)]);
+            const float bt = gb[2 * (t * r + j) + 1];
+            const float* vt = vs + (t * r + j) * D;
+            float o2 = 0.f;
+            for (int c = tid; c < D; c += NT) {
+                float m = 0.f, pq = 0.f;
+#pragma unroll
+                for (int rr = 0; rr < RPP; ++rr) {
+                    m += red[rr * D + c];
+                    pq += red[(RPP + rr) * D + c];
+                }
+                const float delta = bt * (vt[c] - eg * m);
+                ds[c] = delta;
+                const float o = to_f(from_f<T>(eg * pq + kq * delta));
+                os[c] = o;
+                o2 = fmaf(o, o, o2);
+            }
+            o2 = warp_sum(o2);
+            if (lane == 0) wsum[warp] = o2;
+            __syncthreads();
+            // S <- e^g S + k^ delta^T, kept in registers and written to slot t + 1
+            float* S = a.state + ((int64_t)sl[t + 1] * a.H_v + h) * D * D;
+            const float4 d4 = *reinterpret_cast<const float4*>(&ds[cq * 4]);
+#pragma unroll
+            for (int p = 0; p < PASSES; ++p) {
+                const int i = r0 + p * RPP;
+                const float kv = kt[i] * rk;
+                float4 n;
+                n.x = fmaf(kv, d4.x, eg * s[p].x);
+                n.y = fmaf(kv, d4.y, eg * s[p].y);
+                n.z = fmaf(kv, d4.z, eg * s[p].z);
+                n.w = fmaf(kv, d4.w, eg * s[p].w);
+                s[p] = n;
+                __stcs(reinterpret_cast<float4*>(S + (int64_t)i * D) + cq, n);
+            }
+            float tot = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < NW; ++ww) tot += wsum[ww];
+            const float rs = rsqrtf(tot / (float)D + a.eps);
+            const int64_t row = ((int64_t)b * K + t) * a.H_v + h;
+            const T* z = static_cast<const T*>(a.z) + row * D;
+            T* out = static_cast<T*>(a.out) + row * D;
+            const T* nw = static_cast<const T*>(a.norm_w);
+            for (int c = 2 * tid; c < D; c += 2 * NT) {
+                const float2 g = silu2<T>(make_float2(to_f(z[c]), to_f(z[c + 1])));
+                const float2 res = __fmul2_rn(__fmul2_rn(make_float2(to_f(nw[c]), to_f(nw[c + 1])),
+                                                         __fmul2_rn(make_float2(os[c], os[c + 1]), make_float2(rs, rs))),
+                                              g);
+                out[c] = from_f<T>(res.x);
+                out[c + 1] = from_f<T>(res.y);
+            }
+            __syncthreads();  // red, ds, os and wsum are reused by the next token
+        }
+    }
+}
+
+template <int D, int NW>
+size_t verify_smem_bytes(int K, int r) {
+    constexpr int RPP = NW * 32 / (D / 4);
+    return sizeof(float) * ((size_t)2 * K * D + (size_t)K * r * D + 2 * D + 2 * RPP * D + 2 * K * r + 3 * K + NW);
+}
+
+template <typename T>
+cudaError_t decode_verify_t(const DecodeVerifyArgs& a, cudaStream_t s) {
+    const unsigned units = (unsigned)(a.B * a.H_k);
+    if (units == 0 || a.K == 0) return cudaSuccess;
+    const int r = a.H_v / a.H_k;
+    if (r > 8 || a.K > kVerifyMaxK) return cudaErrorNotSupported;
+    if (a.D == 128) {
+        const size_t smem = verify_smem_bytes<128, 8>(a.K, r);
+        cudaError_t e = cudaFuncSetAttribute(decode_verify_kernel<T, 128, 8>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        decode_verify_kernel<T, 128, 8><<<units, 256, smem, s>>>(a);
+    } else {
+        const size_t smem = verify_smem_bytes<16, 1>(a.K, r);
+        cudaError_t e = cudaFuncSetAttribute(decode_verify_kernel<T, 16, 1>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        decode_verify_kernel<T, 16, 1><<<units, 32, smem, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_decode_step(const DecodeStepArgs& a, gdn_dtype_t dt, cudaStream_t s) {
     return dt == GDN_BF16 ? decode_step_t<bf16>(a, s) : decode_step_t<float>(a, s);
+}
+
+cudaError_t launch_decode_verify(const DecodeVerifyArgs& a, gdn_dtype_t dt, cudaStream_t s) {
+    return dt == GDN_BF16 ? decode_verify_t<bf16>(a, s) : decode_verify_t<float>(a, s);
 }
 
 cudaError_t launch_recurrent_decode(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s) {

@@ -243,6 +243,41 @@ gdn_status_t gdn_decode_step(const void* x, const void* conv_w, void* conv_state
     return cuda_status(gdn::launch_decode_step(d, dtype, (cudaStream_t)stream));
 }
 
+gdn_status_t gdn_decode_verify(const void* x, const void* conv_w, void* conv_state, const void* z,
+                               const void* a, const void* b, const float* A_log,
+                               const float* dt_bias, float* state, const void* norm_w,
+                               float norm_eps, const int32_t* slots, int32_t B, int32_t K,
+                               float scale, uint32_t flags, void* out, gdn_dims_t dims,
+                               gdn_dtype_t dtype, void* stream) {
+    gdn_status_t st = check_dims(dims, dtype);
+    if (st != GDN_OK) return st;
+    if (B < 0 || K < 0 || K > gdn::kVerifyMaxK || (int64_t)B * K * dims.H_v > INT32_MAX)
+        return GDN_ERR_INVALID_ARG;
+    if (dims.H_v / dims.H_k > 8) return GDN_ERR_UNSUPPORTED;
+    if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if (!isfinite(scale) || !isfinite(norm_eps) || norm_eps <= 0.f) return GDN_ERR_INVALID_ARG;
+    if (B > 0 && K > 0 &&
+        (x == nullptr || conv_w == nullptr || conv_state == nullptr || z == nullptr || a == nullptr ||
+         b == nullptr || A_log == nullptr || dt_bias == nullptr || state == nullptr ||
+         norm_w == nullptr || slots == nullptr || out == nullptr))
+        return GDN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_state) || !aligned16(z) ||
+        !aligned_n(a, elem_size(dtype)) || !aligned_n(b, elem_size(dtype)) || !aligned_n(A_log, 4) ||
+        !aligned_n(dt_bias, 4) || !aligned16(state) || !aligned16(norm_w) || !aligned_n(slots, 4) ||
+        !aligned16(out))
+        return GDN_ERR_ALIGN;
+    gdn::DecodeVerifyArgs d;
+    memset(&d, 0, sizeof(d));
+    d.x = x; d.conv_w = conv_w; d.conv_state = conv_state; d.z = z; d.a = a; d.b = b;
+    d.A_log = A_log; d.dt_bias = dt_bias; d.state = state; d.norm_w = norm_w; d.slots = slots;
+    d.B = B; d.K = K; d.H_k = dims.H_k; d.H_v = dims.H_v; d.D = dims.d_k;
+    d.scale = scale == 0.f ? 1.0f / sqrtf((float)dims.d_k) : scale;
+    d.eps = norm_eps;
+    d.l2norm = (flags & GDN_QK_L2NORM) != 0;
+    d.out = out;
+    return cuda_status(gdn::launch_decode_verify(d, dtype, (cudaStream_t)stream));
+}
+
 gdn_status_t gdn_selftest_bounded_wait(int64_t limit_ns, void* stream) {
     if (limit_ns < 1000) limit_ns = 1000;
     if (limit_ns > 1000000000) limit_ns = 1000000000;

@@ -75,6 +75,25 @@ struct DecodeStepArgs {
 };
 cudaError_t launch_decode_step(const DecodeStepArgs& a, gdn_dtype_t dt, cudaStream_t s);
 
+// K draft tokens per sequence from the states in slot slots[b][0]; the conv
+// state and the recurrent state after draft token t go to slot slots[b][t + 1].
+struct DecodeVerifyArgs {
+    const void* x;         // [B, K, conv_dim]
+    const void* conv_w;    // [conv_dim, 4]
+    void* conv_state;      // [slots, conv_dim, 3]
+    const void *z, *a, *b; // [B, K, H_v*D], [B, K, H_v], [B, K, H_v]
+    const float *A_log, *dt_bias;
+    float* state;          // [slots, H_v, D, D]
+    const void* norm_w;    // [D]
+    const int32_t* slots;  // [B, K + 1]
+    int B, K, H_k, H_v, D;
+    float scale, eps;
+    int l2norm;
+    void* out;             // [B, K, H_v*D]
+};
+constexpr int kVerifyMaxK = 16;
+cudaError_t launch_decode_verify(const DecodeVerifyArgs& a, gdn_dtype_t dt, cudaStream_t s);
+
 // cuTensorMapEncodeTiled from the driver (nullptr if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensormap_encoder();
 

@@ -345,6 +345,36 @@ gdn_status_t gdn_decode_step(const void* x, const void* conv_w, void* conv_state
                              void* stream);
 
 /*
+ * Speculative decoding, the verification pass: K draft tokens of each of B
+ * sequences through the fused decode step (conv update + SiLU, gates, l2
+ * norms, recurrent rule, RMSNormGated), token after token, in one kernel.  The
+ * pages name multi-token (MTP) speculative decoding as missing (NxD-Inference
+ * Qwen3.6-27B PR, "Known limitations"); each token is the recurrent rule of the
+ * cortex commit's "Delta rule (recurrent, per-token)".  The states are read
+ * from cache slot slots[b][0] and the conv state and recurrent state after
+ * draft token t are written to slot slots[b][t + 1], so accepting the first j
+ * draft tokens of sequence b is continuing from slot slots[b][j] (nothing is
+ * copied); slot slots[b][0] itself is only read unless it is repeated later in
+ * the row.  Each value head's state is read once and written K times.
+ *   x          (device) [B, K, conv_dim]  dtype (pre-conv mixed_qkv of the draft tokens)
+ *   z          (device) [B, K, H_v*d_v];  a, b (device) [B, K, H_v]   dtype
+ *   conv_w, A_log, dt_bias, norm_w, norm_eps, scale, flags as gdn_decode_step
+ *   conv_state (device) [n_slots, conv_dim, 3] dtype;  state (device) [n_slots, H_v, d_k, d_v] f32
+ *   slots      (device) [B, K + 1] int32, required: the slots of all rows distinct
+ *              (slots[b][K] may equal slots[b][0]) and < n_slots (not checked on
+ *              the device: an out-of-range slot is out of bounds)
+ *   out        (device) [B, K, H_v*d_v] dtype
+ * 1 <= K <= 16 (K = 0 or B = 0: nothing to do), H_v / H_k <= 8.  Every output
+ * and every state equals that of K successive gdn_decode_step calls, bit for bit.
+ */
+gdn_status_t gdn_decode_verify(const void* x, const void* conv_w, void* conv_state, const void* z,
+                               const void* a, const void* b, const float* A_log,
+                               const float* dt_bias, float* state, const void* norm_w,
+                               float norm_eps, const int32_t* slots, int32_t B, int32_t K,
+                               float scale, uint32_t flags, void* out, gdn_dims_t dims,
+                               gdn_dtype_t dtype, void* stream);
+
+/*
  * RMSNormGated over each value head.
  * Defined by: cortex GatedDeltaNet commit, "Output": RMSNormGated(core_attn_out, z).
  *   out[t, h*d_v + j] = w[j] * o[t,h,j] / sqrt(mean_j o[t,h,j]^2 + eps) * silu(z[t, h*d_v + j])

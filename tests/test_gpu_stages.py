@@ -437,3 +437,49 @@ def test_fused_decode_step_with_slots(dtype, shape):
     others = [i for i in range(n_slots) if i not in slots.tolist()]
     assert torch.equal(S_f[others].cpu(), S_all[others])
     assert torch.equal(cs_f[others].cpu(), cs_all[others])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [W.TINY, SMALL_128], ids=["d16", "d128"])
+@pytest.mark.parametrize("K", [1, 4, 16])
+def test_decode_verify_equals_successive_fused_steps(dtype, shape, K):
+    """gdn_decode_verify (K draft tokens per sequence in one kernel, states read
+    from slot slots[b, 0] and the states after draft token t written to slot
+    slots[b, t + 1]) gives every output, state and conv state of K successive
+    gdn_decode_step calls bit for bit; slot slots[b, 0] is only read (unless it
+    is repeated as slots[b, K]) and slots of no row are untouched."""
+    B = 5
+    n_slots = B * (K + 1) + 3
+    d = W.decode_inputs(shape, dtype, B, K, seed=43)
+    p = W.layer_params(shape, dtype, seed=43)
+    S_all = W.draw((n_slots, shape.H_v, shape.d_k, shape.d_v), seed=43, stream=62,
+                   dtype=torch.float32, p1=0.02)
+    cs_all = W.draw((n_slots, shape.conv_dim, 3), seed=43, stream=63, dtype=dtype)
+    perm = torch.randperm(n_slots, generator=torch.Generator().manual_seed(K))
+    slots = perm[:B * (K + 1)].view(B, K + 1).to(torch.int32).clone()
+    slots[1, K] = slots[1, 0]  # sequence 1 writes its last state over its first
+    pd = {k: v.cuda() for k, v in p.items()}
+    # inputs as [B, K, ...]
+    x, z, a, b = (d[k].transpose(0, 1).contiguous().cuda() for k in ("qkv", "z", "a", "b"))
+    S_v, cs_v = S_all.clone().cuda(), cs_all.clone().cuda()
+    out = gdn.gdn_decode_verify(x, z, a, b, pd["conv_w"], pd["A_log"], pd["dt_bias"], pd["norm_w"],
+                                _dims(shape), S_v, cs_v, slots.cuda())
+    # the same tokens through gdn_decode_step, in place on a dense copy of slot 0
+    S_r = S_all[slots[:, 0].long()].clone().cuda()
+    cs_r = cs_all[slots[:, 0].long()].clone().cuda()
+    for t in range(K):
+        out_t = gdn.gdn_decode_step(x[:, t].contiguous(), z[:, t].contiguous(), a[:, t].contiguous(),
+                                    b[:, t].contiguous(), pd["conv_w"], pd["A_log"], pd["dt_bias"],
+                                    pd["norm_w"], _dims(shape), S_r, cs_r)
+        gdn.gdn_sync_status()
+        assert torch.equal(out[:, t].cpu(), out_t.cpu()), f"output of draft token {t}"
+        dst = slots[:, t + 1].long()
+        assert torch.equal(S_v[dst].cpu(), S_r.cpu()), f"state after draft token {t}"
+        assert torch.equal(cs_v[dst].cpu(), cs_r.cpu()), f"conv state after draft token {t}"
+    for bb in range(B):
+        if bb != 1:
+            s0 = int(slots[bb, 0])
+            assert torch.equal(S_v[s0].cpu(), S_all[s0]) and torch.equal(cs_v[s0].cpu(), cs_all[s0])
+    others = [i for i in range(n_slots) if i not in slots.flatten().tolist()]
+    assert torch.equal(S_v[others].cpu(), S_all[others])
+    assert torch.equal(cs_v[others].cpu(), cs_all[others])
