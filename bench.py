@@ -420,7 +420,8 @@ def run_ours(args):
         "ms_per_call": round(vms, 4), "calls": nv, "call": "gdn_decode_verify (one kernel per call)",
         "roofline": {"kernel": "gdn_decode_verify", "bound": "hbm", "achieved": round(v_gbs, 1),
                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(v_gbs / pk["hbm_gbs"], 4),
-                     "peak_source": pk["source"] + " (HBM copy)", "traffic": None,
+                     "peak_source": pk["source"] + " (HBM copy)",
+                     "traffic": traffic_record("decode_verify"),
                      "algorithmic_bytes_per_launch": vbytes},
     }
 
