@@ -257,7 +257,9 @@ def run_ours(args):
     clocks.mark(False)
     barrier(dist, dev)
     chunk_launches = gdn.gdn_chunk_prefill_launches(1, T, dims, wp.dtype)
-    step_launches = 2 + chunk_launches + 1  # conv (tile kernel + state kernel), chunk, norm
+    # conv: one kernel (one sequence, no cu_seqlens, state_out apart from state_in:
+    # the tile kernel writes the conv state), chunk, norm
+    step_launches = 1 + chunk_launches + 1
     launches += args.steps * step_launches
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
     conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
@@ -486,7 +488,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     clocks.mark(False)
     barrier(dist, dev)
-    piece_launches = 2 + gdn.gdn_chunk_prefill_launches(
+    piece_launches = 1 + gdn.gdn_chunk_prefill_launches(
         1, gdn._lib.load().gdn_layer_prefill_host_piece(T, gdn._dims(dims), gdn._lib.GDN_BF16),
         dims, wp.dtype) + 1
     launches += args.steps * host_pieces * piece_launches

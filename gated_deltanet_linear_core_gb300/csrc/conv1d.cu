@@ -128,6 +128,42 @@ __global__ void __launch_bounds__(kTileThreads, 3) conv1d_fwd_kernel(const __gri
     auto row = [&](int64_t p, float* dst) {  // input of token p (p >= t0 - 3) from the tile
         unpack16<T>(*reinterpret_cast<const uint4*>(tile + (p - t0 + 3) * kRowBytes + cg * 16), dst);
     };
+    // One sequence and no aliasing (fused_state): the run holding the last
+    // token writes the conv state, and the run holding token m N - 1 the m-th
+    // checkpoint -- the 3 raw inputs ending there, from the tile (its halo
+    // reaches back 3 tokens) or, for a sequence shorter than 3, from state_in
+    // (zeros without one).  Values are bit copies.
+    auto write3 = [&](int64_t last, T* dst) {
+        float flat[3 * V];  // [channel][3] order of the state
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const int64_t p = last - 2 + j;
+            float v[V];
+            if (p >= 0) {
+                row(p, v);
+            } else if (st != nullptr) {
+                load_state_col(st, 0, C, c0, (int)(3 + p), v);
+            } else {
+#pragma unroll
+                for (int q = 0; q < V; ++q) v[q] = 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < V; ++q) flat[q * 3 + j] = v[q];
+        }
+#pragma unroll
+        for (int i = 0; i < 3; ++i) store16(dst + i * V, flat + i * V);
+    };
+    auto fused_state = [&]() {
+        if (!a.fused_state) return;
+        if (a.state_out != nullptr && a.T - 1 < te)
+            write3(a.T - 1, static_cast<T*>(a.state_out) + (int64_t)c0 * 3);
+        if (a.ckpt_every > 0 && a.ckpt != nullptr) {
+            for (int64_t m = (tb + a.ckpt_every) / a.ckpt_every; m * a.ckpt_every - 1 < te; ++m) {
+                if (m - 1 >= a.ckpt_rows) break;
+                write3(m * a.ckpt_every - 1, static_cast<T*>(a.ckpt) + ((m - 1) * C + c0) * 3);
+            }
+        }
+    };
     if (tb - 3 >= s && te <= e) {
         // the run and its halo lie inside one sequence
         float r0[V], r1[V], r2[V], r3[V];
@@ -146,6 +182,7 @@ __global__ void __launch_bounds__(kTileThreads, 3) conv1d_fwd_kernel(const __gri
                 r2[q] = r3[q];
             }
         }
+        fused_state();
         return;
     }
     // a sequence starts inside the run or its halo
@@ -169,6 +206,7 @@ __global__ void __launch_bounds__(kTileThreads, 3) conv1d_fwd_kernel(const __gri
         }
         conv_out2<T>(w, in[0], in[1], in[2], in[3], a.silu, y + t * C + c0);
     }
+    fused_state();
 }
 
 // Conv state after a sequence (and its checkpoints): the 3 newest raw inputs
@@ -271,8 +309,13 @@ __global__ void __launch_bounds__(kThreads) conv1d_update_kernel(const T* __rest
 }
 
 template <typename T>
-cudaError_t conv_fwd_t(const ConvArgs& a, cudaStream_t s) {
+cudaError_t conv_fwd_t(const ConvArgs& args, cudaStream_t s) {
     constexpr int V = Vec16<T>::N;
+    // one sequence whose state_out does not alias state_in: the tile kernel
+    // writes the state and checkpoints (no tile reads what another writes);
+    // otherwise a second pass does, after every tile has read state_in
+    ConvArgs a = args;
+    a.fused_state = a.cu == nullptr && a.T > 0 && (a.state_in == nullptr || a.state_in != a.state_out);
     constexpr int TC = kRowBytes / (int)sizeof(T);
     const int nvec = a.C / V;
     const dim3 blk(kThreads);
@@ -293,7 +336,7 @@ cudaError_t conv_fwd_t(const ConvArgs& a, cudaStream_t s) {
         const dim3 grid((unsigned)((a.T + kTT - 1) / kTT), (unsigned)((a.C + TC - 1) / TC));
         conv1d_fwd_kernel<T><<<grid, kTileThreads, 0, s>>>(xmap, a);
     }
-    if (a.state_out != nullptr || (a.ckpt_every > 0 && a.ckpt != nullptr)) {
+    if (!a.fused_state && (a.state_out != nullptr || (a.ckpt_every > 0 && a.ckpt != nullptr))) {
         const dim3 grid2((unsigned)a.n_seq, (nvec + kThreads - 1) / kThreads);
         conv1d_state_kernel<T><<<grid2, blk, 0, s>>>(a);
     }

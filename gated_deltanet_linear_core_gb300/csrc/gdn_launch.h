@@ -25,6 +25,7 @@ struct ConvArgs {
     int64_t ckpt_rows;
     int silu;
     void* y;
+    int fused_state;  // set by launch_conv1d_fwd: the tile kernel writes the state and checkpoints
 };
 cudaError_t launch_conv1d_fwd(const ConvArgs& a, gdn_dtype_t dt, cudaStream_t s);
 cudaError_t launch_conv1d_update(const void* x, const void* w, void* state, int B, int C,

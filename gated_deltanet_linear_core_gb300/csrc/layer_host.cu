@@ -35,6 +35,7 @@ struct Slot {
 struct HostLayout {
     int64_t piece;  // tokens per piece (a multiple of 64 unless the whole sequence is one piece)
     size_t a, b;    // the whole sequence's gate inputs (copied once)
+    size_t cst[2];  // conv state between pieces, alternating (never read and written by one call)
     Slot slot[kSlots];
     size_t chunk_ws[kSlots], chunk_ws_bytes, total;
 };
@@ -54,6 +55,10 @@ HostLayout host_layout(int64_t T, int H_k, int H_v, int D, int es, bool tensor_c
     size_t off = 0;
     L.a = off; off = align256(off + (size_t)T * H_v * es);
     L.b = off; off = align256(off + (size_t)T * H_v * es);
+    for (int i = 0; i < 2; ++i) {
+        L.cst[i] = off;
+        off = align256(off + (size_t)(2 * H_k + H_v) * D * 3 * es);
+    }
     for (int s = 0; s < kSlots; ++s) {
         Slot& q = L.slot[s];
         q.qkv = off; off = align256(off + (size_t)p * C * es);
@@ -193,8 +198,11 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
         if (e == cudaSuccess) {
             ConvArgs c;
             c.x = ws + q.qkv; c.w = h.conv_w; c.cu = nullptr; c.n_seq = 1; c.T = tp; c.C = (int)C;
-            c.state_in = p == 0 ? h.conv_state_in : h.conv_state_out;
-            c.state_out = h.conv_state_out;
+            // piece p reads the state piece p - 1 wrote and writes the other buffer
+            // (the last piece writes conv_state_out), so no conv call has its
+            // state_out aliasing its state_in
+            c.state_in = p == 0 ? h.conv_state_in : ws + L.cst[(p - 1) & 1];
+            c.state_out = p == n_piece - 1 ? h.conv_state_out : ws + L.cst[p & 1];
             c.ckpt_every = 0; c.ckpt = nullptr; c.ckpt_rows = 0; c.silu = 1; c.y = ws + q.y;
             e = launch_conv1d_fwd(c, dt, pre);
         }

@@ -53,6 +53,34 @@ def test_conv1d_fwd(dtype, shape):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("T", [1, 2, 3, 130, 4101])
+@pytest.mark.parametrize("state", ["none", "separate", "aliased"])
+def test_conv1d_fwd_one_sequence(dtype, T, state):
+    """One sequence without cu_seqlens: with state_out apart from state_in (or
+    no state_in) the tile kernel writes the conv state and the checkpoints
+    itself; aliased, the second pass does.  Both bit-exact, T from 1 to a
+    ragged multi-tile length."""
+    shape = SMALL_128
+    inp = W.layer_inputs(shape, dtype, [T], seed=19, init_state=True)
+    x, w = inp["mixed_qkv"].cuda(), inp["conv_w"].cuda()
+    st_in = None if state == "none" else inp["conv_state0"].cuda()
+    st_out = st_in if state == "aliased" else torch.full((1, shape.conv_dim, 3), float("nan"),
+                                                         dtype=dtype, device="cuda")
+    rows = T // 64
+    ck = torch.full((rows, shape.conv_dim, 3), float("nan"), dtype=dtype, device="cuda") if rows else None
+    y = gdn.gdn_conv1d_fwd(x, w, _dims(shape), None, st_in, st_out, 64 if rows else 0, ck)
+    torch.cuda.synchronize()
+    f = W.to_f64
+    y_ref, st_ref, ck_ref = oracle.conv1d(f(inp["mixed_qkv"]), f(inp["conv_w"]), None,
+                                          None if state == "none" else f(inp["conv_state0"]), True,
+                                          64 if rows else 0)
+    assert_close("y", host(y), y_ref, 1e-6 if dtype == torch.float32 else TOL[dtype])
+    assert np.array_equal(host(st_out), st_ref), "conv state out not bit-exact"
+    if rows:
+        assert np.array_equal(host(ck), ck_ref), "conv checkpoints not bit-exact"
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_conv1d_fwd_zero_state_and_no_silu(dtype):
     shape = SMALL_128
     inp = W.layer_inputs(shape, dtype, [5, 2, 130], seed=12)
