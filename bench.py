@@ -225,15 +225,18 @@ def run_ours(args):
     out = torch.empty((T, s.H_v * s.d_v), dtype=wp.dtype, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    def prefill_step(ev=None):
+    def prefill_step(ev=None, stages=False):
+        # stages: events between the three calls too (for the per-call times);
+        # the headline steps have events only at their ends, since an event
+        # between two kernels keeps the second from being placed early
         if ev:
             ev[0].record(stream)
         gdn.gdn_conv1d_fwd(d["mixed_qkv"], d["conv_w"], dims, None, None, conv_out, y=y)
-        if ev:
+        if ev and stages:
             ev[1].record(stream)
         gdn.gdn_chunk_prefill(y, dims, d["a"], d["b"], d["A_log"], d["dt_bias"], final_state=S,
                               o=o)
-        if ev:
+        if ev and stages:
             ev[2].record(stream)
         gdn.gdn_rmsnorm_gated(o, d["z"], d["norm_w"], dims, out=out)
         if ev:
@@ -256,15 +259,25 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     clocks.mark(False)
     barrier(dist, dev)
-    chunk_launches = gdn.gdn_chunk_prefill_launches(1, T, dims, wp.dtype)
+    chunk_launches = gdn.gdn_chunk_prefill_launches(1, T, dims, wp.dtype, cu_seqlens=None)
     # conv: one kernel (one sequence, no cu_seqlens, state_out apart from state_in:
     # the tile kernel writes the conv state), chunk, norm
     step_launches = 1 + chunk_launches + 1
     launches += args.steps * step_launches
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    chunk_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    norm_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    # the same steps with events between the calls: per-call times
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    clocks.mark(True)
+    for k in range(args.steps):
+        flush.zero_()
+        prefill_step(sevs[k], stages=True)
+    torch.cuda.synchronize(dev)
+    clocks.mark(False)
+    launches += args.steps * step_launches
+    conv_ms = [e[0].elapsed_time(e[1]) for e in sevs]
+    chunk_ms = [e[1].elapsed_time(e[2]) for e in sevs]
+    norm_ms = [e[2].elapsed_time(e[3]) for e in sevs]
     total_s = max_over_ranks(dist, sum(step_ms) / 1e3, dev)
     value = world * T * args.steps / total_s
     chunk_avg = sum(chunk_ms) / len(chunk_ms) / 1e3
@@ -490,7 +503,7 @@ def run_ours(args):
     barrier(dist, dev)
     piece_launches = 1 + gdn.gdn_chunk_prefill_launches(
         1, gdn._lib.load().gdn_layer_prefill_host_piece(T, gdn._dims(dims), gdn._lib.GDN_BF16),
-        dims, wp.dtype) + 1
+        dims, wp.dtype, cu_seqlens=None) + 1
     launches += args.steps * host_pieces * piece_launches
     e_total = max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in eev) / 1e3, dev)
     e2e = {"value": round(world * T * args.steps / e_total, 1), "unit": "tokens/s",

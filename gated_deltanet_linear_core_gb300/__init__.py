@@ -170,9 +170,12 @@ def gdn_chunk_prefill_workspace_size(n_seq: int, T_tot: int, dims, dtype) -> int
                                                             code))
 
 
-def gdn_chunk_prefill_launches(n_seq: int, T_tot: int, dims, dtype) -> int:
+def gdn_chunk_prefill_launches(n_seq: int, T_tot: int, dims, dtype, cu_seqlens=True) -> int:
+    """Kernel launches of one gdn_chunk_prefill call; cu_seqlens: whether the
+    call passes cu_seqlens (a truthy value) or not (None / False)."""
     code = _lib.GDN_BF16 if dtype == torch.bfloat16 else _lib.GDN_F32
-    return int(_lib.load().gdn_chunk_prefill_launches(int(n_seq), int(T_tot), _dims(dims), code))
+    has_cu = 0 if cu_seqlens is None or cu_seqlens is False else 1
+    return int(_lib.load().gdn_chunk_prefill_launches(int(n_seq), int(T_tot), has_cu, _dims(dims), code))
 
 
 def _gate_ptrs(a, b, A_log, dt_bias, g, beta, dt):

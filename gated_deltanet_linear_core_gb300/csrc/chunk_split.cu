@@ -104,6 +104,8 @@ Work work_at(uint8_t* base, const Layout& L, int H_v) {
 // coff[i] = number of chunks of sequences 0..i-1 (one block, any n_seq)
 __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, int n_seq, int64_t T,
                                                              int32_t* coff) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int32_t wsum[32];
     __shared__ int32_t base;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -190,6 +192,8 @@ template <bool NEUMANN>
 __global__ void __launch_bounds__(NT_I, 3)
 chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
                    const __grid_constant__ CUtensorMap umap, DeltaArgs a, Work w, int64_t C0) {
+    pdl_wait();
+    pdl_trigger();
     const int h = blockIdx.x;
     const int64_t gc = C0 + blockIdx.y;
     // first token and length of chunk gc (no loads for one sequence without offsets)
@@ -730,13 +734,17 @@ __global__ void __launch_bounds__(NT_C, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
                    const __grid_constant__ CUtensorMap utmap, const __grid_constant__ CUtensorMap pmap,
                    const __grid_constant__ CUtensorMap omap, DeltaArgs a, Work w, int64_t C0, int64_t segc) {
+    pdl_wait();
+    pdl_trigger();
     using Ly = ChainLayout<VS>;
     constexpr int NV = D / VS, CV = VS / 4;
     const int vp = blockIdx.x % NV;
     const int h = (blockIdx.x / NV) % a.H_v;
     const int seq = blockIdx.x / (NV * a.H_v);
     const int v0 = vp * VS;
-    const int64_t cs = w.coff[seq], ce = w.coff[seq + 1];
+    // chunk offsets of the sequence (one sequence without offsets: [0, ceil(T / C)))
+    const int64_t cs = a.cu == nullptr ? 0 : w.coff[seq];
+    const int64_t ce = a.cu == nullptr ? (a.T + C - 1) / C : w.coff[seq + 1];
     const int64_t c_lo = cs > C0 ? cs : C0, c_hi = ce < C0 + segc ? ce : C0 + segc;
     const int64_t sbase = ((int64_t)seq * a.H_v + h) * D * D;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1110,24 +1118,30 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
         if ((e = cudaEventRecord(ev_pre, s_pre)) != cudaSuccess || (e = cudaStreamWaitEvent(s, ev_pre, 0)) != cudaSuccess)
             return e;
     }
-    chunk_offsets_kernel<<<1, 1024, 0, si>>>(a.cu, a.n_seq, a.T, w.coff);
+    if (a.cu != nullptr && (e = launch_pdl(chunk_offsets_kernel, dim3(1), dim3(1024), 0, si, a.cu, a.n_seq, a.T,
+                                           w.coff)) != cudaSuccess)
+        return e;
     for (int64_t seg = 0; seg < Ly.n_seg; ++seg) {
         const int64_t C0 = seg * Ly.segc;
         if (a.neumann)
-            chunk_intra_kernel<true><<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, si>>>(qmap, wtmap, utmap, a, w, C0);
+            e = launch_pdl(chunk_intra_kernel<true>, dim3((unsigned)a.H_v, (unsigned)Ly.segc), dim3(NT_I), ISMEM, si,
+                           qmap, wtmap, utmap, a, w, C0);
         else
-            chunk_intra_kernel<false><<<dim3((unsigned)a.H_v, (unsigned)Ly.segc), NT_I, ISMEM, si>>>(qmap, wtmap, utmap, a, w, C0);
+            e = launch_pdl(chunk_intra_kernel<false>, dim3((unsigned)a.H_v, (unsigned)Ly.segc), dim3(NT_I), ISMEM,
+                           si, qmap, wtmap, utmap, a, w, C0);
+        if (e != cudaSuccess) return e;
         if (two) {
             if ((e = cudaGetLastError()) != cudaSuccess || (e = cudaEventRecord(ev_pre, si)) != cudaSuccess ||
                 (e = cudaStreamWaitEvent(s, ev_pre, 0)) != cudaSuccess)
                 return e;
         }
         if (split)
-            chunk_chain_kernel<64><<<(unsigned)(a.n_seq * a.H_v * 2), NT_C, ChainLayout<64>::SMEM, s>>>(
-                qmap, wtmap, utmap, pmap, omap, a, w, C0, Ly.segc);
+            e = launch_pdl(chunk_chain_kernel<64>, dim3((unsigned)(a.n_seq * a.H_v * 2)), dim3(NT_C),
+                           ChainLayout<64>::SMEM, s, qmap, wtmap, utmap, pmap, omap, a, w, C0, Ly.segc);
         else
-            chunk_chain_kernel<128><<<(unsigned)(a.n_seq * a.H_v), NT_C, ChainLayout<128>::SMEM, s>>>(
-                qmap, wtmap, utmap, pmap, omap, a, w, C0, Ly.segc);
+            e = launch_pdl(chunk_chain_kernel<128>, dim3((unsigned)(a.n_seq * a.H_v)), dim3(NT_C),
+                           ChainLayout<128>::SMEM, s, qmap, wtmap, utmap, pmap, omap, a, w, C0, Ly.segc);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -1138,8 +1152,8 @@ size_t chunk_split_workspace_bytes(int n_seq, int64_t T, int H_v) {
     return layout_of(n_seq, T, H_v).total;
 }
 
-int chunk_split_launches(int n_seq, int64_t T, int H_v) {
-    return 1 + 2 * (int)layout_of(n_seq, T, H_v).n_seg;
+int chunk_split_launches(int n_seq, int64_t T, int H_v, bool has_cu) {
+    return (has_cu ? 1 : 0) + 2 * (int)layout_of(n_seq, T, H_v).n_seg;
 }
 
 cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s) {

@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(kTileThreads, 3) conv1d_fwd_kernel(const __gri
     constexpr int TC = kRowBytes / (int)sizeof(T);  // channels per tile
     __shared__ alignas(128) uint8_t tile[(kTT + 3) * kRowBytes];
     __shared__ alignas(8) uint64_t bar;
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, cg = tid & 31, tg = tid >> 5;
     const int64_t t0 = (int64_t)blockIdx.x * kTT;
     const int cbase = blockIdx.y * TC;
@@ -216,6 +218,8 @@ __global__ void __launch_bounds__(kTileThreads, 3) conv1d_fwd_kernel(const __gri
 template <typename T>
 __global__ void __launch_bounds__(kThreads) conv1d_state_kernel(ConvArgs a) {
     constexpr int V = Vec16<T>::N;
+    pdl_wait();
+    pdl_trigger();
     const int nvec = a.C / V;
     const int cv = blockIdx.y * blockDim.x + threadIdx.x;
     if (cv >= nvec) return;
@@ -334,11 +338,13 @@ cudaError_t conv_fwd_t(const ConvArgs& args, cudaStream_t s) {
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
         const dim3 grid((unsigned)((a.T + kTT - 1) / kTT), (unsigned)((a.C + TC - 1) / TC));
-        conv1d_fwd_kernel<T><<<grid, kTileThreads, 0, s>>>(xmap, a);
+        const cudaError_t e = launch_pdl(conv1d_fwd_kernel<T>, grid, dim3(kTileThreads), 0, s, xmap, a);
+        if (e != cudaSuccess) return e;
     }
     if (!a.fused_state && (a.state_out != nullptr || (a.ckpt_every > 0 && a.ckpt != nullptr))) {
         const dim3 grid2((unsigned)a.n_seq, (nvec + kThreads - 1) / kThreads);
-        conv1d_state_kernel<T><<<grid2, blk, 0, s>>>(a);
+        const cudaError_t e = launch_pdl(conv1d_state_kernel<T>, grid2, blk, 0, s, a);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -329,10 +329,11 @@ size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t
     return gdn::chunk_split_workspace_bytes(n_seq, T_tot, dims.H_v);
 }
 
-int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, gdn_dims_t dims, gdn_dtype_t dtype) {
+int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_seqlens, gdn_dims_t dims,
+                                   gdn_dtype_t dtype) {
     if (check_dims(dims, dtype) != GDN_OK || n_seq < 1 || T_tot <= 0) return 0;
     if (dtype != GDN_BF16 || dims.d_k != 128) return 1;  // the CUDA-core path: one kernel
-    return gdn::chunk_split_launches(n_seq, T_tot, dims.H_v);
+    return gdn::chunk_split_launches(n_seq, T_tot, dims.H_v, has_cu_seqlens != 0);
 }
 
 gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, const float* A_log,

@@ -66,6 +66,32 @@ __device__ __forceinline__ void store16(T* __restrict__ p, const float* in) {
     *reinterpret_cast<uint4*>(p) = u;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with launch_pdl may have
+// its CTAs placed while the previous kernel on the stream is still finishing;
+// pdl_wait() blocks until that kernel has completed and its writes are
+// visible, so every kernel calls it before touching global memory.
+// pdl_trigger() lets the next kernel's CTAs be placed once every CTA of this
+// grid has started.  Both are no-ops without a programmatic dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- math
 // Full-precision CUDA math functions only (no hand-written approximations).
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }

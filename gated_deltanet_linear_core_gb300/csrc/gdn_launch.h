@@ -110,7 +110,7 @@ cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_by
 cudaError_t launch_chunk_split_two(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s_pre,
                                    cudaStream_t s_chain, cudaEvent_t ev_pre);
 // Kernel launches launch_chunk_split issues: chunk offsets, then intra + chain per segment.
-int chunk_split_launches(int n_seq, int64_t T, int H_v);
+int chunk_split_launches(int n_seq, int64_t T, int H_v, bool has_cu);
 
 // The same chunked prefill with its scratch in a fixed device array of the
 // library (gdn_chunk_prefill_noalloc): no allocation; final_state required.

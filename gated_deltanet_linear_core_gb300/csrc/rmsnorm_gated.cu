@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256) rmsnorm_gated_kernel(const T* o,  // may 
                                                             const T* __restrict__ z,
                                                             const T* __restrict__ w, float eps,
                                                             int64_t rows, T* out) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int V = Vec16<T>::N;
     constexpr int TPR = D / V;  // lanes per row
     static_assert(TPR >= 1 && TPR <= 32 && (32 % TPR) == 0, "row must fit a warp");
@@ -70,12 +72,10 @@ cudaError_t norm_t(const void* o, const void* z, const void* w, float eps, int64
     const int64_t rows_per_block = (int64_t)(256 / 32) * (32 / (D / V));
     const unsigned grid = (unsigned)((rows + rows_per_block - 1) / rows_per_block);
     if (D == 128)
-        rmsnorm_gated_kernel<T, 128><<<grid, 256, 0, s>>>((const T*)o, (const T*)z, (const T*)w,
-                                                          eps, rows, (T*)out);
-    else
-        rmsnorm_gated_kernel<T, 16><<<grid, 256, 0, s>>>((const T*)o, (const T*)z, (const T*)w,
-                                                         eps, rows, (T*)out);
-    return cudaGetLastError();
+        return launch_pdl(rmsnorm_gated_kernel<T, 128>, dim3(grid), dim3(256), 0, s, (const T*)o, (const T*)z,
+                          (const T*)w, eps, rows, (T*)out);
+    return launch_pdl(rmsnorm_gated_kernel<T, 16>, dim3(grid), dim3(256), 0, s, (const T*)o, (const T*)z,
+                      (const T*)w, eps, rows, (T*)out);
 }
 
 }  // namespace

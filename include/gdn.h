@@ -219,9 +219,12 @@ gdn_status_t gdn_selftest_bounded_wait(int64_t limit_ns, void* stream);
 /*
  * Number of kernel launches one gdn_chunk_prefill call with these sizes
  * issues (for profiling and launch accounting; the library has no paper
- * counterpart for it).  0 for T_tot == 0 or invalid dims.
+ * counterpart for it): on the tensor-core path, a chunk-offsets kernel when
+ * cu_seqlens is given (has_cu_seqlens != 0), then an intra and a chain kernel
+ * per workspace segment.  0 for T_tot == 0 or invalid dims.
  */
-int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, gdn_dims_t dims, gdn_dtype_t dtype);
+int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_seqlens, gdn_dims_t dims,
+                                   gdn_dtype_t dtype);
 
 /*
  * Chunked gated delta rule (chunk size 64, WY/UT form) over packed sequences.

@@ -194,12 +194,14 @@ def test_workspace_size(lib):
 
 
 def test_prefill_launch_count(lib):
-    # chunk offsets, then an intra and a chain kernel per workspace segment; the
-    # CUDA-core path is one kernel; nothing for an empty call
+    # chunk offsets (with cu_seqlens), then an intra and a chain kernel per
+    # workspace segment; the CUDA-core path is one kernel; nothing for an empty call
     dims = gdn.GDNDims(16, 48, 128, 128)
     assert gdn.gdn_chunk_prefill_launches(1, 4096, dims, torch.bfloat16) == 3
+    assert gdn.gdn_chunk_prefill_launches(1, 4096, dims, torch.bfloat16, cu_seqlens=None) == 2
     long_run = gdn.gdn_chunk_prefill_launches(1, 262144, dims, torch.bfloat16)
     assert long_run > 3 and long_run % 2 == 1
+    assert gdn.gdn_chunk_prefill_launches(1, 262144, dims, torch.bfloat16, cu_seqlens=None) == long_run - 1
     assert gdn.gdn_chunk_prefill_launches(1, 64, gdn.GDNDims(2, 4, 16, 16), torch.float32) == 1
     assert gdn.gdn_chunk_prefill_launches(1, 0, dims, torch.bfloat16) == 0
 
