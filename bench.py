@@ -1,8 +1,8 @@
 """Benchmark of the GDN layer core on GB300.
 
 Prints ONE JSON line (rank 0).  A step is one pass of the layer core's
-prefill path -- gdn_conv1d_fwd + gdn_chunk_prefill + gdn_rmsnorm_gated --
-over the Qwen3.6-27B prefill workload (B=1, T=4096, 16 QK / 48 V heads,
+prefill path -- one gdn_layer_prefill call: conv1d + SiLU, the chunked rule,
+RMSNormGated -- over the Qwen3.6-27B prefill workload (B=1, T=4096, 16 QK / 48 V heads,
 d=128, bf16 activations, f32 state).  `value` is prefill tokens/s with inputs
 resident in HBM; the same line carries the decode path (gdn_conv1d_update +
 gdn_recurrent_decode + gdn_rmsnorm_gated on the 27B decode workload: 64
@@ -224,23 +224,30 @@ def run_ours(args):
     o = torch.empty((T, s.H_v, s.d_v), dtype=wp.dtype, device=dev)
     out = torch.empty((T, s.H_v * s.d_v), dtype=wp.dtype, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    lws = torch.empty(gdn.gdn_layer_prefill_workspace_size(1, T, dims, wp.dtype), dtype=torch.uint8, device=dev)
+    cws = torch.empty(gdn.gdn_chunk_prefill_workspace_size(1, T, dims, wp.dtype), dtype=torch.uint8, device=dev)
 
-    def prefill_step(ev=None, stages=False):
-        # stages: events between the three calls too (for the per-call times);
-        # the headline steps have events only at their ends, since an event
-        # between two kernels keeps the second from being placed early
+    def prefill_step(ev=None):
+        # the headline step: one gdn_layer_prefill call, events only at its ends
         if ev:
             ev[0].record(stream)
-        gdn.gdn_conv1d_fwd(d["mixed_qkv"], d["conv_w"], dims, None, None, conv_out, y=y)
-        if ev and stages:
-            ev[1].record(stream)
-        gdn.gdn_chunk_prefill(y, dims, d["a"], d["b"], d["A_log"], d["dt_bias"], final_state=S,
-                              o=o)
-        if ev and stages:
-            ev[2].record(stream)
-        gdn.gdn_rmsnorm_gated(o, d["z"], d["norm_w"], dims, out=out)
+        gdn.gdn_layer_prefill(d["mixed_qkv"], d["z"], d["a"], d["b"], d["conv_w"], d["A_log"], d["dt_bias"],
+                              d["norm_w"], dims, out=out, final_state=S, conv_state_out=conv_out, workspace=lws)
         if ev:
             ev[3].record(stream)
+
+    def staged_step(ev):
+        # the same kernels as three calls with events between them, for the
+        # per-call times (an event between two kernels keeps the second from
+        # being placed early, so these steps are a little longer)
+        ev[0].record(stream)
+        gdn.gdn_conv1d_fwd(d["mixed_qkv"], d["conv_w"], dims, None, None, conv_out, y=y)
+        ev[1].record(stream)
+        gdn.gdn_chunk_prefill(y, dims, d["a"], d["b"], d["A_log"], d["dt_bias"], final_state=S, o=o,
+                              workspace=cws)
+        ev[2].record(stream)
+        gdn.gdn_rmsnorm_gated(o, d["z"], d["norm_w"], dims, out=out)
+        ev[3].record(stream)
 
     clocks = ClockSampler(local)
     launches = 0
@@ -261,23 +268,24 @@ def run_ours(args):
     barrier(dist, dev)
     chunk_launches = gdn.gdn_chunk_prefill_launches(1, T, dims, wp.dtype, cu_seqlens=None)
     # conv: one kernel (one sequence, no cu_seqlens, state_out apart from state_in:
-    # the tile kernel writes the conv state), chunk, norm
-    step_launches = 1 + chunk_launches + 1
+    # the tile kernel writes the conv state), the chunk kernels, the norm
+    step_launches = gdn.gdn_layer_prefill_launches(1, T, dims, wp.dtype, cu_seqlens=None)
     launches += args.steps * step_launches
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    # the same steps with events between the calls: per-call times
-    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    # per-call times
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     torch.cuda.synchronize(dev)
     clocks.mark(True)
     for k in range(args.steps):
         flush.zero_()
-        prefill_step(sevs[k], stages=True)
+        staged_step(sev[k])
     torch.cuda.synchronize(dev)
     clocks.mark(False)
     launches += args.steps * step_launches
-    conv_ms = [e[0].elapsed_time(e[1]) for e in sevs]
-    chunk_ms = [e[1].elapsed_time(e[2]) for e in sevs]
-    norm_ms = [e[2].elapsed_time(e[3]) for e in sevs]
+    conv_ms = [e[0].elapsed_time(e[1]) for e in sev]
+    chunk_ms = [e[1].elapsed_time(e[2]) for e in sev]
+    norm_ms = [e[2].elapsed_time(e[3]) for e in sev]
     total_s = max_over_ranks(dist, sum(step_ms) / 1e3, dev)
     value = world * T * args.steps / total_s
     chunk_avg = sum(chunk_ms) / len(chunk_ms) / 1e3
@@ -501,9 +509,10 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     clocks.mark(False)
     barrier(dist, dev)
-    piece_launches = 1 + gdn.gdn_chunk_prefill_launches(
+    # per piece: conv, the chunk kernels, the norm
+    piece_launches = gdn.gdn_layer_prefill_launches(
         1, gdn._lib.load().gdn_layer_prefill_host_piece(T, gdn._dims(dims), gdn._lib.GDN_BF16),
-        dims, wp.dtype, cu_seqlens=None) + 1
+        dims, wp.dtype, cu_seqlens=None)
     launches += args.steps * host_pieces * piece_launches
     e_total = max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in eev) / 1e3, dev)
     e2e = {"value": round(world * T * args.steps / e_total, 1), "unit": "tokens/s",
@@ -527,6 +536,7 @@ def run_ours(args):
                        "d_k": s.d_k, "d_v": s.d_v, "chunk": 64, "state": "f32",
                        "l2": "flushed (512 MiB write) between timed steps",
                        "parallelism": f"replicas x{world}"},
+            "call": "gdn_layer_prefill (conv1d_fwd, chunk_prefill, rmsnorm_gated kernels)",
             "chunk_solve": chunk_solve,
             "per_kernel_ms": {"conv1d_fwd": round(statistics.mean(conv_ms), 4),
                               "chunk_prefill": round(statistics.mean(chunk_ms), 4),

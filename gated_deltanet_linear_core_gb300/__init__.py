@@ -25,6 +25,7 @@ __all__ = [
     "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill_launches", "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode", "gdn_rmsnorm_gated",
     "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_sync_status", "gdn_selftest_bounded_wait",
     "gdn_layer_prefill_host", "gdn_decode_step", "gdn_decode_verify", "gdn_layer_prefill",
+    "gdn_layer_prefill_workspace_size", "gdn_layer_prefill_launches", "gdn_chunk_prefill_norm",
     "gdn_layer_decode",
     "library_path",
 ]
@@ -219,6 +220,39 @@ def gdn_chunk_prefill(qkv, dims, a=None, b=None, A_log=None, dt_bias=None, g=Non
     return o
 
 
+def gdn_chunk_prefill_norm(qkv, z, norm_w, dims, a=None, b=None, A_log=None, dt_bias=None, g=None,
+                           beta=None, cu_seqlens=None, initial_state=None, final_state=None, ckpt_every=0,
+                           state_ckpt_out=None, scale=0.0, l2norm_qk=True, norm_eps=RMSNORM_EPS, out=None,
+                           workspace=None, stream=None, solve="direct"):
+    """gdn_chunk_prefill followed by RMSNormGated(o, z): returns out [T, H_v*d_v]
+    (the rule's output is normalised in place in `out`)."""
+    if solve not in ("direct", "neumann"):
+        raise ValueError(f"solve must be 'direct' or 'neumann', not {solve!r}")
+    dt = qkv.dtype
+    T = int(qkv.shape[0])
+    if out is None:
+        out = torch.empty((T, dims.H_v * dims.d_v), dtype=dt, device=qkv.device)
+    rows = 0 if state_ckpt_out is None else int(state_ckpt_out.shape[0])
+    lib = _lib.load()
+    if workspace is None:
+        need = lib.gdn_chunk_prefill_workspace_size(_nseq(cu_seqlens), T, _dims(dims), _dtype_code(qkv))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=qkv.device)
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.gdn_chunk_prefill_norm(
+        _ptr(qkv, "qkv", dt), *_gate_ptrs(a, b, A_log, dt_bias, g, beta, dt),
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32), _nseq(cu_seqlens), T,
+        _ptr(initial_state, "initial_state", torch.float32),
+        _ptr(final_state, "final_state", torch.float32), int(ckpt_every),
+        _ptr(state_ckpt_out, "state_ckpt_out", torch.float32), rows, float(scale),
+        (_lib.GDN_QK_L2NORM if l2norm_qk else 0) | (_lib.GDN_SOLVE_NEUMANN if solve == "neumann" else 0),
+        _ptr(z, "z", dt, (T, dims.H_v * dims.d_v)), _ptr(norm_w, "norm_w", dt, (dims.d_v,)), float(norm_eps),
+        _ptr(out, "out", dt, (T, dims.H_v * dims.d_v)), _ptr(workspace, "workspace"), ws, _dims(dims),
+        _dtype_code(qkv), _stream(qkv, stream))
+    _lib.check(st, "gdn_chunk_prefill_norm")
+    return out
+
+
 def gdn_chunk_prefill_noalloc(qkv, dims, o, final_state, a=None, b=None, A_log=None,
                               dt_bias=None, g=None, beta=None, cu_seqlens=None,
                               initial_state=None, ckpt_every=0, state_ckpt_out=None, scale=0.0,
@@ -275,37 +309,80 @@ def gdn_rmsnorm_gated(o, z, w, dims, eps=RMSNORM_EPS, out=None, stream=None):
     return out
 
 
+def gdn_layer_prefill_workspace_size(n_seq: int, T_tot: int, dims, dtype) -> int:
+    code = _lib.GDN_BF16 if dtype == torch.bfloat16 else _lib.GDN_F32
+    return int(_lib.load().gdn_layer_prefill_workspace_size(int(n_seq), int(T_tot), _dims(dims), code))
+
+
+def gdn_layer_prefill_launches(n_seq: int, T_tot: int, dims, dtype, cu_seqlens=True) -> int:
+    """Kernel launches of one gdn_layer_prefill call (cu_seqlens as in
+    gdn_chunk_prefill_launches)."""
+    code = _lib.GDN_BF16 if dtype == torch.bfloat16 else _lib.GDN_F32
+    has_cu = 0 if cu_seqlens is None or cu_seqlens is False else 1
+    return int(_lib.load().gdn_layer_prefill_launches(int(n_seq), int(T_tot), has_cu, _dims(dims), code))
+
+
 def gdn_layer_prefill(mixed_qkv, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, cu_seqlens=None,
                       initial_state=None, conv_state=None, ckpt_every=0, scale=0.0,
-                      return_intermediates=False, stream=None):
+                      return_intermediates=False, stream=None, norm_eps=RMSNORM_EPS, out=None,
+                      final_state=None, conv_state_out=None, workspace=None, solve="direct"):
     """Whole layer core over packed sequences: conv1d+SiLU -> chunked delta rule
-    -> RMSNormGated.  Returns a dict with out [T, H_v*d_v], final_state
-    [n_seq, H_v, d_k, d_v] f32, conv_state [n_seq, conv_dim, 3] and, when
-    ckpt_every > 0, state_ckpt / conv_ckpt."""
+    -> RMSNormGated, as one gdn_layer_prefill call.  Returns a dict with out
+    [T, H_v*d_v], final_state [n_seq, H_v, d_k, d_v] f32, conv_state
+    [n_seq, conv_dim, 3] and, when ckpt_every > 0, state_ckpt / conv_ckpt.
+    return_intermediates=True runs the three calls one by one instead and adds
+    the conv output y and the rule's output o to the dict."""
+    if solve not in ("direct", "neumann"):
+        raise ValueError(f"solve must be 'direct' or 'neumann', not {solve!r}")
     dev, dt = mixed_qkv.device, mixed_qkv.dtype
+    T = int(mixed_qkv.shape[0])
     n_seq = _nseq(cu_seqlens)
     C = _conv_dim(dims)
     rows = 0
     if ckpt_every:
         host_cu = (cu_seqlens.to("cpu") if cu_seqlens is not None
-                   else torch.tensor([0, mixed_qkv.shape[0]], dtype=torch.int32))
+                   else torch.tensor([0, T], dtype=torch.int32))
         rows = gdn_ckpt_count(host_cu, ckpt_every)
-    conv_out = torch.empty((n_seq, C, 3), dtype=dt, device=dev)
+    if conv_state_out is None:
+        conv_state_out = torch.empty((n_seq, C, 3), dtype=dt, device=dev)
     conv_ck = torch.empty((rows, C, 3), dtype=dt, device=dev) if rows else None
-    y = gdn_conv1d_fwd(mixed_qkv, conv_w, dims, cu_seqlens, conv_state, conv_out, ckpt_every,
-                       conv_ck, True, stream=stream)
-    S = torch.empty((n_seq, dims.H_v, dims.d_k, dims.d_v), dtype=torch.float32, device=dev)
+    if final_state is None:
+        final_state = torch.empty((n_seq, dims.H_v, dims.d_k, dims.d_v), dtype=torch.float32, device=dev)
     S_ck = (torch.empty((rows, dims.H_v, dims.d_k, dims.d_v), dtype=torch.float32, device=dev)
             if rows else None)
-    o = gdn_chunk_prefill(y, dims, a, b, A_log, dt_bias, cu_seqlens=cu_seqlens,
-                          initial_state=initial_state, final_state=S, ckpt_every=ckpt_every,
-                          state_ckpt_out=S_ck, scale=scale, stream=stream)
-    out = gdn_rmsnorm_gated(o, z, norm_w, dims, stream=stream)
-    r = {"out": out, "final_state": S, "conv_state": conv_out, "state_ckpt": S_ck,
-         "conv_ckpt": conv_ck}
     if return_intermediates:
-        r.update({"y": y, "o": o})
-    return r
+        y = gdn_conv1d_fwd(mixed_qkv, conv_w, dims, cu_seqlens, conv_state, conv_state_out, ckpt_every,
+                           conv_ck, True, stream=stream)
+        o = gdn_chunk_prefill(y, dims, a, b, A_log, dt_bias, cu_seqlens=cu_seqlens,
+                              initial_state=initial_state, final_state=final_state, ckpt_every=ckpt_every,
+                              state_ckpt_out=S_ck, scale=scale, stream=stream, solve=solve)
+        out = gdn_rmsnorm_gated(o, z, norm_w, dims, eps=norm_eps, out=out, stream=stream)
+        return {"out": out, "final_state": final_state, "conv_state": conv_state_out, "state_ckpt": S_ck,
+                "conv_ckpt": conv_ck, "y": y, "o": o}
+    if out is None:
+        out = torch.empty((T, dims.H_v * dims.d_v), dtype=dt, device=dev)
+    lib = _lib.load()
+    if workspace is None:
+        need = lib.gdn_layer_prefill_workspace_size(n_seq, T, _dims(dims), _dtype_code(mixed_qkv))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.gdn_layer_prefill(
+        _ptr(mixed_qkv, "mixed_qkv", dt, (T, C)), _ptr(z, "z", dt), _ptr(a, "a", dt), _ptr(b, "b", dt),
+        _ptr(conv_w, "conv_w", dt, (C, 4)), _ptr(A_log, "A_log", torch.float32),
+        _ptr(dt_bias, "dt_bias", torch.float32), _ptr(norm_w, "norm_w", dt, (dims.d_v,)), float(norm_eps),
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32), n_seq, T,
+        _ptr(initial_state, "initial_state", torch.float32),
+        _ptr(final_state, "final_state", torch.float32, (n_seq, dims.H_v, dims.d_k, dims.d_v)),
+        _ptr(conv_state, "conv_state", dt), _ptr(conv_state_out, "conv_state_out", dt, (n_seq, C, 3)),
+        int(ckpt_every), _ptr(S_ck, "state_ckpt", torch.float32), _ptr(conv_ck, "conv_ckpt", dt), rows,
+        float(scale),
+        _lib.GDN_QK_L2NORM | (_lib.GDN_SOLVE_NEUMANN if solve == "neumann" else 0),
+        _ptr(out, "out", dt, (T, dims.H_v * dims.d_v)), _ptr(workspace, "workspace"), ws, _dims(dims),
+        _dtype_code(mixed_qkv), _stream(mixed_qkv, stream))
+    _lib.check(st, "gdn_layer_prefill")
+    return {"out": out, "final_state": final_state, "conv_state": conv_state_out, "state_ckpt": S_ck,
+            "conv_ckpt": conv_ck}
 
 
 def _hptr(t, name, dtype=None, shape=None):

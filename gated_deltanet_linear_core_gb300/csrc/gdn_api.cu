@@ -336,13 +336,17 @@ int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_
     return gdn::chunk_split_launches(n_seq, T_tot, dims.H_v, has_cu_seqlens != 0);
 }
 
-gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, const float* A_log,
-                               const float* dt_bias, const float* g, const float* beta,
-                               const int32_t* cu_seqlens, int32_t n_seq, int64_t T_tot,
-                               const float* initial_state, float* final_state, int32_t ckpt_every,
-                               float* state_ckpt_out, int64_t ckpt_rows, float scale,
-                               uint32_t flags, void* o, void* workspace, size_t ws_bytes,
-                               gdn_dims_t dims, gdn_dtype_t dtype, void* stream) {
+namespace {
+// gdn_chunk_prefill, and with norm_out set (== o) the same followed by
+// RMSNormGated(o, norm_z) in place over norm_out.
+gdn_status_t chunk_prefill_impl(const void* qkv, const void* a, const void* b, const float* A_log,
+                                const float* dt_bias, const float* g, const float* beta,
+                                const int32_t* cu_seqlens, int32_t n_seq, int64_t T_tot,
+                                const float* initial_state, float* final_state, int32_t ckpt_every,
+                                float* state_ckpt_out, int64_t ckpt_rows, float scale, uint32_t flags, void* o,
+                                void* workspace, size_t ws_bytes, gdn_dims_t dims, gdn_dtype_t dtype,
+                                void* stream, const void* norm_z, const void* norm_w, float norm_eps,
+                                void* norm_out) {
     gdn_status_t st = check_dims(dims, dtype);
     if (st != GDN_OK) return st;
     if ((st = check_seqs(cu_seqlens, n_seq, T_tot)) != GDN_OK) return st;
@@ -374,8 +378,86 @@ gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, co
     d.neumann = (flags & GDN_SOLVE_NEUMANN) != 0;
     d.o = o;
     cudaStream_t s = (cudaStream_t)stream;
-    if (need > 0) return cuda_status(gdn::launch_chunk_split(d, workspace, ws_bytes, s));
-    return cuda_status(gdn::launch_chunk_ffma(d, dtype, s));
+    cudaError_t e = need > 0 ? gdn::launch_chunk_split(d, workspace, ws_bytes, s) : gdn::launch_chunk_ffma(d, dtype, s);
+    if (e == cudaSuccess && norm_out != nullptr)
+        e = gdn::launch_rmsnorm_gated(o, norm_z, norm_w, norm_eps, T_tot, dims.H_v, dims.d_v, norm_out, dtype, s);
+    return cuda_status(e);
+}
+}  // namespace
+
+gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, const float* A_log,
+                               const float* dt_bias, const float* g, const float* beta,
+                               const int32_t* cu_seqlens, int32_t n_seq, int64_t T_tot,
+                               const float* initial_state, float* final_state, int32_t ckpt_every,
+                               float* state_ckpt_out, int64_t ckpt_rows, float scale,
+                               uint32_t flags, void* o, void* workspace, size_t ws_bytes,
+                               gdn_dims_t dims, gdn_dtype_t dtype, void* stream) {
+    return chunk_prefill_impl(qkv, a, b, A_log, dt_bias, g, beta, cu_seqlens, n_seq, T_tot, initial_state,
+                              final_state, ckpt_every, state_ckpt_out, ckpt_rows, scale, flags, o, workspace,
+                              ws_bytes, dims, dtype, stream, nullptr, nullptr, 0.f, nullptr);
+}
+
+gdn_status_t gdn_chunk_prefill_norm(const void* qkv, const void* a, const void* b, const float* A_log,
+                                    const float* dt_bias, const float* g, const float* beta,
+                                    const int32_t* cu_seqlens, int32_t n_seq, int64_t T_tot,
+                                    const float* initial_state, float* final_state, int32_t ckpt_every,
+                                    float* state_ckpt_out, int64_t ckpt_rows, float scale, uint32_t flags,
+                                    const void* z, const void* norm_w, float norm_eps, void* out,
+                                    void* workspace, size_t ws_bytes, gdn_dims_t dims, gdn_dtype_t dtype,
+                                    void* stream) {
+    if (!isfinite(norm_eps) || norm_eps <= 0.f || norm_w == nullptr) return GDN_ERR_INVALID_ARG;
+    if (T_tot > 0 && z == nullptr) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(z) || !aligned16(norm_w)) return GDN_ERR_ALIGN;
+    return chunk_prefill_impl(qkv, a, b, A_log, dt_bias, g, beta, cu_seqlens, n_seq, T_tot, initial_state,
+                              final_state, ckpt_every, state_ckpt_out, ckpt_rows, scale, flags, out, workspace,
+                              ws_bytes, dims, dtype, stream, z, norm_w, norm_eps, T_tot > 0 ? out : nullptr);
+}
+
+size_t gdn_layer_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t dims, gdn_dtype_t dtype) {
+    if (check_dims(dims, dtype) != GDN_OK || n_seq < 1 || T_tot <= 0 || T_tot > (int64_t)INT32_MAX) return 0;
+    const size_t y = ((size_t)T_tot * (size_t)conv_dim_of(dims) * elem_size(dtype) + 255) & ~(size_t)255;
+    return y + gdn_chunk_prefill_workspace_size(n_seq, T_tot, dims, dtype);
+}
+
+int32_t gdn_layer_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_seqlens, gdn_dims_t dims,
+                                   gdn_dtype_t dtype) {
+    if (check_dims(dims, dtype) != GDN_OK || n_seq < 1 || T_tot <= 0) return 0;
+    // the conv, the chunked rule, the norm
+    return 2 + gdn_chunk_prefill_launches(n_seq, T_tot, has_cu_seqlens, dims, dtype);
+}
+
+gdn_status_t gdn_layer_prefill(const void* x, const void* z, const void* a, const void* b, const void* conv_w,
+                               const float* A_log, const float* dt_bias, const void* norm_w, float norm_eps,
+                               const int32_t* cu_seqlens, int32_t n_seq, int64_t T_tot,
+                               const float* initial_state, float* final_state, const void* conv_state_in,
+                               void* conv_state_out, int32_t ckpt_every, float* state_ckpt_out,
+                               void* conv_ckpt_out, int64_t ckpt_rows, float scale, uint32_t flags, void* out,
+                               void* workspace, size_t ws_bytes, gdn_dims_t dims, gdn_dtype_t dtype,
+                               void* stream) {
+    gdn_status_t st = check_dims(dims, dtype);
+    if (st != GDN_OK) return st;
+    if ((st = check_seqs(cu_seqlens, n_seq, T_tot)) != GDN_OK) return st;
+    if ((st = check_ckpt(ckpt_every, state_ckpt_out, ckpt_rows)) != GDN_OK) return st;
+    if ((st = check_ckpt(ckpt_every, conv_ckpt_out, ckpt_rows)) != GDN_OK) return st;
+    if (!isfinite(norm_eps) || norm_eps <= 0.f) return GDN_ERR_INVALID_ARG;
+    if (conv_w == nullptr || norm_w == nullptr || A_log == nullptr || dt_bias == nullptr) return GDN_ERR_INVALID_ARG;
+    if (T_tot > 0 && (x == nullptr || z == nullptr || a == nullptr || b == nullptr || out == nullptr))
+        return GDN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(z) || !aligned16(norm_w) || !aligned16(out) || !aligned16(workspace))
+        return GDN_ERR_ALIGN;
+    const size_t need = gdn_layer_prefill_workspace_size(n_seq, T_tot, dims, dtype);
+    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return GDN_ERR_WORKSPACE;
+    const size_t ybytes = T_tot > 0 ? ((size_t)T_tot * (size_t)conv_dim_of(dims) * elem_size(dtype) + 255) &
+                                          ~(size_t)255
+                                    : 0;
+    void* y = T_tot > 0 ? workspace : nullptr;
+    void* cws = need > ybytes ? static_cast<uint8_t*>(workspace) + ybytes : nullptr;
+    st = gdn_conv1d_fwd(x, conv_w, cu_seqlens, n_seq, T_tot, conv_state_in, conv_state_out, ckpt_every,
+                        conv_ckpt_out, ckpt_rows, 1, y, dims, dtype, stream);
+    if (st != GDN_OK) return st;
+    return gdn_chunk_prefill_norm(y, a, b, A_log, dt_bias, nullptr, nullptr, cu_seqlens, n_seq, T_tot,
+                                  initial_state, final_state, ckpt_every, state_ckpt_out, ckpt_rows, scale, flags,
+                                  z, norm_w, norm_eps, out, cws, need - ybytes, dims, dtype, stream);
 }
 
 gdn_status_t gdn_chunk_prefill_noalloc(const void* qkv, const void* a, const void* b,

@@ -177,7 +177,8 @@ size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t
  * chain + RMSNormGated run on three internal streams of the library and
  * `stream`, starting after the work already queued on `stream` and joined back
  * to it.  The conv state and the recurrent state carry from piece to piece on
- * the device, so the result equals the three device calls bit for bit.
+ * the device, so the result equals gdn_layer_prefill's (and the three device
+ * calls') bit for bit.
  *   h_qkv      (host, page-locked) [T, conv_dim]    dtype
  *   h_z        (host, page-locked) [T, H_v*d_v]     dtype
  *   h_a, h_b   (host, page-locked) [T, H_v]         dtype
@@ -376,6 +377,67 @@ gdn_status_t gdn_decode_verify(const void* x, const void* conv_w, void* conv_sta
                                float norm_eps, const int32_t* slots, int32_t B, int32_t K,
                                float scale, uint32_t flags, void* out, gdn_dims_t dims,
                                gdn_dtype_t dtype, void* stream);
+
+/*
+ * gdn_chunk_prefill followed by RMSNormGated of its output (as
+ * gdn_rmsnorm_gated): out = RMSNormGated(o, z) with weight norm_w.  The rule
+ * writes o into `out` and the norm kernel normalises it in place, so no o
+ * buffer is needed.  Defined by the passages of the two calls (cortex
+ * GatedDeltaNet commit, "Output": RMSNormGated(core_attn_out, z)).
+ *   arguments before z: as gdn_chunk_prefill (workspace:
+ *               gdn_chunk_prefill_workspace_size bytes)
+ *   z          (device) [T_tot, H_v*d_v] dtype;  norm_w (device) [d_v] dtype
+ *   norm_eps   > 0 (the layer uses 1e-6)
+ *   out        (device) [T_tot, H_v*d_v] dtype
+ * Results equal gdn_chunk_prefill then gdn_rmsnorm_gated, bit for bit.
+ * Kernel launches: gdn_chunk_prefill_launches + 1.
+ */
+gdn_status_t gdn_chunk_prefill_norm(const void* qkv, const void* a, const void* b, const float* A_log,
+                                    const float* dt_bias, const float* g, const float* beta,
+                                    const int32_t* cu_seqlens, int32_t n_seq, int64_t T_tot,
+                                    const float* initial_state, float* final_state, int32_t ckpt_every,
+                                    float* state_ckpt_out, int64_t ckpt_rows, float scale, uint32_t flags,
+                                    const void* z, const void* norm_w, float norm_eps, void* out,
+                                    void* workspace, size_t ws_bytes, gdn_dims_t dims, gdn_dtype_t dtype,
+                                    void* stream);
+
+/*
+ * The layer core on device buffers in one call: conv1d + SiLU (as
+ * gdn_conv1d_fwd, with its state and checkpoint outputs), the chunked rule (as
+ * gdn_chunk_prefill) and RMSNormGated (as gdn_rmsnorm_gated), for packed
+ * sequences.  Defined by the passages of those three calls: cortex
+ * GatedDeltaNet commit, "Block" and "Output" (the order conv -> rule ->
+ * RMSNormGated(core_attn_out, z)); the fusion has no counterpart on the pages
+ * beyond the chunked kernel of the NxD-Inference Qwen3.6-27B PR, Summary.
+ * It is gdn_conv1d_fwd (into the workspace) followed by gdn_chunk_prefill_norm.
+ *   x          (device) [T_tot, conv_dim]   raw (pre-conv) mixed_qkv
+ *   z          (device) [T_tot, H_v*d_v];  a, b (device) [T_tot, H_v]    dtype
+ *   conv_w     (device) [conv_dim, 4];  norm_w (device) [d_v]            dtype
+ *   A_log, dt_bias (device) [H_v] f32;  norm_eps > 0 (the layer uses 1e-6)
+ *   cu_seqlens, n_seq, T_tot, initial_state, final_state  as gdn_chunk_prefill
+ *   conv_state_in, conv_state_out   as gdn_conv1d_fwd
+ *   ckpt_every  0 or a positive multiple of 64, for both checkpoint outputs:
+ *               state_ckpt_out [rows, H_v, d_k, d_v] f32 (as gdn_chunk_prefill) and
+ *               conv_ckpt_out [rows, conv_dim, 3] dtype (as gdn_conv1d_fwd);
+ *               ckpt_rows rows allocated in each
+ *   scale, flags  as gdn_chunk_prefill (GDN_QK_L2NORM, optionally | GDN_SOLVE_NEUMANN)
+ *   out        (device) [T_tot, H_v*d_v]   dtype
+ *   workspace  (device) >= gdn_layer_prefill_workspace_size bytes (it holds the
+ *              conv output and the chunk intermediates), 16-byte aligned
+ * Results equal those of the three separate calls bit for bit.  Kernel
+ * launches: gdn_layer_prefill_launches.
+ */
+size_t gdn_layer_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t dims, gdn_dtype_t dtype);
+int32_t gdn_layer_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_seqlens, gdn_dims_t dims,
+                                   gdn_dtype_t dtype);
+gdn_status_t gdn_layer_prefill(const void* x, const void* z, const void* a, const void* b, const void* conv_w,
+                               const float* A_log, const float* dt_bias, const void* norm_w, float norm_eps,
+                               const int32_t* cu_seqlens, int32_t n_seq, int64_t T_tot,
+                               const float* initial_state, float* final_state, const void* conv_state_in,
+                               void* conv_state_out, int32_t ckpt_every, float* state_ckpt_out,
+                               void* conv_ckpt_out, int64_t ckpt_rows, float scale, uint32_t flags, void* out,
+                               void* workspace, size_t ws_bytes, gdn_dims_t dims, gdn_dtype_t dtype,
+                               void* stream);
 
 /*
  * RMSNormGated over each value head.

@@ -181,6 +181,61 @@ def test_decode_update_norm_validation(lib):
     assert norm(z=A + 0x1008) == E.GDN_ERR_ALIGN
 
 
+def layer(lib, **kw):
+    """gdn_layer_prefill with fake device addresses (never dereferenced)."""
+    args = dict(x=A, z=A + 0x1000, a=A + 0x2000, b=A + 0x3000, w=A + 0x4000, A_log=A + 0x5000,
+                dt_bias=A + 0x6000, nw=A + 0x7000, eps=1e-6, cu=None, n_seq=1, T=64, S0=None,
+                Sf=A + 0x10000, cs_in=None, cs_out=A + 0x20000, every=0, sck=None, cck=None, rows=0,
+                scale=0.0, flags=1, out=A + 0x30000, ws=None, ws_bytes=0, dims=DIMS, dt=_lib.GDN_BF16)
+    args.update(kw)
+    return lib.gdn_layer_prefill(
+        args["x"], args["z"], args["a"], args["b"], args["w"], args["A_log"], args["dt_bias"], args["nw"],
+        args["eps"], args["cu"], args["n_seq"], args["T"], args["S0"], args["Sf"], args["cs_in"],
+        args["cs_out"], args["every"], args["sck"], args["cck"], args["rows"], args["scale"], args["flags"],
+        args["out"], args["ws"], args["ws_bytes"], args["dims"], args["dt"], None)
+
+
+@no_gpu
+def test_layer_prefill_validation(lib):
+    E = _lib
+    # everything valid but the workspace: that is what is reported
+    assert layer(lib) == E.GDN_ERR_WORKSPACE
+    need = lib.gdn_layer_prefill_workspace_size(1, 64, DIMS, _lib.GDN_BF16)
+    assert layer(lib, ws_bytes=need) == E.GDN_ERR_WORKSPACE        # NULL workspace
+    assert layer(lib, ws=A + 0x100000, ws_bytes=need - 1) == E.GDN_ERR_WORKSPACE
+    assert layer(lib, eps=0.0) == E.GDN_ERR_INVALID_ARG
+    assert layer(lib, eps=float("nan")) == E.GDN_ERR_INVALID_ARG
+    assert layer(lib, z=None) == E.GDN_ERR_INVALID_ARG
+    assert layer(lib, out=None) == E.GDN_ERR_INVALID_ARG
+    assert layer(lib, nw=None) == E.GDN_ERR_INVALID_ARG
+    assert layer(lib, z=A + 0x1008) == E.GDN_ERR_ALIGN
+    assert layer(lib, out=A + 0x30002) == E.GDN_ERR_ALIGN
+    assert layer(lib, ws=A + 0x100008, ws_bytes=need) == E.GDN_ERR_ALIGN
+    assert layer(lib, every=64, sck=A + 0x40000, cck=None, rows=1) == E.GDN_ERR_INVALID_ARG
+    assert layer(lib, every=64, sck=None, cck=A + 0x50000, rows=1) == E.GDN_ERR_INVALID_ARG
+    assert layer(lib, every=100, sck=A + 0x40000, cck=A + 0x50000, rows=1) == E.GDN_ERR_INVALID_ARG
+    assert layer(lib, n_seq=2) == E.GDN_ERR_INVALID_ARG             # two sequences need cu_seqlens
+    assert layer(lib, T=-1) == E.GDN_ERR_INVALID_ARG
+    assert layer(lib, dims=_lib.Dims(16, 48, 128, 128, 3)) == E.GDN_ERR_UNSUPPORTED
+
+
+def test_layer_prefill_workspace_and_launches(lib):
+    dims = gdn.GDNDims(16, 48, 128, 128)
+    C = dims.conv_dim
+    # the conv output (rounded up to 256 bytes), then the chunk intermediates
+    y = (4096 * C * 2 + 255) // 256 * 256
+    assert gdn.gdn_layer_prefill_workspace_size(1, 4096, dims, torch.bfloat16) == \
+        y + gdn.gdn_chunk_prefill_workspace_size(1, 4096, dims, torch.bfloat16)
+    assert gdn.gdn_layer_prefill_workspace_size(1, 100, dims, torch.float32) == (100 * C * 4 + 255) // 256 * 256
+    assert gdn.gdn_layer_prefill_workspace_size(1, 0, dims, torch.bfloat16) == 0
+    # conv, the chunk kernels, the norm
+    for cu in (True, None):
+        assert gdn.gdn_layer_prefill_launches(1, 4096, dims, torch.bfloat16, cu_seqlens=cu) == \
+            2 + gdn.gdn_chunk_prefill_launches(1, 4096, dims, torch.bfloat16, cu_seqlens=cu)
+    assert gdn.gdn_layer_prefill_launches(1, 64, gdn.GDNDims(2, 4, 16, 16), torch.float32) == 3
+    assert gdn.gdn_layer_prefill_launches(1, 0, dims, torch.bfloat16) == 0
+
+
 def test_workspace_size(lib):
     dims = gdn.GDNDims(16, 32, 128, 128)
     # the CUDA-core (f32) path needs none; the bf16 tensor-core path holds per-chunk

@@ -1,0 +1,154 @@
+"""GPU parity of the one-call entry points: gdn_layer_prefill (conv, chunked
+rule, RMSNormGated; its scratch in one workspace) and gdn_chunk_prefill_norm
+(the rule's output normalised in place in `out`).
+
+Against the three separate calls on the same inputs: every output bit for bit
+(the same kernels on the same values).  Against the f64 oracle: the dtype's
+tolerance.  The cases reach both chain forms of the tensor-core path -- a head
+split into two 64-column CTAs (few sequences) and one CTA per head (more
+(sequence, head) pairs than SMs) -- ragged tails, empty and 1..3-token
+sequences, checkpoints, the Neumann-style solve and the CUDA-core path.
+"""
+import pytest
+import torch
+
+import gated_deltanet_linear_core_gb300 as gdn
+import oracle
+import workloads as W
+from gpu_util import TOL, assert_close, host
+
+pytestmark = pytest.mark.gpu
+
+SHAPE_27B = W.GDNShape(H_k=16, H_v=48, d_k=128, d_v=128)
+SMALL_128 = W.GDNShape(H_k=2, H_v=6, d_k=128, d_v=128)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def _dims(s):
+    return gdn.GDNDims(s.H_k, s.H_v, s.d_k, s.d_v)
+
+
+def _run(inp, shape, one_call, ckpt_every=0, solve="direct"):
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    r = gdn.gdn_layer_prefill(d["mixed_qkv"], d["z"], d["a"], d["b"], d["conv_w"], d["A_log"], d["dt_bias"],
+                              d["norm_w"], _dims(shape), cu_seqlens=d["cu_seqlens"], initial_state=d["S0"],
+                              conv_state=d["conv_state0"], ckpt_every=ckpt_every,
+                              return_intermediates=not one_call, solve=solve)
+    torch.cuda.synchronize()
+    gdn.gdn_sync_status()
+    return r
+
+
+def _compare_with_separate(fz, sp):
+    for k in ("out", "final_state", "conv_state", "state_ckpt", "conv_ckpt"):
+        if sp[k] is None:
+            assert fz[k] is None, k
+        else:
+            assert torch.equal(fz[k], sp[k]), f"{k} differs from the separate calls"
+    assert torch.isfinite(fz["out"].float()).all()
+
+
+def _oracle(inp, shape, ckpt_every=0):
+    f = W.to_f64
+    return oracle.layer_prefill(f(inp["mixed_qkv"]), f(inp["z"]), f(inp["a"]), f(inp["b"]), f(inp["conv_w"]),
+                                f(inp["A_log"]), f(inp["dt_bias"]), f(inp["norm_w"]), shape.H_k, shape.H_v,
+                                shape.d_k, shape.d_v, cu_seqlens=inp["cu_seqlens"].numpy(),
+                                S0=None if inp["S0"] is None else f(inp["S0"]),
+                                conv_state0=None if inp["conv_state0"] is None else f(inp["conv_state0"]),
+                                ckpt_every=ckpt_every)
+
+
+def test_one_sequence_27b_heads_ragged_tail():
+    # 48 value heads x 2 column slices = 96 chain CTAs; 1000 tokens: 15 full
+    # chunks and a 40-token tail stored row by row
+    inp = W.layer_inputs(SHAPE_27B, torch.bfloat16, [1000], seed=31, init_state=True)
+    fz = _run(inp, SHAPE_27B, one_call=True, ckpt_every=256)
+    sp = _run(inp, SHAPE_27B, one_call=False, ckpt_every=256)
+    _compare_with_separate(fz, sp)
+    ref = _oracle(inp, SHAPE_27B, ckpt_every=256)
+    tol = TOL[torch.bfloat16]
+    assert_close("out", host(fz["out"]), ref["out"], tol)
+    assert_close("out per head", host(fz["out"]).reshape(-1, SHAPE_27B.H_v, SHAPE_27B.d_v),
+                 ref["out"].reshape(-1, SHAPE_27B.H_v, SHAPE_27B.d_v), tol, per_head_axis=1)
+    assert_close("S", host(fz["final_state"]), ref["S"], tol, per_head_axis=1)
+
+
+def test_many_sequences_one_cta_per_head():
+    # 4 x 48 x 2 > 152 SMs: one chain CTA per (sequence, head); sequences
+    # shorter than a chunk, exactly one chunk, and with a ragged tail
+    lengths = [70, 1, 300, 64]
+    inp = W.layer_inputs(SHAPE_27B, torch.bfloat16, lengths, seed=32, init_state=True)
+    fz = _run(inp, SHAPE_27B, one_call=True, ckpt_every=64)
+    sp = _run(inp, SHAPE_27B, one_call=False, ckpt_every=64)
+    _compare_with_separate(fz, sp)
+    ref = _oracle(inp, SHAPE_27B, ckpt_every=64)
+    tol = TOL[torch.bfloat16]
+    assert_close("out", host(fz["out"]), ref["out"], tol)
+    assert_close("S", host(fz["final_state"]), ref["S"], tol, per_head_axis=1)
+    assert_close("S ckpt", host(fz["state_ckpt"]), ref["S_ckpt"], tol)
+
+
+@pytest.mark.parametrize("lengths", [[1, 63, 64, 65, 0, 200, 3], [130, 70]], ids=["edge", "two"])
+def test_small_heads_varlen(lengths):
+    # few (sequence, head) pairs: every head split into two chain CTAs; empty
+    # sequences and sequences of 1..3 tokens
+    inp = W.layer_inputs(SMALL_128, torch.bfloat16, lengths, seed=33, init_state=True)
+    fz = _run(inp, SMALL_128, one_call=True)
+    sp = _run(inp, SMALL_128, one_call=False)
+    _compare_with_separate(fz, sp)
+    ref = _oracle(inp, SMALL_128)
+    assert_close("out", host(fz["out"]), ref["out"], TOL[torch.bfloat16])
+
+
+def test_neumann_solve_in_the_layer_call():
+    inp = W.layer_inputs(SMALL_128, torch.bfloat16, [257], seed=34, init_state=False)
+    fz = _run(inp, SMALL_128, one_call=True, solve="neumann")
+    sp = _run(inp, SMALL_128, one_call=False, solve="neumann")
+    _compare_with_separate(fz, sp)
+
+
+@pytest.mark.parametrize("shape", [W.TINY, SMALL_128], ids=["d16", "d128"])
+def test_cuda_core_path_f32(shape):
+    # f32: conv, the CUDA-core rule and the norm kernel in turn
+    inp = W.layer_inputs(shape, torch.float32, [65, 3, 128], seed=35, init_state=True)
+    fz = _run(inp, shape, one_call=True)
+    sp = _run(inp, shape, one_call=False)
+    _compare_with_separate(fz, sp)
+    ref = _oracle(inp, shape)
+    assert_close("out", host(fz["out"]), ref["out"], TOL[torch.float32])
+
+
+def test_empty_call_passes_the_states_through():
+    inp = W.layer_inputs(SMALL_128, torch.bfloat16, [0, 0], seed=36, init_state=True)
+    fz = _run(inp, SMALL_128, one_call=True)
+    assert fz["out"].numel() == 0
+    assert torch.equal(fz["final_state"].cpu(), inp["S0"])
+    assert torch.equal(fz["conv_state"].cpu(), inp["conv_state0"])
+
+
+def test_chunk_prefill_norm_one_sequence_without_offsets():
+    # the form the layer call uses for one sequence: no cu_seqlens, no offsets kernel
+    inp = W.layer_inputs(SHAPE_27B, torch.bfloat16, [1100], seed=37, init_state=True)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    dims = _dims(SHAPE_27B)
+    y = gdn.gdn_conv1d_fwd(d["mixed_qkv"], d["conv_w"], dims, None, d["conv_state0"], None)
+    S1 = torch.empty_like(d["S0"])
+    S2 = torch.empty_like(d["S0"])
+    out = gdn.gdn_chunk_prefill_norm(y, d["z"], d["norm_w"], dims, d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                     initial_state=d["S0"], final_state=S1)
+    o = gdn.gdn_chunk_prefill(y, dims, d["a"], d["b"], d["A_log"], d["dt_bias"], initial_state=d["S0"],
+                              final_state=S2)
+    ref = gdn.gdn_rmsnorm_gated(o, d["z"], d["norm_w"], dims)
+    torch.cuda.synchronize()
+    gdn.gdn_sync_status()
+    assert torch.equal(S1, S2)
+    _compare_with_separate({"out": out, "final_state": S1, "conv_state": None, "state_ckpt": None,
+                            "conv_ckpt": None},
+                           {"out": ref, "final_state": S2, "conv_state": None, "state_ckpt": None,
+                            "conv_ckpt": None})
