@@ -45,6 +45,12 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 FLOP_PER_TOKEN_HEAD = 5 * 64 * 128 + 6 * 128 * 128  # 139,264 (chunked delta rule, C=64, d=128)
 
 
+def chunk_bytes_per_token(s: W.GDNShape) -> int:
+    """Algorithmic bytes of the chunk stage per token (bf16): post-conv q, k, v
+    and the gate inputs a, b read, o written."""
+    return 2 * (s.conv_dim + 2 * s.H_v + s.H_v * s.d_v)
+
+
 def decode_kernel_bytes_per_seq(s: W.GDNShape) -> int:
     """Algorithmic bytes of the recurrent-decode kernel per sequence-step: read
     and write each f32 state once, read q/k/v (bf16) and a, b, write o."""
@@ -77,8 +83,9 @@ def peaks():
         with open(p) as f:
             d = json.load(f)
         return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
                 "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
 def traffic_record(kernel: str):
@@ -317,11 +324,22 @@ def run_ours(args):
     flops = FLOP_PER_TOKEN_HEAD * T * s.H_v
     achieved_tf = flops / chunk_avg / 1e12
     ncu_bytes = traffic_record("chunk_prefill")
+    # the chunk stage's intensity is below the ridge, so HBM co-binds: the
+    # tensor fraction it could reach at full bandwidth is min(1, BW * I / peak)
+    cbytes = chunk_bytes_per_token(s) * T
+    intensity = flops / cbytes
     roofline = {"kernel": "gdn_chunk_prefill", "bound": "tensor", "achieved": round(achieved_tf, 2),
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved_tf / pk["bf16_tflops"], 4),
                 "peak_source": pk["source"] + " (bf16 burst)",
-                "traffic": ncu_bytes, "algorithmic_flop_per_launch": flops}
+                "frac_of_sustained": round(achieved_tf / pk["bf16_tflops_sustained"], 4),
+                "traffic": ncu_bytes, "algorithmic_flop_per_launch": flops,
+                "hbm": {"algorithmic_bytes_per_launch": cbytes,
+                        "algorithmic_gbs": round(cbytes / chunk_avg / 1e9, 1),
+                        "frac": round(cbytes / chunk_avg / 1e9 / pk["hbm_gbs"], 4),
+                        "dram_gbs": None if ncu_bytes is None else round(ncu_bytes / chunk_avg / 1e9, 1),
+                        "dram_frac": None if ncu_bytes is None else round(ncu_bytes / chunk_avg / 1e9 / pk["hbm_gbs"], 4)},
+                "ceiling_frac": round(min(1.0, pk["hbm_gbs"] * 1e9 * intensity / (pk["bf16_tflops"] * 1e12)), 4)}
 
     # ---- decode (64 sequences x one token per step)
     wd = W.WORKLOADS[DECODE]
@@ -628,8 +646,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
