@@ -321,6 +321,32 @@ def run_ours(args):
     neumann_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in nev)
     chunk_solve = {"direct_ms": round(chunk_avg * 1e3, 4), "neumann_ms": round(neumann_ms, 4),
                    "call": "gdn_chunk_prefill, flags GDN_QK_L2NORM vs | GDN_SOLVE_NEUMANN"}
+
+    # chunk-size sweep on the CUDA-core path (f32 arithmetic; the tensor-core
+    # kernels are built around C = 64): the same workload in f32
+    yf = y.float()
+    af, bf_ = d["a"].float(), d["b"].float()
+    of = torch.empty((T, s.H_v, s.d_v), dtype=torch.float32, device=dev)
+    sweep = {}
+    for c in (16, 32, 64):
+        def ffma_chunk():
+            gdn.gdn_chunk_prefill(yf, dims, af, bf_, d["A_log"], d["dt_bias"], final_state=S, o=of, chunk=c)
+        ffma_chunk()
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+        torch.cuda.synchronize(dev)
+        for k in range(3):
+            flush.zero_()
+            cev[k][0].record(stream)
+            ffma_chunk()
+            cev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        launches += 4
+        ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in cev)
+        sweep[str(c)] = {"ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1)}
+    del yf, af, bf_, of
+    chunk_sweep = {"path": "CUDA-core (f32 FFMA), f32 copies of the workload", "by_chunk": sweep,
+                   "tensor_core_c64_ms": round(chunk_avg * 1e3, 4),
+                   "call": "gdn_chunk_prefill, flags | GDN_CHUNK(c)"}
     flops = FLOP_PER_TOKEN_HEAD * T * s.H_v
     achieved_tf = flops / chunk_avg / 1e12
     ncu_bytes = traffic_record("chunk_prefill")
@@ -556,6 +582,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "call": "gdn_layer_prefill (conv1d_fwd, chunk_prefill, rmsnorm_gated kernels)",
             "chunk_solve": chunk_solve,
+            "chunk_sweep": chunk_sweep,
             "per_kernel_ms": {"conv1d_fwd": round(statistics.mean(conv_ms), 4),
                               "chunk_prefill": round(statistics.mean(chunk_ms), 4),
                               "rmsnorm_gated": round(statistics.mean(norm_ms), 4)},

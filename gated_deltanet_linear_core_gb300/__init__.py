@@ -18,7 +18,7 @@ from dataclasses import dataclass
 import torch
 
 from . import _lib
-from ._lib import GDNError, GDN_QK_L2NORM, GDN_SOLVE_NEUMANN  # noqa: F401
+from ._lib import GDNError, GDN_QK_L2NORM, GDN_SOLVE_NEUMANN, GDN_CHUNK  # noqa: F401
 
 __all__ = [
     "GDNDims", "GDNError", "gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
@@ -179,6 +179,13 @@ def gdn_chunk_prefill_launches(n_seq: int, T_tot: int, dims, dtype, cu_seqlens=T
     return int(_lib.load().gdn_chunk_prefill_launches(int(n_seq), int(T_tot), has_cu, _dims(dims), code))
 
 
+def _flags(l2norm_qk, solve, chunk) -> int:
+    if solve not in ("direct", "neumann"):
+        raise ValueError(f"solve must be 'direct' or 'neumann', not {solve!r}")
+    return ((_lib.GDN_QK_L2NORM if l2norm_qk else 0) | (_lib.GDN_SOLVE_NEUMANN if solve == "neumann" else 0) |
+            (0 if chunk == 64 else _lib.GDN_CHUNK(chunk)))
+
+
 def _gate_ptrs(a, b, A_log, dt_bias, g, beta, dt):
     return (_ptr(a, "a", dt), _ptr(b, "b", dt), _ptr(A_log, "A_log", torch.float32),
             _ptr(dt_bias, "dt_bias", torch.float32), _ptr(g, "g", torch.float32),
@@ -188,11 +195,12 @@ def _gate_ptrs(a, b, A_log, dt_bias, g, beta, dt):
 def gdn_chunk_prefill(qkv, dims, a=None, b=None, A_log=None, dt_bias=None, g=None, beta=None,
                       cu_seqlens=None, initial_state=None, final_state=None, ckpt_every=0,
                       state_ckpt_out=None, scale=0.0, l2norm_qk=True, o=None, workspace=None,
-                      stream=None, solve="direct"):
+                      stream=None, solve="direct", chunk=64):
     """Chunked gated delta rule over packed sequences.  qkv [T, conv_dim]
     (post-conv); states [n_seq, H_v, d_k, d_v] f32; returns o [T, H_v, d_v].
     solve="neumann" forms each chunk's (I + A)^-1 as the Neumann-style product
-    (GDN_SOLVE_NEUMANN; tensor-core path only)."""
+    (GDN_SOLVE_NEUMANN; tensor-core path only).  chunk: 16, 32 or 64 tokens
+    (GDN_CHUNK; the tensor-core path takes 64 only)."""
     if solve not in ("direct", "neumann"):
         raise ValueError(f"solve must be 'direct' or 'neumann', not {solve!r}")
     dt = qkv.dtype
@@ -213,8 +221,7 @@ def gdn_chunk_prefill(qkv, dims, a=None, b=None, A_log=None, dt_bias=None, g=Non
         _ptr(initial_state, "initial_state", torch.float32),
         _ptr(final_state, "final_state", torch.float32), int(ckpt_every),
         _ptr(state_ckpt_out, "state_ckpt_out", torch.float32), rows, float(scale),
-        (_lib.GDN_QK_L2NORM if l2norm_qk else 0) | (_lib.GDN_SOLVE_NEUMANN if solve == "neumann" else 0),
-        _ptr(o, "o", dt), _ptr(workspace, "workspace"),
+        _flags(l2norm_qk, solve, chunk), _ptr(o, "o", dt), _ptr(workspace, "workspace"),
         ws, _dims(dims), _dtype_code(qkv), _stream(qkv, stream))
     _lib.check(st, "gdn_chunk_prefill")
     return o
@@ -223,7 +230,7 @@ def gdn_chunk_prefill(qkv, dims, a=None, b=None, A_log=None, dt_bias=None, g=Non
 def gdn_chunk_prefill_norm(qkv, z, norm_w, dims, a=None, b=None, A_log=None, dt_bias=None, g=None,
                            beta=None, cu_seqlens=None, initial_state=None, final_state=None, ckpt_every=0,
                            state_ckpt_out=None, scale=0.0, l2norm_qk=True, norm_eps=RMSNORM_EPS, out=None,
-                           workspace=None, stream=None, solve="direct"):
+                           workspace=None, stream=None, solve="direct", chunk=64):
     """gdn_chunk_prefill followed by RMSNormGated(o, z): returns out [T, H_v*d_v]
     (the rule's output is normalised in place in `out`)."""
     if solve not in ("direct", "neumann"):
@@ -245,8 +252,7 @@ def gdn_chunk_prefill_norm(qkv, z, norm_w, dims, a=None, b=None, A_log=None, dt_
         _ptr(initial_state, "initial_state", torch.float32),
         _ptr(final_state, "final_state", torch.float32), int(ckpt_every),
         _ptr(state_ckpt_out, "state_ckpt_out", torch.float32), rows, float(scale),
-        (_lib.GDN_QK_L2NORM if l2norm_qk else 0) | (_lib.GDN_SOLVE_NEUMANN if solve == "neumann" else 0),
-        _ptr(z, "z", dt, (T, dims.H_v * dims.d_v)), _ptr(norm_w, "norm_w", dt, (dims.d_v,)), float(norm_eps),
+        _flags(l2norm_qk, solve, chunk), _ptr(z, "z", dt, (T, dims.H_v * dims.d_v)), _ptr(norm_w, "norm_w", dt, (dims.d_v,)), float(norm_eps),
         _ptr(out, "out", dt, (T, dims.H_v * dims.d_v)), _ptr(workspace, "workspace"), ws, _dims(dims),
         _dtype_code(qkv), _stream(qkv, stream))
     _lib.check(st, "gdn_chunk_prefill_norm")
@@ -325,7 +331,7 @@ def gdn_layer_prefill_launches(n_seq: int, T_tot: int, dims, dtype, cu_seqlens=T
 def gdn_layer_prefill(mixed_qkv, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, cu_seqlens=None,
                       initial_state=None, conv_state=None, ckpt_every=0, scale=0.0,
                       return_intermediates=False, stream=None, norm_eps=RMSNORM_EPS, out=None,
-                      final_state=None, conv_state_out=None, workspace=None, solve="direct"):
+                      final_state=None, conv_state_out=None, workspace=None, solve="direct", chunk=64):
     """Whole layer core over packed sequences: conv1d+SiLU -> chunked delta rule
     -> RMSNormGated, as one gdn_layer_prefill call.  Returns a dict with out
     [T, H_v*d_v], final_state [n_seq, H_v, d_k, d_v] f32, conv_state
@@ -355,7 +361,7 @@ def gdn_layer_prefill(mixed_qkv, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, 
                            conv_ck, True, stream=stream)
         o = gdn_chunk_prefill(y, dims, a, b, A_log, dt_bias, cu_seqlens=cu_seqlens,
                               initial_state=initial_state, final_state=final_state, ckpt_every=ckpt_every,
-                              state_ckpt_out=S_ck, scale=scale, stream=stream, solve=solve)
+                              state_ckpt_out=S_ck, scale=scale, stream=stream, solve=solve, chunk=chunk)
         out = gdn_rmsnorm_gated(o, z, norm_w, dims, eps=norm_eps, out=out, stream=stream)
         return {"out": out, "final_state": final_state, "conv_state": conv_state_out, "state_ckpt": S_ck,
                 "conv_ckpt": conv_ck, "y": y, "o": o}
@@ -377,7 +383,7 @@ def gdn_layer_prefill(mixed_qkv, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, 
         _ptr(conv_state, "conv_state", dt), _ptr(conv_state_out, "conv_state_out", dt, (n_seq, C, 3)),
         int(ckpt_every), _ptr(S_ck, "state_ckpt", torch.float32), _ptr(conv_ck, "conv_ckpt", dt), rows,
         float(scale),
-        _lib.GDN_QK_L2NORM | (_lib.GDN_SOLVE_NEUMANN if solve == "neumann" else 0),
+        _flags(True, solve, chunk),
         _ptr(out, "out", dt, (T, dims.H_v * dims.d_v)), _ptr(workspace, "workspace"), ws, _dims(dims),
         _dtype_code(mixed_qkv), _stream(mixed_qkv, stream))
     _lib.check(st, "gdn_layer_prefill")

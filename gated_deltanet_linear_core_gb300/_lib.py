@@ -24,6 +24,11 @@ GDN_QK_L2NORM = 1
 GDN_SOLVE_NEUMANN = 2
 
 
+def GDN_CHUNK(c: int) -> int:
+    """The chunk-size field of the prefill flags (bits 8..15)."""
+    return (int(c) & 0xFF) << 8
+
+
 class Dims(ctypes.Structure):
     _fields_ = [("H_k", ctypes.c_int32), ("H_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("conv_k", ctypes.c_int32)]

@@ -148,18 +148,22 @@ __global__ void __launch_bounds__(kNT) chunk_ffma_kernel(DeltaArgs a) {
             }
         }
         if (warp == kNT / 32 - 1) {
-            // inclusive scan of g over the chunk (C <= 64: two values per lane)
+            // inclusive scan of g over the chunk, 32 values per pass (lanes past
+            // C, when C = 16, carry zeros and write nothing)
             float run = 0.f;
             for (int base = 0; base < C; base += 32) {
-                float v = Gs[base + lane];
+                const bool in = base + lane < C;
+                float v = in ? Gs[base + lane] : 0.f;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float u = __shfl_up_sync(0xffffffffu, v, o);
                     if (lane >= o) v += u;
                 }
                 v += run;
-                Gs[base + lane] = v;
-                EGs[base + lane] = expf(v);
+                if (in) {
+                    Gs[base + lane] = v;
+                    EGs[base + lane] = expf(v);
+                }
                 run = __shfl_sync(0xffffffffu, v, 31);
             }
             __syncwarp();
@@ -263,9 +267,8 @@ __global__ void __launch_bounds__(kNT) chunk_ffma_kernel(DeltaArgs a) {
     }
 }
 
-template <typename T, int D, int BV>
-cudaError_t launch_t(const DeltaArgs& a, cudaStream_t s) {
-    constexpr int C = 64;
+template <typename T, int D, int BV, int C>
+cudaError_t launch_tc(const DeltaArgs& a, cudaStream_t s) {
     using L = FfmaSmem<D, BV, C>;
     auto kern = chunk_ffma_kernel<T, D, BV, C>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -275,6 +278,15 @@ cudaError_t launch_t(const DeltaArgs& a, cudaStream_t s) {
     if (grid == 0) return cudaSuccess;
     kern<<<grid, kNT, L::bytes, s>>>(a);
     return cudaGetLastError();
+}
+
+// chunk size a.chunk (16, 32 or 64; 0 means 64)
+template <typename T, int D, int BV>
+cudaError_t launch_t(const DeltaArgs& a, cudaStream_t s) {
+    if (a.chunk == 16) return launch_tc<T, D, BV, 16>(a, s);
+    if (a.chunk == 32) return launch_tc<T, D, BV, 32>(a, s);
+    if (a.chunk == 0 || a.chunk == 64) return launch_tc<T, D, BV, 64>(a, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace

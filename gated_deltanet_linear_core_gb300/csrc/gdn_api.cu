@@ -352,8 +352,12 @@ gdn_status_t chunk_prefill_impl(const void* qkv, const void* a, const void* b, c
     if ((st = check_seqs(cu_seqlens, n_seq, T_tot)) != GDN_OK) return st;
     if ((st = check_ckpt(ckpt_every, state_ckpt_out, ckpt_rows)) != GDN_OK) return st;
     if (T_tot > 0 && (st = check_gates(a, b, A_log, dt_bias, g, beta, dtype)) != GDN_OK) return st;
-    if (flags & ~(GDN_QK_L2NORM | GDN_SOLVE_NEUMANN)) return GDN_ERR_INVALID_ARG;
-    if ((flags & GDN_SOLVE_NEUMANN) && !(dtype == GDN_BF16 && dims.d_k == 128)) return GDN_ERR_UNSUPPORTED;
+    if (flags & ~(GDN_QK_L2NORM | GDN_SOLVE_NEUMANN | GDN_CHUNK(0xff))) return GDN_ERR_INVALID_ARG;
+    const int chunk = ((flags >> 8) & 0xffu) == 0 ? 64 : (int)((flags >> 8) & 0xffu);
+    if (chunk != 16 && chunk != 32 && chunk != 64) return GDN_ERR_INVALID_ARG;
+    const bool tensor_core = dtype == GDN_BF16 && dims.d_k == 128;
+    if ((flags & GDN_SOLVE_NEUMANN) && !tensor_core) return GDN_ERR_UNSUPPORTED;
+    if (chunk != 64 && tensor_core) return GDN_ERR_UNSUPPORTED;
     if (!isfinite(scale)) return GDN_ERR_INVALID_ARG;
     if (T_tot > 0 && (qkv == nullptr || o == nullptr)) return GDN_ERR_INVALID_ARG;
     if (!aligned16(qkv) || !aligned16(o) || !aligned16(initial_state) || !aligned16(final_state) ||
@@ -376,6 +380,7 @@ gdn_status_t chunk_prefill_impl(const void* qkv, const void* a, const void* b, c
     d.scale = scale == 0.f ? 1.0f / sqrtf((float)dims.d_k) : scale;
     d.l2norm = (flags & GDN_QK_L2NORM) != 0;
     d.neumann = (flags & GDN_SOLVE_NEUMANN) != 0;
+    d.chunk = chunk;
     d.o = o;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = need > 0 ? gdn::launch_chunk_split(d, workspace, ws_bytes, s) : gdn::launch_chunk_ffma(d, dtype, s);

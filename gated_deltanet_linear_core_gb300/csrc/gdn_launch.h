@@ -52,6 +52,7 @@ struct DeltaArgs {
     int l2norm;
     void* o;  // [T, H_v, D]
     int neumann;  // chunk inverse by the Neumann-style product (tensor-core path)
+    int chunk;    // chunk size of the CUDA-core path: 16, 32 or 64 (0: 64)
 };
 // Chunked prefill on CUDA cores (f32 arithmetic; any supported D and dtype).
 cudaError_t launch_chunk_ffma(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s);

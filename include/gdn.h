@@ -76,6 +76,16 @@ typedef struct {
  * inverse is far from the identity (slow decay, correlated keys); shipped to
  * compare the two.  Other paths: GDN_ERR_UNSUPPORTED. */
 #define GDN_SOLVE_NEUMANN 2u
+/* gdn_chunk_prefill (and the calls built on it): the chunk size C, in flag
+ * bits 8..15 -- GDN_CHUNK(16), GDN_CHUNK(32) or GDN_CHUNK(64); the field left
+ * at 0 means 64.  Any C gives the per-token rule's result up to rounding
+ * (cortex GatedDeltaNet commit, "Performance note": chunk_size=64 is one
+ * choice of the chunked algorithm); it trades per-chunk matrix work (which
+ * grows with C) against the number of sequential chunk steps.  The CUDA-core
+ * path takes all three; the tensor-core path (bf16, d = 128) is built around
+ * C = 64 and returns GDN_ERR_UNSUPPORTED for the others.  Other values:
+ * GDN_ERR_INVALID_ARG. */
+#define GDN_CHUNK(c) ((((uint32_t)(c)) & 0xffu) << 8)
 
 /* Text for a status code (static storage, never NULL). */
 const char* gdn_status_string(gdn_status_t status);
@@ -251,7 +261,7 @@ int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_
  *               [gdn_ckpt_count rows, H_v, d_k, d_v] f32: state after m*ckpt_every tokens
  *   ckpt_rows   rows allocated in state_ckpt_out; rows past it are never written
  *   scale       query scale; 0 means d_k^-1/2
- *   flags       GDN_QK_L2NORM, optionally | GDN_SOLVE_NEUMANN, or 0
+ *   flags       GDN_QK_L2NORM, optionally | GDN_SOLVE_NEUMANN | GDN_CHUNK(c), or 0
  *   o          (device) [T_tot, H_v, d_v]   (dtype)
  *   workspace  (device) >= gdn_chunk_prefill_workspace_size bytes, or NULL if that is 0
  */

@@ -139,6 +139,14 @@ def test_chunk_prefill_validation(lib):
     neu = E.GDN_QK_L2NORM | E.GDN_SOLVE_NEUMANN
     assert chunk(lib, flags=neu) == E.GDN_ERR_WORKSPACE
     assert chunk(lib, flags=neu, dt=E.GDN_F32, a=A + 0x1000, b=A + 0x2000) == E.GDN_ERR_UNSUPPORTED
+    # the chunk-size field (bits 8..15): 16, 32, 64 or 0; the tensor-core path takes 64 only
+    assert chunk(lib, flags=1 | E.GDN_CHUNK(48)) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, flags=1 | E.GDN_CHUNK(128)) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, flags=1 | E.GDN_CHUNK(8)) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, flags=1 | (1 << 16)) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, flags=1 | E.GDN_CHUNK(16)) == E.GDN_ERR_UNSUPPORTED
+    assert chunk(lib, flags=1 | E.GDN_CHUNK(32)) == E.GDN_ERR_UNSUPPORTED
+    assert chunk(lib, flags=1 | E.GDN_CHUNK(64)) == E.GDN_ERR_WORKSPACE  # valid; no workspace given
     assert chunk(lib, scale=float("nan")) == E.GDN_ERR_INVALID_ARG
     assert chunk(lib, scale=float("inf")) == E.GDN_ERR_INVALID_ARG
     assert chunk(lib, o=None) == E.GDN_ERR_INVALID_ARG

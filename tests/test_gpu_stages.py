@@ -168,6 +168,40 @@ def test_chunk_prefill_varlen_states_ckpts(dtype, shape):
     assert torch.equal(Sf[z].cpu(), inp["S0"][z])
 
 
+@pytest.mark.parametrize("chunk", [16, 32])
+@pytest.mark.parametrize("dtype,shape", [(torch.float32, W.TINY), (torch.bfloat16, W.TINY),
+                                         (torch.float32, SMALL_128)], ids=["f32-d16", "bf16-d16", "f32-d128"])
+def test_chunk_prefill_chunk_sizes(chunk, dtype, shape):
+    """The CUDA-core path at chunk sizes 16 and 32 (GDN_CHUNK): the same rule,
+    so the same oracle and tolerance as C = 64, over sequences of 0..200 tokens
+    (not multiples of the chunk), with checkpoints every 64 tokens."""
+    inp = _delta_inputs(shape, dtype, LENGTHS, seed=16)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    N = len(LENGTHS)
+    rows = gdn.gdn_ckpt_count(inp["cu_seqlens"], 64)
+    ck = torch.full((rows, shape.H_v, shape.d_k, shape.d_v), float("nan"), device="cuda")
+    Sf = torch.full((N, shape.H_v, shape.d_k, shape.d_v), float("nan"), device="cuda")
+    o = gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(shape), d["a"], d["b"], d["A_log"], d["dt_bias"],
+                              cu_seqlens=d["cu_seqlens"], initial_state=d["S0"], final_state=Sf, ckpt_every=64,
+                              state_ckpt_out=ck, chunk=chunk)
+    torch.cuda.synchronize()
+    o_ref, S_ref, ck_ref = _oracle_delta(inp, shape, ckpt_every=64)
+    tol = TOL[dtype]
+    assert_close("o", host(o), o_ref, tol, per_head_axis=1)
+    assert_close("S_final", host(Sf), S_ref, tol, per_head_axis=1)
+    assert_close("ckpt", host(ck), ck_ref, tol)
+    z = LENGTHS.index(0)
+    assert torch.equal(Sf[z].cpu(), inp["S0"][z])
+
+
+def test_chunk_size_other_than_64_is_refused_on_the_tensor_core_path():
+    inp = _delta_inputs(SMALL_128, torch.bfloat16, [70], seed=17)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    with pytest.raises(gdn.GDNError):
+        gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(SMALL_128), d["a"], d["b"], d["A_log"], d["dt_bias"],
+                              cu_seqlens=d["cu_seqlens"], chunk=32)
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("keys", ["random", "correlated"])
 def test_chunk_prefill_slow_decay(dtype, keys):
