@@ -47,7 +47,9 @@ gdn_status_t check_ckpt(int32_t every, const void* ckpt, int64_t rows) {
     if (every < 0) return GDN_ERR_INVALID_ARG;
     if (every > 0) {
         if (every % 64 != 0) return GDN_ERR_INVALID_ARG;
-        if (ckpt == nullptr || rows < 0) return GDN_ERR_INVALID_ARG;
+        // a buffer is needed only when rows are allocated (a call whose sequences are
+        // all shorter than the cadence has none)
+        if (rows < 0 || (ckpt == nullptr && rows > 0)) return GDN_ERR_INVALID_ARG;
     }
     return GDN_OK;
 }

@@ -142,7 +142,8 @@ gdn_status_t gdn_sync_status(void* stream);
  *   ckpt_every     0 (off) or a positive multiple of 64: conv_ckpt_out row r holds the
  *                  conv state after m*ckpt_every tokens of a sequence, m = 1..floor(L/N),
  *                  rows in sequence order (gdn_ckpt_count rows), [rows, conv_dim, 3]
- *   ckpt_rows      rows allocated in conv_ckpt_out; rows past it are never written
+ *   ckpt_rows      rows allocated in conv_ckpt_out; rows past it are never written;
+ *                  with 0 rows conv_ckpt_out may be NULL
  *   apply_silu     nonzero: y = silu(conv)
  *   y          (device) [T_tot, conv_dim]  (must not alias x)
  * Arithmetic: f32 accumulation; y is rounded once to `dtype`.
@@ -259,7 +260,8 @@ int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_
  *   final_state   (device) [n_seq, H_v, d_k, d_v] f32 or NULL; may alias initial_state
  *   ckpt_every  0 or a positive multiple of 64; state_ckpt_out (device)
  *               [gdn_ckpt_count rows, H_v, d_k, d_v] f32: state after m*ckpt_every tokens
- *   ckpt_rows   rows allocated in state_ckpt_out; rows past it are never written
+ *   ckpt_rows   rows allocated in state_ckpt_out; rows past it are never written;
+ *               with 0 rows state_ckpt_out may be NULL
  *   scale       query scale; 0 means d_k^-1/2
  *   flags       GDN_QK_L2NORM, optionally | GDN_SOLVE_NEUMANN | GDN_CHUNK(c), or 0
  *   o          (device) [T_tot, H_v, d_v]   (dtype)
@@ -429,7 +431,7 @@ gdn_status_t gdn_chunk_prefill_norm(const void* qkv, const void* a, const void* 
  *   ckpt_every  0 or a positive multiple of 64, for both checkpoint outputs:
  *               state_ckpt_out [rows, H_v, d_k, d_v] f32 (as gdn_chunk_prefill) and
  *               conv_ckpt_out [rows, conv_dim, 3] dtype (as gdn_conv1d_fwd);
- *               ckpt_rows rows allocated in each
+ *               ckpt_rows rows allocated in each (with 0, both may be NULL)
  *   scale, flags  as gdn_chunk_prefill (GDN_QK_L2NORM, optionally | GDN_SOLVE_NEUMANN)
  *   out        (device) [T_tot, H_v*d_v]   dtype
  *   workspace  (device) >= gdn_layer_prefill_workspace_size bytes (it holds the

@@ -154,7 +154,10 @@ def test_chunk_prefill_validation(lib):
     assert chunk(lib, S0=A + 0x6008) == E.GDN_ERR_ALIGN
     assert chunk(lib, Sf=A + 0x6004) == E.GDN_ERR_ALIGN
     assert chunk(lib, every=4000, ck=A + 0x7000, rows=1) == E.GDN_ERR_INVALID_ARG
-    assert chunk(lib, every=4096, ck=None) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, every=4096, ck=None, rows=1) == E.GDN_ERR_INVALID_ARG
+    assert chunk(lib, every=4096, ck=None, rows=-1) == E.GDN_ERR_INVALID_ARG
+    # no rows allocated (every sequence shorter than the cadence): no buffer needed
+    assert chunk(lib, every=4096, ck=None, rows=0) == E.GDN_ERR_WORKSPACE
     assert chunk(lib, dims=_lib.Dims(16, 48, 128, 64, 4)) == E.GDN_ERR_UNSUPPORTED
     assert chunk(lib, dims=_lib.Dims(16, 48, 32, 32, 4)) == E.GDN_ERR_UNSUPPORTED
 

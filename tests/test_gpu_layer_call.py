@@ -152,3 +152,33 @@ def test_chunk_prefill_norm_one_sequence_without_offsets():
                             "conv_ckpt": None},
                            {"out": ref, "final_state": S2, "conv_state": None, "state_ckpt": None,
                             "conv_ckpt": None})
+
+
+@pytest.mark.parametrize("dtype,shape", [(torch.bfloat16, SMALL_128), (torch.float32, SMALL_128),
+                                         (torch.float32, W.TINY)], ids=["bf16-tensor-core", "f32-d128", "f32-d16"])
+def test_packed_sequences_equal_separate_calls(dtype, shape):
+    """A packed (cu_seqlens) call equals one call per sequence, bit for bit:
+    rows past a sequence's last token (the next sequence's tokens when packed,
+    zeros when alone) enter only through factors that are exactly zero."""
+    lengths = [70, 1, 200, 64]
+    every = 64
+    inp = W.layer_inputs(shape, dtype, lengths, seed=38, init_state=True)
+    packed = _run(inp, shape, one_call=True, ckpt_every=every)
+    cu = inp["cu_seqlens"].tolist()
+    row = 0
+    for i, L in enumerate(lengths):
+        one = {k: inp[k][cu[i]:cu[i + 1]] for k in ("mixed_qkv", "z", "a", "b")}
+        for k in ("conv_w", "A_log", "dt_bias", "norm_w"):
+            one[k] = inp[k]
+        one["cu_seqlens"] = W.cu_seqlens_of([L])
+        one["S0"] = inp["S0"][i:i + 1]
+        one["conv_state0"] = inp["conv_state0"][i:i + 1]
+        r = _run(one, shape, one_call=True, ckpt_every=every)
+        assert torch.equal(r["out"], packed["out"][cu[i]:cu[i + 1]]), f"out of sequence {i}"
+        assert torch.equal(r["final_state"][0], packed["final_state"][i]), f"state of sequence {i}"
+        assert torch.equal(r["conv_state"][0], packed["conv_state"][i]), f"conv state of sequence {i}"
+        n_ck = L // every
+        if n_ck:
+            assert torch.equal(r["state_ckpt"], packed["state_ckpt"][row:row + n_ck]), f"ckpts of sequence {i}"
+            assert torch.equal(r["conv_ckpt"], packed["conv_ckpt"][row:row + n_ck]), f"conv ckpts of sequence {i}"
+        row += n_ck
