@@ -26,6 +26,7 @@ __all__ = [
     "gdn_ckpt_count", "gdn_check_cu_seqlens", "gdn_sync_status", "gdn_selftest_bounded_wait",
     "gdn_layer_prefill_host", "gdn_decode_step", "gdn_decode_verify", "gdn_layer_prefill",
     "gdn_layer_prefill_workspace_size", "gdn_layer_prefill_launches", "gdn_chunk_prefill_norm",
+    "HeadShard", "head_shard",
     "gdn_layer_decode",
     "library_path",
 ]
@@ -514,3 +515,37 @@ def gdn_layer_decode(x, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, state, co
     y = gdn_conv1d_update(x, conv_w, conv_state, dims, True, stream=stream)
     o = gdn_recurrent_decode(y, state, dims, a, b, A_log, dt_bias, scale=scale, stream=stream)
     return gdn_rmsnorm_gated(o, z, norm_w, dims, stream=stream)
+
+
+@dataclass(frozen=True)
+class HeadShard:
+    """One rank's part of the layer core under head sharding: key heads
+    [kh0, kh1), their value heads [h0, h1), and the matching conv channels
+    (its q, k and v slices of conv_dim, in that order)."""
+    dims: GDNDims
+    kh0: int
+    kh1: int
+    h0: int
+    h1: int
+    channels: torch.Tensor  # int64 [conv_dim of the shard], indices into the full conv_dim
+
+
+def head_shard(dims, rank: int, world: int) -> HeadShard:
+    """Head sharding of the layer core over `world` ranks: rank takes a contiguous
+    block of H_k / world key heads with their H_v / H_k value heads each.  Heads,
+    their conv channels and their states are independent through the whole core,
+    so every rank calls the same entry points with `shard.dims` on its slices
+    (q, k, v channels, z and out columns, a, b, A_log and dt_bias entries, state
+    heads) and no exchange is needed inside the core; the pages' tensor-parallel
+    runs split the layer this way, with the one all-reduce after out_proj.
+    world must divide H_k."""
+    if world < 1 or rank < 0 or rank >= world or dims.H_k % world != 0:
+        raise ValueError(f"head_shard: world {world} must divide H_k {dims.H_k} (rank {rank})")
+    r = dims.H_v // dims.H_k
+    nk = dims.H_k // world
+    kh0, kh1 = rank * nk, (rank + 1) * nk
+    h0, h1 = kh0 * r, kh1 * r
+    dk, dv = dims.d_k, dims.d_v
+    ch = torch.cat([torch.arange(kh0 * dk, kh1 * dk), torch.arange(dims.H_k * dk + kh0 * dk, dims.H_k * dk + kh1 * dk),
+                    torch.arange(2 * dims.H_k * dk + h0 * dv, 2 * dims.H_k * dk + h1 * dv)])
+    return HeadShard(GDNDims(nk, h1 - h0, dk, dv, dims.conv_k), kh0, kh1, h0, h1, ch)

@@ -182,3 +182,30 @@ def test_packed_sequences_equal_separate_calls(dtype, shape):
             assert torch.equal(r["state_ckpt"], packed["state_ckpt"][row:row + n_ck]), f"ckpts of sequence {i}"
             assert torch.equal(r["conv_ckpt"], packed["conv_ckpt"][row:row + n_ck]), f"conv ckpts of sequence {i}"
         row += n_ck
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_head_shards_equal_the_full_call(world):
+    """Head sharding (tensor parallel over key heads): each shard's call on its
+    slices equals the full call's slice bit for bit; no exchange inside the
+    core.  The shards run one after another on this GPU."""
+    s = SHAPE_27B
+    inp = W.layer_inputs(s, torch.bfloat16, [600, 400], seed=39, init_state=True)
+    full = _run(inp, s, one_call=True, ckpt_every=256)
+    for r in range(world):
+        sh = gdn.head_shard(_dims(s), r, world)
+        zc = slice(sh.h0 * s.d_v, sh.h1 * s.d_v)
+        part_in = {"mixed_qkv": inp["mixed_qkv"][:, sh.channels].contiguous(), "z": inp["z"][:, zc].contiguous(),
+                   "a": inp["a"][:, sh.h0:sh.h1].contiguous(), "b": inp["b"][:, sh.h0:sh.h1].contiguous(),
+                   "conv_w": inp["conv_w"][sh.channels].contiguous(), "A_log": inp["A_log"][sh.h0:sh.h1].contiguous(),
+                   "dt_bias": inp["dt_bias"][sh.h0:sh.h1].contiguous(), "norm_w": inp["norm_w"],
+                   "cu_seqlens": inp["cu_seqlens"], "S0": inp["S0"][:, sh.h0:sh.h1].contiguous(),
+                   "conv_state0": inp["conv_state0"][:, sh.channels].contiguous()}
+        shape = W.GDNShape(sh.dims.H_k, sh.dims.H_v, s.d_k, s.d_v)
+        part = _run(part_in, shape, one_call=True, ckpt_every=256)
+        ch = sh.channels.cuda()
+        assert torch.equal(part["out"], full["out"][:, zc]), f"out of shard {r}"
+        assert torch.equal(part["final_state"], full["final_state"][:, sh.h0:sh.h1]), f"state of shard {r}"
+        assert torch.equal(part["state_ckpt"], full["state_ckpt"][:, sh.h0:sh.h1]), f"ckpts of shard {r}"
+        assert torch.equal(part["conv_state"], full["conv_state"][:, ch]), f"conv state of shard {r}"
+        assert torch.equal(part["conv_ckpt"], full["conv_ckpt"][:, ch]), f"conv ckpts of shard {r}"
