@@ -9,6 +9,7 @@ split into two 64-column CTAs (few sequences) and one CTA per head (more
 (sequence, head) pairs than SMs) -- ragged tails, empty and 1..3-token
 sequences, checkpoints, the Neumann-style solve and the CUDA-core path.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -209,3 +210,36 @@ def test_head_shards_equal_the_full_call(world):
         assert torch.equal(part["state_ckpt"], full["state_ckpt"][:, sh.h0:sh.h1]), f"ckpts of shard {r}"
         assert torch.equal(part["conv_state"], full["conv_state"][:, ch]), f"conv state of shard {r}"
         assert torch.equal(part["conv_ckpt"], full["conv_ckpt"][:, ch]), f"conv ckpts of shard {r}"
+
+
+@pytest.mark.parametrize("H_k,H_v", [(4, 4), (2, 4), (1, 8)], ids=["r1", "r2", "r8"])
+def test_head_ratios_prefill_then_fused_decode(H_k, H_v):
+    """Value heads per key head r = 1, 2 and 8 (the fused decode CTA's
+    largest): the layer prefill on the tensor-core path against the oracle,
+    then two fused decode steps from the prefill's own states against the
+    oracle started from those same states (so the decode kernel is measured
+    alone, not the bf16 prefill's state error carried into it)."""
+    s = W.GDNShape(H_k=H_k, H_v=H_v, d_k=128, d_v=128)
+    lengths = [130, 70]
+    inp = W.layer_inputs(s, torch.bfloat16, lengths, seed=43, init_state=True)
+    r = _run(inp, s, one_call=True)
+    ref = _oracle(inp, s)
+    tol = TOL[torch.bfloat16]
+    assert_close("out", host(r["out"]), ref["out"], tol)
+    assert_close("S", host(r["final_state"]), ref["S"], tol, per_head_axis=1)
+    f = W.to_f64
+    dec = W.decode_inputs(s, torch.bfloat16, len(lengths), 2, seed=44)
+    S, cs = r["final_state"].clone(), r["conv_state"].clone()
+    S_ref, cs_ref = host(r["final_state"]), host(r["conv_state"])
+    dev = {k: v.cuda() for k, v in dec.items()}
+    p = {k: inp[k].cuda() for k in ("conv_w", "A_log", "dt_bias", "norm_w")}
+    for t in range(2):
+        out = gdn.gdn_decode_step(dev["qkv"][t], dev["z"][t], dev["a"][t], dev["b"][t], p["conv_w"], p["A_log"],
+                                  p["dt_bias"], p["norm_w"], _dims(s), S, cs)
+        torch.cuda.synchronize()
+        out_ref, S_ref, cs_ref, _ = oracle.layer_decode_step(
+            f(dec["qkv"][t]), f(dec["z"][t]), f(dec["a"][t]), f(dec["b"][t]), f(inp["conv_w"]), f(inp["A_log"]),
+            f(inp["dt_bias"]), f(inp["norm_w"]), s.H_k, s.H_v, s.d_k, s.d_v, S_ref, cs_ref)
+        assert_close(f"decode out, step {t}", host(out), out_ref, tol)
+    assert_close("decode S", host(S), S_ref, tol, per_head_axis=1)
+    assert np.array_equal(host(cs), cs_ref)
