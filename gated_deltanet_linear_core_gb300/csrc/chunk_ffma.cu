@@ -20,7 +20,9 @@
 // overflows; a decay that underflows is a true zero.
 //
 // One CTA per (sequence, value head, BV-column block of the state); columns of
-// the state evolve independently, so the blocks need no communication.
+// the state evolve independently, so the blocks need no communication.  The
+// chunk size C is 16, 32 or 64 (the caller's choice; any C gives the same
+// rule up to rounding).
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
 

@@ -5,7 +5,8 @@
 // per-token)", computed with the chunked algorithm (chunk_size=64) its
 // "Performance note" names; NxD-Inference PR "Add Qwen3.6-27B hybrid
 // DeltaNet/GQA contrib model and vLLM serving path": chunked context encoding,
-// recurrent-state checkpoints, and the direct (not Neumann-style) solve.
+// recurrent-state checkpoints, and its "Known limitations": the direct solve,
+// with the Neumann-style product as the alternative (GDN_SOLVE_NEUMANN).
 //
 // Of the per-chunk work only two products depend on the state S carried from
 // chunk to chunk.  With G the chunk-local cumulative decay, rq / rk the
