@@ -381,6 +381,14 @@ decode_verify_kernel(DecodeVerifyArgs a) {
         for (int p = 0; p < PASSES; ++p)
             s[p] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(r0 + p * RPP) * D) + cq);
     };
+    // a value head's state into L2 ahead of its register loads (which wait for
+    // the registers: the conv's window first, then the previous head)
+    auto prefetch_state = [&](int j) {
+        const char* S = reinterpret_cast<const char*>(a.state + (s_in * a.H_v + kh * r + j) * D * D);
+        for (int off = tid * 128; off < D * D * 4; off += NT * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(S + off));
+    };
+    prefetch_state(0);
 
     // 1. conv over the K tokens: q, k, then the r heads' v, one 16-byte vector
     //    of channels per thread; the window slides over [state | x_0 .. x_{K-1}]
@@ -461,6 +469,7 @@ decode_verify_kernel(DecodeVerifyArgs a) {
     for (int j = 0; j < r; ++j) {
         const int h = kh * r + j;
         if (j > 0) load_state(j);
+        if (j + 1 < r) prefetch_state(j + 1);
         for (int t = 0; t < K; ++t) {
             const float rq = nrm[3 * t], rk = nrm[3 * t + 1], kq = nrm[3 * t + 2];
             const float* kt = ks + t * D;
