@@ -156,8 +156,8 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
     cudaStream_t cin, cout, pre;
     cudaError_t e = copy_streams(&cin, &cout, &pre);
     if (e != cudaSuccess) return e;
-    constexpr int NEV = 4 * kSlots + 1;
-    cudaEvent_t ev[NEV];  // in, comp, out, pre per slot; start
+    constexpr int NEV = 5 * kSlots + 1;
+    cudaEvent_t ev[NEV];  // in (qkv), in (z), comp, out, pre per slot; start
     int made = 0;
     for (; made < NEV && e == cudaSuccess; ++made)
         e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
@@ -165,7 +165,8 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
     cudaEvent_t* ev_comp = ev + kSlots;
     cudaEvent_t* ev_out = ev + 2 * kSlots;
     cudaEvent_t* ev_pre = ev + 3 * kSlots;
-    cudaEvent_t ev_start = ev[4 * kSlots];
+    cudaEvent_t* ev_inz = ev + 4 * kSlots;
+    cudaEvent_t ev_start = ev[5 * kSlots];
     // the other streams start after whatever the caller queued on `s`
     if (e == cudaSuccess) e = cudaEventRecord(ev_start, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cin, ev_start, 0);
@@ -187,12 +188,15 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
         // inputs of piece p, once piece p - kSlots (same slot) has finished with the
         // slot's buffers and chunk workspace
         if (p >= kSlots) e = cudaStreamWaitEvent(cin, ev_comp[sl], 0);
+        // qkv first, on its own event: the conv and the chunk kernels need only it,
+        // and only the norm waits for z
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(ws + q.qkv, hq + (size_t)t0 * C * es, (size_t)tp * C * es, cudaMemcpyHostToDevice, cin);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_in[sl], cin);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(ws + q.z, static_cast<const uint8_t*>(h.h_z) + (size_t)t0 * O * es,
                                 (size_t)tp * O * es, cudaMemcpyHostToDevice, cin);
-        if (e == cudaSuccess) e = cudaEventRecord(ev_in[sl], cin);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_inz[sl], cin);
         // conv and the chunk-local kernels on the pre stream once the inputs are in
         if (e == cudaSuccess) e = cudaStreamWaitEvent(pre, ev_in[sl], 0);
         if (e == cudaSuccess) {
@@ -227,6 +231,7 @@ cudaError_t launch_layer_prefill_host(const HostLayerArgs& h, gdn_dtype_t dt, vo
                 }
             }
         }
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_inz[sl], 0);
         if (e == cudaSuccess)
             e = launch_rmsnorm_gated(ws + q.o, ws + q.z, h.norm_w, h.eps, tp, h.H_v, h.D, ws + q.out, dt, s);
         if (e == cudaSuccess) e = cudaEventRecord(ev_comp[sl], s);
