@@ -366,7 +366,8 @@ decode_verify_kernel(DecodeVerifyArgs a) {
     float* qs = vsm;                  // [K][D]
     float* ks = qs + K * D;           // [K][D]
     float* vs = ks + K * D;           // [K][r][D]
-    float* ds = vs + K * r * D;       // [D]
+    float* zs = vs + K * r * D;       // [K][r][D]: the gate input z
+    float* ds = zs + K * r * D;       // [D]
     float* os = ds + D;               // [D]
     float* red = os + D;              // [2][RPP][D]
     float* gb = red + 2 * RPP * D;    // [K][r][2]: g, beta
@@ -434,6 +435,16 @@ decode_verify_kernel(DecodeVerifyArgs a) {
             const int64_t gi = ((int64_t)b * K + t) * a.H_v + h;
             gb[2 * e] = gate_g(to_f(static_cast<const T*>(a.a)[gi]), a.A_log[h], a.dt_bias[h]);
             gb[2 * e + 1] = sigmoid_f(to_f(static_cast<const T*>(a.b)[gi]));
+        }
+        // z of the CTA's r heads for the K tokens (contiguous r * D per token),
+        // staged once so that the K * r norm epilogues do not wait on DRAM
+        const T* zg = static_cast<const T*>(a.z) + ((int64_t)b * K * a.H_v + kh * r) * D;
+        for (int e = tid; e < K * r * D / V; e += NT) {
+            const int t = (e * V) / (r * D), o = e * V - t * r * D;
+            float zv[V];
+            load16(zg + (int64_t)t * a.H_v * D + o, zv);
+#pragma unroll
+            for (int q = 0; q < V; ++q) zs[t * r * D + o + q] = zv[q];
         }
     }
     __syncthreads();
@@ -527,11 +538,11 @@ decode_verify_kernel(DecodeVerifyArgs a) {
             for (int ww = 0; ww < NW; ++ww) tot += wsum[ww];
             const float rs = rsqrtf(tot / (float)D + a.eps);
             const int64_t row = ((int64_t)b * K + t) * a.H_v + h;
-            const T* z = static_cast<const T*>(a.z) + row * D;
+            const float* z = zs + (t * r + j) * D;
             T* out = static_cast<T*>(a.out) + row * D;
             const T* nw = static_cast<const T*>(a.norm_w);
             for (int c = 2 * tid; c < D; c += 2 * NT) {
-                const float2 g = silu2<T>(make_float2(to_f(z[c]), to_f(z[c + 1])));
+                const float2 g = silu2<T>(make_float2(z[c], z[c + 1]));
                 const float2 res = __fmul2_rn(__fmul2_rn(make_float2(to_f(nw[c]), to_f(nw[c + 1])),
                                                          __fmul2_rn(make_float2(os[c], os[c + 1]), make_float2(rs, rs))),
                                               g);
@@ -546,7 +557,7 @@ decode_verify_kernel(DecodeVerifyArgs a) {
 template <int D, int NW>
 size_t verify_smem_bytes(int K, int r) {
     constexpr int RPP = NW * 32 / (D / 4);
-    return sizeof(float) * ((size_t)2 * K * D + (size_t)K * r * D + 2 * D + 2 * RPP * D + 2 * K * r + 3 * K + NW);
+    return sizeof(float) * ((size_t)2 * K * D + (size_t)2 * K * r * D + 2 * D + 2 * RPP * D + 2 * K * r + 3 * K + NW);
 }
 
 template <typename T>
