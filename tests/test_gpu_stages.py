@@ -502,7 +502,10 @@ def test_fused_decode_step_with_slots(dtype, shape):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("shape", [W.TINY, SMALL_128], ids=["d16", "d128"])
+# r = 8 value heads per key head with K = 16 is the largest shared-memory request
+# of the verification kernel (158 KB)
+@pytest.mark.parametrize("shape", [W.TINY, SMALL_128, W.GDNShape(H_k=1, H_v=8, d_k=128, d_v=128)],
+                         ids=["d16", "d128", "d128r8"])
 @pytest.mark.parametrize("K", [1, 4, 16])
 def test_decode_verify_equals_successive_fused_steps(dtype, shape, K):
     """gdn_decode_verify (K draft tokens per sequence in one kernel, states read
