@@ -192,6 +192,48 @@ def test_decode_update_norm_validation(lib):
     assert norm(z=A + 0x1008) == E.GDN_ERR_ALIGN
 
 
+def _fused_decode(lib, verify, **kw):
+    """gdn_decode_step / gdn_decode_verify with fake device addresses."""
+    g = kw.get
+    head = [g("x", A), g("w", A + 0x1000), g("cs", A + 0x2000), g("z", A + 0x3000), g("a", A + 0x4000),
+            g("b", A + 0x5000), g("A_log", A + 0x6000), g("dt_bias", A + 0x7000), g("state", A + 0x10000),
+            g("nw", A + 0x8000), g("eps", 1e-6), g("slots", A + 0x9000), g("B", 4)]
+    tail = [g("scale", 0.0), g("flags", 1), g("out", A + 0x20000), g("dims", DIMS), _lib.GDN_BF16, None]
+    if verify:
+        return lib.gdn_decode_verify(*head, g("K", 4), *tail)
+    return lib.gdn_decode_step(*head, *tail)
+
+
+@no_gpu
+@pytest.mark.parametrize("verify", [False, True], ids=["decode_step", "decode_verify"])
+def test_fused_decode_validation(lib, verify):
+    E = _lib
+    call = lambda **kw: _fused_decode(lib, verify, **kw)
+    assert call(B=-1) == E.GDN_ERR_INVALID_ARG
+    assert call(dims=_lib.Dims(16, 40, 128, 128, 4)) == E.GDN_ERR_INVALID_ARG  # H_v % H_k != 0
+    assert call(dims=_lib.Dims(2, 32, 128, 128, 4)) == E.GDN_ERR_UNSUPPORTED   # 16 value heads per key head
+    assert call(dims=_lib.Dims(16, 48, 64, 64, 4)) == E.GDN_ERR_UNSUPPORTED
+    assert call(flags=2) == E.GDN_ERR_INVALID_ARG                               # only GDN_QK_L2NORM
+    assert call(eps=0.0) == E.GDN_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == E.GDN_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == E.GDN_ERR_INVALID_ARG
+    for name in ("x", "w", "cs", "z", "a", "b", "A_log", "dt_bias", "state", "nw", "out"):
+        assert call(**{name: None}) == E.GDN_ERR_INVALID_ARG, name
+    assert call(z=A + 0x3008) == E.GDN_ERR_ALIGN
+    assert call(state=A + 0x10008) == E.GDN_ERR_ALIGN
+    assert call(a=A + 0x4001) == E.GDN_ERR_ALIGN                                # bf16 gate input
+    assert call(slots=A + 0x9002) == E.GDN_ERR_ALIGN
+    assert call(out=A + 0x20004) == E.GDN_ERR_ALIGN
+    # no work: nothing is read, so no buffer is needed, and nothing is launched
+    nulls = dict.fromkeys(("x", "w", "cs", "z", "a", "b", "A_log", "dt_bias", "state", "nw", "slots", "out"))
+    assert call(B=0, **nulls) == E.GDN_OK
+    if verify:
+        assert call(K=-1) == E.GDN_ERR_INVALID_ARG
+        assert call(K=17) == E.GDN_ERR_INVALID_ARG                              # at most 16 draft tokens
+        assert call(slots=None) == E.GDN_ERR_INVALID_ARG                        # slots are required
+        assert call(K=0, **nulls) == E.GDN_OK
+
+
 def layer(lib, **kw):
     """gdn_layer_prefill with fake device addresses (never dereferenced)."""
     args = dict(x=A, z=A + 0x1000, a=A + 0x2000, b=A + 0x3000, w=A + 0x4000, A_log=A + 0x5000,
