@@ -168,7 +168,7 @@ gdn_status_t gdn_layer_prefill_host(const void* h_qkv, const void* h_z, const vo
     if (st != GDN_OK) return st;
     if (T < 0 || T > (int64_t)INT32_MAX) return GDN_ERR_INVALID_ARG;
     if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
-    if (!isfinite(scale) || !isfinite(norm_eps) || norm_eps < 0.f) return GDN_ERR_INVALID_ARG;
+    if (!isfinite(scale) || !isfinite(norm_eps) || norm_eps <= 0.f) return GDN_ERR_INVALID_ARG;
     if (conv_w == nullptr || A_log == nullptr || dt_bias == nullptr || norm_w == nullptr ||
         final_state == nullptr || conv_state_out == nullptr)
         return GDN_ERR_INVALID_ARG;

@@ -199,7 +199,7 @@ size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t
  *   final_state    (device) [1, H_v, d_k, d_v] f32, required; may alias initial_state
  *   conv_state_in  (device) [1, conv_dim, 3] dtype, or NULL (zeros)
  *   conv_state_out (device) [1, conv_dim, 3] dtype, required; may alias conv_state_in
- *   scale      0 -> d_k^-1/2;  flags: GDN_QK_L2NORM;  norm_eps: RMSNormGated epsilon
+ *   scale      0 -> d_k^-1/2;  flags: GDN_QK_L2NORM;  norm_eps > 0 (the layer uses 1e-6)
  *   h_out      (host, page-locked) [T, H_v*d_v] dtype
  *   workspace  (device) >= gdn_layer_prefill_host_workspace_size(T, dims, dtype) bytes
  * Host buffers that are not page-locked: GDN_ERR_INVALID_ARG.  No checkpoints.

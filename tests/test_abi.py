@@ -272,6 +272,36 @@ def test_layer_prefill_validation(lib):
     assert layer(lib, dims=_lib.Dims(16, 48, 128, 128, 3)) == E.GDN_ERR_UNSUPPORTED
 
 
+def host_layer(lib, **kw):
+    """gdn_layer_prefill_host with fake addresses (never dereferenced): every
+    case below is rejected before the page-lock check, which asks the driver."""
+    g = kw.get
+    return lib.gdn_layer_prefill_host(
+        g("hq", A), g("hz", A + 0x1000), g("ha", A + 0x2000), g("hb", A + 0x3000), g("w", A + 0x4000),
+        g("A_log", A + 0x5000), g("dt_bias", A + 0x6000), g("nw", A + 0x7000), g("T", 64), None,
+        g("Sf", A + 0x10000), None, g("cs_out", A + 0x20000), g("scale", 0.0), g("flags", 1), g("eps", 1e-6),
+        g("hout", A + 0x30000), g("ws", A + 0x100000), g("ws_bytes", 1 << 30), g("dims", DIMS), _lib.GDN_BF16,
+        None)
+
+
+@no_gpu
+def test_layer_prefill_host_validation(lib):
+    E = _lib
+    assert host_layer(lib, T=-1) == E.GDN_ERR_INVALID_ARG
+    assert host_layer(lib, flags=2) == E.GDN_ERR_INVALID_ARG        # no Neumann option on this path
+    assert host_layer(lib, eps=0.0) == E.GDN_ERR_INVALID_ARG         # as every RMSNormGated entry point
+    assert host_layer(lib, eps=-1.0) == E.GDN_ERR_INVALID_ARG
+    assert host_layer(lib, eps=float("nan")) == E.GDN_ERR_INVALID_ARG
+    assert host_layer(lib, scale=float("inf")) == E.GDN_ERR_INVALID_ARG
+    for name in ("w", "A_log", "dt_bias", "nw", "Sf", "cs_out", "hq", "hz", "ha", "hb", "hout"):
+        assert host_layer(lib, **{name: None}) == E.GDN_ERR_INVALID_ARG, name
+    assert host_layer(lib, w=A + 0x4008) == E.GDN_ERR_ALIGN
+    assert host_layer(lib, Sf=A + 0x10004) == E.GDN_ERR_ALIGN
+    assert host_layer(lib, ws=A + 0x100008) == E.GDN_ERR_ALIGN
+    assert host_layer(lib, dims=_lib.Dims(16, 48, 64, 64, 4)) == E.GDN_ERR_UNSUPPORTED
+    assert host_layer(lib, dims=_lib.Dims(16, 40, 128, 128, 4)) == E.GDN_ERR_INVALID_ARG
+
+
 def test_layer_prefill_workspace_and_launches(lib):
     dims = gdn.GDNDims(16, 48, 128, 128)
     C = dims.conv_dim
