@@ -253,7 +253,6 @@ decode_step_kernel(DecodeStepArgs a) {
     for (int j = 0; j < r; ++j) {
         const int h = kh * r + j;
         float* __restrict__ S = a.state + (slot * a.H_v + h) * D * D;
-        if (j > 0) load_state(j);
         float mk[4] = {0.f, 0.f, 0.f, 0.f}, mq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int p = 0; p < PASSES; ++p) {
@@ -299,6 +298,9 @@ decode_step_kernel(DecodeStepArgs a) {
             n.w = fmaf(kv, d4.w, eg * s[p].w);
             __stcs(reinterpret_cast<float4*>(S + (int64_t)i * D) + cq, n);
         }
+        // the registers are free: the next head's state streams in during
+        // this head's norm epilogue
+        if (j + 1 < r) load_state(j + 1);
         // RMSNormGated of the head's output row
         float tot = 0.f;
 #pragma unroll
