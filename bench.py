@@ -1,14 +1,18 @@
 """Benchmark of the GDN layer core on GB300.
 
-Prints ONE JSON line (rank 0).  A step is one pass of the layer core's
+Prints ONE JSON line (rank 0).  A call is one pass of the layer core's
 prefill path -- one gdn_layer_prefill call: conv1d + SiLU, the chunked rule,
 RMSNormGated -- over the Qwen3.6-27B prefill workload (B=1, T=4096, 16 QK / 48 V heads,
-d=128, bf16 activations, f32 state).  `value` is prefill tokens/s with inputs
-resident in HBM; the same line carries the decode path (gdn_conv1d_update +
-gdn_recurrent_decode + gdn_rmsnorm_gated on the 27B decode workload: 64
-sequences, one token each per step) under "decode", each with the roofline
-of its dominant kernel, the end-to-end rate through host buffers ("e2e"), the
-oracle's CPU rate ("cpu_baseline") and the SM clocks seen while timing.
+d=128, bf16 activations, f32 state); a timed step is --calls such calls, each
+on its own copy of the inputs (a ring of 16 copies, so every call starts with
+its inputs out of L2).  `value` is prefill tokens/s with inputs resident in
+HBM; the same line carries the other prefill workloads (Coder-Next varlen with
+resumed states; the 262144-token sequence with checkpoints every 4096 tokens
+and its 128-step decode tail) under "prefill_workloads", the decode path (the
+27B decode workload: 64 sequences, one token each per step) under "decode",
+each with the roofline of its dominant kernel, the end-to-end rate through
+host buffers ("e2e"), the oracle's CPU rate on all cores and on one
+("cpu_baseline") and the SM clocks seen while timing.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -42,6 +46,7 @@ METRIC = "GDN prefill tokens/s and decode tokens/s per layer; % tensor-core / HB
 PREFILL = "qwen36_27b_prefill"
 DECODE = "qwen36_27b_decode"
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+RING = 16  # input copies the headline prefill step cycles through
 FLOP_PER_TOKEN_HEAD = 5 * 64 * 128 + 6 * 128 * 128  # 139,264 (chunked delta rule, C=64, d=128)
 
 
@@ -207,6 +212,116 @@ def barrier(dist, dev):
         dist.barrier(device_ids=[dev.index] if dev.type == "cuda" else None)
 
 
+# --------------------------------------------------------------------------- other prefill workloads
+def prefill_workload(gdn, name, args, dev, stream, flush, clocks, pk, steps, warmup):
+    """Time gdn_layer_prefill on the named workload (device-resident inputs, its
+    own cu_seqlens, initial states and checkpoint cadence), L2 flushed between
+    calls; then the chunk stage alone (gdn_chunk_prefill on the conv output)
+    for its tensor-peak fraction; for a workload with a decode tail, the fused
+    decode steps that follow from the prefill's final states.  Returns (dict,
+    launches)."""
+    w = W.WORKLOADS[name]
+    s = w.shape
+    dims = gdn.GDNDims(s.H_k, s.H_v, s.d_k, s.d_v)
+    t_gen = time.perf_counter()
+    inp = W.workload_inputs(name)
+    t_gen = time.perf_counter() - t_gen
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    T = int(inp["mixed_qkv"].shape[0])
+    n = len(w.lengths)
+    cu = d["cu_seqlens"] if n > 1 else None
+    host_cu = inp["cu_seqlens"]
+    rows = gdn.gdn_ckpt_count(host_cu, w.ckpt_every) if w.ckpt_every else 0
+    out = torch.empty((T, s.H_v * s.d_v), dtype=w.dtype, device=dev)
+    Sf = torch.empty((n, s.H_v, s.d_k, s.d_v), dtype=torch.float32, device=dev)
+    csf = torch.empty((n, s.conv_dim, 3), dtype=w.dtype, device=dev)
+    Sck = torch.empty((rows, s.H_v, s.d_k, s.d_v), dtype=torch.float32, device=dev) if rows else None
+    cck = torch.empty((rows, s.conv_dim, 3), dtype=w.dtype, device=dev) if rows else None
+    ws = torch.empty(gdn.gdn_layer_prefill_workspace_size(n, T, dims, w.dtype), dtype=torch.uint8, device=dev)
+
+    def call():
+        gdn.gdn_layer_prefill(d["mixed_qkv"], d["z"], d["a"], d["b"], d["conv_w"], d["A_log"], d["dt_bias"],
+                              d["norm_w"], dims, cu_seqlens=cu, initial_state=d["S0"],
+                              conv_state=d["conv_state0"], ckpt_every=w.ckpt_every, out=out, final_state=Sf,
+                              conv_state_out=csf, workspace=ws, state_ckpt_out=Sck, conv_ckpt_out=cck)
+
+    def timed(fn, k_steps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k_steps)]
+        torch.cuda.synchronize(dev)
+        clocks.mark(True)
+        for k in range(k_steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            fn()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        clocks.mark(False)
+        return [a_.elapsed_time(b_) for a_, b_ in ev]
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    ms = timed(call, steps)
+    launches = steps * gdn.gdn_layer_prefill_launches(n, T, dims, w.dtype, cu_seqlens=cu is not None)
+    # the chunk stage alone, on the conv output of the same inputs
+    y = torch.empty_like(d["mixed_qkv"])
+    gdn.gdn_conv1d_fwd(d["mixed_qkv"], d["conv_w"], dims, cu, d["conv_state0"], torch.empty_like(csf), y=y)
+    o = torch.empty((T, s.H_v, s.d_v), dtype=w.dtype, device=dev)
+    cws = torch.empty(gdn.gdn_chunk_prefill_workspace_size(n, T, dims, w.dtype), dtype=torch.uint8, device=dev)
+
+    def chunk():
+        gdn.gdn_chunk_prefill(y, dims, d["a"], d["b"], d["A_log"], d["dt_bias"], cu_seqlens=cu,
+                              initial_state=d["S0"], final_state=Sf, ckpt_every=w.ckpt_every,
+                              state_ckpt_out=Sck, o=o, workspace=cws)
+
+    chunk()
+    cms = timed(chunk, steps)
+    launches += 1 + steps * gdn.gdn_chunk_prefill_launches(n, T, dims, w.dtype, cu_seqlens=cu is not None)
+    del y
+    c_avg = statistics.mean(cms) / 1e3
+    flops = FLOP_PER_TOKEN_HEAD * T * s.H_v
+    res = {
+        "workload": name, "tokens_per_call": T, "sequences": n, "H_k": s.H_k, "H_v": s.H_v,
+        "ckpt_every": w.ckpt_every, "initial_states": w.init_state,
+        "value": round(T / (statistics.mean(ms) / 1e3), 1), "unit": "tokens/s",
+        "ms_per_call": round(statistics.mean(ms), 4), "calls": steps,
+        "call": "gdn_layer_prefill (conv1d_fwd, chunk_prefill, rmsnorm_gated kernels)",
+        "chunk_prefill_ms": round(c_avg * 1e3, 4),
+        "roofline": {"kernel": "gdn_chunk_prefill", "bound": "tensor",
+                     "achieved": round(flops / c_avg / 1e12, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(flops / c_avg / 1e12 / pk["bf16_tflops"], 4),
+                     "frac_of_sustained": round(flops / c_avg / 1e12 / pk["bf16_tflops_sustained"], 4),
+                     "algorithmic_flop_per_launch": flops},
+        "l2": "flushed (512 MiB write) between timed calls",
+        "input_generation_s": round(t_gen, 1),
+    }
+    if w.decode_steps and w.decode_batch:
+        # the decode tail: fused steps of one token per sequence from the final states
+        dec = W.decode_inputs(s, w.dtype, w.decode_batch, w.decode_steps, seed=w.seed + 100)
+        dd = {k: v.to(dev) for k, v in dec.items()}
+        Sd, csd = Sf.clone(), csf.clone()
+        outd = torch.empty((w.decode_batch, s.H_v * s.d_v), dtype=w.dtype, device=dev)
+        it = iter(range(w.decode_steps))
+
+        def dstep():
+            t = next(it)
+            gdn.gdn_decode_step(dd["qkv"][t], dd["z"][t], dd["a"][t], dd["b"][t], d["conv_w"], d["A_log"],
+                                d["dt_bias"], d["norm_w"], dims, Sd, csd, out=outd)
+
+        dms = timed(dstep, w.decode_steps)
+        launches += w.decode_steps
+        dbytes = w.decode_batch * decode_step_bytes_per_seq(s)
+        res["decode_tail"] = {
+            "batch": w.decode_batch, "steps": w.decode_steps,
+            "value": round(w.decode_batch * w.decode_steps / (sum(dms) / 1e3), 1), "unit": "tokens/s",
+            "ms_per_step": round(statistics.mean(dms), 4), "call": "gdn_decode_step (one kernel per step)",
+            "hbm_frac": round(dbytes / (statistics.mean(dms) / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+            "note": "one sequence per step: launch-latency bound (6.5 MB per step)"}
+    del d, inp
+    torch.cuda.empty_cache()
+    return res, launches
+
+
 # --------------------------------------------------------------------------- our arm
 def run_ours(args):
     import gated_deltanet_linear_core_gb300 as gdn
@@ -225,6 +340,11 @@ def run_ours(args):
     inp = W.workload_inputs(PREFILL)
     T = int(inp["mixed_qkv"].shape[0])
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    # RING copies of the per-call inputs: call i of a step reads copy i % RING,
+    # last touched RING - 1 calls (> 2 GB of traffic) earlier, so every call
+    # starts with its inputs out of the 129 MB L2
+    ring = [{k: d[k].clone() for k in ("mixed_qkv", "z", "a", "b")} for _ in range(RING)]
+    ring_out = [torch.empty((T, s.H_v * s.d_v), dtype=wp.dtype, device=dev) for _ in range(RING)]
     y = torch.empty_like(d["mixed_qkv"])
     conv_out = torch.empty((1, s.conv_dim, 3), dtype=wp.dtype, device=dev)
     S = torch.empty((1, s.H_v, s.d_k, s.d_v), dtype=torch.float32, device=dev)
@@ -235,11 +355,15 @@ def run_ours(args):
     cws = torch.empty(gdn.gdn_chunk_prefill_workspace_size(1, T, dims, wp.dtype), dtype=torch.uint8, device=dev)
 
     def prefill_step(ev=None):
-        # the headline step: one gdn_layer_prefill call, events only at its ends
+        # the headline step: args.calls gdn_layer_prefill calls of one 4096-token
+        # sequence each, over the ring of input copies; events only at its ends
         if ev:
             ev[0].record(stream)
-        gdn.gdn_layer_prefill(d["mixed_qkv"], d["z"], d["a"], d["b"], d["conv_w"], d["A_log"], d["dt_bias"],
-                              d["norm_w"], dims, out=out, final_state=S, conv_state_out=conv_out, workspace=lws)
+        for i in range(args.calls):
+            x = ring[i % RING]
+            gdn.gdn_layer_prefill(x["mixed_qkv"], x["z"], x["a"], x["b"], d["conv_w"], d["A_log"], d["dt_bias"],
+                                  d["norm_w"], dims, out=ring_out[i % RING], final_state=S,
+                                  conv_state_out=conv_out, workspace=lws)
         if ev:
             ev[3].record(stream)
 
@@ -277,7 +401,7 @@ def run_ours(args):
     # conv: one kernel (one sequence, no cu_seqlens, state_out apart from state_in:
     # the tile kernel writes the conv state), the chunk kernels, the norm
     step_launches = gdn.gdn_layer_prefill_launches(1, T, dims, wp.dtype, cu_seqlens=None)
-    launches += args.steps * step_launches
+    launches += args.steps * args.calls * step_launches
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
 
     # per-call times
@@ -294,7 +418,7 @@ def run_ours(args):
     chunk_ms = [e[1].elapsed_time(e[2]) for e in sev]
     norm_ms = [e[2].elapsed_time(e[3]) for e in sev]
     total_s = max_over_ranks(dist, sum(step_ms) / 1e3, dev)
-    value = world * T * args.steps / total_s
+    value = world * T * args.calls * args.steps / total_s
     chunk_avg = sum(chunk_ms) / len(chunk_ms) / 1e3
 
     # the same chunk stage with each chunk's (I + A)^-1 formed as the
@@ -519,6 +643,15 @@ def run_ours(args):
         "l2": "flushed between steps",
     }
 
+    # ---- the other prefill workloads: packed sequences with resumed states,
+    # and the 262144-token sequence with checkpoints and its decode tail
+    workloads = {}
+    if not args.no_extra_workloads:
+        for wname, k_steps in (("coder_next_varlen", args.steps), ("qwen36_27b_long", min(args.steps, 5))):
+            r_w, l_w = prefill_workload(gdn, wname, args, dev, stream, flush, clocks, pk, k_steps, 3)
+            workloads[wname] = r_w
+            launches += l_w
+
     # ---- end to end through the C-ABI call with pinned host buffers
     # (gdn_layer_prefill_host: the copies in and out run inside the call,
     # overlapped piece by piece with the kernels)
@@ -576,9 +709,11 @@ def run_ours(args):
             "ms_per_step": round(total_s * 1e3 / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) activations, random layer parameters)",
-            "config": {"workload": PREFILL, "tokens_per_step": T, "H_k": s.H_k, "H_v": s.H_v,
+            "config": {"workload": PREFILL, "tokens_per_call": T, "calls_per_step": args.calls,
+                       "tokens_per_step": T * args.calls, "H_k": s.H_k, "H_v": s.H_v,
                        "d_k": s.d_k, "d_v": s.d_v, "chunk": 64, "state": "f32",
-                       "l2": "flushed (512 MiB write) between timed steps",
+                       "l2": f"each call reads one of {RING} input copies ({RING} x 135 MB), last read "
+                             f"{RING - 1} calls earlier; L2 also flushed (512 MiB write) between steps",
                        "parallelism": f"replicas x{world}"},
             "call": "gdn_layer_prefill (conv1d_fwd, chunk_prefill, rmsnorm_gated kernels)",
             "chunk_solve": chunk_solve,
@@ -587,6 +722,7 @@ def run_ours(args):
                               "chunk_prefill": round(statistics.mean(chunk_ms), 4),
                               "rmsnorm_gated": round(statistics.mean(norm_ms), 4)},
             "roofline": roofline,
+            "prefill_workloads": workloads,
             "decode": decode,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -614,10 +750,20 @@ def cpu_baseline(inp, s, seconds):
         dt = time.perf_counter() - t0
         if dt >= seconds:
             break
+    # one core: a bounded prefix of the same workload (the rule's cost per token
+    # does not depend on the position)
+    n1 = 512
+    a1 = [x[:n1] for x in args]
+    t1 = time.perf_counter()
+    oracle.layer_prefill(*a1, *params, s.H_k, s.H_v, s.d_k, s.d_v, nthreads=1)
+    t1 = time.perf_counter() - t1
     return {"value": round(passes * T / dt, 2), "unit": "tokens/s", "cores": oracle.max_threads(),
             "kind": "oracle",
             "sample": f"{passes} passes over the whole {PREFILL} workload ({T} tokens, all "
-                      f"{s.H_v} heads), f64, {dt:.1f} s"}
+                      f"{s.H_v} heads), f64, {dt:.1f} s",
+            "one_core": {"value": round(n1 / t1, 2), "unit": "tokens/s", "cores": 1,
+                         "sample": f"the first {n1} tokens of {PREFILL} (all {s.H_v} heads), f64, "
+                                   f"{t1:.1f} s"}}
 
 
 # --------------------------------------------------------------------------- reference arm
@@ -680,6 +826,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--calls", type=int, default=64,
+                    help="gdn_layer_prefill calls (4096-token sequences) per timed prefill step")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="skip the varlen and 262144-token prefill workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

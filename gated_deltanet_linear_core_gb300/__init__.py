@@ -332,13 +332,15 @@ def gdn_layer_prefill_launches(n_seq: int, T_tot: int, dims, dtype, cu_seqlens=T
 def gdn_layer_prefill(mixed_qkv, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, cu_seqlens=None,
                       initial_state=None, conv_state=None, ckpt_every=0, scale=0.0,
                       return_intermediates=False, stream=None, norm_eps=RMSNORM_EPS, out=None,
-                      final_state=None, conv_state_out=None, workspace=None, solve="direct", chunk=64):
+                      final_state=None, conv_state_out=None, workspace=None, solve="direct", chunk=64,
+                      state_ckpt_out=None, conv_ckpt_out=None):
     """Whole layer core over packed sequences: conv1d+SiLU -> chunked delta rule
     -> RMSNormGated, as one gdn_layer_prefill call.  Returns a dict with out
     [T, H_v*d_v], final_state [n_seq, H_v, d_k, d_v] f32, conv_state
     [n_seq, conv_dim, 3] and, when ckpt_every > 0, state_ckpt / conv_ckpt.
     return_intermediates=True runs the three calls one by one instead and adds
-    the conv output y and the rule's output o to the dict."""
+    the conv output y and the rule's output o to the dict.  state_ckpt_out and
+    conv_ckpt_out may pass preallocated checkpoint buffers."""
     if solve not in ("direct", "neumann"):
         raise ValueError(f"solve must be 'direct' or 'neumann', not {solve!r}")
     dev, dt = mixed_qkv.device, mixed_qkv.dtype
@@ -352,11 +354,17 @@ def gdn_layer_prefill(mixed_qkv, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, 
         rows = gdn_ckpt_count(host_cu, ckpt_every)
     if conv_state_out is None:
         conv_state_out = torch.empty((n_seq, C, 3), dtype=dt, device=dev)
-    conv_ck = torch.empty((rows, C, 3), dtype=dt, device=dev) if rows else None
+    conv_ck = conv_ckpt_out
+    if conv_ck is None and rows:
+        conv_ck = torch.empty((rows, C, 3), dtype=dt, device=dev)
     if final_state is None:
         final_state = torch.empty((n_seq, dims.H_v, dims.d_k, dims.d_v), dtype=torch.float32, device=dev)
-    S_ck = (torch.empty((rows, dims.H_v, dims.d_k, dims.d_v), dtype=torch.float32, device=dev)
-            if rows else None)
+    S_ck = state_ckpt_out
+    if S_ck is None and rows:
+        S_ck = torch.empty((rows, dims.H_v, dims.d_k, dims.d_v), dtype=torch.float32, device=dev)
+    if rows and (tuple(S_ck.shape) != (rows, dims.H_v, dims.d_k, dims.d_v) or
+                 tuple(conv_ck.shape) != (rows, C, 3)):
+        raise ValueError(f"checkpoint buffers must hold {rows} rows")
     if return_intermediates:
         y = gdn_conv1d_fwd(mixed_qkv, conv_w, dims, cu_seqlens, conv_state, conv_state_out, ckpt_every,
                            conv_ck, True, stream=stream)

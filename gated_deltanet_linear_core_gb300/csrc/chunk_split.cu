@@ -13,11 +13,18 @@
 // l2-norm factors of raw q / k rows and T' = (I + A)^-1:
 //   intra (independent per chunk, all chunks of all heads in parallel):
 //     D1 = [K; Q] K^T,  A = beta rk e^{G_i-G_j} rk k.k (j<i),  P = rq e^{G_i-G_j} rk q.k (j<=i)
-//     W^T = K^T (T' diag(beta e^G rk))^T,  U^T = V^T (T' diag(beta))^T
-//     -> workspace: W (row-major), U^T, P (bf16) and e^G rq, e^{G_n-G_j} rk, e^{G_n} (f32)
+//     W^T = K^T (T' diag(beta e^G rk))^T,  U^T = V^T (T' diag(beta))^T,
+//     K_dec = diag(e^{G_n-G_j} rk) K
+//     -> workspace: W (bf16), U, P, K_dec (fp16) and e^G rq, e^{G_n} (f32)
 //   chain (sequential per sequence and value head):
-//     U'^T = U^T - S^T W^T;  O^T = (S^T Q^T) diag(e^G rq) + U'^T P^T
-//     S^T <- e^{G_n} S^T + U'^T diag(e^{G_n-G_j} rk) K
+//     U' = U - W S;  O = diag(e^G rq) (Q S) + P U';  S <- e^{G_n} S + K_dec^T U'
+// Precision: the operands the kernels form for the products of the state
+// update and of P U' -- T' diag(.), K_dec, U' -- are fp16 (11 significant
+// bits against bf16's 8, at the same MMA rate), and so are K and V where they
+// meet T' in the intra kernel (re-encoded in shared memory, exact for
+// |x| in [2^-14, 65504]); the products with the raw bf16 q (D1, [Q; W] S)
+// stay bf16.  This keeps the state's rounding error well inside the bf16
+// tolerance when decay is slow and the state carries across many chunks.
 // The chunks of a call are processed in segments (a range of chunk indices
 // over all sequences) whose intermediates fit in the workspace and, at the
 // default size, in L2; the state crosses segments through final_state (or a
@@ -37,21 +44,23 @@ __device__ int g_device_error;  // bit 0: a bounded wait gave up
 namespace {
 
 using namespace tc;
+typedef __half f16;
 
 constexpr int C = 64;
 constexpr int D = 128;
 constexpr uint64_t kWaitNs = 1000000000ull;
-constexpr size_t kSegBytes = 128ull << 20;  // workspace intermediates per segment
+constexpr size_t kSegBytes = 256ull << 20;  // workspace intermediates per segment
 
 // per (chunk, value head) unit in the workspace
-constexpr size_t U_WT = 16384, U_UT = 16384, U_P = 8192, U_VEC = 1024;
-constexpr size_t UNIT_BYTES = U_WT + U_UT + U_P + U_VEC;
+constexpr size_t U_WT = 16384, U_UT = 16384, U_P = 8192, U_VEC = 1024, U_KD = 16384;
+constexpr size_t UNIT_BYTES = U_WT + U_UT + U_P + U_VEC + U_KD;
 
 struct Work {
     bf16* wt;       // W, [U][64][128] (row i of W = 128 d-values)
-    bf16* ut;       // U, [U][64][128] (row i of U = 128 v-values)
-    bf16* p;        // [U][64][64]
+    f16* ut;        // U, [U][64][128] (row i of U = 128 v-values), fp16
+    f16* p;         // P, [U][64][64], fp16
     float* vec;     // [U][256]: e^G rq (0..63), e^{G_n-G_j} rk (64..127), e^{G_n} (128)
+    f16* kd;        // K_dec, [U][64][128] (row j = e^{G_n-G_j} rk_j k_j), fp16
     int32_t* coff;  // [n_seq + 1] chunk offsets
     float* carry;   // state between segments (final_state or workspace), may be null
 };
@@ -95,9 +104,10 @@ Work work_at(uint8_t* base, const Layout& L, int H_v) {
     Work w;
     w.coff = reinterpret_cast<int32_t*>(base + L.off_coff);
     w.wt = reinterpret_cast<bf16*>(un);
-    w.ut = reinterpret_cast<bf16*>(un + U * U_WT);
-    w.p = reinterpret_cast<bf16*>(un + U * (U_WT + U_UT));
+    w.ut = reinterpret_cast<f16*>(un + U * U_WT);
+    w.p = reinterpret_cast<f16*>(un + U * (U_WT + U_UT));
     w.vec = reinterpret_cast<float*>(un + U * (U_WT + U_UT + U_P));
+    w.kd = reinterpret_cast<f16*>(un + U * (U_WT + U_UT + U_P + U_VEC));
     w.carry = L.carry_bytes ? reinterpret_cast<float*>(base + L.off_carry) : nullptr;
     return w;
 }
@@ -156,13 +166,13 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, 
 constexpr int NT_I = 256;
 constexpr int IS_KQ = 0;                          // [cb0: K | Q][cb1: K | Q]; the Q halves then hold T'
 constexpr int IS_V = IS_KQ + 32768;               // V, then the W staging tile
-constexpr int IS_A = IS_V + 16384;                // A, f32 [64][68]; then B_W | B_U (bf16)
+constexpr int IS_A = IS_V + 16384;                // A, f32 [64][68]; then B_W | B_U (fp16)
 constexpr int A_PITCH = 68;
 constexpr int IS_X = IS_A + 64 * A_PITCH * 4;     // solve temporaries, f32 [32][36]
 constexpr int X_PITCH = 36;
 constexpr int IS_VEC = IS_X + 32 * X_PITCH * 4;   // G (log2), beta, beta e^G rk, rk, rq,
-                                                  // G - log2 rk
-constexpr int IS_BAR = IS_VEC + 6 * 64 * 4;
+                                                  // G - log2 rk, e^{G_n-G} rk
+constexpr int IS_BAR = IS_VEC + 7 * 64 * 4;
 constexpr int IS_TOTAL = IS_BAR + 64;
 constexpr int ISMEM = IS_TOTAL + 1024;
 constexpr uint32_t TI_D1 = 0, TI_DW = 0, TI_DU = 64, TI_COLS = 128;  // D1 (128 columns) is dead before W, U
@@ -232,6 +242,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     float* RKs = Gs + 192;
     float* RQs = Gs + 256;
     float* Ms = Gs + 320;
+    float* DECs = Gs + 384;
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + IS_BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 2);
@@ -357,7 +368,9 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 RKs[i] = f;
                 FWs[i] = Bs[i] * eg * f;
                 Ms[i] = Gs[i] - lg2_approx(f);
-                vec[64 + i] = i < n ? exp2f(Gn - Gs[i]) * f : 0.f;
+                const float dec = i < n ? exp2f(Gn - Gs[i]) * f : 0.f;
+                vec[64 + i] = dec;
+                DECs[i] = dec;
                 if (i == 0) vec[128] = exp2f(Gn);
             } else {
                 RQs[i] = f;
@@ -367,7 +380,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             tmem_wait_ld();
         }
         __syncthreads();
-        {   // A (k rows -> shared, f32) and P (q rows -> workspace, bf16):
+        {   // A (k rows -> shared, f32) and P (q rows -> workspace, fp16):
             //   A_ij = beta_i rk_i rk_j e^{G_i-G_j} k_i.k_j (j<i), P_ij = rq_i rk_j e^{G_i-G_j} q_i.k_j (j<=i)
             // with the row and column factors folded into the exponent:
             //   f_i rk_j 2^{G_i-G_j} = 2^{(G_i + log2 f_i) - (G_j - log2 rk_j)}
@@ -405,16 +418,38 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                     *reinterpret_cast<float4*>(&Am[i * A_PITCH + j0 + 4 * g4]) =
                         make_float4(d1[4 * g4], d1[4 * g4 + 1], d1[4 * g4 + 2], d1[4 * g4 + 3]);
             } else {
-                bf16* pp = w.p + u * (U_P / 2) + i * 64 + j0;
+                f16* pp = w.p + u * (U_P / 2) + i * 64 + j0;
 #pragma unroll
-                for (int g = 0; g < 4; ++g) store16(pp + 8 * g, d1 + 8 * g);
+                for (int g = 0; g < 4; ++g)
+                    *reinterpret_cast<uint4*>(pp + 8 * g) =
+                        make_uint4(pack_h2(d1[8 * g], d1[8 * g + 1]), pack_h2(d1[8 * g + 2], d1[8 * g + 3]),
+                                   pack_h2(d1[8 * g + 4], d1[8 * g + 5]), pack_h2(d1[8 * g + 6], d1[8 * g + 7]));
             }
         }
         __syncthreads();
+        // D1 has read K: K and V are re-encoded in place as the fp16 operands
+        // of the W and U products, and K_dec = diag(e^{G_n-G_j} rk) K goes to
+        // the workspace (fp16, rows of 128 d) -- by the threads the solve's
+        // first step leaves free
+        auto convert_kv = [&](int t, int nt) {
+            f16* kd = w.kd + u * (U_KD / 2);
+            for (int e = t; e < 1024; e += nt) {
+                const int blk = e >> 9, r = (e >> 3) & 63, pc = e & 7;
+                uint4* src = reinterpret_cast<uint4*>(kq + blk * 16384 + (e & 511) * 16);
+                float x[8];
+                unpack16<bf16>(*src, x);
+                const float dc = DECs[r];
+                *src = make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]), pack_h2(x[6], x[7]));
+                *reinterpret_cast<uint4*>(kd + r * 128 + blk * 64 + ((pc ^ (r & 7)) << 3)) =
+                    make_uint4(pack_h2(x[0] * dc, x[1] * dc), pack_h2(x[2] * dc, x[3] * dc),
+                               pack_h2(x[4] * dc, x[5] * dc), pack_h2(x[6] * dc, x[7] * dc));
+            }
+            bf16_to_h_inplace(vv, 16384, t, nt);
+        };
         if constexpr (!NEUMANN) {
             // T' = (I + A)^-1 (unit lower triangular): the four diagonal 16-blocks
             // by forward substitution (f32), then the off-diagonal blocks by
-            // doubling on warp-level tf32 MMAs (T' is rounded to bf16 right after),
+            // doubling on warp-level tf32 MMAs (T' is rounded to fp16 right after),
             //   T'_{10} = -D_1 A_{10} D_0 (and T'_{32}),  T'_{[23][01]} = -T'_{[23][23]} A_{[23][01]} T'_{[01][01]}
             if (tid < 64) {
                 const int r0 = (tid >> 4) * 16, cl = tid & 15;
@@ -429,7 +464,8 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 for (int r = 0; r < 16; ++r) *tp_at(kq, r0 + r, r0 + cl) = x[r];
             } else {
                 // meanwhile the other threads zero T' above its diagonal blocks
-                // (blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)), 2 float4 each
+                // (blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)), 2 float4 each,
+                // and re-encode K and V
     #pragma unroll
                 for (int e = tid - 64; e < 384; e += NT_I - 64) {
                     const int blk = e >> 6, br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
@@ -437,6 +473,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                     *reinterpret_cast<float4*>(tp_at(kq, 16 * br + ((e >> 2) & 15), 16 * bc + (e & 3) * 4)) =
                         make_float4(0.f, 0.f, 0.f, 0.f);
                 }
+                convert_kv(tid - 64, NT_I - 64);
             }
             __syncthreads();
             const int fg = lane >> 2, ft = lane & 3;  // MMA fragment row group, thread in group
@@ -509,6 +546,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             // T' = I + N, then five times P <- P P and T' <- T' + T' P.  Each
             // product is a full 64 x 64 x 64 tf32 MMA, a 16 x 32 tile per warp,
             // accumulated in registers and written back in place after a barrier.
+            convert_kv(tid, NT_I);
             for (int e = tid; e < 64 * 64; e += NT_I) {
                 const int r = e >> 6, c = e & 63;
                 const float nv = c < r ? -Am[r * A_PITCH + c] : 0.f;
@@ -571,7 +609,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 __syncthreads();
             }
         }
-        {   // B_W = T' diag(beta e^G rk), B_U = T' diag(beta) (bf16) into the A region
+        {   // B_W = T' diag(beta e^G rk), B_U = T' diag(beta) (fp16) into the A region
             const int which = tid >> 7, i = (tid >> 1) & 63, c0 = (tid & 1) * 32;
             const float* Fc = (which == 0 ? FWs : Bs) + c0;
             float vals[32];  // T' is zero above its diagonal (all of it is written)
@@ -586,7 +624,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 vals[4 * g4 + 2] = hi.x;
                 vals[4 * g4 + 3] = hi.y;
             }
-            store_row_bf16(sm + IS_A + which * 8192, i, c0, vals, 32);
+            store_row_h(sm + IS_A + which * 8192, i, c0, vals, 32);
         }
         fence_async_smem();
         tc_fence_before();
@@ -599,9 +637,9 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 mma_bf16(tb + TI_DW, sdesc_sw128(akq + k * 2048, 16384, 1024),
-                         sdesc_sw128(bw + k * 32, 16, 1024), idesc_bf16_f32(128, 64, 1, 0), k > 0);
+                         sdesc_sw128(bw + k * 32, 16, 1024), idesc_f16_f32(128, 64, 1, 0), k > 0);
                 mma_bf16(tb + TI_DU, sdesc_sw128(av + k * 2048, 8192, 1024),
-                         sdesc_sw128(bu + k * 32, 16, 1024), idesc_bf16_f32(128, 64, 1, 0), k > 0);
+                         sdesc_sw128(bu + k * 32, 16, 1024), idesc_f16_f32(128, 64, 1, 0), k > 0);
             }
             mma_commit(bar_mma);
         }
@@ -611,7 +649,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     if (ok) {
         mma_pending = false;
         tc_fence_after();
-        // W and U as row-major bf16 tiles for TMA stores: the accumulators
+        // W (bf16) and U (fp16) as row-major tiles for TMA stores: the accumulators
         // (lanes = d, columns = i) are read in the 16x256b shape, whose
         // fragments stmatrix.trans writes transposed -- 16 bytes of a row at a
         // time -- into 128-byte-swizzled staging tiles (W in the consumed V
@@ -629,7 +667,9 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 tmem_ld16x256b_x2(tb + ((uint32_t)d0 << 16) + col + 16 * (q >> 1), r);
                 tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 4; ++k) p[k] = pack_bf16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+                for (int k = 0; k < 4; ++k)
+                    p[k] = acc == 0 ? pack_bf16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]))
+                                    : pack_h2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
                 // matrices: 0 (d0.., i0..), 1 (d0+8.., i0..), 2 (d0.., i0+8..), 3 (d0+8.., i0+8..)
                 const int ri = i0 + 8 * (mk >> 1) + mr, rd = d0 + 8 * (mk & 1);
                 stmatrix_x4_trans(stg + (rd >> 6) * 8192 + sw128_off(ri, rd & 63), p);
@@ -659,11 +699,11 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 // of the state are independent under the delta rule, so a head's state can be
 // split across CTAs when there are few (sequence, head) pairs.  Per chunk,
 // with the chunk's rows on TMEM lanes and the slice's columns as the MMA N:
-//   MMA1  [Q S; W S]      M = 128 (q rows | w rows), N = VS, K = d   (A = [Q; W], B = S, MN-major)
-//   U' = U - W S          (w-row lanes; bf16 operands U' and U' diag(e^{G_n-G_j} rk))
-//   MMA2  dS = K^T U'_dec M = d, N = VS, K = j
+//   MMA1  [Q S; W S]      M = 128 (q rows | w rows), N = VS, K = d   (A = [Q; W], B = S, MN-major; bf16)
+//   U' = U - W S          (w-row lanes; fp16 operand U')
+//   MMA2  dS = K_dec^T U' M = d, N = VS, K = j (fp16)
 //   S <- e^{G_n} S + dS   (f32 in registers; bf16 operand for the next MMA1)
-//   MMA3  P U'            M = 128 (P and 64 rows of padding), N = VS, K = j
+//   MMA3  P U'            M = 128 (P and 64 rows of padding), N = VS, K = j (fp16)
 //   O = (Q S) diag(e^G rq) + P U'  (q-row lanes, stored straight to global)
 // Warp roles: 16 compute warps, one warp that issues the MMAs and one that
 // issues the TMA copies; they hand work to each other through mbarriers, so
@@ -677,7 +717,7 @@ template <int VS>
 struct ChainLayout {
     static constexpr int NB = VS / 64;                  // 64-column blocks of the slice
     static constexpr int SG_QW = 0;                     // per 64-wide d block: Q rows | W rows (16 KB)
-    static constexpr int SG_P = 32768;                  // P; K follows, as the padded P operand's rows 64-127
+    static constexpr int SG_P = 32768;                  // P; K_dec follows, as the padded P operand's rows 64-127
     static constexpr int SG_K = SG_P + 8192;
     static constexpr int SG_UT = SG_K + 16384;          // U rows of the slice, NB blocks of [64][64]
     static constexpr int STAGE = SG_UT + VS * 128;
@@ -685,9 +725,8 @@ struct ChainLayout {
     static constexpr int VEC = 528;                     // bytes of a chunk's vectors copied (129 floats used)
     static constexpr int CS_S = 0;                      // S [d][v] bf16, NB blocks of 16 KB
     static constexpr int CS_STAGE = CS_S + NB * 16384;
-    static constexpr int CS_UP = CS_STAGE + NST * STAGE;  // U' [j][v] bf16, NB blocks of 8 KB
-    static constexpr int CS_UD = CS_UP + NB * 8192;     // U' diag(e^{G_n-G_j} rk)
-    static constexpr int CS_VEC = CS_UD + NB * 8192;    // the stages' vectors, NST x VEC
+    static constexpr int CS_UP = CS_STAGE + NST * STAGE;  // U' [j][v] fp16, NB blocks of 8 KB
+    static constexpr int CS_VEC = CS_UP + NB * 8192;    // the stages' vectors, NST x VEC
     static constexpr int CS_BAR = CS_VEC + NST * VEC;
     static constexpr int SMEM = CS_BAR + 128 + 1024;    // 15 barrier / flag words
     // TMEM: two buffers of [Q S; W S], dS, and OPB buffers of P U' (two when they
@@ -734,7 +773,8 @@ template <int VS>
 __global__ void __launch_bounds__(NT_C, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
                    const __grid_constant__ CUtensorMap utmap, const __grid_constant__ CUtensorMap pmap,
-                   const __grid_constant__ CUtensorMap omap, DeltaArgs a, Work w, int64_t C0, int64_t segc) {
+                   const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap kdmap, DeltaArgs a,
+                   Work w, int64_t C0, int64_t segc) {
     pdl_wait();
     pdl_trigger();
     using Ly = ChainLayout<VS>;
@@ -760,7 +800,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         return;
     }
     const int kh = h / (a.H_v / a.H_k);
-    const int xq = kh * D, xk = a.H_k * D + kh * D;
+    const int xq = kh * D;
     int64_t s0, s1;
     seq_bounds(a.cu, seq, a.T, s0, s1);
     const int64_t L = s1 - s0;
@@ -822,8 +862,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 tma_load_2d(st + Ly::SG_QW + 16384, &qmap, &full[b], xq + 64, y);
                 tma_load_2d(st + Ly::SG_QW + 24576, &wmap, &full[b], 64, (int)(uu * 64));
                 tma_load_2d(st + Ly::SG_P, &pmap, &full[b], 0, (int)(uu * 64));
-                tma_load_2d(st + Ly::SG_K, &qmap, &full[b], xk, y);
-                tma_load_2d(st + Ly::SG_K + 8192, &qmap, &full[b], xk + 64, y);
+                tma_load_2d(st + Ly::SG_K, &kdmap, &full[b], 0, (int)(uu * 64));
+                tma_load_2d(st + Ly::SG_K + 8192, &kdmap, &full[b], 64, (int)(uu * 64));
 #pragma unroll
                 for (int nb = 0; nb < Ly::NB; ++nb)
                     tma_load_2d(st + Ly::SG_UT + nb * 8192, &utmap, &full[b], v0 + 64 * nb, (int)(uu * 64));
@@ -839,7 +879,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         // ------------------------------------------------ MMA issuer (lane 0)
         if (lane == 0) {
             const uint32_t bs = smem_u32(sm + Ly::CS_S);
-            const uint32_t bud = smem_u32(sm + Ly::CS_UD), bup = smem_u32(sm + Ly::CS_UP);
+            const uint32_t bup = smem_u32(sm + Ly::CS_UP);
             uint64_t* last = nullptr;  // the last commit, for the drain on abort
             uint32_t last_parity = 0;
             for (int k = 0; k < nch; ++k) {
@@ -862,7 +902,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     mma_bf16(tb + Ly::T_DS, sdesc_sw128(st + Ly::SG_K + q * 2048, 8192, 1024),
-                             sdesc_sw128(bud + q * 2048, 8192, 1024), idesc_bf16_f32(128, VS, 1, 1), q > 0);
+                             sdesc_sw128(bup + q * 2048, 8192, 1024), idesc_f16_f32(128, VS, 1, 1), q > 0);
                 mma_commit(m2);
                 last = m2;
                 // P U' into buffer ob once the O epilogue of its previous use is done
@@ -874,7 +914,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     mma_bf16(tb + Ly::T_OP + VS * ob, sdesc_sw128(st + Ly::SG_P + q * 32, 16, 1024),
-                             sdesc_sw128(bup + q * 2048, 8192, 1024), idesc_bf16_f32(128, VS, 0, 1), q > 0);
+                             sdesc_sw128(bup + q * 2048, 8192, 1024), idesc_f16_f32(128, VS, 0, 1), q > 0);
                 mma_commit(m3);
                 mma_commit(&empty[k % NST]);
                 last = m3;
@@ -891,8 +931,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         const uint32_t lo = (uint32_t)(quarter * 32) << 16;
         const bool qrow = quarter < 2;
         uint8_t* s_op = sm + Ly::CS_S + (c0 >> 6) * 16384;    // this thread's block of the S operand
-        uint8_t* up_op = sm + Ly::CS_UP + (c0 >> 6) * 8192;   // ... of U'
-        uint8_t* ud_op = sm + Ly::CS_UD + (c0 >> 6) * 8192;   // ... of U'_dec
+        uint8_t* up_op = sm + Ly::CS_UP + (c0 >> 6) * 8192;   // ... of U' (fp16)
         const int cb = c0 & 63;
         int64_t ck_row0 = 0;
         if (a.ckpt_every > 0 && a.ckpt != nullptr) ck_row0 = ckpt_row0(a.cu, seq, a.T, a.ckpt_every);
@@ -935,23 +974,19 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             const float eGn = vs[128];
             float erq = 0.f;
             if (!qrow) {
-                // U' = U - W S for w row j, and its copy scaled by e^{G_n-G_j} rk_j
+                // U' = U - W S for w row j (fp16 operand of MMA2 and MMA3)
                 const int j = lrow - 64;
-                const float dj = vs[64 + j];
                 const uint8_t* ut = st + Ly::SG_UT + (c0 >> 6) * 8192;
 #pragma unroll
                 for (int h16 = 0; h16 < CV; h16 += 16) {
                     float ws[16], up[16];
                     tmem_ld16(tb + lo + Ly::T_QW + VS * b + c0 + h16, ws);
-                    unpack16<bf16>(*reinterpret_cast<const uint4*>(ut + sw128_off(j, cb + h16)), up);
-                    unpack16<bf16>(*reinterpret_cast<const uint4*>(ut + sw128_off(j, cb + h16 + 8)), up + 8);
+                    unpack8_h(*reinterpret_cast<const uint4*>(ut + sw128_off(j, cb + h16)), up);
+                    unpack8_h(*reinterpret_cast<const uint4*>(ut + sw128_off(j, cb + h16 + 8)), up + 8);
                     tmem_wait_ld();
 #pragma unroll
                     for (int q = 0; q < 16; ++q) up[q] -= ws[q];
-                    store_row_bf16(up_op, j, cb + h16, up, 16);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) ws[q] = up[q] * dj;
-                    store_row_bf16(ud_op, j, cb + h16, ws, 16);
+                    store_row_h(up_op, j, cb + h16, up, 16);
                 }
                 fence_async_smem();
             } else {
@@ -1059,17 +1094,42 @@ PFN_cuTensorMapEncodeTiled_v12000 tensormap_encoder() {
     return fn;
 }
 
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+    });
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&c) != CUDA_SUCCESS || c == nullptr ||
+        get_id(c, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
 namespace {
 
 bool encode2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-              uint32_t box_rows) {
+              uint32_t box_rows, CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensormap_encoder();
     if (enc == nullptr) return false;
     cuuint64_t gdim[2] = {cols, rows};
     cuuint64_t gstr[1] = {cols * 2};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t es[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstr, box,
+    return enc(map, type, 2, const_cast<void*>(base), gdim, gstr, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1096,9 +1156,11 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
     const uint64_t conv_dim = 2ull * a.H_k * D + (uint64_t)a.H_v * D;
     const uint64_t U = (uint64_t)Ly.segc * a.H_v;
     const bool split = (int64_t)a.n_seq * a.H_v * 2 <= sm_count();
-    CUtensorMap qmap, wtmap, utmap, pmap, omap;
+    CUtensorMap qmap, wtmap, utmap, pmap, omap, kdmap;
+    constexpr CUtensorMapDataType F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) || !encode2d(&wtmap, w.wt, 128, U * 64, 64, 64) ||
-        !encode2d(&utmap, w.ut, 128, U * 64, 64, 64) || !encode2d(&pmap, w.p, 64, U * 64, 64, 64) ||
+        !encode2d(&utmap, w.ut, 128, U * 64, 64, 64, F16) || !encode2d(&pmap, w.p, 64, U * 64, 64, 64, F16) ||
+        !encode2d(&kdmap, w.kd, 128, U * 64, 64, 64, F16) ||
         !encode2d(&omap, a.o, (uint64_t)a.H_v * D, (uint64_t)a.T, 64, 64))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
@@ -1138,10 +1200,10 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
         }
         if (split)
             e = launch_pdl(chunk_chain_kernel<64>, dim3((unsigned)(a.n_seq * a.H_v * 2)), dim3(NT_C),
-                           ChainLayout<64>::SMEM, s, qmap, wtmap, utmap, pmap, omap, a, w, C0, Ly.segc);
+                           ChainLayout<64>::SMEM, s, qmap, wtmap, utmap, pmap, omap, kdmap, a, w, C0, Ly.segc);
         else
             e = launch_pdl(chunk_chain_kernel<128>, dim3((unsigned)(a.n_seq * a.H_v)), dim3(NT_C),
-                           ChainLayout<128>::SMEM, s, qmap, wtmap, utmap, pmap, omap, a, w, C0, Ly.segc);
+                           ChainLayout<128>::SMEM, s, qmap, wtmap, utmap, pmap, omap, kdmap, a, w, C0, Ly.segc);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
@@ -1222,7 +1284,8 @@ constexpr int kStaticMaxSeq = 16384;
 static __device__ __align__(256) uint8_t g_prefill_scratch[kStaticScratchBytes];
 
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[128];  // device address of g_prefill_scratch, per device ordinal
+void* g_scratch_ptr[128];                // device address of g_prefill_scratch, per device ordinal
+unsigned long long g_scratch_ctx[128];   // ... valid in the context with this id
 
 Layout static_layout(int n_seq, int64_t T, int H_v) {
     return layout_for(n_seq, T, H_v, kStaticScratchBytes - align256(4 * ((size_t)kStaticMaxSeq + 1)) - 256,
@@ -1240,8 +1303,9 @@ bool chunk_split_static_fits(int n_seq, int H_v) {
 
 cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s) {
     if (!chunk_split_static_fits(a.n_seq, a.H_v) || a.S_final == nullptr) return cudaErrorInvalidValue;
-    // set-up once per device, with that device current: the host-side name of
-    // the array is not a device address
+    // set-up once per device (per context of that device: a device reset
+    // creates a new context, in which the array may sit elsewhere), with that
+    // device current: the host-side name of the array is not a device address
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1249,11 +1313,13 @@ cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s) {
     uint8_t* base = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_scratch_mu);
-        if (g_scratch_ptr[dev] == nullptr) {
+        const unsigned long long ctx = current_context_id();
+        if (g_scratch_ptr[dev] == nullptr || ctx == 0 || ctx != g_scratch_ctx[dev]) {
             void* p = nullptr;
             e = cudaGetSymbolAddress(&p, g_prefill_scratch);
             if (e != cudaSuccess) return e;
             g_scratch_ptr[dev] = p;
+            g_scratch_ctx[dev] = current_context_id();  // the lookup made the device's context current
         }
         base = static_cast<uint8_t*>(g_scratch_ptr[dev]);
     }

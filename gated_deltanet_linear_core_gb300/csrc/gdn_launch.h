@@ -98,6 +98,11 @@ cudaError_t launch_decode_verify(const DecodeVerifyArgs& a, gdn_dtype_t dt, cuda
 
 // cuTensorMapEncodeTiled from the driver (nullptr if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensormap_encoder();
+// Unique id of the calling thread's current CUDA context, 0 if there is none
+// (or the driver cannot tell).  Caches of device objects key on it, so that a
+// context destroyed and created again (a device reset) never reuses objects of
+// the old one.
+unsigned long long current_context_id();
 
 // Chunked prefill on tcgen05 tensor cores (bf16 operands, f32 state, D = 128)
 // in two kernels: the state-independent work of every chunk in parallel (into

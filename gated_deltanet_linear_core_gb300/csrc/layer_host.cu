@@ -22,6 +22,7 @@ namespace {
 constexpr int kMaxDev = 128;
 std::mutex g_host_mu;
 cudaStream_t g_copy_in[kMaxDev], g_copy_out[kMaxDev], g_pre[kMaxDev];
+unsigned long long g_stream_ctx[kMaxDev];  // context the streams of a device belong to
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -120,11 +121,22 @@ cudaError_t copy_streams(cudaStream_t* in, cudaStream_t* out, cudaStream_t* pre)
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_host_mu);
-    if (g_copy_in[dev] == nullptr) {
+    // created once per device context: after a device reset the old handles
+    // belong to a destroyed context and new streams are made
+    unsigned long long ctx = current_context_id();
+    if (ctx == 0) {
+        if ((e = cudaFree(nullptr)) != cudaSuccess) return e;  // makes the device's context current
+        ctx = current_context_id();
+    }
+    if (g_copy_in[dev] == nullptr || ctx != g_stream_ctx[dev]) {
         e = cudaStreamCreateWithFlags(&g_copy_in[dev], cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g_copy_out[dev], cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g_pre[dev], cudaStreamNonBlocking);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) {
+            g_copy_in[dev] = nullptr;
+            return e;
+        }
+        g_stream_ctx[dev] = ctx;
     }
     *in = g_copy_in[dev];
     *out = g_copy_out[dev];

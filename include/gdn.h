@@ -19,9 +19,12 @@
  * Conventions shared by every call
  * --------------------------------
  * - Pointers marked (device) are CUDA device pointers; (host) are host memory.
- *   The caller owns every buffer.  The library allocates nothing persistent;
- *   the only memory it allocates is a caller-sized workspace it never asks for
- *   (see gdn_chunk_prefill_workspace_size).
+ *   The caller owns every buffer.  The library allocates no device memory:
+ *   scratch is a caller-sized workspace (see gdn_chunk_prefill_workspace_size).
+ *   Its persistent objects are two: a fixed scratch array compiled into the
+ *   library for gdn_chunk_prefill_noalloc, and three CUDA streams per device
+ *   context that gdn_layer_prefill_host creates on its first call there
+ *   (released with the context).
  * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *   default stream), except where a call says it synchronises.
  * - Tensors are dense, row-major, in the shapes given per argument.  Device
@@ -291,8 +294,8 @@ gdn_status_t gdn_chunk_prefill(const void* qkv, const void* a, const void* b, co
  *     the other shapes);
  *   - final_state is required (it carries the state between the call's
  *     segments); it may alias initial_state;
- *   - limits: n_seq <= 16384 and H_v * 41,984 bytes must fit in the array
- *     (H_v <= 597); calls beyond them return GDN_ERR_WORKSPACE;
+ *   - limits: n_seq <= 16384 and H_v * 58,368 bytes must fit in the array
+ *     (H_v <= 430); calls beyond them return GDN_ERR_WORKSPACE;
  *   - the first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any
  *     stream capture;

@@ -1,14 +1,16 @@
-"""Rounding model of the tensor-core chunked prefill, for deriving tolerances.
+"""Rounding model of the tensor-core chunked prefill, for reading its error.
 
 Test infrastructure (CPU, numpy).  It restates the chunked form of the gated
 delta rule (cortex commit "feat(stage-8c): linear-attention layer", "chunked
 algorithm ... chunk_size=64") with the operand precisions the bf16 tensor-core
-path uses and nothing else from it: every product's operands are rounded to
-bf16 where that path feeds bf16 operands to the tensor cores, accumulation and
-the state stay in f64 (the path's f32 accumulation is finer than the bf16
-operands), and (I + A)^-1 is exact.  The rel-L2 of this model against the
-oracle is the error the operand precisions alone imply; a GPU result within a
-small factor of it shows the kernel adds no error of its own.
+path uses and nothing else from it: the products with the raw bf16 q, [Q; W] S,
+take W and S rounded to bf16; T' diag(beta e^G rk), T' diag(beta), U, P, U' and
+diag(e^{G_n - G_j} rk) K are rounded to fp16 where they meet the tensor cores
+(the bf16 activations k, v are exact in fp16); accumulation and the state stay
+in f64, (I + A)^-1 is exact, and o is rounded to bf16.  The rel-L2 of this
+model against the oracle is the error the operand precisions alone imply; a
+GPU result close to it shows the kernels add little error of their own.  It
+sets no tolerance.
 """
 from __future__ import annotations
 
@@ -17,6 +19,11 @@ import math
 import numpy as np
 
 from test_solve_forms import bf16
+
+
+def fp16(x):
+    """x rounded to the nearest fp16 value."""
+    return np.asarray(x, dtype=np.float16).astype(np.float64)
 
 
 def chunked_bf16_operands(q, k, v, g, beta, S0, scale, C=64):
@@ -38,12 +45,12 @@ def chunked_bf16_operands(q, k, v, g, beta, S0, scale, C=64):
         KK = K @ K.T
         A = np.tril(bb[:, None] * rk[sl][:, None] * rk[sl][None, :] * Dm * KK, -1)
         Ti = np.linalg.solve(np.eye(n) + A, np.eye(n))
-        W = bf16(bf16(Ti * (bb * np.exp(G) * rk[sl])[None, :]) @ K)
-        U = bf16(bf16(Ti * bb[None, :]) @ V)
-        P = bf16(rq[sl][:, None] * rk[sl][None, :] * Dm * (Q @ K.T))
+        W = bf16(fp16(Ti * (bb * np.exp(G) * rk[sl])[None, :]) @ K)
+        U = fp16(fp16(Ti * bb[None, :]) @ V)
+        P = fp16(rq[sl][:, None] * rk[sl][None, :] * Dm * (Q @ K.T))
         Sb = bf16(S)
-        Up = U - W @ Sb
-        dec = np.exp(G[-1] - G) * rk[sl]
-        O[sl] = bf16((np.exp(G) * rq[sl])[:, None] * (Q @ Sb) + P @ bf16(Up))
-        S = math.exp(G[-1]) * S + K.T @ bf16(dec[:, None] * Up)
+        Up = fp16(U - W @ Sb)
+        Kd = fp16((np.exp(G[-1] - G) * rk[sl])[:, None] * K)
+        O[sl] = bf16((np.exp(G) * rq[sl])[:, None] * (Q @ Sb) + P @ Up)
+        S = math.exp(G[-1]) * S + Kd.T @ Up
     return O, S

@@ -16,7 +16,7 @@ import torch
 import gated_deltanet_linear_core_gb300 as gdn
 import oracle
 import workloads as W
-from gpu_util import TOL, assert_close, host
+from gpu_util import TOL, assert_close, host, oracle_heads_prefill
 
 pytestmark = pytest.mark.gpu
 
@@ -193,6 +193,14 @@ def test_head_shards_equal_the_full_call(world):
     s = SHAPE_27B
     inp = W.layer_inputs(s, torch.bfloat16, [600, 400], seed=39, init_state=True)
     full = _run(inp, s, one_call=True, ckpt_every=256)
+    # the full call itself against the oracle, on one value head of each shard
+    tol = TOL[torch.bfloat16]
+    heads = [gdn.head_shard(_dims(s), r, world).h0 for r in range(world)]
+    out = full["out"].view(-1, s.H_v, s.d_v)
+    for h, ref in oracle_heads_prefill(inp, s, heads, ckpt_every=256).items():
+        assert_close(f"out head {h}", host(out[:, h]), ref["out"], tol)
+        assert_close(f"S head {h}", host(full["final_state"][:, h]), ref["S"][:, 0], tol)
+        assert_close(f"ckpts head {h}", host(full["state_ckpt"][:, h]), ref["S_ckpt"][:, 0], tol)
     for r in range(world):
         sh = gdn.head_shard(_dims(s), r, world)
         zc = slice(sh.h0 * s.d_v, sh.h1 * s.d_v)

@@ -208,7 +208,8 @@ def test_chunk_prefill_slow_decay(dtype, keys):
     """Slow decay, A_log = ln U(1e-3, 1e-2), so the state carries across many
     chunks; with 'correlated' keys (one shared direction per key head, cosine
     ~0.8) and beta ~ 0.9 the chunk matrix (I + A)^-1 is far from the identity
-    -- the case where a Neumann-product inverse loses all accuracy."""
+    -- the case where a Neumann-product inverse loses all accuracy.  Held to
+    the fixed tolerances (1e-4 f32, 5e-3 bf16) like every workload."""
     shape = SMALL_128
     inp = _delta_inputs(shape, dtype, [1000, 300], seed=18)
     gen = torch.Generator().manual_seed(18)
@@ -229,12 +230,9 @@ def test_chunk_prefill_slow_decay(dtype, keys):
                               final_state=Sf)
     torch.cuda.synchronize()
     o_ref, S_ref, _ = _oracle_delta(inp, shape)
-    tol_o = tol_S = TOL[dtype]
     if dtype == torch.bfloat16:
-        # The bf16 tolerance is set for the configs' fast decay.  Here the state
-        # carries across ~16 chunks, and the bf16 state operand's rounding
-        # accumulates.  The bound is derived from the rounding model of the
-        # tensor-core path (its bf16 operands, nothing else), with 20 % margin.
+        # for the record: the error the tensor-core path's operand precisions
+        # alone imply (rounding model); the bar below is the fixed bf16 one
         f = W.to_f64
         q, k, v = oracle.split_qkv(f(inp["mixed_qkv"]), shape.H_k, shape.H_v, shape.d_k, shape.d_v)
         g, beta = oracle.gates(f(inp["a"]), f(inp["b"]), f(inp["A_log"]), f(inp["dt_bias"]))
@@ -247,9 +245,9 @@ def test_chunk_prefill_slow_decay(dtype, keys):
                 o_m[sl, h], S_m[i, h] = chunked_bf16_operands(
                     q[sl, h // r], k[sl, h // r], v[sl, h], g[sl, h], beta[sl, h],
                     f(inp["S0"])[i, h], shape.d_k ** -0.5)
-        e_o, e_S = rel_l2(o_m, o_ref), rel_l2(S_m, S_ref)
-        print(f"\nslow decay, {keys} keys: operand-rounding model o {e_o:.2e}, S {e_S:.2e}")
-        tol_o, tol_S = max(tol_o, 1.2 * e_o), max(tol_S, 1.2 * e_S)
+        print(f"\nslow decay, {keys} keys: operand-rounding model o {rel_l2(o_m, o_ref):.2e}, "
+              f"S {rel_l2(S_m, S_ref):.2e}")
+    tol_o = tol_S = TOL[dtype]
     eo = assert_close("o", host(o), o_ref, tol_o, per_head_axis=1)
     es = assert_close("S_final", host(Sf), S_ref, tol_S, per_head_axis=1)
     print(f"GPU o {eo:.2e}, S {es:.2e}")

@@ -149,6 +149,10 @@ def test_coder_next_varlen_resumed_prefill():
     assert torch.isfinite(r["out"]).all() and torch.isfinite(r["final_state"]).all()
 
 
+# one decode step's output row of one head (128 bf16 values), config-4 tail
+STEP_TOL = 2.5e-2
+
+
 @pytest.mark.slow
 def test_qwen36_27b_long_prefill_ckpts_then_decode():
     w = W.WORKLOADS["qwen36_27b_long"]
@@ -197,11 +201,17 @@ def test_qwen36_27b_long_prefill_ckpts_then_decode():
                 f(inp["A_log"][h:h + 1]), f(inp["dt_bias"][h:h + 1]), f(inp["norm_w"]), 1, 1,
                 s.d_k, s.d_v, S_h, cs_h)
             ref_steps.append(o_ref[0])
-        # rel-L2 per output tensor: this head's 128-step decode output
+        # rel-L2 per output tensor (this head's 128-step decode output) at the
+        # bf16 tolerance, and every single step -- one head's 128-value output
+        # row -- within STEP_TOL: a row carries the bf16 roundings of the conv
+        # output, o and out on its own, and those alone, applied to the
+        # oracle's exact states, put single rows of these two heads at up to
+        # 1.05e-2 and 1.99e-2
         got, ref = host(outs[:, h]), np.stack(ref_steps)
         worst = max(rel_l2(got[t], ref[t]) for t in range(len(ref)))
-        e = assert_close(f"decode out head {h} (worst single step {worst:.2e})", got, ref, tol)
+        e = assert_close(f"decode out head {h}", got, ref, tol)
         print(f"decode head {h}: rel-L2 {e:.2e}, worst single step {worst:.2e}")
+        assert worst <= STEP_TOL, f"decode head {h}: worst single step rel-L2 {worst:.3e} > {STEP_TOL:.1e}"
         assert_close(f"decode S head {h}", host(S[0, h]), S_h[0, 0], tol)
 
 
