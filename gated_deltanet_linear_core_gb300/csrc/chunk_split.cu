@@ -49,7 +49,7 @@ typedef __half f16;
 constexpr int C = 64;
 constexpr int D = 128;
 constexpr uint64_t kWaitNs = 1000000000ull;
-constexpr size_t kSegBytes = 256ull << 20;  // workspace intermediates per segment
+constexpr size_t kSegBytes = 1024ull << 20;  // workspace intermediates per segment
 
 // per (chunk, value head) unit in the workspace
 constexpr size_t U_WT = 16384, U_UT = 16384, U_P = 8192, U_VEC = 1024, U_KD = 16384;
@@ -66,18 +66,23 @@ struct Work {
 };
 
 // Segment size and the places of the intermediates inside one scratch area:
-// chunk offsets, then the per-unit arrays, then the carry.
+// chunk offsets, then the per-unit arrays (two sets when segments alternate
+// between them), then the carry.
 struct Layout {
     int64_t segc;    // chunks per segment
     int64_t n_seg;
-    size_t off_coff, off_units, off_carry, carry_bytes, total;
+    size_t off_coff, off_units, off_units2, off_carry, carry_bytes, total;
+    bool two_bufs() const { return off_units2 != off_units; }
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // seg_bytes bounds the per-segment intermediates; coff_slots is the number of
-// chunk-offset entries reserved (at least n_seq + 1).
-Layout layout_for(int n_seq, int64_t T, int H_v, size_t seg_bytes, size_t coff_slots, bool carry) {
+// chunk-offset entries reserved (at least n_seq + 1); with two_bufs, calls of
+// more than one segment get a second set of intermediates, so that the intra
+// kernel of a segment can run while the chain of the previous one does.
+Layout layout_for(int n_seq, int64_t T, int H_v, size_t seg_bytes, size_t coff_slots, bool carry,
+                  bool two_bufs) {
     Layout L;
     const int64_t max_chunks = T / C + n_seq;
     int64_t segc = (int64_t)(seg_bytes / ((size_t)H_v * UNIT_BYTES));
@@ -88,19 +93,22 @@ Layout layout_for(int n_seq, int64_t T, int H_v, size_t seg_bytes, size_t coff_s
     L.n_seg = (max_chunks + segc - 1) / segc;
     L.off_coff = 0;
     L.off_units = align256(4 * coff_slots);
-    L.off_carry = L.off_units + (size_t)segc * H_v * UNIT_BYTES;
+    const size_t ub = (size_t)segc * H_v * UNIT_BYTES;
+    L.off_units2 = two_bufs && L.n_seg > 1 ? L.off_units + ub : L.off_units;
+    L.off_carry = L.off_units2 + ub;
     L.carry_bytes = carry && L.n_seg > 1 ? (size_t)n_seq * H_v * D * D * 4 : 0;
     L.total = L.off_carry + L.carry_bytes;
     return L;
 }
 
 Layout layout_of(int n_seq, int64_t T, int H_v) {
-    return layout_for(n_seq, T, H_v, kSegBytes, (size_t)n_seq + 1, true);
+    return layout_for(n_seq, T, H_v, kSegBytes, (size_t)n_seq + 1, true, true);
 }
 
-Work work_at(uint8_t* base, const Layout& L, int H_v) {
+// The intermediates of buffer `buf` (0 or 1) of a layout.
+Work work_at(uint8_t* base, const Layout& L, int H_v, int buf = 0) {
     const size_t U = (size_t)L.segc * H_v;
-    uint8_t* un = base + L.off_units;
+    uint8_t* un = base + (buf == 0 ? L.off_units : L.off_units2);
     Work w;
     w.coff = reinterpret_cast<int32_t*>(base + L.off_coff);
     w.wt = reinterpret_cast<bf16*>(un);
@@ -1150,19 +1158,25 @@ int sm_count() {
 // head's state into two 64-column slices when that still leaves at most one
 // CTA per SM.  With a second stream s_pre and an event (one segment only), the
 // offsets and intra kernels run on s_pre and the chain on s after the event,
-// so the caller can overlap them with other work.
-cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cudaStream_t s,
+// so the caller can overlap them with other work.  With two sets of
+// intermediates (w[0], w[1]) and more than one segment, the intra kernels run
+// on a stream of this call, each as soon as the chain two segments earlier is
+// done with its buffer, so that a segment's intra kernel runs on the SMs the
+// previous segment's chain leaves free; events order the two streams.
+cudaError_t run_segments(const DeltaArgs& a, const Work* w, int nbuf, const Layout& Ly, cudaStream_t s,
                          cudaStream_t s_pre = nullptr, cudaEvent_t ev_pre = nullptr) {
     const uint64_t conv_dim = 2ull * a.H_k * D + (uint64_t)a.H_v * D;
     const uint64_t U = (uint64_t)Ly.segc * a.H_v;
     const bool split = (int64_t)a.n_seq * a.H_v * 2 <= sm_count();
-    CUtensorMap qmap, wtmap, utmap, pmap, omap, kdmap;
     constexpr CUtensorMapDataType F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) || !encode2d(&wtmap, w.wt, 128, U * 64, 64, 64) ||
-        !encode2d(&utmap, w.ut, 128, U * 64, 64, 64, F16) || !encode2d(&pmap, w.p, 64, U * 64, 64, 64, F16) ||
-        !encode2d(&kdmap, w.kd, 128, U * 64, 64, 64, F16) ||
+    CUtensorMap qmap, omap, wtmap[2], utmap[2], pmap[2], kdmap[2];
+    if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) ||
         !encode2d(&omap, a.o, (uint64_t)a.H_v * D, (uint64_t)a.T, 64, 64))
         return cudaErrorInvalidValue;
+    for (int i = 0; i < nbuf; ++i)
+        if (!encode2d(&wtmap[i], w[i].wt, 128, U * 64, 64, 64) || !encode2d(&utmap[i], w[i].ut, 128, U * 64, 64, 64, F16) ||
+            !encode2d(&pmap[i], w[i].p, 64, U * 64, 64, 64, F16) || !encode2d(&kdmap[i], w[i].kd, 128, U * 64, 64, 64, F16))
+            return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(chunk_intra_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
@@ -1175,38 +1189,75 @@ cudaError_t run_segments(const DeltaArgs& a, const Work& w, const Layout& Ly, cu
     if (e != cudaSuccess) return e;
 
     const bool two = ev_pre != nullptr && Ly.n_seg == 1;
-    cudaStream_t si = two ? s_pre : s;
+    const bool overlap = ev_pre == nullptr && nbuf == 2 && Ly.n_seg > 1;
     if (ev_pre != nullptr && !two) {
         // more than one segment: everything in order on s, after s_pre's work
         if ((e = cudaEventRecord(ev_pre, s_pre)) != cudaSuccess || (e = cudaStreamWaitEvent(s, ev_pre, 0)) != cudaSuccess)
             return e;
     }
+    // the overlapped schedule's stream and events, released (once their work
+    // is done) when the call returns
+    cudaStream_t aux = nullptr;
+    cudaEvent_t ev_go = nullptr, ev_i[2] = {nullptr, nullptr}, ev_c[2] = {nullptr, nullptr};
+    auto release = [&]() {
+        for (cudaEvent_t ev : {ev_go, ev_i[0], ev_i[1], ev_c[0], ev_c[1]})
+            if (ev != nullptr) cudaEventDestroy(ev);
+        if (aux != nullptr) cudaStreamDestroy(aux);
+    };
+    if (overlap) {
+        e = cudaStreamCreateWithFlags(&aux, cudaStreamNonBlocking);
+        for (cudaEvent_t* ev : {&ev_go, &ev_i[0], &ev_i[1], &ev_c[0], &ev_c[1]})
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            release();
+            return e;
+        }
+    }
+    cudaStream_t si = two ? s_pre : s;
     if (a.cu != nullptr && (e = launch_pdl(chunk_offsets_kernel, dim3(1), dim3(1024), 0, si, a.cu, a.n_seq, a.T,
-                                           w.coff)) != cudaSuccess)
+                                           w[0].coff)) != cudaSuccess) {
+        release();
         return e;
-    for (int64_t seg = 0; seg < Ly.n_seg; ++seg) {
+    }
+    if (overlap) {
+        // the intra kernels start after everything queued on s so far
+        if ((e = cudaEventRecord(ev_go, s)) != cudaSuccess || (e = cudaStreamWaitEvent(aux, ev_go, 0)) != cudaSuccess) {
+            release();
+            return e;
+        }
+        si = aux;
+    }
+    for (int64_t seg = 0; seg < Ly.n_seg && e == cudaSuccess; ++seg) {
         const int64_t C0 = seg * Ly.segc;
+        const int b = overlap ? (int)(seg & 1) : 0;
+        // buffer b was last read by the chain of segment seg - 2
+        if (overlap && seg >= 2 && (e = cudaStreamWaitEvent(aux, ev_c[b], 0)) != cudaSuccess) break;
         if (a.neumann)
             e = launch_pdl(chunk_intra_kernel<true>, dim3((unsigned)a.H_v, (unsigned)Ly.segc), dim3(NT_I), ISMEM, si,
-                           qmap, wtmap, utmap, a, w, C0);
+                           qmap, wtmap[b], utmap[b], a, w[b], C0);
         else
             e = launch_pdl(chunk_intra_kernel<false>, dim3((unsigned)a.H_v, (unsigned)Ly.segc), dim3(NT_I), ISMEM,
-                           si, qmap, wtmap, utmap, a, w, C0);
-        if (e != cudaSuccess) return e;
-        if (two) {
-            if ((e = cudaGetLastError()) != cudaSuccess || (e = cudaEventRecord(ev_pre, si)) != cudaSuccess ||
-                (e = cudaStreamWaitEvent(s, ev_pre, 0)) != cudaSuccess)
-                return e;
+                           si, qmap, wtmap[b], utmap[b], a, w[b], C0);
+        if (e != cudaSuccess) break;
+        if (two || overlap) {
+            cudaEvent_t ev = two ? ev_pre : ev_i[b];
+            if ((e = cudaGetLastError()) != cudaSuccess || (e = cudaEventRecord(ev, si)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(s, ev, 0)) != cudaSuccess)
+                break;
         }
         if (split)
             e = launch_pdl(chunk_chain_kernel<64>, dim3((unsigned)(a.n_seq * a.H_v * 2)), dim3(NT_C),
-                           ChainLayout<64>::SMEM, s, qmap, wtmap, utmap, pmap, omap, kdmap, a, w, C0, Ly.segc);
+                           ChainLayout<64>::SMEM, s, qmap, wtmap[b], utmap[b], pmap[b], omap, kdmap[b], a, w[b], C0,
+                           Ly.segc);
         else
             e = launch_pdl(chunk_chain_kernel<128>, dim3((unsigned)(a.n_seq * a.H_v)), dim3(NT_C),
-                           ChainLayout<128>::SMEM, s, qmap, wtmap, utmap, pmap, omap, kdmap, a, w, C0, Ly.segc);
-        if (e != cudaSuccess) return e;
+                           ChainLayout<128>::SMEM, s, qmap, wtmap[b], utmap[b], pmap[b], omap, kdmap[b], a, w[b], C0,
+                           Ly.segc);
+        if (e != cudaSuccess) break;
+        if (overlap && (e = cudaEventRecord(ev_c[b], s)) != cudaSuccess) break;
     }
-    return cudaGetLastError();
+    release();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -1222,9 +1273,13 @@ int chunk_split_launches(int n_seq, int64_t T, int H_v, bool has_cu) {
 cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s) {
     const Layout Ly = layout_of(a.n_seq, a.T, a.H_v);
     if (workspace == nullptr || ws_bytes < Ly.total) return cudaErrorInvalidValue;
-    Work w = work_at(static_cast<uint8_t*>(workspace), Ly, a.H_v);
-    if (a.S_final != nullptr) w.carry = a.S_final;
-    return run_segments(a, w, Ly, s);
+    Work w[2];
+    const int nbuf = Ly.two_bufs() ? 2 : 1;
+    for (int i = 0; i < nbuf; ++i) {
+        w[i] = work_at(static_cast<uint8_t*>(workspace), Ly, a.H_v, i);
+        if (a.S_final != nullptr) w[i].carry = a.S_final;
+    }
+    return run_segments(a, w, nbuf, Ly, s);
 }
 
 cudaError_t launch_chunk_split_two(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s_pre,
@@ -1233,7 +1288,7 @@ cudaError_t launch_chunk_split_two(const DeltaArgs& a, void* workspace, size_t w
     if (workspace == nullptr || ws_bytes < Ly.total || ev_pre == nullptr) return cudaErrorInvalidValue;
     Work w = work_at(static_cast<uint8_t*>(workspace), Ly, a.H_v);
     if (a.S_final != nullptr) w.carry = a.S_final;
-    return run_segments(a, w, Ly, s_chain, s_pre, ev_pre);
+    return run_segments(a, &w, 1, Ly, s_chain, s_pre, ev_pre);
 }
 
 namespace {
@@ -1289,7 +1344,7 @@ unsigned long long g_scratch_ctx[128];   // ... valid in the context with this i
 
 Layout static_layout(int n_seq, int64_t T, int H_v) {
     return layout_for(n_seq, T, H_v, kStaticScratchBytes - align256(4 * ((size_t)kStaticMaxSeq + 1)) - 256,
-                      (size_t)kStaticMaxSeq + 1, false);
+                      (size_t)kStaticMaxSeq + 1, false, false);
 }
 
 }  // namespace
@@ -1297,7 +1352,7 @@ Layout static_layout(int n_seq, int64_t T, int H_v) {
 bool chunk_split_static_fits(int n_seq, int H_v) {
     if (n_seq < 1 || n_seq > kStaticMaxSeq) return false;
     // one chunk per segment must fit
-    const Layout L = layout_for(n_seq, 0, H_v, 0, (size_t)kStaticMaxSeq + 1, false);
+    const Layout L = layout_for(n_seq, 0, H_v, 0, (size_t)kStaticMaxSeq + 1, false, false);
     return L.off_units + (size_t)H_v * UNIT_BYTES <= kStaticScratchBytes;
 }
 
@@ -1330,7 +1385,7 @@ cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s) {
     if (Ly.total > kStaticScratchBytes) return cudaErrorInvalidValue;
     Work w = work_at(base, Ly, a.H_v);
     w.carry = a.S_final;
-    return run_segments(a, w, Ly, s);
+    return run_segments(a, &w, 1, Ly, s);
 }
 
 }  // namespace gdn

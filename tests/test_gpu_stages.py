@@ -546,3 +546,44 @@ def test_decode_verify_equals_successive_fused_steps(dtype, shape, K):
     others = [i for i in range(n_slots) if i not in slots.flatten().tolist()]
     assert torch.equal(S_v[others].cpu(), S_all[others])
     assert torch.equal(cs_v[others].cpu(), cs_all[others])
+
+
+def test_overlapped_segments_equal_sequential_segments():
+    """A call long enough for more than one workspace segment runs each
+    segment's intra kernel beside the previous segment's chain (two sets of
+    intermediates, a stream of the call's own).  Its outputs, final states and
+    checkpoints must equal, bit for bit, those of the no-allocation call, which
+    runs the same kernels one small segment after another; one value head is
+    also checked against the oracle."""
+    shape = W.QWEN36_27B
+    lengths = [20000, 13001]
+    inp = _delta_inputs(shape, torch.bfloat16, lengths, seed=23)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    dims = _dims(shape)
+    T, N = sum(lengths), len(lengths)
+    assert gdn.gdn_chunk_prefill_launches(N, T, dims, torch.bfloat16) > 3, "expected several segments"
+    rows = gdn.gdn_ckpt_count(inp["cu_seqlens"], 4096)
+    sdims = (shape.H_v, shape.d_k, shape.d_v)
+    S1, ck1 = torch.empty((N,) + sdims, device="cuda"), torch.empty((rows,) + sdims, device="cuda")
+    o1 = gdn.gdn_chunk_prefill(d["mixed_qkv"], dims, d["a"], d["b"], d["A_log"], d["dt_bias"],
+                               cu_seqlens=d["cu_seqlens"], initial_state=d["S0"], final_state=S1,
+                               ckpt_every=4096, state_ckpt_out=ck1)
+    o2 = torch.empty_like(o1)
+    S2, ck2 = torch.empty_like(S1), torch.empty_like(ck1)
+    gdn.gdn_chunk_prefill_noalloc(d["mixed_qkv"], dims, o2, S2, d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                  cu_seqlens=d["cu_seqlens"], initial_state=d["S0"], ckpt_every=4096,
+                                  state_ckpt_out=ck2)
+    gdn.gdn_sync_status()
+    assert torch.equal(o1, o2) and torch.equal(S1, S2) and torch.equal(ck1, ck2)
+    f = W.to_f64
+    h = 7
+    q, k, v = oracle.split_qkv(f(inp["mixed_qkv"]), shape.H_k, shape.H_v, shape.d_k, shape.d_v)
+    g, beta = oracle.gates(f(inp["a"]), f(inp["b"]), f(inp["A_log"]), f(inp["dt_bias"]))
+    r = shape.H_v // shape.H_k
+    o_h, S_h, ck_h = oracle.delta_rule(q[:, h // r:h // r + 1], k[:, h // r:h // r + 1], v[:, h:h + 1],
+                                       g[:, h:h + 1], beta[:, h:h + 1], inp["cu_seqlens"].numpy(),
+                                       f(inp["S0"])[:, h:h + 1], None, True, 4096)
+    tol = TOL[torch.bfloat16]
+    assert_close("o", host(o1[:, h]), o_h[:, 0], tol)
+    assert_close("S", host(S1[:, h]), S_h[:, 0], tol)
+    assert_close("ckpt", host(ck1[:, h]), ck_h[:, 0], tol)
