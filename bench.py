@@ -417,6 +417,38 @@ def run_ours(args):
     conv_ms = [e[0].elapsed_time(e[1]) for e in sev]
     chunk_ms = [e[1].elapsed_time(e[2]) for e in sev]
     norm_ms = [e[2].elapsed_time(e[3]) for e in sev]
+
+    # the conv and RMSNormGated calls alone, each with the L2 flushed right
+    # before it (in the staged pass the norm reads o straight after the chunk
+    # kernel wrote it, much of it from L2): their HBM rooflines
+    def alone(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        torch.cuda.synchronize(dev)
+        clocks.mark(True)
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            fn()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        clocks.mark(False)
+        return statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev) / 1e3
+
+    conv_alone = alone(lambda: gdn.gdn_conv1d_fwd(d["mixed_qkv"], d["conv_w"], dims, None, None, conv_out, y=y))
+    norm_alone = alone(lambda: gdn.gdn_rmsnorm_gated(o, d["z"], d["norm_w"], dims, out=out))
+    launches += 2 * args.steps
+    # algorithmic bytes: conv reads x and writes y (2 B each per channel-token)
+    # plus the conv state out; the norm reads o and z and writes out
+    conv_bytes = T * s.conv_dim * 2 * 2 + s.conv_dim * 3 * 2
+    norm_bytes = T * s.H_v * s.d_v * 2 * 3
+    hbm_alone = {
+        kname: {"kernel": kname, "bound": "hbm", "ms": round(t * 1e3, 4),
+                "achieved": round(nb / t / 1e9, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(nb / t / 1e9 / pk["hbm_gbs"], 4), "algorithmic_bytes_per_launch": nb,
+                "l2": "flushed right before the call"}
+        for kname, t, nb in (("gdn_conv1d_fwd", conv_alone, conv_bytes),
+                             ("gdn_rmsnorm_gated", norm_alone, norm_bytes))}
     total_s = max_over_ranks(dist, sum(step_ms) / 1e3, dev)
     value = world * T * args.calls * args.steps / total_s
     chunk_avg = sum(chunk_ms) / len(chunk_ms) / 1e3
@@ -722,6 +754,7 @@ def run_ours(args):
                               "chunk_prefill": round(statistics.mean(chunk_ms), 4),
                               "rmsnorm_gated": round(statistics.mean(norm_ms), 4)},
             "roofline": roofline,
+            "hbm_kernels": hbm_alone,
             "prefill_workloads": workloads,
             "decode": decode,
             "e2e": e2e,
