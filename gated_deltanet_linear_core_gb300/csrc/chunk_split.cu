@@ -713,13 +713,14 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 //   S <- e^{G_n} S + dS   (f32 in registers; bf16 operand for the next MMA1)
 //   MMA3  P U'            M = 128 (P and 64 rows of padding), N = VS, K = j (fp16)
 //   O = (Q S) diag(e^G rq) + P U'  (q-row lanes, stored straight to global)
-// Warp roles: 16 compute warps, one warp that issues the MMAs and one that
-// issues the TMA copies; they hand work to each other through mbarriers, so
-// the copies, the O epilogue and the P U' product run off the state's
-// critical path (MMA1 -> U' -> MMA2 -> S update -> next MMA1).
+// Warp roles: 16 compute warps, one warp that issues the MMAs, one that
+// issues the TMA loads and one that stores each chunk's O tile; they hand work
+// to each other through mbarriers, so the copies, the O epilogue and the P U'
+// product run off the state's critical path (MMA1 -> U' -> MMA2 -> S update ->
+// next MMA1).
 constexpr int NT_COMP = 512;
-constexpr int NT_C = NT_COMP + 64;
-constexpr int W_MMA = NT_COMP / 32, W_TMA = W_MMA + 1;
+constexpr int NT_C = NT_COMP + 96;
+constexpr int W_MMA = NT_COMP / 32, W_TMA = W_MMA + 1, W_ST = W_MMA + 2;
 
 template <int VS>
 struct ChainLayout {
@@ -736,7 +737,7 @@ struct ChainLayout {
     static constexpr int CS_UP = CS_STAGE + NST * STAGE;  // U' [j][v] fp16, NB blocks of 8 KB
     static constexpr int CS_VEC = CS_UP + NB * 8192;    // the stages' vectors, NST x VEC
     static constexpr int CS_BAR = CS_VEC + NST * VEC;
-    static constexpr int SMEM = CS_BAR + 128 + 1024;    // 15 barrier / flag words
+    static constexpr int SMEM = CS_BAR + 192 + 1024;    // 18 barrier / flag words
     // TMEM: two buffers of [Q S; W S], dS, and OPB buffers of P U' (two when they
     // fit: the next chunk's P U' then needs no wait for this chunk's O epilogue)
     static constexpr int OPB = 5 * VS <= 512 ? 2 : 1;
@@ -828,6 +829,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     uint64_t* o_done = bars + 11; // [2] O epilogue's TMEM reads of a P U' buffer done (8 q-row warps)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 13);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14);
+    uint64_t* o_staged = bars + 15;  // [NST] the stage's O tile staged (8 q-row warps)
     auto stage_of = [&](int k) { return sm + Ly::CS_STAGE + (k % NST) * Ly::STAGE; };
     auto vec_of = [&](int k) { return sm + Ly::CS_VEC + (k % NST) * Ly::VEC; };
 
@@ -841,6 +843,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         mbar_init(u_rdy, NT_COMP / 32);
         mbar_init(&o_done[0], NT_COMP / 64);
         mbar_init(&o_done[1], NT_COMP / 64);
+        for (int i = 0; i < NST; ++i) mbar_init(&o_staged[i], NT_COMP / 64);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -882,6 +885,26 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             if (*abort_flag)
                 for (int k = issued - NST > 0 ? issued - NST : 0; k < issued; ++k)
                     mbar_wait(&full[k % NST], (uint32_t)((k / NST) & 1), kWaitNs);
+        }
+    } else if (warp == W_ST) {
+        // ------------------------------------------------ O stores (lane 0)
+        // once the 8 q-row warps have staged a full chunk's O tile, store it
+        // by TMA; the stage is released when the store has read it
+        if (lane == 0) {
+            for (int k = 0; k < nch; ++k) {
+                if (!mbar_wait_or_abort(&o_staged[k % NST], (uint32_t)((k / NST) & 1), abort_flag)) break;
+                const int64_t lc = c_lo + k - cs;
+                if (L - lc * C >= C) {
+                    uint8_t* otile = stage_of(k) + Ly::SG_P;
+#pragma unroll
+                    for (int nb = 0; nb < Ly::NB; ++nb)
+                        tma_store_2d(&omap, otile + nb * 8192, h * D + v0 + 64 * nb, (int)(s0 + lc * C));
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
+                mbar_arrive(&empty[k % NST]);
+            }
+            bulk_wait_all();  // O stores complete before the CTA exits
         }
     } else if (warp == W_MMA) {
         // ------------------------------------------------ MMA issuer (lane 0)
@@ -1054,18 +1077,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 fence_async_smem();
                 const int ob = Ly::OPB == 2 ? b : 0;
                 warp_arrive(&o_done[ob], lane);
-                // thread 0 stores the tile once all 8 q-row warps have staged it
-                if (tid == 0 && mbar_wait_or_abort(&o_done[ob], (uint32_t)((k / Ly::OPB) & 1), abort_flag)) {
-                    if (n == C) {
-                        uint8_t* otile = st + Ly::SG_P;
-#pragma unroll
-                        for (int nb = 0; nb < Ly::NB; ++nb)
-                            tma_store_2d(&omap, otile + nb * 8192, h * D + v0 + 64 * nb, (int)t0);
-                        bulk_commit();
-                        bulk_wait_read_all();
-                    }
-                    mbar_arrive(&empty[k % NST]);
-                }
+                if (lane == 0) mbar_arrive(&o_staged[k % NST]);
             }
         }
         if (!*abort_flag) {
@@ -1078,7 +1090,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             }
         }
     }
-    if (tid == 0) bulk_wait_all();  // O stores complete before the CTA exits
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && *abort_flag) atomicOr(&g_device_error, 1);
