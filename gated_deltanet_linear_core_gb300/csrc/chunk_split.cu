@@ -62,6 +62,7 @@ struct Work {
     float* vec;     // [U][256]: e^G rq (0..63), e^{G_n-G_j} rk (64..127), e^{G_n} (128)
     f16* kd;        // K_dec, [U][64][128] (row j = e^{G_n-G_j} rk_j k_j), fp16
     int32_t* coff;  // [n_seq + 1] chunk offsets
+    int32_t* order; // [n_seq] the sequences, most chunks first (null: in order)
     float* carry;   // state between segments (final_state or workspace), may be null
 };
 
@@ -71,18 +72,19 @@ struct Work {
 struct Layout {
     int64_t segc;    // chunks per segment
     int64_t n_seg;
-    size_t off_coff, off_units, off_units2, off_carry, carry_bytes, total;
+    size_t off_coff, off_order, off_units, off_units2, off_carry, carry_bytes, total;
     bool two_bufs() const { return off_units2 != off_units; }
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // seg_bytes bounds the per-segment intermediates; coff_slots is the number of
-// chunk-offset entries reserved (at least n_seq + 1); with two_bufs, calls of
+// chunk-offset entries reserved (at least n_seq + 1), followed by n_seq slots
+// of the sequences' order when `order` is set; with two_bufs, calls of
 // more than one segment get a second set of intermediates, so that the intra
 // kernel of a segment can run while the chain of the previous one does.
 Layout layout_for(int n_seq, int64_t T, int H_v, size_t seg_bytes, size_t coff_slots, bool carry,
-                  bool two_bufs) {
+                  bool two_bufs, bool order = false) {
     Layout L;
     const int64_t max_chunks = T / C + n_seq;
     int64_t segc = (int64_t)(seg_bytes / ((size_t)H_v * UNIT_BYTES));
@@ -92,7 +94,8 @@ Layout layout_for(int n_seq, int64_t T, int H_v, size_t seg_bytes, size_t coff_s
     L.segc = segc;
     L.n_seg = (max_chunks + segc - 1) / segc;
     L.off_coff = 0;
-    L.off_units = align256(4 * coff_slots);
+    L.off_order = order ? 4 * coff_slots : 0;
+    L.off_units = align256(4 * (coff_slots + (order ? (size_t)n_seq : 0)));
     const size_t ub = (size_t)segc * H_v * UNIT_BYTES;
     L.off_units2 = two_bufs && L.n_seg > 1 ? L.off_units + ub : L.off_units;
     L.off_carry = L.off_units2 + ub;
@@ -102,7 +105,7 @@ Layout layout_for(int n_seq, int64_t T, int H_v, size_t seg_bytes, size_t coff_s
 }
 
 Layout layout_of(int n_seq, int64_t T, int H_v) {
-    return layout_for(n_seq, T, H_v, kSegBytes, (size_t)n_seq + 1, true, true);
+    return layout_for(n_seq, T, H_v, kSegBytes, (size_t)n_seq + 1, true, true, true);
 }
 
 // The intermediates of buffer `buf` (0 or 1) of a layout.
@@ -111,6 +114,7 @@ Work work_at(uint8_t* base, const Layout& L, int H_v, int buf = 0) {
     uint8_t* un = base + (buf == 0 ? L.off_units : L.off_units2);
     Work w;
     w.coff = reinterpret_cast<int32_t*>(base + L.off_coff);
+    w.order = L.off_order ? reinterpret_cast<int32_t*>(base + L.off_order) : nullptr;
     w.wt = reinterpret_cast<bf16*>(un);
     w.ut = reinterpret_cast<f16*>(un + U * U_WT);
     w.p = reinterpret_cast<f16*>(un + U * (U_WT + U_UT));
@@ -120,9 +124,12 @@ Work work_at(uint8_t* base, const Layout& L, int H_v, int buf = 0) {
     return w;
 }
 
-// coff[i] = number of chunks of sequences 0..i-1 (one block, any n_seq)
+// coff[i] = number of chunks of sequences 0..i-1 (one block, any n_seq); with
+// `order`, also the sequences sorted by chunk count, most first (ties in
+// sequence order; up to 1024 sequences, else in order), so that the chain
+// kernel starts the longest sequences' CTAs first
 __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, int n_seq, int64_t T,
-                                                             int32_t* coff) {
+                                                             int32_t* coff, int32_t* order) {
     pdl_wait();
     pdl_trigger();
     __shared__ int32_t wsum[32];
@@ -164,6 +171,20 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, 
         __syncthreads();
         if (tid == 1023) base += incl;
         __syncthreads();
+    }
+    if (order == nullptr) return;
+    __shared__ int32_t len[1024];
+    if (n_seq > 1024) {
+        for (int i = tid; i < n_seq; i += 1024) order[i] = i;
+        return;
+    }
+    if (tid < n_seq) len[tid] = coff[tid + 1] - coff[tid];
+    __syncthreads();
+    if (tid < n_seq) {
+        const int li = len[tid];
+        int rank = 0;
+        for (int j = 0; j < n_seq; ++j) rank += (len[j] > li) || (len[j] == li && j < tid);
+        order[rank] = tid;
     }
 }
 
@@ -790,7 +811,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     constexpr int NV = D / VS, CV = VS / 4;
     const int vp = blockIdx.x % NV;
     const int h = (blockIdx.x / NV) % a.H_v;
-    const int seq = blockIdx.x / (NV * a.H_v);
+    const int seq_rank = blockIdx.x / (NV * a.H_v);  // CTAs start in this order: longest sequences first
+    const int seq = a.cu != nullptr && w.order != nullptr ? w.order[seq_rank] : seq_rank;
     const int v0 = vp * VS;
     // chunk offsets of the sequence (one sequence without offsets: [0, ceil(T / C)))
     const int64_t cs = a.cu == nullptr ? 0 : w.coff[seq];
@@ -1226,7 +1248,7 @@ cudaError_t run_segments(const DeltaArgs& a, const Work* w, int nbuf, const Layo
     }
     cudaStream_t si = two ? s_pre : s;
     if (a.cu != nullptr && (e = launch_pdl(chunk_offsets_kernel, dim3(1), dim3(1024), 0, si, a.cu, a.n_seq, a.T,
-                                           w[0].coff)) != cudaSuccess) {
+                                           w[0].coff, w[0].order)) != cudaSuccess) {
         release();
         return e;
     }
