@@ -335,7 +335,8 @@ def gdn_layer_prefill(mixed_qkv, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, 
                       final_state=None, conv_state_out=None, workspace=None, solve="direct", chunk=64,
                       state_ckpt_out=None, conv_ckpt_out=None):
     """Whole layer core over packed sequences: conv1d+SiLU -> chunked delta rule
-    -> RMSNormGated, as one gdn_layer_prefill call.  Returns a dict with out
+    -> RMSNormGated, as one gdn_layer_prefill call (bf16, d = 128: the conv
+    inside the chunk kernels).  Returns a dict with out
     [T, H_v*d_v], final_state [n_seq, H_v, d_k, d_v] f32, conv_state
     [n_seq, conv_dim, 3] and, when ckpt_every > 0, state_ckpt / conv_ckpt.
     return_intermediates=True runs the three calls one by one instead and adds

@@ -25,6 +25,12 @@
 // |x| in [2^-14, 65504]); the products with the raw bf16 q (D1, [Q; W] S)
 // stay bf16.  This keeps the state's rounding error well inside the bf16
 // tolerance when decay is slow and the state carries across many chunks.
+// The intra kernel can also compute the layer's conv1d + SiLU itself (cortex
+// "Block": depthwise causal conv, k = 4, then SiLU): it then loads raw x tiles
+// with their 3-token halo, convolves them in place in shared memory with the
+// conv kernel's own arithmetic (so y is the same bit for bit), and stores the
+// conv'd q tile of each key head to the workspace for the chain; y never goes
+// to HBM.
 // The chunks of a call are processed in segments (a range of chunk indices
 // over all sequences) whose intermediates fit in the workspace and, at the
 // default size, in L2; the state crosses segments through final_state (or a
@@ -54,6 +60,8 @@ constexpr size_t kSegBytes = 1024ull << 20;  // workspace intermediates per segm
 // per (chunk, value head) unit in the workspace
 constexpr size_t U_WT = 16384, U_UT = 16384, U_P = 8192, U_VEC = 1024, U_KD = 16384;
 constexpr size_t UNIT_BYTES = U_WT + U_UT + U_P + U_VEC + U_KD;
+// per (chunk, key head), with the conv inside the kernels: the conv'd q tile
+constexpr size_t U_Q = 16384;
 
 struct Work {
     bf16* wt;       // W, [U][64][128] (row i of W = 128 d-values)
@@ -64,6 +72,7 @@ struct Work {
     int32_t* coff;  // [n_seq + 1] chunk offsets
     int32_t* order; // [n_seq] the sequences, most chunks first (null: in order)
     float* carry;   // state between segments (final_state or workspace), may be null
+    bf16* q;        // conv'd q, [segc][H_k][64][128] (conv inside the kernels; else null: q from qkv)
 };
 
 // Segment size and the places of the intermediates inside one scratch area:
@@ -72,6 +81,7 @@ struct Work {
 struct Layout {
     int64_t segc;    // chunks per segment
     int64_t n_seg;
+    int q_heads;     // key heads of the conv'd q tiles after each set of units (0: none)
     size_t off_coff, off_order, off_units, off_units2, off_carry, carry_bytes, total;
     bool two_bufs() const { return off_units2 != off_units; }
 };
@@ -83,8 +93,11 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // of the sequences' order when `order` is set; with two_bufs, calls of
 // more than one segment get a second set of intermediates, so that the intra
 // kernel of a segment can run while the chain of the previous one does.
+// With q_heads > 0 each set of units is followed by the segment's conv'd q
+// tiles (segc x q_heads x U_Q; not counted in seg_bytes, so the segments are
+// those of the call without them).
 Layout layout_for(int n_seq, int64_t T, int H_v, size_t seg_bytes, size_t coff_slots, bool carry,
-                  bool two_bufs, bool order = false) {
+                  bool two_bufs, bool order = false, int q_heads = 0) {
     Layout L;
     const int64_t max_chunks = T / C + n_seq;
     int64_t segc = (int64_t)(seg_bytes / ((size_t)H_v * UNIT_BYTES));
@@ -93,10 +106,11 @@ Layout layout_for(int n_seq, int64_t T, int H_v, size_t seg_bytes, size_t coff_s
     if (segc > 65535) segc = 65535;  // grid.y of the intra kernel
     L.segc = segc;
     L.n_seg = (max_chunks + segc - 1) / segc;
+    L.q_heads = q_heads;
     L.off_coff = 0;
     L.off_order = order ? 4 * coff_slots : 0;
     L.off_units = align256(4 * (coff_slots + (order ? (size_t)n_seq : 0)));
-    const size_t ub = (size_t)segc * H_v * UNIT_BYTES;
+    const size_t ub = (size_t)segc * ((size_t)H_v * UNIT_BYTES + (size_t)q_heads * U_Q);
     L.off_units2 = two_bufs && L.n_seg > 1 ? L.off_units + ub : L.off_units;
     L.off_carry = L.off_units2 + ub;
     L.carry_bytes = carry && L.n_seg > 1 ? (size_t)n_seq * H_v * D * D * 4 : 0;
@@ -104,8 +118,8 @@ Layout layout_for(int n_seq, int64_t T, int H_v, size_t seg_bytes, size_t coff_s
     return L;
 }
 
-Layout layout_of(int n_seq, int64_t T, int H_v) {
-    return layout_for(n_seq, T, H_v, kSegBytes, (size_t)n_seq + 1, true, true, true);
+Layout layout_of(int n_seq, int64_t T, int H_v, int q_heads = 0) {
+    return layout_for(n_seq, T, H_v, kSegBytes, (size_t)n_seq + 1, true, true, true, q_heads);
 }
 
 // The intermediates of buffer `buf` (0 or 1) of a layout.
@@ -120,6 +134,7 @@ Work work_at(uint8_t* base, const Layout& L, int H_v, int buf = 0) {
     w.p = reinterpret_cast<f16*>(un + U * (U_WT + U_UT));
     w.vec = reinterpret_cast<float*>(un + U * (U_WT + U_UT + U_P));
     w.kd = reinterpret_cast<f16*>(un + U * (U_WT + U_UT + U_P + U_VEC));
+    w.q = L.q_heads > 0 ? reinterpret_cast<bf16*>(un + U * UNIT_BYTES) : nullptr;
     w.carry = L.carry_bytes ? reinterpret_cast<float*>(base + L.off_carry) : nullptr;
     return w;
 }
@@ -228,17 +243,21 @@ __device__ __forceinline__ float select_lane(const float (&v)[32], int lane) {
     return (lane & 1) ? d[1] : d[0];
 }
 
-template <bool NEUMANN>
+// qmap covers qkv (y, or the raw x with CONV); qsmap, with CONV, the
+// segment's conv'd q tiles in the workspace.
+template <bool NEUMANN, bool CONV>
 __global__ void __launch_bounds__(NT_I, 3)
 chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
-                   const __grid_constant__ CUtensorMap umap, DeltaArgs a, Work w, int64_t C0) {
+                   const __grid_constant__ CUtensorMap umap, const __grid_constant__ CUtensorMap qsmap,
+                   DeltaArgs a, Work w, int64_t C0) {
     pdl_wait();
     pdl_trigger();
     const int h = blockIdx.x;
     const int64_t gc = C0 + blockIdx.y;
-    // first token and length of chunk gc (no loads for one sequence without offsets)
-    int64_t t0;
-    int n;
+    // first token and length of chunk gc, its sequence and that sequence's
+    // first and end tokens (no loads for one sequence without offsets)
+    int64_t t0, s0 = 0, s1 = a.T;
+    int n, seq = 0;
     if (a.cu == nullptr) {
         t0 = gc * C;
         if (t0 >= a.T) return;  // past the last chunk of the call
@@ -250,8 +269,8 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             const int mid = (lo_s + hi_s + 1) >> 1;
             if ((int64_t)w.coff[mid] <= gc) lo_s = mid; else hi_s = mid - 1;
         }
-        int64_t s0, s1;
         seq_bounds(a.cu, lo_s, a.T, s0, s1);
+        seq = lo_s;
         t0 = s0 + (gc - w.coff[lo_s]) * C;
         n = (int)(s1 - t0 < C ? s1 - t0 : C);
     }
@@ -287,7 +306,8 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         mbar_init(bar_mma, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(bar_tma, 6 * 8192);
-        const int y = (int)t0;
+        // with CONV, tile row j holds token t0 - 3 + j (rows before token 0 read as zeros)
+        const int y = CONV ? (int)t0 - 3 : (int)t0;
         tma_load_2d(kq, &qmap, bar_tma, xk, y);
         tma_load_2d(kq + 16384, &qmap, bar_tma, xk + 64, y);
         tma_load_2d(kq + 8192, &qmap, bar_tma, xq, y);
@@ -298,6 +318,31 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     if (warp == 0) {
         tmem_alloc(tslot, TI_COLS);
         tmem_relinquish();
+    }
+    // CONV: threads 0-191 each take 8 channels (16-byte column cc of 64-channel
+    // block cb: K, K, Q, Q, V, V halves) of 16 rows [16 rg, 16 rg + 16); their
+    // taps are fetched into L1 and, for the last row group, the 3 raw inputs
+    // past the tile (tokens t0 + 61 .. t0 + 63) loaded while the tile is in flight
+    const int conv_dim = 2 * a.H_k * D + a.H_v * D;
+    const int rg = tid / 48, cb = (tid % 48) >> 3, cc = tid & 7;
+    const bool cthr = tid < 192;
+    const int cch = (cb < 2 ? xk : (cb < 4 ? xq : xv)) + (cb & 1) * 64 + cc * 8;
+    uint8_t* cblk = cb < 4 ? kq + (cb & 1) * 16384 + (cb >> 1) * 8192 : vv + (cb & 1) * 8192;
+    const uint4* tap_src = reinterpret_cast<const uint4*>(static_cast<const bf16*>(a.conv_w) + (int64_t)cch * 4);
+    uint4 look[3];
+    if constexpr (CONV) {
+        if (cthr) {
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(tap_src));
+            if (rg == 3) {
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int64_t t = t0 + 61 + j;
+                    look[j] = t < a.T ? *reinterpret_cast<const uint4*>(static_cast<const bf16*>(a.qkv) +
+                                                                        t * conv_dim + cch)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        }
     }
     if (warp == 1) {
         // beta = sigmoid(b) and g = -exp(A_log) softplus(a + dt_bias) of tokens
@@ -348,6 +393,152 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     tc_fence_after();
     const uint32_t tb = *tslot;
     bool ok = __syncthreads_and(mbar_wait(bar_tma, 0, kWaitNs));
+    if constexpr (CONV) {
+        // y = silu(conv(x)) in place: output row r (token t0 + r) takes tile
+        // rows r .. r + 3 and overwrites row r, which no later output of the
+        // same thread reads; the first rows another thread overwrites are read
+        // before the barrier
+        if (ok && cthr && rg < 3) {
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+                look[j] = *reinterpret_cast<const uint4*>(cblk + sw128_off(16 * rg + 16 + j, 8 * cc));
+        }
+        __syncthreads();
+        if (ok && rg == 4 && (cb >= 4 || h % (a.H_v / a.H_k) == 0)) {
+            // meanwhile threads 192-239, one per column: the conv state after the
+            // sequence and the conv checkpoints in this chunk, for the CTA's V
+            // channels and, in the first value head of the key head, its K and Q
+            // ones -- the 3 raw inputs ending at the sequence's last token, or at
+            // its token m ckpt_every - 1 ([channel][3], bit copies, as the conv
+            // kernels write them; inputs before the sequence from conv_state0)
+            const uint16_t* xs = static_cast<const uint16_t*>(a.qkv);
+            auto write3 = [&](int64_t last, uint16_t* dst) {
+                uint16_t v[24];
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int64_t p = last - 2 + j;
+                    if (p >= s0) {
+                        const uint4 r = *reinterpret_cast<const uint4*>(xs + p * conv_dim + cch);
+                        const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) v[3 * q + j] = (uint16_t)(wv[q >> 1] >> (16 * (q & 1)));
+                    } else {
+                        const uint16_t* st = static_cast<const uint16_t*>(a.conv_state0);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            v[3 * q + j] = st != nullptr ? st[((int64_t)seq * conv_dim + cch + q) * 3 + 3 - (s0 - p)] : 0;
+                    }
+                }
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                for (int i = 0; i < 3; ++i)
+                    d4[i] = make_uint4(v[8 * i] | (uint32_t)v[8 * i + 1] << 16, v[8 * i + 2] | (uint32_t)v[8 * i + 3] << 16,
+                                       v[8 * i + 4] | (uint32_t)v[8 * i + 5] << 16, v[8 * i + 6] | (uint32_t)v[8 * i + 7] << 16);
+            };
+            if (a.conv_state_out != nullptr && t0 + n == s1)
+                write3(s1 - 1, static_cast<uint16_t*>(a.conv_state_out) + ((int64_t)seq * conv_dim + cch) * 3);
+            if (a.conv_ckpt != nullptr && a.ckpt_every > 0) {
+                const int64_t N = a.ckpt_every;
+                int64_t row0 = -1;
+                for (int64_t m = (t0 - s0) / N + 1; s0 + m * N - 1 < t0 + n; ++m) {
+                    if (s0 + m * N - 1 < t0) continue;
+                    if (row0 < 0) row0 = ckpt_row0(a.cu, seq, a.T, a.ckpt_every);
+                    if (row0 + m - 1 >= a.ckpt_rows) break;
+                    write3(s0 + m * N - 1,
+                           static_cast<uint16_t*>(a.conv_ckpt) + ((row0 + m - 1) * conv_dim + cch) * 3);
+                }
+            }
+        }
+        if (ok && cthr) {
+            // two passes of 4 channels (8 bytes of each row's 16); each
+            // channel's arithmetic is the conv kernel's
+#pragma unroll 1
+            for (int p = 0; p < 2; ++p) {
+                float2 taps[2][4];
+                {
+                    const uint4 raw[2] = {tap_src[2 * p], tap_src[2 * p + 1]};
+                    conv_taps_bf16_2(raw, taps);
+                }
+                auto row4 = [&](int r, float* x) {  // channels 4p .. 4p + 3 of tile row r
+                    const uint2 v = *reinterpret_cast<const uint2*>(cblk + sw128_off(r, 8 * cc) + 8 * p);
+                    x[0] = __uint_as_float(v.x << 16);
+                    x[1] = __uint_as_float(v.x & 0xffff0000u);
+                    x[2] = __uint_as_float(v.y << 16);
+                    x[3] = __uint_as_float(v.y & 0xffff0000u);
+                };
+                float x0[4], x1[4], x2[4], x3[4];
+                if (rg == 0 && t0 == s0) {
+                    // a sequence's first chunk: the inputs before it are its conv
+                    // state ([conv_dim][3], column 0 oldest), or zeros
+                    float st[12];
+                    if (a.conv_state0 != nullptr) {
+                        const bf16* sp = static_cast<const bf16*>(a.conv_state0) +
+                                         ((int64_t)seq * conv_dim + cch + 4 * p) * 3;
+#pragma unroll
+                        for (int i = 0; i < 12; ++i) st[i] = to_f(sp[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 12; ++i) st[i] = 0.f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        x0[q] = st[3 * q];
+                        x1[q] = st[3 * q + 1];
+                        x2[q] = st[3 * q + 2];
+                    }
+                } else {
+                    row4(16 * rg, x0);
+                    row4(16 * rg + 1, x1);
+                    row4(16 * rg + 2, x2);
+                }
+                // four rows at a time: the inputs r + 3 .. r + 6 are read before
+                // the outputs r .. r + 3 are written
+#pragma unroll
+                for (int i0 = 0; i0 < 16; i0 += 4) {
+                    float xn[4][4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int i = i0 + k;
+                        if (i < 13) {
+                            row4(16 * rg + i + 3, xn[k]);
+                        } else {
+                            const uint32_t lo = p ? look[i - 13].z : look[i - 13].x;
+                            const uint32_t hi = p ? look[i - 13].w : look[i - 13].y;
+                            xn[k][0] = __uint_as_float(lo << 16);
+                            xn[k][1] = __uint_as_float(lo & 0xffff0000u);
+                            xn[k][2] = __uint_as_float(hi << 16);
+                            xn[k][3] = __uint_as_float(hi & 0xffff0000u);
+                        }
+                    }
+                    uint2 yv[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float out[4];
+                        conv4_pairs<2, bf16>(taps, x0, x1, x2, xn[k], 1, out);
+                        yv[k] = make_uint2(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]));
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            x0[q] = x1[q];
+                            x1[q] = x2[q];
+                            x2[q] = xn[k][q];
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint2*>(cblk + sw128_off(16 * rg + i0 + k, 8 * cc) + 8 * p) = yv[k];
+                }
+            }
+            fence_async_smem();  // the tiles are read by the MMAs and the q store
+        }
+        __syncthreads();
+        // the chain's q tile, once per key head
+        if (ok && tid == 0 && h % (a.H_v / a.H_k) == 0) {
+            const int qr = (int)(((int64_t)blockIdx.y * a.H_k + kh) * 64);
+            tma_store_2d(&qsmap, kq + 8192, 0, qr);
+            tma_store_2d(&qsmap, kq + 24576, 64, qr);
+            bulk_commit();
+        }
+    }
     bool mma_pending = false;
     uint32_t mma_phase = 0;
     if (ok) {
@@ -455,6 +646,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                                    pack_h2(d1[8 * g + 4], d1[8 * g + 5]), pack_h2(d1[8 * g + 6], d1[8 * g + 7]));
             }
         }
+        if (CONV && tid == 0) bulk_wait_read_all();  // the q store has read the Q halves that T' takes
         __syncthreads();
         // D1 has read K: K and V are re-encoded in place as the fp16 operands
         // of the W and U products, and K_dec = diag(e^{G_n-G_j} rk) K goes to
@@ -709,6 +901,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         atomicOr(&g_device_error, 1);
         if (mma_pending) mbar_wait(bar_mma, mma_phase, kWaitNs);
         mbar_wait(bar_tma, 0, kWaitNs);
+        if (CONV) bulk_wait_read_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -805,8 +998,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                    const __grid_constant__ CUtensorMap utmap, const __grid_constant__ CUtensorMap pmap,
                    const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap kdmap, DeltaArgs a,
                    Work w, int64_t C0, int64_t segc) {
+    // the next kernel's CTAs are placed only once this grid is done with its
+    // work (pdl_trigger at the end): placed earlier, their waiting CTAs slowed
+    // the chain's last CTAs
     pdl_wait();
-    pdl_trigger();
     using Ly = ChainLayout<VS>;
     constexpr int NV = D / VS, CV = VS / 4;
     const int vp = blockIdx.x % NV;
@@ -828,6 +1023,21 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 const int64_t off = sbase + (int64_t)(e / VS) * D + v0 + e % VS;
                 a.S_final[off] = a.S0 != nullptr ? a.S0[off] : 0.f;
             }
+        // with the conv inside the kernels, so is its conv state: its V
+        // channels and (first value head of the key head) its K and Q ones
+        if (cs == ce && C0 == 0 && a.conv_state_out != nullptr && vp == 0) {
+            const int r = a.H_v / a.H_k, kh = h / r;
+            const int64_t cd = 2 * a.H_k * D + a.H_v * D;
+            const uint16_t* src = static_cast<const uint16_t*>(a.conv_state0);
+            uint16_t* dst = static_cast<uint16_t*>(a.conv_state_out);
+            for (int e = tid; e < 3 * 3 * D; e += NT_C) {
+                const int part = e / (3 * D), i = e % (3 * D);  // V, K, Q channel blocks
+                if (part > 0 && h % r != 0) break;
+                const int64_t ch = part == 0 ? 2 * a.H_k * D + h * D : (part == 1 ? a.H_k * D : 0) + kh * D;
+                const int64_t off = ((int64_t)seq * cd + ch) * 3 + i;
+                dst[off] = src != nullptr ? src[off] : 0;
+            }
+        }
         return;
     }
     const int kh = h / (a.H_v / a.H_k);
@@ -887,12 +1097,14 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 if (k >= NST && !mbar_wait_or_abort(&empty[b], (uint32_t)((k / NST - 1) & 1), abort_flag)) break;
                 const int64_t gcc = c_lo + k;
                 uint8_t* st = stage_of(k);
-                const int y = (int)(s0 + (gcc - cs) * C);
                 const int64_t uu = (gcc - C0) * a.H_v + h;
+                // q from qkv, or the intra kernel's conv'd q tile of (chunk, key head)
+                const int qx = w.q != nullptr ? 0 : xq;
+                const int qy = w.q != nullptr ? (int)(((gcc - C0) * a.H_k + kh) * 64) : (int)(s0 + (gcc - cs) * C);
                 mbar_arrive_expect_tx(&full[b], Ly::STAGE + Ly::VEC);
-                tma_load_2d(st + Ly::SG_QW, &qmap, &full[b], xq, y);
+                tma_load_2d(st + Ly::SG_QW, &qmap, &full[b], qx, qy);
                 tma_load_2d(st + Ly::SG_QW + 8192, &wmap, &full[b], 0, (int)(uu * 64));
-                tma_load_2d(st + Ly::SG_QW + 16384, &qmap, &full[b], xq + 64, y);
+                tma_load_2d(st + Ly::SG_QW + 16384, &qmap, &full[b], qx + 64, qy);
                 tma_load_2d(st + Ly::SG_QW + 24576, &wmap, &full[b], 64, (int)(uu * 64));
                 tma_load_2d(st + Ly::SG_P, &pmap, &full[b], 0, (int)(uu * 64));
                 tma_load_2d(st + Ly::SG_K, &kdmap, &full[b], 0, (int)(uu * 64));
@@ -1114,6 +1326,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     }
     tc_fence_before();
     __syncthreads();
+    pdl_trigger();
     if (tid == 0 && *abort_flag) atomicOr(&g_device_error, 1);
     if (warp == 0) tmem_dealloc(tb, Ly::T_COLS);
 }
@@ -1202,17 +1415,25 @@ cudaError_t run_segments(const DeltaArgs& a, const Work* w, int nbuf, const Layo
     const uint64_t U = (uint64_t)Ly.segc * a.H_v;
     const bool split = (int64_t)a.n_seq * a.H_v * 2 <= sm_count();
     constexpr CUtensorMapDataType F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap qmap, omap, wtmap[2], utmap[2], pmap[2], kdmap[2];
+    const bool conv = a.conv_w != nullptr;
+    if (conv != (w[0].q != nullptr)) return cudaErrorInvalidValue;
+    // qmap: qkv (x with the conv inside); cq[i]: where the chain reads q from
+    CUtensorMap qmap, omap, wtmap[2], utmap[2], pmap[2], kdmap[2], cq[2];
     if (!encode2d(&qmap, a.qkv, conv_dim, (uint64_t)a.T, 64, 64) ||
         !encode2d(&omap, a.o, (uint64_t)a.H_v * D, (uint64_t)a.T, 64, 64))
         return cudaErrorInvalidValue;
-    for (int i = 0; i < nbuf; ++i)
+    for (int i = 0; i < nbuf; ++i) {
         if (!encode2d(&wtmap[i], w[i].wt, 128, U * 64, 64, 64) || !encode2d(&utmap[i], w[i].ut, 128, U * 64, 64, 64, F16) ||
             !encode2d(&pmap[i], w[i].p, 64, U * 64, 64, 64, F16) || !encode2d(&kdmap[i], w[i].kd, 128, U * 64, 64, 64, F16))
             return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(chunk_intra_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
+        cq[i] = qmap;
+        if (conv && !encode2d(&cq[i], w[i].q, 128, (uint64_t)Ly.segc * a.H_k * 64, 64, 64))
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaSuccess;
+    for (const void* k : {(const void*)chunk_intra_kernel<false, false>, (const void*)chunk_intra_kernel<true, false>,
+                          (const void*)chunk_intra_kernel<false, true>, (const void*)chunk_intra_kernel<true, true>})
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(chunk_chain_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  ChainLayout<64>::SMEM);
@@ -1265,12 +1486,17 @@ cudaError_t run_segments(const DeltaArgs& a, const Work* w, int nbuf, const Layo
         const int b = overlap ? (int)(seg & 1) : 0;
         // buffer b was last read by the chain of segment seg - 2
         if (overlap && seg >= 2 && (e = cudaStreamWaitEvent(aux, ev_c[b], 0)) != cudaSuccess) break;
-        if (a.neumann)
-            e = launch_pdl(chunk_intra_kernel<true>, dim3((unsigned)a.H_v, (unsigned)Ly.segc), dim3(NT_I), ISMEM, si,
-                           qmap, wtmap[b], utmap[b], a, w[b], C0);
+        const dim3 ig((unsigned)a.H_v, (unsigned)Ly.segc);
+        if (conv)
+            e = a.neumann ? launch_pdl(chunk_intra_kernel<true, true>, ig, dim3(NT_I), ISMEM, si, qmap, wtmap[b],
+                                       utmap[b], cq[b], a, w[b], C0)
+                          : launch_pdl(chunk_intra_kernel<false, true>, ig, dim3(NT_I), ISMEM, si, qmap, wtmap[b],
+                                       utmap[b], cq[b], a, w[b], C0);
         else
-            e = launch_pdl(chunk_intra_kernel<false>, dim3((unsigned)a.H_v, (unsigned)Ly.segc), dim3(NT_I), ISMEM,
-                           si, qmap, wtmap[b], utmap[b], a, w[b], C0);
+            e = a.neumann ? launch_pdl(chunk_intra_kernel<true, false>, ig, dim3(NT_I), ISMEM, si, qmap, wtmap[b],
+                                       utmap[b], cq[b], a, w[b], C0)
+                          : launch_pdl(chunk_intra_kernel<false, false>, ig, dim3(NT_I), ISMEM, si, qmap, wtmap[b],
+                                       utmap[b], cq[b], a, w[b], C0);
         if (e != cudaSuccess) break;
         if (two || overlap) {
             cudaEvent_t ev = two ? ev_pre : ev_i[b];
@@ -1280,11 +1506,11 @@ cudaError_t run_segments(const DeltaArgs& a, const Work* w, int nbuf, const Layo
         }
         if (split)
             e = launch_pdl(chunk_chain_kernel<64>, dim3((unsigned)(a.n_seq * a.H_v * 2)), dim3(NT_C),
-                           ChainLayout<64>::SMEM, s, qmap, wtmap[b], utmap[b], pmap[b], omap, kdmap[b], a, w[b], C0,
+                           ChainLayout<64>::SMEM, s, cq[b], wtmap[b], utmap[b], pmap[b], omap, kdmap[b], a, w[b], C0,
                            Ly.segc);
         else
             e = launch_pdl(chunk_chain_kernel<128>, dim3((unsigned)(a.n_seq * a.H_v)), dim3(NT_C),
-                           ChainLayout<128>::SMEM, s, qmap, wtmap[b], utmap[b], pmap[b], omap, kdmap[b], a, w[b], C0,
+                           ChainLayout<128>::SMEM, s, cq[b], wtmap[b], utmap[b], pmap[b], omap, kdmap[b], a, w[b], C0,
                            Ly.segc);
         if (e != cudaSuccess) break;
         if (overlap && (e = cudaEventRecord(ev_c[b], s)) != cudaSuccess) break;
@@ -1299,12 +1525,16 @@ size_t chunk_split_workspace_bytes(int n_seq, int64_t T, int H_v) {
     return layout_of(n_seq, T, H_v).total;
 }
 
+size_t chunk_split_conv_workspace_bytes(int n_seq, int64_t T, int H_k, int H_v) {
+    return layout_of(n_seq, T, H_v, H_k).total;
+}
+
 int chunk_split_launches(int n_seq, int64_t T, int H_v, bool has_cu) {
     return (has_cu ? 1 : 0) + 2 * (int)layout_of(n_seq, T, H_v).n_seg;
 }
 
 cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s) {
-    const Layout Ly = layout_of(a.n_seq, a.T, a.H_v);
+    const Layout Ly = layout_of(a.n_seq, a.T, a.H_v, a.conv_w != nullptr ? a.H_k : 0);
     if (workspace == nullptr || ws_bytes < Ly.total) return cudaErrorInvalidValue;
     Work w[2];
     const int nbuf = Ly.two_bufs() ? 2 : 1;
@@ -1318,7 +1548,8 @@ cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_by
 cudaError_t launch_chunk_split_two(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s_pre,
                                    cudaStream_t s_chain, cudaEvent_t ev_pre) {
     const Layout Ly = layout_of(a.n_seq, a.T, a.H_v);
-    if (workspace == nullptr || ws_bytes < Ly.total || ev_pre == nullptr) return cudaErrorInvalidValue;
+    if (workspace == nullptr || ws_bytes < Ly.total || ev_pre == nullptr || a.conv_w != nullptr)
+        return cudaErrorInvalidValue;
     Work w = work_at(static_cast<uint8_t*>(workspace), Ly, a.H_v);
     if (a.S_final != nullptr) w.carry = a.S_final;
     return run_segments(a, &w, 1, Ly, s_chain, s_pre, ev_pre);
@@ -1390,7 +1621,8 @@ bool chunk_split_static_fits(int n_seq, int H_v) {
 }
 
 cudaError_t launch_chunk_split_static(const DeltaArgs& a, cudaStream_t s) {
-    if (!chunk_split_static_fits(a.n_seq, a.H_v) || a.S_final == nullptr) return cudaErrorInvalidValue;
+    if (!chunk_split_static_fits(a.n_seq, a.H_v) || a.S_final == nullptr || a.conv_w != nullptr)
+        return cudaErrorInvalidValue;
     // set-up once per device (per context of that device: a device reset
     // creates a new context, in which the array may sit elsewhere), with that
     // device current: the host-side name of the array is not a device address

@@ -39,41 +39,13 @@ __device__ __forceinline__ void load_state_col(const T* __restrict__ st, int64_t
     for (int e = 0; e < V; ++e) dst[e] = to_f(st[((int64_t)seq * C + c0 + e) * 3 + col]);
 }
 
-// One 16-byte vector of outputs from the inputs at t-3..t, channel pairs in
-// packed f32x2 arithmetic (same products and order as the scalar form).
+// One 16-byte vector of outputs from the inputs at t-3..t, stored at dst.
 template <typename T>
 __device__ __forceinline__ void conv_out2(const float2 (&w)[Vec16<T>::N / 2][4], const float* x0,
                                           const float* x1, const float* x2, const float* x3, int silu,
                                           T* __restrict__ dst) {
-    constexpr int P = Vec16<T>::N / 2;
-    float out[2 * P];
-#pragma unroll
-    for (int k = 0; k < P; ++k) {
-        float2 acc = __fmul2_rn(w[k][0], make_float2(x0[2 * k], x0[2 * k + 1]));
-        acc = __ffma2_rn(w[k][1], make_float2(x1[2 * k], x1[2 * k + 1]), acc);
-        acc = __ffma2_rn(w[k][2], make_float2(x2[2 * k], x2[2 * k + 1]), acc);
-        acc = __ffma2_rn(w[k][3], make_float2(x3[2 * k], x3[2 * k + 1]), acc);
-        if (silu) acc = silu2<T>(acc);
-        out[2 * k] = acc.x;
-        out[2 * k + 1] = acc.y;
-    }
-    store16(dst, out);
-}
-
-template <typename T>
-__device__ __forceinline__ void conv_out(const float (&w)[Vec16<T>::N][4], const float* w0,
-                                         const float* w1, const float* w2, const float* cur,
-                                         int silu, T* __restrict__ dst) {
-    constexpr int V = Vec16<T>::N;
-    float out[V];
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-        float acc = w[e][0] * w0[e];
-        acc = fmaf(w[e][1], w1[e], acc);
-        acc = fmaf(w[e][2], w2[e], acc);
-        acc = fmaf(w[e][3], cur[e], acc);
-        out[e] = silu ? silu_fast(acc) : acc;
-    }
+    float out[Vec16<T>::N];
+    conv4_vec<T>(w, x0, x1, x2, x3, silu, out);
     store16(dst, out);
 }
 
@@ -101,16 +73,7 @@ __global__ void __launch_bounds__(kTileThreads, 3) conv1d_fwd_kernel(const __gri
     const int c0 = cbase + cg * V;
     const bool cv = c0 < C;
     float2 w[V / 2][4];  // (channel 2k, channel 2k + 1) x tap
-    if (cv) {
-        const T* wp = static_cast<const T*>(a.w) + (int64_t)c0 * 4;
-        float tmp[4 * V];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) load16(wp + i * V, tmp + i * V);
-#pragma unroll
-        for (int k = 0; k < V / 2; ++k)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) w[k][j] = make_float2(tmp[(2 * k) * 4 + j], tmp[(2 * k + 1) * 4 + j]);
-    }
+    if (cv) load_conv_taps(static_cast<const T*>(a.w), c0, w);
     const int64_t tb = t0 + 8 * tg;
     const int64_t te = tb + 8 < a.T ? tb + 8 : a.T;
     int seq = 0;
@@ -367,6 +330,15 @@ cudaError_t read_and_clear_conv_error(cudaStream_t s, int* flags) {
 
 cudaError_t launch_conv1d_fwd(const ConvArgs& a, gdn_dtype_t dt, cudaStream_t s) {
     return dt == GDN_BF16 ? conv_fwd_t<bf16>(a, s) : conv_fwd_t<float>(a, s);
+}
+
+cudaError_t launch_conv1d_state(const ConvArgs& a, gdn_dtype_t dt, cudaStream_t s) {
+    if (a.T == 0 || (a.state_out == nullptr && (a.ckpt_every <= 0 || a.ckpt == nullptr))) return cudaSuccess;
+    const int V = dt == GDN_BF16 ? 8 : 4;
+    const dim3 grid((unsigned)a.n_seq, (unsigned)((a.C / V + kThreads - 1) / kThreads));
+    const cudaError_t e = dt == GDN_BF16 ? launch_pdl(conv1d_state_kernel<bf16>, grid, dim3(kThreads), 0, s, a)
+                                         : launch_pdl(conv1d_state_kernel<float>, grid, dim3(kThreads), 0, s, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_conv1d_update(const void* x, const void* w, void* state, int B, int C,

@@ -422,15 +422,19 @@ gdn_status_t gdn_chunk_prefill_norm(const void* qkv, const void* a, const void* 
 
 size_t gdn_layer_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t dims, gdn_dtype_t dtype) {
     if (check_dims(dims, dtype) != GDN_OK || n_seq < 1 || T_tot <= 0 || T_tot > (int64_t)INT32_MAX) return 0;
-    const size_t y = ((size_t)T_tot * (size_t)conv_dim_of(dims) * elem_size(dtype) + 255) & ~(size_t)255;
-    return y + gdn_chunk_prefill_workspace_size(n_seq, T_tot, dims, dtype);
+    // tensor-core path: the conv runs inside the chunk kernels (no y buffer)
+    if (dtype == GDN_BF16 && dims.d_k == 128) return gdn::chunk_split_conv_workspace_bytes(n_seq, T_tot, dims.H_k, dims.H_v);
+    return ((size_t)T_tot * (size_t)conv_dim_of(dims) * elem_size(dtype) + 255) & ~(size_t)255;
 }
 
 int32_t gdn_layer_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_seqlens, gdn_dims_t dims,
                                    gdn_dtype_t dtype) {
     if (check_dims(dims, dtype) != GDN_OK || n_seq < 1 || T_tot <= 0) return 0;
-    // the conv, the chunked rule, the norm
-    return 2 + gdn_chunk_prefill_launches(n_seq, T_tot, has_cu_seqlens, dims, dtype);
+    // the chunked rule and the norm, and the conv (on the tensor-core path it
+    // runs in the chunk kernels, which with conv_state_out not conv_state_in
+    // also write the conv state)
+    const bool tc = dtype == GDN_BF16 && dims.d_k == 128;
+    return (tc ? 1 : 2) + gdn_chunk_prefill_launches(n_seq, T_tot, has_cu_seqlens, dims, dtype);
 }
 
 gdn_status_t gdn_layer_prefill(const void* x, const void* z, const void* a, const void* b, const void* conv_w,
@@ -454,6 +458,60 @@ gdn_status_t gdn_layer_prefill(const void* x, const void* z, const void* a, cons
         return GDN_ERR_ALIGN;
     const size_t need = gdn_layer_prefill_workspace_size(n_seq, T_tot, dims, dtype);
     if (need > 0 && (workspace == nullptr || ws_bytes < need)) return GDN_ERR_WORKSPACE;
+    if (T_tot > 0 && dtype == GDN_BF16 && dims.d_k == 128) {
+        // tensor-core path: conv1d + SiLU, the conv state and the conv
+        // checkpoints inside the chunk kernels (the state in place: by a pass
+        // after them), then RMSNormGated
+        if ((st = check_gates(a, b, A_log, dt_bias, nullptr, nullptr, dtype)) != GDN_OK) return st;
+        if (flags & ~(GDN_QK_L2NORM | GDN_SOLVE_NEUMANN)) {
+            if (flags & ~(GDN_QK_L2NORM | GDN_SOLVE_NEUMANN | GDN_CHUNK(0xff))) return GDN_ERR_INVALID_ARG;
+            const uint32_t c = (flags >> 8) & 0xffu;
+            if (c != 0 && c != 64) return c == 16 || c == 32 ? GDN_ERR_UNSUPPORTED : GDN_ERR_INVALID_ARG;
+        }
+        if (!isfinite(scale)) return GDN_ERR_INVALID_ARG;
+        if (!aligned16(conv_w) || !aligned16(conv_state_in) || !aligned16(conv_state_out) ||
+            !aligned16(conv_ckpt_out) || !aligned16(initial_state) || !aligned16(final_state) ||
+            !aligned16(state_ckpt_out))
+            return GDN_ERR_ALIGN;
+        if ((int64_t)n_seq * dims.H_v * 8 > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+        gdn::DeltaArgs d;
+        memset(&d, 0, sizeof(d));
+        d.qkv = x; d.a = a; d.b = b; d.A_log = A_log; d.dt_bias = dt_bias;
+        d.cu = cu_seqlens; d.n_seq = n_seq; d.T = T_tot;
+        d.H_k = dims.H_k; d.H_v = dims.H_v; d.D = dims.d_k;
+        d.S0 = initial_state; d.S_final = final_state;
+        d.ckpt_every = ckpt_every; d.ckpt = ckpt_every > 0 ? state_ckpt_out : nullptr;
+        d.ckpt_rows = ckpt_rows;
+        d.scale = scale == 0.f ? 1.0f / sqrtf((float)dims.d_k) : scale;
+        d.l2norm = (flags & GDN_QK_L2NORM) != 0;
+        d.neumann = (flags & GDN_SOLVE_NEUMANN) != 0;
+        d.chunk = 64;
+        d.o = out;
+        d.conv_w = conv_w;
+        d.conv_state0 = conv_state_in;
+        // the kernels write the conv state and checkpoints unless the state is
+        // updated in place (the kernels of other chunks still read it)
+        const bool in_place = conv_state_out != nullptr && conv_state_out == conv_state_in;
+        if (!in_place) {
+            d.conv_state_out = conv_state_out;
+            d.conv_ckpt = ckpt_every > 0 ? conv_ckpt_out : nullptr;
+        }
+        cudaStream_t s = (cudaStream_t)stream;
+        cudaError_t e = gdn::launch_chunk_split(d, workspace, ws_bytes, s);
+        if (e == cudaSuccess && in_place) {
+            gdn::ConvArgs c;
+            memset(&c, 0, sizeof(c));
+            c.x = x; c.w = conv_w; c.cu = cu_seqlens; c.n_seq = n_seq; c.T = T_tot;
+            c.C = (int)conv_dim_of(dims);
+            c.state_in = conv_state_in; c.state_out = conv_state_out;
+            c.ckpt_every = ckpt_every; c.ckpt = ckpt_every > 0 ? conv_ckpt_out : nullptr;
+            c.ckpt_rows = ckpt_rows; c.silu = 1;
+            e = gdn::launch_conv1d_state(c, dtype, s);
+        }
+        if (e == cudaSuccess)
+            e = gdn::launch_rmsnorm_gated(out, z, norm_w, norm_eps, T_tot, dims.H_v, dims.d_v, out, dtype, s);
+        return cuda_status(e);
+    }
     const size_t ybytes = T_tot > 0 ? ((size_t)T_tot * (size_t)conv_dim_of(dims) * elem_size(dtype) + 255) &
                                           ~(size_t)255
                                     : 0;

@@ -119,6 +119,72 @@ __device__ __forceinline__ float2 silu2(float2 x) {
     else return make_float2(silu_fast(x.x), silu_fast(x.y));
 }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// ---------------------------------------------------------------- depthwise conv1d (k = 4)
+// cortex commit "feat(stage-8c): linear-attention layer", "Block": depthwise
+// causal conv (k = 4), then SiLU.  The helpers below are the conv's whole
+// arithmetic, shared by every kernel that computes it, so that they agree bit
+// for bit.  w is [C][4] (tap 0 multiplies the oldest input); taps are held as
+// (channel 2k, channel 2k + 1) pairs per tap.
+// Taps of the Vec16<T>::N channels from c0; raw[i] is the 16-byte vector of w
+// from element 4 c0 + i Vec16<T>::N on.
+template <typename T>
+__device__ __forceinline__ void conv_taps(const uint4 (&raw)[4], float2 (&taps)[Vec16<T>::N / 2][4]) {
+    constexpr int V = Vec16<T>::N;
+    float tmp[4 * V];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) unpack16<T>(raw[i], tmp + i * V);
+#pragma unroll
+    for (int k = 0; k < V / 2; ++k)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) taps[k][j] = make_float2(tmp[(2 * k) * 4 + j], tmp[(2 * k + 1) * 4 + j]);
+}
+template <typename T>
+__device__ __forceinline__ void load_conv_taps(const T* __restrict__ w, int64_t c0,
+                                               float2 (&taps)[Vec16<T>::N / 2][4]) {
+    uint4 raw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) raw[i] = *reinterpret_cast<const uint4*>(w + c0 * 4 + i * Vec16<T>::N);
+    conv_taps<T>(raw, taps);
+}
+// bf16 taps of the two channel pairs from c0 (c0 even): raw = w[4 c0 .. 4 c0 + 16)
+__device__ __forceinline__ void conv_taps_bf16_2(const uint4 (&raw)[2], float2 (&taps)[2][4]) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float t[8];
+        unpack16<bf16>(raw[k], t);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) taps[k][j] = make_float2(t[j], t[4 + j]);
+    }
+}
+
+// NP channel pairs of outputs at token t from the inputs at t-3 (x0) .. t
+// (x3): w0 x0 + w1 x1 + w2 x2 + w3 x3 in that order, in packed f32x2
+// arithmetic, then SiLU when `silu`.  Each channel's result does not depend
+// on NP.
+template <int NP, typename T>
+__device__ __forceinline__ void conv4_pairs(const float2 (&w)[NP][4], const float* x0, const float* x1,
+                                            const float* x2, const float* x3, int silu, float* out) {
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        float2 acc = __fmul2_rn(w[k][0], make_float2(x0[2 * k], x0[2 * k + 1]));
+        acc = __ffma2_rn(w[k][1], make_float2(x1[2 * k], x1[2 * k + 1]), acc);
+        acc = __ffma2_rn(w[k][2], make_float2(x2[2 * k], x2[2 * k + 1]), acc);
+        acc = __ffma2_rn(w[k][3], make_float2(x3[2 * k], x3[2 * k + 1]), acc);
+        if (silu) acc = silu2<T>(acc);
+        out[2 * k] = acc.x;
+        out[2 * k + 1] = acc.y;
+    }
+}
+
+// One 16-byte vector of outputs at token t from the inputs at t-3 (x0) .. t (x3).
+template <typename T>
+__device__ __forceinline__ void conv4_vec(const float2 (&w)[Vec16<T>::N / 2][4], const float* x0,
+                                          const float* x1, const float* x2, const float* x3, int silu,
+                                          float* out) {
+    conv4_pairs<Vec16<T>::N / 2, T>(w, x0, x1, x2, x3, silu, out);
+}
+
 // softplus with the identity branch above 20 (cortex unit test "softplus small/large branches")
 __device__ __forceinline__ float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
 

@@ -28,6 +28,9 @@ struct ConvArgs {
     int fused_state;  // set by launch_conv1d_fwd: the tile kernel writes the state and checkpoints
 };
 cudaError_t launch_conv1d_fwd(const ConvArgs& a, gdn_dtype_t dt, cudaStream_t s);
+// Only the conv state after each sequence and the conv checkpoints (no y): the
+// state pass of launch_conv1d_fwd, for callers that compute y elsewhere.
+cudaError_t launch_conv1d_state(const ConvArgs& a, gdn_dtype_t dt, cudaStream_t s);
 cudaError_t launch_conv1d_update(const void* x, const void* w, void* state, int B, int C,
                                  int silu, void* y, gdn_dtype_t dt, cudaStream_t s);
 
@@ -53,6 +56,17 @@ struct DeltaArgs {
     void* o;  // [T, H_v, D]
     int neumann;  // chunk inverse by the Neumann-style product (tensor-core path)
     int chunk;    // chunk size of the CUDA-core path: 16, 32 or 64 (0: 64)
+    // Conv1d + SiLU inside the chunk kernels (tensor-core path): with conv_w
+    // set, qkv is the raw conv input x and the kernels compute y themselves
+    // from x, these taps ([conv_dim][4]) and the sequences' conv states before
+    // their first tokens ([n_seq][conv_dim][3], null: zeros).
+    const void* conv_w;
+    const void* conv_state0;
+    // ... and, when set, the kernels also write the conv state after each
+    // sequence ([n_seq][conv_dim][3]; never the conv_state0 array) and the
+    // conv checkpoints ([ckpt_rows][conv_dim][3], every ckpt_every tokens)
+    void* conv_state_out;
+    void* conv_ckpt;
 };
 // Chunked prefill on CUDA cores (f32 arithmetic; any supported D and dtype).
 cudaError_t launch_chunk_ffma(const DeltaArgs& a, gdn_dtype_t dt, cudaStream_t s);
@@ -108,6 +122,9 @@ unsigned long long current_context_id();
 // in two kernels: the state-independent work of every chunk in parallel (into
 // `workspace`), then the sequential state recurrence.
 size_t chunk_split_workspace_bytes(int n_seq, int64_t T, int H_v);
+// ... when the conv is computed inside the kernels (DeltaArgs::conv_w): the
+// same plus the conv'd q tiles of each segment's chunks and key heads.
+size_t chunk_split_conv_workspace_bytes(int n_seq, int64_t T, int H_k, int H_v);
 cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes,
                                cudaStream_t s);
 // The same with the chunk offsets and intra kernels on s_pre and the chain on

@@ -424,7 +424,13 @@ gdn_status_t gdn_chunk_prefill_norm(const void* qkv, const void* a, const void* 
  * GatedDeltaNet commit, "Block" and "Output" (the order conv -> rule ->
  * RMSNormGated(core_attn_out, z)); the fusion has no counterpart on the pages
  * beyond the chunked kernel of the NxD-Inference Qwen3.6-27B PR, Summary.
- * It is gdn_conv1d_fwd (into the workspace) followed by gdn_chunk_prefill_norm.
+ * bf16 with d_k = 128 (the tensor-core path): the conv runs inside the chunk
+ * kernels -- each chunk's tiles of x and their 3-token halo (or the
+ * sequence's conv state) are convolved in shared memory, so the conv output
+ * never goes to device memory -- and the same kernels write the conv state and
+ * checkpoints, unless conv_state_out is conv_state_in (then a pass after them
+ * does).  Otherwise it is gdn_conv1d_fwd (into the workspace) followed by
+ * gdn_chunk_prefill_norm.
  *   x          (device) [T_tot, conv_dim]   raw (pre-conv) mixed_qkv
  *   z          (device) [T_tot, H_v*d_v];  a, b (device) [T_tot, H_v]    dtype
  *   conv_w     (device) [conv_dim, 4];  norm_w (device) [d_v]            dtype
@@ -437,10 +443,12 @@ gdn_status_t gdn_chunk_prefill_norm(const void* qkv, const void* a, const void* 
  *               ckpt_rows rows allocated in each (with 0, both may be NULL)
  *   scale, flags  as gdn_chunk_prefill (GDN_QK_L2NORM, optionally | GDN_SOLVE_NEUMANN)
  *   out        (device) [T_tot, H_v*d_v]   dtype
- *   workspace  (device) >= gdn_layer_prefill_workspace_size bytes (it holds the
- *              conv output and the chunk intermediates), 16-byte aligned
+ *   workspace  (device) >= gdn_layer_prefill_workspace_size bytes, 16-byte
+ *              aligned (tensor-core path: the chunk intermediates and the conv'd
+ *              q tiles the state chain reads; otherwise the conv output)
  * Results equal those of the three separate calls bit for bit.  Kernel
- * launches: gdn_layer_prefill_launches.
+ * launches: gdn_layer_prefill_launches (with conv_state_out not conv_state_in;
+ * one more in place on the tensor-core path).
  */
 size_t gdn_layer_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t dims, gdn_dtype_t dtype);
 int32_t gdn_layer_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_seqlens, gdn_dims_t dims,

@@ -305,16 +305,18 @@ def test_layer_prefill_host_validation(lib):
 def test_layer_prefill_workspace_and_launches(lib):
     dims = gdn.GDNDims(16, 48, 128, 128)
     C = dims.conv_dim
-    # the conv output (rounded up to 256 bytes), then the chunk intermediates
-    y = (4096 * C * 2 + 255) // 256 * 256
-    assert gdn.gdn_layer_prefill_workspace_size(1, 4096, dims, torch.bfloat16) == \
-        y + gdn.gdn_chunk_prefill_workspace_size(1, 4096, dims, torch.bfloat16)
+    # bf16 with d = 128: the conv runs inside the chunk kernels, so no conv
+    # output; the chunk intermediates plus the conv'd q tile of every chunk and
+    # key head (4096 tokens: one segment of 65 chunk slots, 16 KiB per tile)
+    ws_c = gdn.gdn_chunk_prefill_workspace_size(1, 4096, dims, torch.bfloat16)
+    assert gdn.gdn_layer_prefill_workspace_size(1, 4096, dims, torch.bfloat16) == ws_c + 65 * 16 * 16384
+    # f32: the conv output (rounded up to 256 bytes); the CUDA-core rule needs none
     assert gdn.gdn_layer_prefill_workspace_size(1, 100, dims, torch.float32) == (100 * C * 4 + 255) // 256 * 256
     assert gdn.gdn_layer_prefill_workspace_size(1, 0, dims, torch.bfloat16) == 0
-    # conv, the chunk kernels, the norm
+    # the chunk kernels (the conv inside them) and the norm; f32: conv, rule, norm
     for cu in (True, None):
         assert gdn.gdn_layer_prefill_launches(1, 4096, dims, torch.bfloat16, cu_seqlens=cu) == \
-            2 + gdn.gdn_chunk_prefill_launches(1, 4096, dims, torch.bfloat16, cu_seqlens=cu)
+            1 + gdn.gdn_chunk_prefill_launches(1, 4096, dims, torch.bfloat16, cu_seqlens=cu)
     assert gdn.gdn_layer_prefill_launches(1, 64, gdn.GDNDims(2, 4, 16, 16), torch.float32) == 3
     assert gdn.gdn_layer_prefill_launches(1, 0, dims, torch.bfloat16) == 0
 
@@ -322,10 +324,10 @@ def test_layer_prefill_workspace_and_launches(lib):
 def test_workspace_size(lib):
     dims = gdn.GDNDims(16, 32, 128, 128)
     # the CUDA-core (f32) path needs none; the bf16 tensor-core path holds per-chunk
-    # intermediates (41,984 B per chunk and value head) plus chunk offsets
+    # intermediates (58,368 B per chunk and value head) plus chunk offsets
     assert gdn.gdn_chunk_prefill_workspace_size(8, 32768, dims, torch.float32) == 0
     ws = gdn.gdn_chunk_prefill_workspace_size(8, 32768, dims, torch.bfloat16)
-    assert ws >= 32 * 41984
+    assert ws >= 32 * 58368
     assert gdn.gdn_chunk_prefill_workspace_size(8, 0, dims, torch.bfloat16) == 0
     assert gdn.gdn_chunk_prefill_workspace_size(1, 64, gdn.GDNDims(2, 4, 16, 16),
                                                 torch.bfloat16) == 0

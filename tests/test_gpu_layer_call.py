@@ -7,7 +7,8 @@ Against the three separate calls on the same inputs: every output bit for bit
 tolerance.  The cases reach both chain forms of the tensor-core path -- a head
 split into two 64-column CTAs (few sequences) and one CTA per head (more
 (sequence, head) pairs than SMs) -- ragged tails, empty and 1..3-token
-sequences, checkpoints, the Neumann-style solve and the CUDA-core path.
+sequences, checkpoints, the conv state updated in place, the Neumann-style
+solve and the CUDA-core path.
 """
 import numpy as np
 import pytest
@@ -105,6 +106,29 @@ def test_small_heads_varlen(lengths):
     _compare_with_separate(fz, sp)
     ref = _oracle(inp, SMALL_128)
     assert_close("out", host(fz["out"]), ref["out"], TOL[torch.bfloat16])
+
+
+def test_conv_state_in_place_equals_out_of_place():
+    # bf16 with d = 128 runs the conv inside the chunk kernels, which then also
+    # write the conv state and checkpoints -- unless the state is updated in
+    # place, where a pass after them does; empty and 1..3-token sequences take
+    # their state from conv_state0
+    lengths = [1, 63, 0, 200, 3, 130]
+    inp = W.layer_inputs(SMALL_128, torch.bfloat16, lengths, seed=37, init_state=True)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    args = (d["mixed_qkv"], d["z"], d["a"], d["b"], d["conv_w"], d["A_log"], d["dt_bias"], d["norm_w"],
+            _dims(SMALL_128))
+    kw = dict(cu_seqlens=d["cu_seqlens"], initial_state=d["S0"], ckpt_every=64)
+    cs = d["conv_state0"].clone()
+    ref = gdn.gdn_layer_prefill(*args, conv_state=d["conv_state0"], **kw)
+    got = gdn.gdn_layer_prefill(*args, conv_state=cs, conv_state_out=cs, **kw)
+    torch.cuda.synchronize()
+    gdn.gdn_sync_status()
+    assert got["conv_state"].data_ptr() == cs.data_ptr()
+    for k in ("out", "final_state", "conv_state", "state_ckpt", "conv_ckpt"):
+        assert torch.equal(got[k], ref[k]), k
+    sp = _run(inp, SMALL_128, one_call=False, ckpt_every=64)
+    _compare_with_separate(ref, sp)
 
 
 def test_neumann_solve_in_the_layer_call():
