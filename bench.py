@@ -215,8 +215,8 @@ def barrier(dist, dev):
 # --------------------------------------------------------------------------- other prefill workloads
 def prefill_workload(gdn, name, args, dev, stream, flush, clocks, pk, steps, warmup):
     """Time gdn_layer_prefill on the named workload (device-resident inputs, its
-    own cu_seqlens, initial states and checkpoint cadence), L2 flushed between
-    calls; then the chunk stage alone (gdn_chunk_prefill on the conv output)
+    own cu_seqlens, initial states and checkpoint cadence), calls back to back
+    (the inputs are larger than L2); then the chunk stage alone (gdn_chunk_prefill on the conv output)
     for its tensor-peak fraction; for a workload with a decode tail, the fused
     decode steps that follow from the prefill's final states.  Returns (dict,
     launches)."""
@@ -245,12 +245,16 @@ def prefill_workload(gdn, name, args, dev, stream, flush, clocks, pk, steps, war
                               conv_state=d["conv_state0"], ckpt_every=w.ckpt_every, out=out, final_state=Sf,
                               conv_state_out=csf, workspace=ws, state_ckpt_out=Sck, conv_ckpt_out=cck)
 
-    def timed(fn, k_steps):
+    def timed(fn, k_steps, gap=False):
+        # gap: an L2 flush before each timed call, which also keeps the host's
+        # launches ahead of a short call (back to back, a one-sequence decode
+        # step would time the host's launch path)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k_steps)]
         torch.cuda.synchronize(dev)
         clocks.mark(True)
         for k in range(k_steps):
-            flush.zero_()
+            if gap:
+                flush.zero_()
             ev[k][0].record(stream)
             fn()
             ev[k][1].record(stream)
@@ -259,7 +263,6 @@ def prefill_workload(gdn, name, args, dev, stream, flush, clocks, pk, steps, war
         return [a_.elapsed_time(b_) for a_, b_ in ev]
 
     for _ in range(warmup):
-        flush.zero_()
         call()
     ms = timed(call, steps)
     launches = steps * gdn.gdn_layer_prefill_launches(n, T, dims, w.dtype, cu_seqlens=cu is not None)
@@ -292,7 +295,8 @@ def prefill_workload(gdn, name, args, dev, stream, flush, clocks, pk, steps, war
                      "frac": round(flops / c_avg / 1e12 / pk["bf16_tflops"], 4),
                      "frac_of_sustained": round(flops / c_avg / 1e12 / pk["bf16_tflops_sustained"], 4),
                      "algorithmic_flop_per_launch": flops},
-        "l2": "flushed (512 MiB write) between timed calls",
+        "l2": "calls back to back; inputs larger than L2 (a flush right before a call would leave its "
+              "own dirty lines for the call to write back)",
         "input_generation_s": round(t_gen, 1),
     }
     if w.decode_steps and w.decode_batch:
@@ -308,7 +312,7 @@ def prefill_workload(gdn, name, args, dev, stream, flush, clocks, pk, steps, war
             gdn.gdn_decode_step(dd["qkv"][t], dd["z"][t], dd["a"][t], dd["b"][t], d["conv_w"], d["A_log"],
                                 d["dt_bias"], d["norm_w"], dims, Sd, csd, out=outd)
 
-        dms = timed(dstep, w.decode_steps)
+        dms = timed(dstep, w.decode_steps, gap=True)
         launches += w.decode_steps
         dbytes = w.decode_batch * decode_step_bytes_per_seq(s)
         res["decode_tail"] = {
@@ -316,7 +320,7 @@ def prefill_workload(gdn, name, args, dev, stream, flush, clocks, pk, steps, war
             "value": round(w.decode_batch * w.decode_steps / (sum(dms) / 1e3), 1), "unit": "tokens/s",
             "ms_per_step": round(statistics.mean(dms), 4), "call": "gdn_decode_step (one kernel per step)",
             "hbm_frac": round(dbytes / (statistics.mean(dms) / 1e3) / 1e9 / pk["hbm_gbs"], 4),
-            "note": "one sequence per step: launch-latency bound (6.5 MB per step)"}
+            "note": "one sequence per step, L2 flushed before each: launch-latency bound (6.5 MB per step)"}
     del d, inp
     torch.cuda.empty_cache()
     return res, launches
