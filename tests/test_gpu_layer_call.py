@@ -108,6 +108,23 @@ def test_small_heads_varlen(lengths):
     assert_close("out", host(fz["out"]), ref["out"], TOL[torch.bfloat16])
 
 
+def test_many_short_sequences_conv_inside_the_chunk_kernels():
+    # 40 packed sequences of 0-150 tokens (many shorter than the conv's 3-token
+    # window, some empty, several with a checkpoint): the intra kernel takes
+    # each sequence's conv state at its first chunk and writes the conv state
+    # and checkpoints at its last; everything equals the separate calls
+    g = np.random.default_rng(38)
+    lengths = [int(x) for x in g.choice([0, 1, 2, 3, 4, 63, 64, 65, 127, 128, 150], size=40)]
+    inp = W.layer_inputs(SMALL_128, torch.bfloat16, lengths, seed=38, init_state=True)
+    fz = _run(inp, SMALL_128, one_call=True, ckpt_every=64)
+    sp = _run(inp, SMALL_128, one_call=False, ckpt_every=64)
+    _compare_with_separate(fz, sp)
+    ref = _oracle(inp, SMALL_128, ckpt_every=64)
+    assert_close("out", host(fz["out"]), ref["out"], TOL[torch.bfloat16])
+    assert_close("S", host(fz["final_state"]), ref["S"], TOL[torch.bfloat16], per_head_axis=1)
+    assert np.array_equal(host(fz["conv_state"]), ref["conv_state"])
+
+
 def test_conv_state_in_place_equals_out_of_place():
     # bf16 with d = 128 runs the conv inside the chunk kernels, which then also
     # write the conv state and checkpoints -- unless the state is updated in
