@@ -125,6 +125,23 @@ def test_many_short_sequences_conv_inside_the_chunk_kernels():
     assert np.array_equal(host(fz["conv_state"]), ref["conv_state"])
 
 
+def test_more_sequences_than_the_longest_first_order_covers():
+    # 1500 packed sequences (0-69 tokens): above 1024 the chunk-offsets kernel
+    # leaves the chain's CTAs in sequence order instead of longest first; one
+    # 128-column chain CTA per (sequence, head); every result against the
+    # separate calls bit for bit and against the oracle
+    g = np.random.default_rng(39)
+    lengths = [int(x) for x in g.integers(0, 70, size=1500)]
+    inp = W.layer_inputs(SMALL_128, torch.bfloat16, lengths, seed=39, init_state=True)
+    fz = _run(inp, SMALL_128, one_call=True, ckpt_every=64)
+    sp = _run(inp, SMALL_128, one_call=False, ckpt_every=64)
+    _compare_with_separate(fz, sp)
+    ref = _oracle(inp, SMALL_128, ckpt_every=64)
+    assert_close("out", host(fz["out"]), ref["out"], TOL[torch.bfloat16])
+    assert_close("S", host(fz["final_state"]), ref["S"], TOL[torch.bfloat16], per_head_axis=1)
+    assert np.array_equal(host(fz["conv_state"]), ref["conv_state"])
+
+
 def test_conv_state_in_place_equals_out_of_place():
     # bf16 with d = 128 runs the conv inside the chunk kernels, which then also
     # write the conv state and checkpoints -- unless the state is updated in
