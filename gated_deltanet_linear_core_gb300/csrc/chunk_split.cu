@@ -13,17 +13,16 @@
 // l2-norm factors of raw q / k rows and T' = (I + A)^-1:
 //   intra (independent per chunk, all chunks of all heads in parallel):
 //     D1 = [K; Q] K^T,  A = beta rk e^{G_i-G_j} rk k.k (j<i),  P = rq e^{G_i-G_j} rk q.k (j<=i)
-//     W^T = K^T (T' diag(beta e^G rk))^T,  U^T = V^T (T' diag(beta))^T,
+//     W^T = (diag(beta e^G rk) K)^T T'^T,  U^T = (diag(beta) V)^T T'^T,
 //     K_dec = diag(e^{G_n-G_j} rk) K
 //     -> workspace: W (bf16), U, P, K_dec (fp16) and e^G rq, e^{G_n} (f32)
 //   chain (sequential per sequence and value head):
 //     U' = U - W S;  O = diag(e^G rq) (Q S) + P U';  S <- e^{G_n} S + K_dec^T U'
 // Precision: the operands the kernels form for the products of the state
-// update and of P U' -- T' diag(.), K_dec, U' -- are fp16 (11 significant
-// bits against bf16's 8, at the same MMA rate), and so are K and V where they
-// meet T' in the intra kernel (re-encoded in shared memory, exact for
-// |x| in [2^-14, 65504]); the products with the raw bf16 q (D1, [Q; W] S)
-// stay bf16.  This keeps the state's rounding error well inside the bf16
+// update and of P U' -- T', K_dec, U' -- are fp16 (11 significant bits
+// against bf16's 8, at the same MMA rate), and so are K and V, scaled by
+// their row factors, where they meet T' in the intra kernel (re-encoded in
+// shared memory); the products with the raw bf16 q (D1, [Q; W] S) stay bf16.  This keeps the state's rounding error well inside the bf16
 // tolerance when decay is slow and the state carries across many chunks.
 // The intra kernel can also compute the layer's conv1d + SiLU itself (cortex
 // "Block": depthwise causal conv, k = 4, then SiLU): it then loads raw x tiles
@@ -210,7 +209,7 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, 
 constexpr int NT_I = 256;
 constexpr int IS_KQ = 0;                          // [cb0: K | Q][cb1: K | Q]; the Q halves then hold T'
 constexpr int IS_V = IS_KQ + 32768;               // V, then the W staging tile
-constexpr int IS_A = IS_V + 16384;                // A, f32 [64][68]; then B_W | B_U (fp16)
+constexpr int IS_A = IS_V + 16384;                // A, f32 [64][68]; then T' (fp16) and the U staging tile
 constexpr int A_PITCH = 68;
 constexpr int IS_X = IS_A + 64 * A_PITCH * 4;     // solve temporaries, f32 [32][36]
 constexpr int X_PITCH = 36;
@@ -291,6 +290,8 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     float* RQs = Gs + 256;
     float* Ms = Gs + 320;
     float* DECs = Gs + 384;
+    float* EMs = Xs;  // rk_j 2^{-G_j}, and the flag below: in the solve's scratch, free until the solve
+    int* fact_flag = reinterpret_cast<int*>(Xs + 64);
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + IS_BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 2);
@@ -385,8 +386,19 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 x[1] += y1;
             }
         }
+        const float G1 = x[1] + __shfl_sync(0xffffffffu, x[0], 31);
         Gs[lane] = x[0];
-        Gs[lane + 32] = x[1] + __shfl_sync(0xffffffffu, x[0], 31);
+        Gs[lane + 32] = G1;
+        // with every |G| < 100 (log2) the factors 2^{G_i} and 2^{-G_j} of A and P
+        // stay normal f32 numbers, and A, P are formed from them instead of one
+        // exponential per element
+        float glo = fminf(x[0], G1), ghi = fmaxf(x[0], G1);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            glo = fminf(glo, __shfl_xor_sync(0xffffffffu, glo, o));
+            ghi = fmaxf(ghi, __shfl_xor_sync(0xffffffffu, ghi, o));
+        }
+        if (lane == 0) *fact_flag = glo > -100.f && ghi < 100.f ? 1 : 0;
     }
     tc_fence_before();
     __syncthreads();
@@ -588,6 +600,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 RKs[i] = f;
                 FWs[i] = Bs[i] * eg * f;
                 Ms[i] = Gs[i] - lg2_approx(f);
+                EMs[i] = f * ex2_approx(-Gs[i]);
                 const float dec = i < n ? exp2f(Gn - Gs[i]) * f : 0.f;
                 vec[64 + i] = dec;
                 DECs[i] = dec;
@@ -606,27 +619,45 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             //   f_i rk_j 2^{G_i-G_j} = 2^{(G_i + log2 f_i) - (G_j - log2 rk_j)}
             if (j0 <= (i | 31)) {  // else every (i, j) of this warp has j > i
                 float fi = i < n ? (isk ? Bs[i] * RKs[i] : RQs[i]) : 0.f;
-                if (fi < 0.f) {  // a negative q scale (or beta): its sign stays outside the exponent
-                    fi = -fi;
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) d1[q] = -d1[q];
-                }
-                const float Li = Gs[i] + lg2_approx(fi);  // -inf when f_i = 0
                 const int jmax = isk ? i - 1 : i;
+                if (*fact_flag) {
+                    // (f_i 2^{G_i}) (rk_j 2^{-G_j}) d_ij: one exponential per row and per column
+                    const float Ei = fi * ex2_approx(Gs[i]);
 #pragma unroll
-                for (int g4 = 0; g4 < 8; ++g4) {
-                    const float4 M4 = *reinterpret_cast<const float4*>(Ms + j0 + 4 * g4);
-                    const float2 x01 = __fadd2_rn(make_float2(Li, Li), make_float2(-M4.x, -M4.y));
-                    const float2 x23 = __fadd2_rn(make_float2(Li, Li), make_float2(-M4.z, -M4.w));
-                    const float2 p01 = __fmul2_rn(make_float2(d1[4 * g4], d1[4 * g4 + 1]),
-                                                  make_float2(ex2_approx(x01.x), ex2_approx(x01.y)));
-                    const float2 p23 = __fmul2_rn(make_float2(d1[4 * g4 + 2], d1[4 * g4 + 3]),
-                                                  make_float2(ex2_approx(x23.x), ex2_approx(x23.y)));
-                    const int j = j0 + 4 * g4;
-                    d1[4 * g4 + 0] = j + 0 <= jmax ? p01.x : 0.f;
-                    d1[4 * g4 + 1] = j + 1 <= jmax ? p01.y : 0.f;
-                    d1[4 * g4 + 2] = j + 2 <= jmax ? p23.x : 0.f;
-                    d1[4 * g4 + 3] = j + 3 <= jmax ? p23.y : 0.f;
+                    for (int g4 = 0; g4 < 8; ++g4) {
+                        const float4 F4 = *reinterpret_cast<const float4*>(EMs + j0 + 4 * g4);
+                        const float2 a01 = __fmul2_rn(make_float2(d1[4 * g4], d1[4 * g4 + 1]), make_float2(Ei, Ei));
+                        const float2 a23 = __fmul2_rn(make_float2(d1[4 * g4 + 2], d1[4 * g4 + 3]), make_float2(Ei, Ei));
+                        const float2 p01 = __fmul2_rn(a01, make_float2(F4.x, F4.y));
+                        const float2 p23 = __fmul2_rn(a23, make_float2(F4.z, F4.w));
+                        const int j = j0 + 4 * g4;
+                        d1[4 * g4 + 0] = j + 0 <= jmax ? p01.x : 0.f;
+                        d1[4 * g4 + 1] = j + 1 <= jmax ? p01.y : 0.f;
+                        d1[4 * g4 + 2] = j + 2 <= jmax ? p23.x : 0.f;
+                        d1[4 * g4 + 3] = j + 3 <= jmax ? p23.y : 0.f;
+                    }
+                } else {
+                    if (fi < 0.f) {  // a negative q scale (or beta): its sign stays outside the exponent
+                        fi = -fi;
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) d1[q] = -d1[q];
+                    }
+                    const float Li = Gs[i] + lg2_approx(fi);  // -inf when f_i = 0
+#pragma unroll
+                    for (int g4 = 0; g4 < 8; ++g4) {
+                        const float4 M4 = *reinterpret_cast<const float4*>(Ms + j0 + 4 * g4);
+                        const float2 x01 = __fadd2_rn(make_float2(Li, Li), make_float2(-M4.x, -M4.y));
+                        const float2 x23 = __fadd2_rn(make_float2(Li, Li), make_float2(-M4.z, -M4.w));
+                        const float2 p01 = __fmul2_rn(make_float2(d1[4 * g4], d1[4 * g4 + 1]),
+                                                      make_float2(ex2_approx(x01.x), ex2_approx(x01.y)));
+                        const float2 p23 = __fmul2_rn(make_float2(d1[4 * g4 + 2], d1[4 * g4 + 3]),
+                                                      make_float2(ex2_approx(x23.x), ex2_approx(x23.y)));
+                        const int j = j0 + 4 * g4;
+                        d1[4 * g4 + 0] = j + 0 <= jmax ? p01.x : 0.f;
+                        d1[4 * g4 + 1] = j + 1 <= jmax ? p01.y : 0.f;
+                        d1[4 * g4 + 2] = j + 2 <= jmax ? p23.x : 0.f;
+                        d1[4 * g4 + 3] = j + 3 <= jmax ? p23.y : 0.f;
+                    }
                 }
             } else {
 #pragma unroll
@@ -649,9 +680,10 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         if (CONV && tid == 0) bulk_wait_read_all();  // the q store has read the Q halves that T' takes
         __syncthreads();
         // D1 has read K: K and V are re-encoded in place as the fp16 operands
-        // of the W and U products, and K_dec = diag(e^{G_n-G_j} rk) K goes to
-        // the workspace (fp16, rows of 128 d) -- by the threads the solve's
-        // first step leaves free
+        // of the W and U products with their row factors, diag(beta e^G rk) K
+        // and diag(beta) V (so that both products take T' itself), and
+        // K_dec = diag(e^{G_n-G_j} rk) K goes to the workspace (fp16, rows of
+        // 128 d) -- by the threads the solve's first step leaves free
         auto convert_kv = [&](int t, int nt) {
             f16* kd = w.kd + u * (U_KD / 2);
             for (int e = t; e < 1024; e += nt) {
@@ -659,13 +691,22 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 uint4* src = reinterpret_cast<uint4*>(kq + blk * 16384 + (e & 511) * 16);
                 float x[8];
                 unpack16<bf16>(*src, x);
-                const float dc = DECs[r];
-                *src = make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]), pack_h2(x[6], x[7]));
+                const float dc = DECs[r], fw = FWs[r];
+                *src = make_uint4(pack_h2(x[0] * fw, x[1] * fw), pack_h2(x[2] * fw, x[3] * fw),
+                                  pack_h2(x[4] * fw, x[5] * fw), pack_h2(x[6] * fw, x[7] * fw));
                 *reinterpret_cast<uint4*>(kd + r * 128 + blk * 64 + ((pc ^ (r & 7)) << 3)) =
                     make_uint4(pack_h2(x[0] * dc, x[1] * dc), pack_h2(x[2] * dc, x[3] * dc),
                                pack_h2(x[4] * dc, x[5] * dc), pack_h2(x[6] * dc, x[7] * dc));
             }
-            bf16_to_h_inplace(vv, 16384, t, nt);
+            for (int e = t; e < 1024; e += nt) {
+                const int r = (e >> 3) & 63;
+                uint4* src = reinterpret_cast<uint4*>(vv + (e >> 9) * 8192 + (e & 511) * 16);
+                float x[8];
+                unpack16<bf16>(*src, x);
+                const float bt = Bs[r];
+                *src = make_uint4(pack_h2(x[0] * bt, x[1] * bt), pack_h2(x[2] * bt, x[3] * bt),
+                                  pack_h2(x[4] * bt, x[5] * bt), pack_h2(x[6] * bt, x[7] * bt));
+            }
         };
         if constexpr (!NEUMANN) {
             // T' = (I + A)^-1 (unit lower triangular): the four diagonal 16-blocks
@@ -830,37 +871,33 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 __syncthreads();
             }
         }
-        {   // B_W = T' diag(beta e^G rk), B_U = T' diag(beta) (fp16) into the A region
-            const int which = tid >> 7, i = (tid >> 1) & 63, c0 = (tid & 1) * 32;
-            const float* Fc = (which == 0 ? FWs : Bs) + c0;
-            float vals[32];  // T' is zero above its diagonal (all of it is written)
+        {   // T' (fp16) into the A region: the B operand of both products
+            const int i = tid >> 2, c0 = (tid & 3) * 16;
+            float vals[16];  // T' is zero above its diagonal (all of it is written)
 #pragma unroll
-            for (int g4 = 0; g4 < 8; ++g4) {
+            for (int g4 = 0; g4 < 4; ++g4) {
                 const float4 t4 = *reinterpret_cast<const float4*>(tp_at(kq, i, c0 + 4 * g4));
-                const float4 f4 = *reinterpret_cast<const float4*>(Fc + 4 * g4);
-                const float2 lo = __fmul2_rn(make_float2(t4.x, t4.y), make_float2(f4.x, f4.y));
-                const float2 hi = __fmul2_rn(make_float2(t4.z, t4.w), make_float2(f4.z, f4.w));
-                vals[4 * g4 + 0] = lo.x;
-                vals[4 * g4 + 1] = lo.y;
-                vals[4 * g4 + 2] = hi.x;
-                vals[4 * g4 + 3] = hi.y;
+                vals[4 * g4 + 0] = t4.x;
+                vals[4 * g4 + 1] = t4.y;
+                vals[4 * g4 + 2] = t4.z;
+                vals[4 * g4 + 3] = t4.w;
             }
-            store_row_h(sm + IS_A + which * 8192, i, c0, vals, 32);
+            store_row_h(sm + IS_A, i, c0, vals, 16);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // W^T = K^T B_W^T,  U^T = V^T B_U^T  (M = d, N = i, K = j)
+        // W^T = (diag(beta e^G rk) K)^T T'^T,  U^T = (diag(beta) V)^T T'^T  (M = d, N = i, K = j)
         if (tid == 0) {
             tc_fence_after();
             const uint32_t akq = smem_u32(kq), av = smem_u32(vv);
-            const uint32_t bw = smem_u32(sm + IS_A), bu = bw + 8192;
+            const uint32_t bt = smem_u32(sm + IS_A);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 mma_bf16(tb + TI_DW, sdesc_sw128(akq + k * 2048, 16384, 1024),
-                         sdesc_sw128(bw + k * 32, 16, 1024), idesc_f16_f32(128, 64, 1, 0), k > 0);
+                         sdesc_sw128(bt + k * 32, 16, 1024), idesc_f16_f32(128, 64, 1, 0), k > 0);
                 mma_bf16(tb + TI_DU, sdesc_sw128(av + k * 2048, 8192, 1024),
-                         sdesc_sw128(bu + k * 32, 16, 1024), idesc_f16_f32(128, 64, 1, 0), k > 0);
+                         sdesc_sw128(bt + k * 32, 16, 1024), idesc_f16_f32(128, 64, 1, 0), k > 0);
             }
             mma_commit(bar_mma);
         }
@@ -874,7 +911,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         // (lanes = d, columns = i) are read in the 16x256b shape, whose
         // fragments stmatrix.trans writes transposed -- 16 bytes of a row at a
         // time -- into 128-byte-swizzled staging tiles (W in the consumed V
-        // tile, U in the consumed B_W | B_U region).  Warp (quarter, half):
+        // tile, U in the consumed A region).  Warp (quarter, half):
         // d in [32 quarter, +32), i in [32 half, +32).
         const int mk = lane >> 3, mr = lane & 7;  // this thread's row address: matrix mk, row mr
 #pragma unroll

@@ -4,10 +4,10 @@ Test infrastructure (CPU, numpy).  It restates the chunked form of the gated
 delta rule (cortex commit "feat(stage-8c): linear-attention layer", "chunked
 algorithm ... chunk_size=64") with the operand precisions the bf16 tensor-core
 path uses and nothing else from it: the products with the raw bf16 q, [Q; W] S,
-take W and S rounded to bf16; T' diag(beta e^G rk), T' diag(beta), U, P, U' and
-diag(e^{G_n - G_j} rk) K are rounded to fp16 where they meet the tensor cores
-(the bf16 activations k, v are exact in fp16); accumulation and the state stay
-in f64, (I + A)^-1 is exact, and o is rounded to bf16.  The rel-L2 of this
+take W and S rounded to bf16; T', the row-scaled diag(beta e^G rk) K and
+diag(beta) V, U, P, U' and diag(e^{G_n - G_j} rk) K are rounded to fp16 where
+they meet the tensor cores; accumulation and the state stay in f64,
+(I + A)^-1 is exact, and o is rounded to bf16.  The rel-L2 of this
 model against the oracle is the error the operand precisions alone imply; a
 GPU result close to it shows the kernels add little error of their own.  It
 sets no tolerance.
@@ -45,8 +45,9 @@ def chunked_bf16_operands(q, k, v, g, beta, S0, scale, C=64):
         KK = K @ K.T
         A = np.tril(bb[:, None] * rk[sl][:, None] * rk[sl][None, :] * Dm * KK, -1)
         Ti = np.linalg.solve(np.eye(n) + A, np.eye(n))
-        W = bf16(fp16(Ti * (bb * np.exp(G) * rk[sl])[None, :]) @ K)
-        U = fp16(fp16(Ti * bb[None, :]) @ V)
+        Th = fp16(Ti)
+        W = bf16(Th @ fp16((bb * np.exp(G) * rk[sl])[:, None] * K))
+        U = fp16(Th @ fp16(bb[:, None] * V))
         P = fp16(rq[sl][:, None] * rk[sl][None, :] * Dm * (Q @ K.T))
         Sb = bf16(S)
         Up = fp16(U - W @ Sb)
