@@ -253,6 +253,42 @@ def test_chunk_prefill_slow_decay(dtype, keys):
     print(f"GPU o {eo:.2e}, S {es:.2e}")
 
 
+def test_chunk_prefill_decay_range_forms():
+    """The tensor-core intra kernel forms A and P from row and column
+    exponentials 2^{G_i}, 2^{-G_j} when a chunk's cumulative decay stays
+    within |G| < 100 (log2), and from one exponential of G_i - G_j per entry
+    otherwise.  Six value heads whose decay per token runs from ~0.008 to ~16
+    (A_log = ln 0.01 .. ln 20, dt_bias = 0) put whole sequences on either side
+    of that bound, and the short and partial chunks of the strongly decaying
+    heads back under it; both forms are held to the bf16 tolerance of the
+    oracle, on o and on the final state."""
+    shape = SMALL_128
+    inp = _delta_inputs(shape, torch.bfloat16, [1000, 300, 64, 1, 130, 7], seed=23)
+    inp["A_log"] = torch.log(torch.tensor([0.01, 0.3, 1.0, 1.6, 2.5, 20.0]))
+    inp["dt_bias"] = torch.zeros(shape.H_v)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    Sf = torch.empty_like(d["S0"])
+    o = gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(shape), d["a"], d["b"], d["A_log"],
+                              d["dt_bias"], cu_seqlens=d["cu_seqlens"], initial_state=d["S0"],
+                              final_state=Sf)
+    torch.cuda.synchronize()
+    o_ref, S_ref, _ = _oracle_delta(inp, shape)
+    # the chunks' decay ranges, from the oracle's gates, for the record
+    f = W.to_f64
+    g, _ = oracle.gates(f(inp["a"]), f(inp["b"]), f(inp["A_log"]), f(inp["dt_bias"]))
+    cu = inp["cu_seqlens"].tolist()
+    wide = [0] * shape.H_v
+    for i in range(len(cu) - 1):
+        for c0 in range(cu[i], cu[i + 1], 64):
+            c1 = min(c0 + 64, cu[i + 1])
+            for h in range(shape.H_v):
+                wide[h] += int(-g[c0:c1, h].sum() / np.log(2.0) >= 100.0)
+    print(f"\nchunks past |G| = 100 (log2) per head: {wide}")
+    assert wide[0] == 0 and wide[-1] > 0, "the inputs should cover both forms"
+    assert_close("o", host(o), o_ref, TOL[torch.bfloat16], per_head_axis=1)
+    assert_close("S_final", host(Sf), S_ref, TOL[torch.bfloat16], per_head_axis=1)
+
+
 def test_chunk_prefill_neumann_solve():
     """GDN_SOLVE_NEUMANN (tensor-core path): within the bf16 tolerance of the
     oracle on N(0,1) activations with the configs' gate distributions, where
