@@ -321,6 +321,221 @@ decode_step_kernel(DecodeStepArgs a) {
     }
 }
 
+// Thread-block cluster helpers: barrier phases over the CTAs of a cluster, and
+// a 16-byte store into the same shared-memory variable of another CTA of it.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(const void* local, uint32_t rank, float4 v) {
+    const uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+
+// The fused decode step for small batches: one CTA per (sequence, value head),
+// r times the CTAs of decode_step_kernel, so that a few sequences still spread
+// over many SMs.  The r value heads of a key head form a thread-block cluster;
+// its first CTA owns the q and k conv channels (it reads their old conv state,
+// writes the shifted one in place and sends the conv outputs to the others
+// through distributed shared memory), and every CTA owns its head's v
+// channels.  Per head the arithmetic and its order are decode_step_kernel's,
+// so states and outputs are the same bit for bit.
+template <typename T, int D, int NW>
+__global__ void __launch_bounds__(NW * 32, (D >= 128 ? 2 : 1))
+decode_step_head_kernel(DecodeStepArgs a) {
+    constexpr int NT = NW * 32;
+    constexpr int TPR = D / 4;
+    constexpr int RPP = NT / TPR;
+    constexpr int PASSES = D / RPP;
+    static_assert(NT % TPR == 0 && D % RPP == 0 && NT >= D, "layout");
+
+    const int r = a.H_v / a.H_k;
+    const int b = blockIdx.x / a.H_v;
+    const int h = blockIdx.x - b * a.H_v;
+    const int kh = h / r, rank = h - kh * r;  // rank in the key head's cluster
+    const bool cl = r > 1;
+    if (cl) cluster_arrive_relaxed();  // this CTA has started (waited for before any remote store)
+    const int64_t slot = a.slots != nullptr ? a.slots[b] : b;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cq = tid % TPR;
+    const int r0 = tid / TPR;
+    const int C = 2 * a.H_k * D + a.H_v * D;
+
+    __shared__ __align__(16) float qs[D], ks[D], vs[D], ds[D], os[D];
+    __shared__ __align__(16) float red[2][RPP][D];
+    __shared__ float gb[2];
+    __shared__ float wsum[NW];
+
+    // the head's state streams in while the conv runs
+    float* __restrict__ S = a.state + (slot * a.H_v + h) * D * D;
+    float4 s[PASSES];
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p)
+        s[p] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(r0 + p * RPP) * D) + cq);
+
+    // 1. conv update of the channels this CTA owns (q and k in the first CTA
+    //    of the cluster, then the head's v), as in decode_step_kernel
+    {
+        constexpr int V = Vec16<T>::N;
+        const T* x = static_cast<const T*>(a.x) + (int64_t)b * C;
+        const T* w = static_cast<const T*>(a.conv_w);
+        T* cs = static_cast<T*>(a.conv_state) + slot * C * 3;
+        const int g0 = rank == 0 ? 0 : 2;
+        const int nvec = (3 - g0) * D / V;
+        for (int e = tid; e < nvec; e += NT) {
+            const int grp = g0 + (e * V) / D, i0 = e * V - (grp - g0) * D;
+            const int c0 = grp == 0 ? kh * D + i0 : grp == 1 ? a.H_k * D + kh * D + i0 : 2 * a.H_k * D + h * D + i0;
+            float xv[V], st[3 * V], wt[4 * V];
+            load16(x + c0, xv);
+#pragma unroll
+            for (int k = 0; k < 3; ++k) load16(cs + (int64_t)c0 * 3 + k * V, st + k * V);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) load16(w + (int64_t)c0 * 4 + k * V, wt + k * V);
+            float* dst = grp == 0 ? qs + i0 : grp == 1 ? ks + i0 : vs + i0;
+            float nst[3 * V];
+#pragma unroll
+            for (int q = 0; q < V; ++q) {
+                float acc = wt[q * 4] * st[q * 3];
+                acc = fmaf(wt[q * 4 + 1], st[q * 3 + 1], acc);
+                acc = fmaf(wt[q * 4 + 2], st[q * 3 + 2], acc);
+                acc = fmaf(wt[q * 4 + 3], xv[q], acc);
+                dst[q] = to_f(from_f<T>(silu_f(acc)));
+                nst[q * 3] = st[q * 3 + 1];
+                nst[q * 3 + 1] = st[q * 3 + 2];
+                nst[q * 3 + 2] = xv[q];
+            }
+#pragma unroll
+            for (int k = 0; k < 3; ++k) store16(cs + (int64_t)c0 * 3 + k * V, nst + k * V);
+        }
+        if (tid == 0) {
+            const int64_t gi = (int64_t)b * a.H_v + h;
+            gb[0] = gate_g(to_f(static_cast<const T*>(a.a)[gi]), a.A_log[h], a.dt_bias[h]);
+            gb[1] = sigmoid_f(to_f(static_cast<const T*>(a.b)[gi]));
+        }
+    }
+    __syncthreads();
+    if (cl) {
+        // q and k from the first CTA to the others, once every CTA has started
+        cluster_wait();
+        if (rank == 0) {
+            for (int e = tid; e < (r - 1) * (D / 2); e += NT) {
+                const int dst = 1 + e / (D / 2), i = e % (D / 2);
+                const float* src = i < D / 4 ? qs + 4 * i : ks + 4 * (i - D / 4);
+                st_cluster_v4(src, (uint32_t)dst, *reinterpret_cast<const float4*>(src));
+            }
+        }
+        cluster_sync();
+    }
+    float sq = 0.f, sk = 0.f, sqk = 0.f;
+    for (int i = lane; i < D; i += 32) {
+        sq = fmaf(qs[i], qs[i], sq);
+        sk = fmaf(ks[i], ks[i], sk);
+        sqk = fmaf(qs[i], ks[i], sqk);
+    }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    sqk = warp_sum(sqk);
+    float rq = a.scale, rk = 1.f;
+    if (a.l2norm) {
+        rq = a.scale / sqrtf(sq + 1e-6f);
+        rk = 1.f / sqrtf(sk + 1e-6f);
+    }
+    const float kq = sqk * rq * rk;
+
+    // 2. the recurrence of head h, then RMSNormGated of its output row
+    float mk[4] = {0.f, 0.f, 0.f, 0.f}, mq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+        const int i = r0 + p * RPP;
+        const float kv = ks[i] * rk, qv = qs[i] * rq;
+        mk[0] = fmaf(s[p].x, kv, mk[0]); mk[1] = fmaf(s[p].y, kv, mk[1]);
+        mk[2] = fmaf(s[p].z, kv, mk[2]); mk[3] = fmaf(s[p].w, kv, mk[3]);
+        mq[0] = fmaf(s[p].x, qv, mq[0]); mq[1] = fmaf(s[p].y, qv, mq[1]);
+        mq[2] = fmaf(s[p].z, qv, mq[2]); mq[3] = fmaf(s[p].w, qv, mq[3]);
+    }
+    *reinterpret_cast<float4*>(&red[0][r0][cq * 4]) = make_float4(mk[0], mk[1], mk[2], mk[3]);
+    *reinterpret_cast<float4*>(&red[1][r0][cq * 4]) = make_float4(mq[0], mq[1], mq[2], mq[3]);
+    __syncthreads();
+    const float eg = expf(gb[0]);
+    const float bt = gb[1];
+    float o2 = 0.f;
+    for (int c = tid; c < D; c += NT) {
+        float m = 0.f, pq = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < RPP; ++rr) {
+            m += red[0][rr][c];
+            pq += red[1][rr][c];
+        }
+        const float delta = bt * (vs[c] - eg * m);
+        ds[c] = delta;
+        const float o = to_f(from_f<T>(eg * pq + kq * delta));  // o as the separate call stores it
+        os[c] = o;
+        o2 = fmaf(o, o, o2);
+    }
+    o2 = warp_sum(o2);
+    if (lane == 0) wsum[warp] = o2;
+    __syncthreads();
+    const float4 d4 = *reinterpret_cast<const float4*>(&ds[cq * 4]);
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+        const int i = r0 + p * RPP;
+        const float kv = ks[i] * rk;
+        float4 n;
+        n.x = fmaf(kv, d4.x, eg * s[p].x);
+        n.y = fmaf(kv, d4.y, eg * s[p].y);
+        n.z = fmaf(kv, d4.z, eg * s[p].z);
+        n.w = fmaf(kv, d4.w, eg * s[p].w);
+        __stcs(reinterpret_cast<float4*>(S + (int64_t)i * D) + cq, n);
+    }
+    float tot = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < NW; ++ww) tot += wsum[ww];
+    const float rs = rsqrtf(tot / (float)D + a.eps);
+    const T* z = static_cast<const T*>(a.z) + ((int64_t)b * a.H_v + h) * D;
+    T* out = static_cast<T*>(a.out) + ((int64_t)b * a.H_v + h) * D;
+    const T* nw = static_cast<const T*>(a.norm_w);
+    for (int c = 2 * tid; c < D; c += 2 * NT) {
+        const float2 g = silu2<T>(make_float2(to_f(z[c]), to_f(z[c + 1])));
+        const float2 res = __fmul2_rn(__fmul2_rn(make_float2(to_f(nw[c]), to_f(nw[c + 1])),
+                                                 __fmul2_rn(make_float2(os[c], os[c + 1]), make_float2(rs, rs))),
+                                      g);
+        out[c] = from_f<T>(res.x);
+        out[c + 1] = from_f<T>(res.y);
+    }
+}
+
+template <typename K>
+cudaError_t launch_cluster(K kernel, unsigned grid, unsigned block, unsigned cluster, cudaStream_t s,
+                           const DecodeStepArgs& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = cluster;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+int device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
 template <typename T>
 cudaError_t decode_step_t(const DecodeStepArgs& a, cudaStream_t s) {
     const unsigned units = (unsigned)(a.B * a.H_k);
@@ -330,6 +545,14 @@ cudaError_t decode_step_t(const DecodeStepArgs& a, cudaStream_t s) {
     // same thread layout (and so the same summation order of S^T k and S^T q)
     // as the recurrent decode kernel: the fused step's state is bit-identical
     // to the separate calls'
+    // at most one (sequence, key head) unit per two SMs: one clustered CTA per
+    // value head instead (27B at B = 1: 12.0 against 16.4 us per step; from
+    // B = 8 the per-key-head CTAs are faster)
+    if ((int64_t)units * 2 <= device_sms()) {
+        const unsigned heads = (unsigned)(a.B * a.H_v);
+        return a.D == 128 ? launch_cluster(decode_step_head_kernel<T, 128, 8>, heads, 256, (unsigned)r, s, a)
+                          : launch_cluster(decode_step_head_kernel<T, 16, 1>, heads, 32, (unsigned)r, s, a);
+    }
     if (a.D == 128)
         decode_step_kernel<T, 128, 8, 8><<<units, 256, 0, s>>>(a);
     else

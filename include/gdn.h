@@ -337,7 +337,10 @@ gdn_status_t gdn_recurrent_decode(const void* qkv, const void* a, const void* b,
  * One fused decode step of the layer core: conv update + SiLU (as
  * gdn_conv1d_update), gates and l2 norms, the recurrent rule (as
  * gdn_recurrent_decode) and RMSNormGated (as gdn_rmsnorm_gated) for one token
- * of each of B sequences, in one kernel (one CTA per sequence and key head).
+ * of each of B sequences, in one kernel (one CTA per sequence and key head;
+ * for batches whose B*H_k is at most half the SM count, one CTA per sequence
+ * and value head, the value heads of a key head as a thread-block cluster,
+ * with the same results bit for bit).
  * Defined by the passages of those three calls; the fusion has no counterpart
  * on the pages beyond the hybrid cache they describe (NxD-Inference PR "Add
  * Qwen3.6-27B hybrid DeltaNet/GQA contrib model and vLLM serving path",

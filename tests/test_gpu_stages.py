@@ -535,6 +535,40 @@ def test_fused_decode_step_with_slots(dtype, shape):
     assert torch.equal(cs_f[others].cpu(), cs_all[others])
 
 
+@pytest.mark.parametrize("heads", [(16, 48), (2, 16), (4, 4)])
+def test_fused_decode_step_alone_equals_inside_a_batch(heads):
+    """gdn_decode_step runs one CTA per (sequence, key head) for large batches
+    and, when those would leave most SMs idle, one clustered CTA per (sequence,
+    value head) with the same per-head arithmetic.  A sequence stepped alone
+    (the per-value-head form) gives the same output row, state and conv state
+    bit for bit as the same sequence inside a batch of 64 (the per-key-head
+    form), for r = 3, 8 and 1 value heads per key head (clusters of 3, 8 and
+    1 CTAs), three steps in a row."""
+    H_k, H_v = heads
+    shape = W.GDNShape(H_k=H_k, H_v=H_v, d_k=128, d_v=128)
+    B, steps = 64, 3
+    d = W.decode_inputs(shape, torch.bfloat16, B, steps, seed=47)
+    p = {k: v.cuda() for k, v in W.layer_params(shape, torch.bfloat16, seed=47).items()}
+    S0 = W.draw((B, H_v, 128, 128), seed=47, stream=62, dtype=torch.float32, p1=0.02).cuda()
+    cs0 = W.draw((B, shape.conv_dim, 3), seed=47, stream=63, dtype=torch.bfloat16).cuda()
+    S_b, cs_b = S0.clone(), cs0.clone()
+    picks = [0, 29, 63]
+    S_1 = [S0[i:i + 1].clone() for i in picks]
+    cs_1 = [cs0[i:i + 1].clone() for i in picks]
+    args = (p["conv_w"], p["A_log"], p["dt_bias"], p["norm_w"], _dims(shape))
+    for t in range(steps):
+        x, z, a, b = (d[k][t].cuda() for k in ("qkv", "z", "a", "b"))
+        out_b = gdn.gdn_decode_step(x, z, a, b, *args, S_b, cs_b)
+        for j, i in enumerate(picks):
+            out_1 = gdn.gdn_decode_step(x[i:i + 1], z[i:i + 1], a[i:i + 1], b[i:i + 1], *args,
+                                        S_1[j], cs_1[j])
+            assert torch.equal(out_1[0], out_b[i]), f"output, sequence {i}, step {t}"
+        gdn.gdn_sync_status()
+        for j, i in enumerate(picks):
+            assert torch.equal(S_1[j][0], S_b[i]), f"state, sequence {i}, step {t}"
+            assert torch.equal(cs_1[j][0], cs_b[i]), f"conv state, sequence {i}, step {t}"
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 # r = 8 value heads per key head with K = 16 is the largest shared-memory request
 # of the verification kernel (158 KB)
