@@ -775,7 +775,9 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             {   // level 2, X = A_{[23][01]} T'_{[01][01]} (32 x 32); warp = (16 rows, 8 columns)
                 const int mt = warp >> 2, nt = warp & 3, r0 = 32 + 16 * mt;
                 float c[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int ks = nt; ks < 4; ++ks) {  // T'(k, c) = 0 for k < c
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {  // T'(k, c) = 0 for k < c
+                    if (ks < nt) continue;
                     const int k0 = 8 * ks;
                     const float af[4] = {Am[(r0 + fg) * A_PITCH + k0 + ft], Am[(r0 + fg + 8) * A_PITCH + k0 + ft],
                                          Am[(r0 + fg) * A_PITCH + k0 + ft + 4], Am[(r0 + fg + 8) * A_PITCH + k0 + ft + 4]};
@@ -790,7 +792,9 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             {   // T'_{[23][01]} = -T'_{[23][23]} X
                 const int mt = warp >> 2, nt = warp & 3, r0 = 32 + 16 * mt;
                 float c[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int ks = 0; ks < 2 * mt + 2; ++ks) {  // T'(r, 32 + k) = 0 for k > r - 32
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {  // T'(r, 32 + k) = 0 for k > r - 32
+                    if (ks >= 2 * mt + 2) break;
                     const int k0 = 8 * ks;
                     const float af[4] = {*tp_at(kq, r0 + fg, 32 + k0 + ft), *tp_at(kq, r0 + fg + 8, 32 + k0 + ft),
                                          *tp_at(kq, r0 + fg, 32 + k0 + ft + 4),
