@@ -511,12 +511,13 @@ decode_step_head_kernel(DecodeStepArgs a) {
     }
 }
 
-template <typename K>
-cudaError_t launch_cluster(K kernel, unsigned grid, unsigned block, unsigned cluster, cudaStream_t s,
-                           const DecodeStepArgs& a) {
+template <typename K, typename Args>
+cudaError_t launch_cluster(K kernel, unsigned grid, unsigned block, size_t smem, unsigned cluster, cudaStream_t s,
+                           const Args& a) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -550,8 +551,8 @@ cudaError_t decode_step_t(const DecodeStepArgs& a, cudaStream_t s) {
     // B = 8 the per-key-head CTAs are faster)
     if ((int64_t)units * 2 <= device_sms()) {
         const unsigned heads = (unsigned)(a.B * a.H_v);
-        return a.D == 128 ? launch_cluster(decode_step_head_kernel<T, 128, 8>, heads, 256, (unsigned)r, s, a)
-                          : launch_cluster(decode_step_head_kernel<T, 16, 1>, heads, 32, (unsigned)r, s, a);
+        return a.D == 128 ? launch_cluster(decode_step_head_kernel<T, 128, 8>, heads, 256, 0, (unsigned)r, s, a)
+                          : launch_cluster(decode_step_head_kernel<T, 16, 1>, heads, 32, 0, (unsigned)r, s, a);
     }
     if (a.D == 128)
         decode_step_kernel<T, 128, 8, 8><<<units, 256, 0, s>>>(a);
@@ -779,6 +780,224 @@ decode_verify_kernel(DecodeVerifyArgs a) {
     }
 }
 
+// Verification for small batches: one CTA per (sequence, value head), the r
+// value heads of a key head as a thread-block cluster, as the small-batch
+// decode step.  The first CTA of the cluster convolves q and k over the K
+// tokens (writing their conv states to the slots) and sends them to the others
+// through distributed shared memory; every CTA convolves its head's v and runs
+// its head through the K tokens with decode_verify_kernel's arithmetic, so the
+// states and outputs are the same bit for bit.
+template <typename T, int D, int NW>
+__global__ void __launch_bounds__(NW * 32, (D >= 128 ? 2 : 1))
+decode_verify_head_kernel(DecodeVerifyArgs a) {
+    constexpr int NT = NW * 32;
+    constexpr int TPR = D / 4;
+    constexpr int RPP = NT / TPR;
+    constexpr int PASSES = D / RPP;
+    constexpr int V = Vec16<T>::N;
+    static_assert(NT % TPR == 0 && D % RPP == 0 && NT >= D, "layout");
+
+    const int r = a.H_v / a.H_k, K = a.K;
+    const int b = blockIdx.x / a.H_v;
+    const int h = blockIdx.x - b * a.H_v;
+    const int kh = h / r, rank = h - kh * r;  // rank in the key head's cluster
+    const bool cl = r > 1;
+    if (cl) cluster_arrive_relaxed();  // this CTA has started (waited for before any remote store)
+    const int32_t* sl = a.slots + (int64_t)b * (K + 1);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cq = tid % TPR;
+    const int r0 = tid / TPR;
+    const int C = 2 * a.H_k * D + a.H_v * D;
+
+    extern __shared__ __align__(16) float vsm[];
+    float* qs = vsm;                  // [K][D]
+    float* ks = qs + K * D;           // [K][D]
+    float* vs = ks + K * D;           // [K][D]
+    float* zs = vs + K * D;           // [K][D]: the gate input z
+    float* ds = zs + K * D;           // [D]
+    float* os = ds + D;               // [D]
+    float* red = os + D;              // [2][RPP][D]
+    float* gb = red + 2 * RPP * D;    // [K][2]: g, beta
+    float* nrm = gb + 2 * K;          // [K][3]: rq, rk, k.q rq rk
+    float* wsum = nrm + 3 * K;        // [NW]
+
+    const int64_t s_in = sl[0];
+    {   // the head's state into L2 ahead of its register loads
+        const char* S = reinterpret_cast<const char*>(a.state + (s_in * a.H_v + h) * D * D);
+        for (int off = tid * 128; off < D * D * 4; off += NT * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(S + off));
+    }
+    // 1. conv over the K tokens of the channels this CTA owns (q and k in the
+    //    first CTA of the cluster, then the head's v)
+    {
+        const T* x = static_cast<const T*>(a.x) + (int64_t)b * K * C;
+        const T* w = static_cast<const T*>(a.conv_w);
+        T* cs = static_cast<T*>(a.conv_state);
+        const int g0 = rank == 0 ? 0 : 2;
+        const int nvec = (3 - g0) * D / V;
+        for (int e = tid; e < nvec; e += NT) {
+            const int grp = g0 + (e * V) / D, i0 = e * V - (grp - g0) * D;
+            const int c0 = grp == 0 ? kh * D + i0 : grp == 1 ? a.H_k * D + kh * D + i0 : 2 * a.H_k * D + h * D + i0;
+            float st[3 * V], wt[4 * V];
+#pragma unroll
+            for (int k = 0; k < 3; ++k) load16(cs + (s_in * C + c0) * 3 + k * V, st + k * V);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) load16(w + (int64_t)c0 * 4 + k * V, wt + k * V);
+            float* dst = (grp == 0 ? qs : grp == 1 ? ks : vs) + i0;
+            for (int t = 0; t < K; ++t) {
+                float xv[V];
+                load16(x + (int64_t)t * C + c0, xv);
+#pragma unroll
+                for (int q = 0; q < V; ++q) {
+                    float acc = wt[q * 4] * st[q * 3];
+                    acc = fmaf(wt[q * 4 + 1], st[q * 3 + 1], acc);
+                    acc = fmaf(wt[q * 4 + 2], st[q * 3 + 2], acc);
+                    acc = fmaf(wt[q * 4 + 3], xv[q], acc);
+                    dst[t * D + q] = to_f(from_f<T>(silu_f(acc)));
+                    st[q * 3] = st[q * 3 + 1];  // the window moves one token
+                    st[q * 3 + 1] = st[q * 3 + 2];
+                    st[q * 3 + 2] = xv[q];
+                }
+                T* out_cs = cs + ((int64_t)sl[t + 1] * C + c0) * 3;
+#pragma unroll
+                for (int k = 0; k < 3; ++k) store16(out_cs + k * V, st + k * V);
+            }
+        }
+        for (int t = tid; t < K; t += NT) {
+            const int64_t gi = ((int64_t)b * K + t) * a.H_v + h;
+            gb[2 * t] = gate_g(to_f(static_cast<const T*>(a.a)[gi]), a.A_log[h], a.dt_bias[h]);
+            gb[2 * t + 1] = sigmoid_f(to_f(static_cast<const T*>(a.b)[gi]));
+        }
+        const T* zg = static_cast<const T*>(a.z) + ((int64_t)b * K * a.H_v + h) * D;
+        for (int e = tid; e < K * D / V; e += NT) {
+            const int t = (e * V) / D, o = e * V - t * D;
+            float zv[V];
+            load16(zg + (int64_t)t * a.H_v * D + o, zv);
+#pragma unroll
+            for (int q = 0; q < V; ++q) zs[t * D + o + q] = zv[q];
+        }
+    }
+    __syncthreads();
+    if (cl) {
+        // q and k of the K tokens from the first CTA to the others
+        cluster_wait();
+        if (rank == 0) {
+            const int per = K * D / 2;  // float4s of qs and ks (contiguous)
+            for (int e = tid; e < (r - 1) * per; e += NT) {
+                const int dst = 1 + e / per, i = e - (dst - 1) * per;
+                st_cluster_v4(qs + 4 * i, (uint32_t)dst, *reinterpret_cast<const float4*>(qs + 4 * i));
+            }
+        }
+        cluster_sync();
+    }
+    float4 s[PASSES];
+    {
+        const float* S = a.state + (s_in * a.H_v + h) * D * D;
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p)
+            s[p] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(r0 + p * RPP) * D) + cq);
+    }
+    for (int t = warp; t < K; t += NW) {
+        float sq = 0.f, sk = 0.f, sqk = 0.f;
+        for (int i = lane; i < D; i += 32) {
+            sq = fmaf(qs[t * D + i], qs[t * D + i], sq);
+            sk = fmaf(ks[t * D + i], ks[t * D + i], sk);
+            sqk = fmaf(qs[t * D + i], ks[t * D + i], sqk);
+        }
+        sq = warp_sum(sq);
+        sk = warp_sum(sk);
+        sqk = warp_sum(sqk);
+        float rq = a.scale, rk = 1.f;
+        if (a.l2norm) {
+            rq = a.scale / sqrtf(sq + 1e-6f);
+            rk = 1.f / sqrtf(sk + 1e-6f);
+        }
+        if (lane == 0) {
+            nrm[3 * t] = rq;
+            nrm[3 * t + 1] = rk;
+            nrm[3 * t + 2] = sqk * rq * rk;
+        }
+    }
+    __syncthreads();
+
+    // 2. the head through the K tokens, its state in registers
+    for (int t = 0; t < K; ++t) {
+        const float rq = nrm[3 * t], rk = nrm[3 * t + 1], kq = nrm[3 * t + 2];
+        const float* kt = ks + t * D;
+        const float* qt = qs + t * D;
+        float mk[4] = {0.f, 0.f, 0.f, 0.f}, mq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p) {
+            const int i = r0 + p * RPP;
+            const float kv = kt[i] * rk, qv = qt[i] * rq;
+            mk[0] = fmaf(s[p].x, kv, mk[0]); mk[1] = fmaf(s[p].y, kv, mk[1]);
+            mk[2] = fmaf(s[p].z, kv, mk[2]); mk[3] = fmaf(s[p].w, kv, mk[3]);
+            mq[0] = fmaf(s[p].x, qv, mq[0]); mq[1] = fmaf(s[p].y, qv, mq[1]);
+            mq[2] = fmaf(s[p].z, qv, mq[2]); mq[3] = fmaf(s[p].w, qv, mq[3]);
+        }
+        *reinterpret_cast<float4*>(&red[r0 * D + cq * 4]) = make_float4(mk[0], mk[1], mk[2], mk[3]);
+        *reinterpret_cast<float4*>(&red[(RPP + r0) * D + cq * 4]) = make_float4(mq[0], mq[1], mq[2], mq[3]);
+        __syncthreads();
+        const float eg = expf(gb[2 * t]);
+        const float bt = gb[2 * t + 1];
+        const float* vt = vs + t * D;
+        float o2 = 0.f;
+        for (int c = tid; c < D; c += NT) {
+            float m = 0.f, pq = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < RPP; ++rr) {
+                m += red[rr * D + c];
+                pq += red[(RPP + rr) * D + c];
+            }
+            const float delta = bt * (vt[c] - eg * m);
+            ds[c] = delta;
+            const float o = to_f(from_f<T>(eg * pq + kq * delta));
+            os[c] = o;
+            o2 = fmaf(o, o, o2);
+        }
+        o2 = warp_sum(o2);
+        if (lane == 0) wsum[warp] = o2;
+        __syncthreads();
+        float* S = a.state + ((int64_t)sl[t + 1] * a.H_v + h) * D * D;
+        const float4 d4 = *reinterpret_cast<const float4*>(&ds[cq * 4]);
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p) {
+            const int i = r0 + p * RPP;
+            const float kv = kt[i] * rk;
+            float4 n;
+            n.x = fmaf(kv, d4.x, eg * s[p].x);
+            n.y = fmaf(kv, d4.y, eg * s[p].y);
+            n.z = fmaf(kv, d4.z, eg * s[p].z);
+            n.w = fmaf(kv, d4.w, eg * s[p].w);
+            s[p] = n;
+            __stcs(reinterpret_cast<float4*>(S + (int64_t)i * D) + cq, n);
+        }
+        float tot = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < NW; ++ww) tot += wsum[ww];
+        const float rs = rsqrtf(tot / (float)D + a.eps);
+        const int64_t row = ((int64_t)b * K + t) * a.H_v + h;
+        const float* z = zs + t * D;
+        T* out = static_cast<T*>(a.out) + row * D;
+        const T* nw = static_cast<const T*>(a.norm_w);
+        for (int c = 2 * tid; c < D; c += 2 * NT) {
+            const float2 g = silu2<T>(make_float2(z[c], z[c + 1]));
+            const float2 res = __fmul2_rn(__fmul2_rn(make_float2(to_f(nw[c]), to_f(nw[c + 1])),
+                                                     __fmul2_rn(make_float2(os[c], os[c + 1]), make_float2(rs, rs))),
+                                          g);
+            out[c] = from_f<T>(res.x);
+            out[c + 1] = from_f<T>(res.y);
+        }
+        __syncthreads();  // red, ds, os and wsum are reused by the next token
+    }
+}
+
+template <int D, int NW>
+size_t verify_head_smem_bytes(int K) {
+    constexpr int RPP = NW * 32 / (D / 4);
+    return sizeof(float) * ((size_t)4 * K * D + 2 * D + 2 * RPP * D + 2 * K + 3 * K + NW);
+}
+
 template <int D, int NW>
 size_t verify_smem_bytes(int K, int r) {
     constexpr int RPP = NW * 32 / (D / 4);
@@ -791,6 +1010,25 @@ cudaError_t decode_verify_t(const DecodeVerifyArgs& a, cudaStream_t s) {
     if (units == 0 || a.K == 0) return cudaSuccess;
     const int r = a.H_v / a.H_k;
     if (r > 8 || a.K > kVerifyMaxK) return cudaErrorNotSupported;
+    if ((int64_t)units * 2 <= device_sms()) {
+        // few (sequence, key head) units: one clustered CTA per value head (27B,
+        // B = 1, K = 4: 21.8 against 34.8 us; from B = 8 the per-key-head CTAs
+        // are faster)
+        const unsigned heads = (unsigned)(a.B * a.H_v);
+        if (a.D == 128) {
+            const size_t smem = verify_head_smem_bytes<128, 8>(a.K);
+            cudaError_t e = cudaFuncSetAttribute(decode_verify_head_kernel<T, 128, 8>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            return e != cudaSuccess ? e
+                                    : launch_cluster(decode_verify_head_kernel<T, 128, 8>, heads, 256, smem,
+                                                     (unsigned)r, s, a);
+        }
+        const size_t smem = verify_head_smem_bytes<16, 1>(a.K);
+        cudaError_t e = cudaFuncSetAttribute(decode_verify_head_kernel<T, 16, 1>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        return e != cudaSuccess ? e
+                                : launch_cluster(decode_verify_head_kernel<T, 16, 1>, heads, 32, smem, (unsigned)r, s, a);
+    }
     if (a.D == 128) {
         const size_t smem = verify_smem_bytes<128, 8>(a.K, r);
         cudaError_t e = cudaFuncSetAttribute(decode_verify_kernel<T, 128, 8>,

@@ -569,6 +569,37 @@ def test_fused_decode_step_alone_equals_inside_a_batch(heads):
             assert torch.equal(cs_1[j][0], cs_b[i]), f"conv state, sequence {i}, step {t}"
 
 
+@pytest.mark.parametrize("heads,K", [((16, 48), 4), ((2, 16), 16), ((4, 4), 3)])
+def test_decode_verify_alone_equals_inside_a_batch(heads, K):
+    """gdn_decode_verify, like the fused step, runs one clustered CTA per
+    (sequence, value head) for small batches and one CTA per (sequence, key
+    head) for large ones.  A sequence verified alone gives the same outputs,
+    states and conv states in every slot bit for bit as the same sequence
+    inside a batch of 64 (r = 3, 8, 1; K = 4, 16, 3)."""
+    H_k, H_v = heads
+    shape = W.GDNShape(H_k=H_k, H_v=H_v, d_k=128, d_v=128)
+    B = 64
+    d = {k: v.cuda() for k, v in W.decode_inputs(shape, torch.bfloat16, B * K, 1, seed=53).items()}
+    x, z, a, b = (d[k][0].reshape(B, K, -1) for k in ("qkv", "z", "a", "b"))
+    p = {k: v.cuda() for k, v in W.layer_params(shape, torch.bfloat16, seed=53).items()}
+    n_slots = B * (K + 1)
+    S0 = W.draw((n_slots, H_v, 128, 128), seed=53, stream=64, dtype=torch.float32, p1=0.02).cuda()
+    cs0 = W.draw((n_slots, shape.conv_dim, 3), seed=53, stream=65, dtype=torch.bfloat16).cuda()
+    slots = torch.arange(n_slots, dtype=torch.int32).reshape(B, K + 1).flip(1).contiguous().cuda()
+    args = (p["conv_w"], p["A_log"], p["dt_bias"], p["norm_w"], _dims(shape))
+    S_b, cs_b = S0.clone(), cs0.clone()
+    out_b = gdn.gdn_decode_verify(x, z, a, b, *args, S_b, cs_b, slots)
+    for i in [0, 41, 63]:
+        S_1, cs_1 = S0.clone(), cs0.clone()
+        out_1 = gdn.gdn_decode_verify(x[i:i + 1], z[i:i + 1], a[i:i + 1], b[i:i + 1], *args, S_1, cs_1,
+                                      slots[i:i + 1])
+        gdn.gdn_sync_status()
+        assert torch.equal(out_1[0], out_b[i]), f"outputs, sequence {i}"
+        own = slots[i].long()
+        assert torch.equal(S_1[own], S_b[own]), f"states, sequence {i}"
+        assert torch.equal(cs_1[own], cs_b[own]), f"conv states, sequence {i}"
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 # r = 8 value heads per key head with K = 16 is the largest shared-memory request
 # of the verification kernel (158 KB)
