@@ -388,6 +388,9 @@ gdn_status_t gdn_decode_step(const void* x, const void* conv_w, void* conv_state
  *   out        (device) [B, K, H_v*d_v] dtype
  * 1 <= K <= 16 (K = 0 or B = 0: nothing to do), H_v / H_k <= 8.  Every output
  * and every state equals that of K successive gdn_decode_step calls, bit for bit.
+ * Batches whose B*H_k is at most half the SM count run, like the fused step,
+ * one CTA per sequence and value head (clustered per key head), with the same
+ * results.
  */
 gdn_status_t gdn_decode_verify(const void* x, const void* conv_w, void* conv_state, const void* z,
                                const void* a, const void* b, const float* A_log,
