@@ -497,8 +497,33 @@ def run_ours(args):
     chunk_solve = {"direct_ms": round(chunk_avg * 1e3, 4), "neumann_ms": round(neumann_ms, 4),
                    "call": "gdn_chunk_prefill, flags GDN_QK_L2NORM vs | GDN_SOLVE_NEUMANN"}
 
-    # chunk-size sweep on the CUDA-core path (f32 arithmetic; the tensor-core
-    # kernels are built around C = 64): the same workload in f32
+    # chunk-size sweep on the tensor-core path (bf16; a chunk of 16 or 32 tokens
+    # fills the first rows of a 64-row tile, over more workspace segments)
+    tc_sweep = {}
+    for c in (16, 32, 64):
+        def tc_chunk():
+            gdn.gdn_chunk_prefill(y, dims, d["a"], d["b"], d["A_log"], d["dt_bias"], final_state=S, o=o, chunk=c)
+        for _ in range(args.warmup):
+            flush.zero_()
+            tc_chunk()
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        torch.cuda.synchronize(dev)
+        clocks.mark(True)
+        for k in range(args.steps):
+            flush.zero_()
+            cev[k][0].record(stream)
+            tc_chunk()
+            cev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        clocks.mark(False)
+        launches += args.steps * gdn.gdn_chunk_prefill_launches(1, T, dims, wp.dtype, cu_seqlens=None, chunk=c)
+        ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in cev)
+        tc_sweep[str(c)] = {"ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1),
+                            "launches": gdn.gdn_chunk_prefill_launches(1, T, dims, wp.dtype, cu_seqlens=None,
+                                                                       chunk=c)}
+
+    # and on the CUDA-core path (f32 arithmetic): the same workload in f32
     yf = y.float()
     af, bf_ = d["a"].float(), d["b"].float()
     of = torch.empty((T, s.H_v, s.d_v), dtype=torch.float32, device=dev)
@@ -519,8 +544,8 @@ def run_ours(args):
         ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in cev)
         sweep[str(c)] = {"ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1)}
     del yf, af, bf_, of
-    chunk_sweep = {"path": "CUDA-core (f32 FFMA), f32 copies of the workload", "by_chunk": sweep,
-                   "tensor_core_c64_ms": round(chunk_avg * 1e3, 4),
+    chunk_sweep = {"tensor_core": {"path": "tcgen05 (bf16 operands, f32 state)", "by_chunk": tc_sweep},
+                   "cuda_core": {"path": "CUDA-core (f32 FFMA), f32 copies of the workload", "by_chunk": sweep},
                    "call": "gdn_chunk_prefill, flags | GDN_CHUNK(c)"}
     flops = FLOP_PER_TOKEN_HEAD * T * s.H_v
     achieved_tf = flops / chunk_avg / 1e12

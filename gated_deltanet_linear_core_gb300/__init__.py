@@ -172,12 +172,14 @@ def gdn_chunk_prefill_workspace_size(n_seq: int, T_tot: int, dims, dtype) -> int
                                                             code))
 
 
-def gdn_chunk_prefill_launches(n_seq: int, T_tot: int, dims, dtype, cu_seqlens=True) -> int:
+def gdn_chunk_prefill_launches(n_seq: int, T_tot: int, dims, dtype, cu_seqlens=True, chunk=64) -> int:
     """Kernel launches of one gdn_chunk_prefill call; cu_seqlens: whether the
-    call passes cu_seqlens (a truthy value) or not (None / False)."""
+    call passes cu_seqlens (a truthy value) or not (None / False); chunk: its
+    chunk size (16, 32 or 64)."""
     code = _lib.GDN_BF16 if dtype == torch.bfloat16 else _lib.GDN_F32
     has_cu = 0 if cu_seqlens is None or cu_seqlens is False else 1
-    return int(_lib.load().gdn_chunk_prefill_launches(int(n_seq), int(T_tot), has_cu, _dims(dims), code))
+    return int(_lib.load().gdn_chunk_prefill_launches(int(n_seq), int(T_tot), has_cu, _dims(dims), code,
+                                                      _flags(False, "direct", chunk)))
 
 
 def _flags(l2norm_qk, solve, chunk) -> int:
@@ -201,7 +203,7 @@ def gdn_chunk_prefill(qkv, dims, a=None, b=None, A_log=None, dt_bias=None, g=Non
     (post-conv); states [n_seq, H_v, d_k, d_v] f32; returns o [T, H_v, d_v].
     solve="neumann" forms each chunk's (I + A)^-1 as the Neumann-style product
     (GDN_SOLVE_NEUMANN; tensor-core path only).  chunk: 16, 32 or 64 tokens
-    (GDN_CHUNK; the tensor-core path takes 64 only)."""
+    (GDN_CHUNK; on the tensor-core path 16 and 32 need final_state)."""
     if solve not in ("direct", "neumann"):
         raise ValueError(f"solve must be 'direct' or 'neumann', not {solve!r}")
     dt = qkv.dtype
@@ -321,12 +323,13 @@ def gdn_layer_prefill_workspace_size(n_seq: int, T_tot: int, dims, dtype) -> int
     return int(_lib.load().gdn_layer_prefill_workspace_size(int(n_seq), int(T_tot), _dims(dims), code))
 
 
-def gdn_layer_prefill_launches(n_seq: int, T_tot: int, dims, dtype, cu_seqlens=True) -> int:
-    """Kernel launches of one gdn_layer_prefill call (cu_seqlens as in
-    gdn_chunk_prefill_launches)."""
+def gdn_layer_prefill_launches(n_seq: int, T_tot: int, dims, dtype, cu_seqlens=True, chunk=64) -> int:
+    """Kernel launches of one gdn_layer_prefill call (cu_seqlens and chunk as
+    in gdn_chunk_prefill_launches)."""
     code = _lib.GDN_BF16 if dtype == torch.bfloat16 else _lib.GDN_F32
     has_cu = 0 if cu_seqlens is None or cu_seqlens is False else 1
-    return int(_lib.load().gdn_layer_prefill_launches(int(n_seq), int(T_tot), has_cu, _dims(dims), code))
+    return int(_lib.load().gdn_layer_prefill_launches(int(n_seq), int(T_tot), has_cu, _dims(dims), code,
+                                                      _flags(False, "direct", chunk)))
 
 
 def gdn_layer_prefill(mixed_qkv, z, a, b, conv_w, A_log, dt_bias, norm_w, dims, cu_seqlens=None,

@@ -59,7 +59,7 @@ SIGNATURES = {
     "gdn_conv1d_fwd": (ST, [P, P, P, I32, I64, P, P, I32, P, I64, I32, P, Dims, ST, P]),
     "gdn_conv1d_update": (ST, [P, P, P, I32, I32, P, Dims, ST, P]),
     "gdn_chunk_prefill_workspace_size": (SZ, [I32, I64, Dims, ST]),
-    "gdn_chunk_prefill_launches": (I32, [I32, I64, I32, Dims, ST]),
+    "gdn_chunk_prefill_launches": (I32, [I32, I64, I32, Dims, ST, U32]),
     "gdn_chunk_prefill": (ST, [P, P, P, P, P, P, P, P, I32, I64, P, P, I32, P, I64, F32, U32, P,
                                P, SZ, Dims, ST, P]),
     "gdn_chunk_prefill_noalloc": (ST, [P, P, P, P, P, P, P, P, I32, I64, P, P, I32, P, I64, F32, U32,
@@ -68,7 +68,7 @@ SIGNATURES = {
     "gdn_chunk_prefill_norm": (ST, [P, P, P, P, P, P, P, P, I32, I64, P, P, I32, P, I64, F32, U32, P, P, F32,
                                     P, P, SZ, Dims, ST, P]),
     "gdn_layer_prefill_workspace_size": (SZ, [I32, I64, Dims, ST]),
-    "gdn_layer_prefill_launches": (I32, [I32, I64, I32, Dims, ST]),
+    "gdn_layer_prefill_launches": (I32, [I32, I64, I32, Dims, ST, U32]),
     "gdn_layer_prefill": (ST, [P, P, P, P, P, P, P, P, F32, P, I32, I64, P, P, P, P, I32, P, P, I64, F32, U32,
                                P, P, SZ, Dims, ST, P]),
     "gdn_rmsnorm_gated": (ST, [P, P, P, F32, I64, P, Dims, ST, P]),

@@ -52,6 +52,12 @@ using namespace tc;
 typedef __half f16;
 
 constexpr int C = 64;
+
+// Tokens per chunk: C, or 16 or 32 (GDN_CHUNK).  The kernels' tiles stay C rows;
+// a shorter chunk fills the first rows of its tile, as a partial chunk does.
+__host__ __device__ __forceinline__ int chunk_len(const DeltaArgs& a) {
+    return a.chunk == 16 || a.chunk == 32 ? a.chunk : C;
+}
 constexpr int D = 128;
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr size_t kSegBytes = 1024ull << 20;  // workspace intermediates per segment
@@ -121,6 +127,13 @@ Layout layout_of(int n_seq, int64_t T, int H_v, int q_heads = 0) {
     return layout_for(n_seq, T, H_v, kSegBytes, (size_t)n_seq + 1, true, true, true, q_heads);
 }
 
+// Segments of a call whose chunks hold clen tokens, with the layout's segment
+// size (so the same buffers): for clen < C more of them.
+int64_t segments_for(const Layout& L, int n_seq, int64_t T, int clen) {
+    const int64_t max_chunks = T / clen + n_seq;
+    return (max_chunks + L.segc - 1) / L.segc;
+}
+
 // The intermediates of buffer `buf` (0 or 1) of a layout.
 Work work_at(uint8_t* base, const Layout& L, int H_v, int buf = 0) {
     const size_t U = (size_t)L.segc * H_v;
@@ -142,7 +155,7 @@ Work work_at(uint8_t* base, const Layout& L, int H_v, int buf = 0) {
 // `order`, also the sequences sorted by chunk count, most first (ties in
 // sequence order; up to 1024 sequences, else in order), so that the chain
 // kernel starts the longest sequences' CTAs first
-__global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, int n_seq, int64_t T,
+__global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, int n_seq, int64_t T, int clen,
                                                              int32_t* coff, int32_t* order) {
     pdl_wait();
     pdl_trigger();
@@ -160,7 +173,7 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, 
         if (i < n_seq) {
             int64_t s, e;
             seq_bounds(cu, i, T, s, e);
-            v = (int)((e - s + C - 1) / C);
+            v = (int)((e - s + clen - 1) / clen);
         }
         int x = v;
 #pragma unroll
@@ -255,12 +268,13 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     const int64_t gc = C0 + blockIdx.y;
     // first token and length of chunk gc, its sequence and that sequence's
     // first and end tokens (no loads for one sequence without offsets)
+    const int clen = chunk_len(a);
     int64_t t0, s0 = 0, s1 = a.T;
     int n, seq = 0;
     if (a.cu == nullptr) {
-        t0 = gc * C;
+        t0 = gc * clen;
         if (t0 >= a.T) return;  // past the last chunk of the call
-        n = (int)(a.T - t0 < C ? a.T - t0 : C);
+        n = (int)(a.T - t0 < clen ? a.T - t0 : clen);
     } else {
         if (gc >= w.coff[a.n_seq]) return;
         int lo_s = 0, hi_s = a.n_seq - 1;  // sequence of chunk gc
@@ -270,8 +284,8 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         }
         seq_bounds(a.cu, lo_s, a.T, s0, s1);
         seq = lo_s;
-        t0 = s0 + (gc - w.coff[lo_s]) * C;
-        n = (int)(s1 - t0 < C ? s1 - t0 : C);
+        t0 = s0 + (gc - w.coff[lo_s]) * clen;
+        n = (int)(s1 - t0 < clen ? s1 - t0 : clen);
     }
     const int kh = h / (a.H_v / a.H_k);
     const int xq = kh * D, xk = a.H_k * D + kh * D, xv = 2 * a.H_k * D + h * D;
@@ -478,7 +492,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                     x[2] = __uint_as_float(v.y << 16);
                     x[3] = __uint_as_float(v.y & 0xffff0000u);
                 };
-                float x0[4], x1[4], x2[4], x3[4];
+                float x0[4], x1[4], x2[4];
                 if (rg == 0 && t0 == s0) {
                     // a sequence's first chunk: the inputs before it are its conv
                     // state ([conv_dim][3], column 0 oldest), or zeros
@@ -1033,7 +1047,9 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
     if (lane == 0) mbar_arrive(bar);
 }
 
-template <int VS>
+// CL: tokens per chunk (C, or 16 / 32), fixed at compile time so that the
+// per-chunk arithmetic of C-token chunks stays constant-folded
+template <int VS, int CL>
 __global__ void __launch_bounds__(NT_C, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
                    const __grid_constant__ CUtensorMap utmap, const __grid_constant__ CUtensorMap pmap,
@@ -1050,9 +1066,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     const int seq_rank = blockIdx.x / (NV * a.H_v);  // CTAs start in this order: longest sequences first
     const int seq = a.cu != nullptr && w.order != nullptr ? w.order[seq_rank] : seq_rank;
     const int v0 = vp * VS;
-    // chunk offsets of the sequence (one sequence without offsets: [0, ceil(T / C)))
+    // chunk offsets of the sequence (one sequence without offsets: [0, ceil(T / CL)))
+    constexpr int clen = CL;
     const int64_t cs = a.cu == nullptr ? 0 : w.coff[seq];
-    const int64_t ce = a.cu == nullptr ? (a.T + C - 1) / C : w.coff[seq + 1];
+    const int64_t ce = a.cu == nullptr ? (a.T + clen - 1) / clen : w.coff[seq + 1];
     const int64_t c_lo = cs > C0 ? cs : C0, c_hi = ce < C0 + segc ? ce : C0 + segc;
     const int64_t sbase = ((int64_t)seq * a.H_v + h) * D * D;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1141,7 +1158,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 const int64_t uu = (gcc - C0) * a.H_v + h;
                 // q from qkv, or the intra kernel's conv'd q tile of (chunk, key head)
                 const int qx = w.q != nullptr ? 0 : xq;
-                const int qy = w.q != nullptr ? (int)(((gcc - C0) * a.H_k + kh) * 64) : (int)(s0 + (gcc - cs) * C);
+                const int qy = w.q != nullptr ? (int)(((gcc - C0) * a.H_k + kh) * 64) : (int)(s0 + (gcc - cs) * clen);
                 mbar_arrive_expect_tx(&full[b], Ly::STAGE + Ly::VEC);
                 tma_load_2d(st + Ly::SG_QW, &qmap, &full[b], qx, qy);
                 tma_load_2d(st + Ly::SG_QW + 8192, &wmap, &full[b], 0, (int)(uu * 64));
@@ -1169,7 +1186,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             for (int k = 0; k < nch; ++k) {
                 if (!mbar_wait_or_abort(&o_staged[k % NST], (uint32_t)((k / NST) & 1), abort_flag)) break;
                 const int64_t lc = c_lo + k - cs;
-                if (L - lc * C >= C) {
+                if (clen == C && L - lc * C >= C) {  // a full tile of C rows
                     uint8_t* otile = stage_of(k) + Ly::SG_P;
 #pragma unroll
                     for (int nb = 0; nb < Ly::NB; ++nb)
@@ -1269,8 +1286,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             const float* vs = reinterpret_cast<const float*>(vec_of(k));
             const int64_t gcc = c_lo + k;
             const int64_t lc = gcc - cs;
-            const int64_t t0 = s0 + lc * C;
-            const int n = (int)(L - lc * C < C ? L - lc * C : C);
+            const int64_t t0 = s0 + lc * clen;
+            const int n = (int)(L - lc * clen < clen ? L - lc * clen : clen);
 
             if (!warp_wait(&full[k % NST], (uint32_t)((k / NST) & 1), abort_flag)) break;
             if (!warp_wait(m1, par, abort_flag)) break;
@@ -1304,7 +1321,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             if (!warp_wait(m2, par, abort_flag)) break;
             tc_fence_after();
             {
-                const int64_t done = lc * C + n;
+                const int64_t done = lc * clen + n;
                 float* ck = nullptr;
                 if (a.ckpt_every > 0 && a.ckpt != nullptr && done % a.ckpt_every == 0) {
                     const int64_t crow = ck_row0 + done / a.ckpt_every - 1;
@@ -1475,12 +1492,16 @@ cudaError_t run_segments(const DeltaArgs& a, const Work* w, int nbuf, const Layo
     for (const void* k : {(const void*)chunk_intra_kernel<false, false>, (const void*)chunk_intra_kernel<true, false>,
                           (const void*)chunk_intra_kernel<false, true>, (const void*)chunk_intra_kernel<true, true>})
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ISMEM);
+    // the chain kernel for this call's chunk length
+    const int clen = chunk_len(a);
+    auto chain64 = clen == 16 ? chunk_chain_kernel<64, 16> : clen == 32 ? chunk_chain_kernel<64, 32>
+                                                                        : chunk_chain_kernel<64, C>;
+    auto chain128 = clen == 16 ? chunk_chain_kernel<128, 16> : clen == 32 ? chunk_chain_kernel<128, 32>
+                                                                          : chunk_chain_kernel<128, C>;
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(chunk_chain_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ChainLayout<64>::SMEM);
+        e = cudaFuncSetAttribute(chain64, cudaFuncAttributeMaxDynamicSharedMemorySize, ChainLayout<64>::SMEM);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(chunk_chain_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ChainLayout<128>::SMEM);
+        e = cudaFuncSetAttribute(chain128, cudaFuncAttributeMaxDynamicSharedMemorySize, ChainLayout<128>::SMEM);
     if (e != cudaSuccess) return e;
 
     const bool two = ev_pre != nullptr && Ly.n_seg == 1;
@@ -1509,7 +1530,7 @@ cudaError_t run_segments(const DeltaArgs& a, const Work* w, int nbuf, const Layo
         }
     }
     cudaStream_t si = two ? s_pre : s;
-    if (a.cu != nullptr && (e = launch_pdl(chunk_offsets_kernel, dim3(1), dim3(1024), 0, si, a.cu, a.n_seq, a.T,
+    if (a.cu != nullptr && (e = launch_pdl(chunk_offsets_kernel, dim3(1), dim3(1024), 0, si, a.cu, a.n_seq, a.T, chunk_len(a),
                                            w[0].coff, w[0].order)) != cudaSuccess) {
         release();
         return e;
@@ -1546,11 +1567,11 @@ cudaError_t run_segments(const DeltaArgs& a, const Work* w, int nbuf, const Layo
                 break;
         }
         if (split)
-            e = launch_pdl(chunk_chain_kernel<64>, dim3((unsigned)(a.n_seq * a.H_v * 2)), dim3(NT_C),
+            e = launch_pdl(chain64, dim3((unsigned)(a.n_seq * a.H_v * 2)), dim3(NT_C),
                            ChainLayout<64>::SMEM, s, cq[b], wtmap[b], utmap[b], pmap[b], omap, kdmap[b], a, w[b], C0,
                            Ly.segc);
         else
-            e = launch_pdl(chunk_chain_kernel<128>, dim3((unsigned)(a.n_seq * a.H_v)), dim3(NT_C),
+            e = launch_pdl(chain128, dim3((unsigned)(a.n_seq * a.H_v)), dim3(NT_C),
                            ChainLayout<128>::SMEM, s, cq[b], wtmap[b], utmap[b], pmap[b], omap, kdmap[b], a, w[b], C0,
                            Ly.segc);
         if (e != cudaSuccess) break;
@@ -1570,12 +1591,13 @@ size_t chunk_split_conv_workspace_bytes(int n_seq, int64_t T, int H_k, int H_v) 
     return layout_of(n_seq, T, H_v, H_k).total;
 }
 
-int chunk_split_launches(int n_seq, int64_t T, int H_v, bool has_cu) {
-    return (has_cu ? 1 : 0) + 2 * (int)layout_of(n_seq, T, H_v).n_seg;
+int chunk_split_launches(int n_seq, int64_t T, int H_v, bool has_cu, int chunk) {
+    const int clen = chunk == 16 || chunk == 32 ? chunk : C;
+    return (has_cu ? 1 : 0) + 2 * (int)segments_for(layout_of(n_seq, T, H_v), n_seq, T, clen);
 }
 
 cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s) {
-    const Layout Ly = layout_of(a.n_seq, a.T, a.H_v, a.conv_w != nullptr ? a.H_k : 0);
+    Layout Ly = layout_of(a.n_seq, a.T, a.H_v, a.conv_w != nullptr ? a.H_k : 0);
     if (workspace == nullptr || ws_bytes < Ly.total) return cudaErrorInvalidValue;
     Work w[2];
     const int nbuf = Ly.two_bufs() ? 2 : 1;
@@ -1583,6 +1605,10 @@ cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_by
         w[i] = work_at(static_cast<uint8_t*>(workspace), Ly, a.H_v, i);
         if (a.S_final != nullptr) w[i].carry = a.S_final;
     }
+    // shorter chunks: the same buffers over more segments, the state carried
+    // between them through final_state when the layout has no carry of its own
+    Ly.n_seg = segments_for(Ly, a.n_seq, a.T, chunk_len(a));
+    if (Ly.n_seg > 1 && w[0].carry == nullptr) return cudaErrorInvalidValue;
     return run_segments(a, w, nbuf, Ly, s);
 }
 

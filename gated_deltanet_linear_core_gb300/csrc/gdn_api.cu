@@ -332,10 +332,10 @@ size_t gdn_chunk_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t
 }
 
 int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_seqlens, gdn_dims_t dims,
-                                   gdn_dtype_t dtype) {
+                                   gdn_dtype_t dtype, uint32_t flags) {
     if (check_dims(dims, dtype) != GDN_OK || n_seq < 1 || T_tot <= 0) return 0;
     if (dtype != GDN_BF16 || dims.d_k != 128) return 1;  // the CUDA-core path: one kernel
-    return gdn::chunk_split_launches(n_seq, T_tot, dims.H_v, has_cu_seqlens != 0);
+    return gdn::chunk_split_launches(n_seq, T_tot, dims.H_v, has_cu_seqlens != 0, (int)((flags >> 8) & 0xffu));
 }
 
 namespace {
@@ -359,7 +359,9 @@ gdn_status_t chunk_prefill_impl(const void* qkv, const void* a, const void* b, c
     if (chunk != 16 && chunk != 32 && chunk != 64) return GDN_ERR_INVALID_ARG;
     const bool tensor_core = dtype == GDN_BF16 && dims.d_k == 128;
     if ((flags & GDN_SOLVE_NEUMANN) && !tensor_core) return GDN_ERR_UNSUPPORTED;
-    if (chunk != 64 && tensor_core) return GDN_ERR_UNSUPPORTED;
+    // shorter chunks on the tensor-core path run in more workspace segments,
+    // between which the state crosses through final_state
+    if (chunk != 64 && tensor_core && T_tot > 0 && final_state == nullptr) return GDN_ERR_UNSUPPORTED;
     if (!isfinite(scale)) return GDN_ERR_INVALID_ARG;
     if (T_tot > 0 && (qkv == nullptr || o == nullptr)) return GDN_ERR_INVALID_ARG;
     if (!aligned16(qkv) || !aligned16(o) || !aligned16(initial_state) || !aligned16(final_state) ||
@@ -428,13 +430,13 @@ size_t gdn_layer_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t
 }
 
 int32_t gdn_layer_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_seqlens, gdn_dims_t dims,
-                                   gdn_dtype_t dtype) {
+                                   gdn_dtype_t dtype, uint32_t flags) {
     if (check_dims(dims, dtype) != GDN_OK || n_seq < 1 || T_tot <= 0) return 0;
     // the chunked rule and the norm, and the conv (on the tensor-core path it
     // runs in the chunk kernels, which with conv_state_out not conv_state_in
     // also write the conv state)
     const bool tc = dtype == GDN_BF16 && dims.d_k == 128;
-    return (tc ? 1 : 2) + gdn_chunk_prefill_launches(n_seq, T_tot, has_cu_seqlens, dims, dtype);
+    return (tc ? 1 : 2) + gdn_chunk_prefill_launches(n_seq, T_tot, has_cu_seqlens, dims, dtype, flags);
 }
 
 gdn_status_t gdn_layer_prefill(const void* x, const void* z, const void* a, const void* b, const void* conv_w,
@@ -463,10 +465,12 @@ gdn_status_t gdn_layer_prefill(const void* x, const void* z, const void* a, cons
         // checkpoints inside the chunk kernels (the state in place: by a pass
         // after them), then RMSNormGated
         if ((st = check_gates(a, b, A_log, dt_bias, nullptr, nullptr, dtype)) != GDN_OK) return st;
-        if (flags & ~(GDN_QK_L2NORM | GDN_SOLVE_NEUMANN)) {
-            if (flags & ~(GDN_QK_L2NORM | GDN_SOLVE_NEUMANN | GDN_CHUNK(0xff))) return GDN_ERR_INVALID_ARG;
-            const uint32_t c = (flags >> 8) & 0xffu;
-            if (c != 0 && c != 64) return c == 16 || c == 32 ? GDN_ERR_UNSUPPORTED : GDN_ERR_INVALID_ARG;
+        if (flags & ~(GDN_QK_L2NORM | GDN_SOLVE_NEUMANN | GDN_CHUNK(0xff))) return GDN_ERR_INVALID_ARG;
+        const uint32_t c = (flags >> 8) & 0xffu;
+        if (c != 0 && c != 16 && c != 32 && c != 64) return GDN_ERR_INVALID_ARG;
+        // shorter chunks: more segments, the state crossing them through final_state
+        if (c == 16 || c == 32) {
+            if (final_state == nullptr) return GDN_ERR_UNSUPPORTED;
         }
         if (!isfinite(scale)) return GDN_ERR_INVALID_ARG;
         if (!aligned16(conv_w) || !aligned16(conv_state_in) || !aligned16(conv_state_out) ||
@@ -485,7 +489,7 @@ gdn_status_t gdn_layer_prefill(const void* x, const void* z, const void* a, cons
         d.scale = scale == 0.f ? 1.0f / sqrtf((float)dims.d_k) : scale;
         d.l2norm = (flags & GDN_QK_L2NORM) != 0;
         d.neumann = (flags & GDN_SOLVE_NEUMANN) != 0;
-        d.chunk = 64;
+        d.chunk = c == 0 ? 64 : (int)c;
         d.o = out;
         d.conv_w = conv_w;
         d.conv_state0 = conv_state_in;

@@ -55,7 +55,7 @@ struct DeltaArgs {
     int l2norm;
     void* o;  // [T, H_v, D]
     int neumann;  // chunk inverse by the Neumann-style product (tensor-core path)
-    int chunk;    // chunk size of the CUDA-core path: 16, 32 or 64 (0: 64)
+    int chunk;    // tokens per chunk: 16, 32 or 64 (0: 64)
     // Conv1d + SiLU inside the chunk kernels (tensor-core path): with conv_w
     // set, qkv is the raw conv input x and the kernels compute y themselves
     // from x, these taps ([conv_dim][4]) and the sequences' conv states before
@@ -132,8 +132,9 @@ cudaError_t launch_chunk_split(const DeltaArgs& a, void* workspace, size_t ws_by
 // one workspace segment everything runs on s_chain after ev_pre.
 cudaError_t launch_chunk_split_two(const DeltaArgs& a, void* workspace, size_t ws_bytes, cudaStream_t s_pre,
                                    cudaStream_t s_chain, cudaEvent_t ev_pre);
-// Kernel launches launch_chunk_split issues: chunk offsets, then intra + chain per segment.
-int chunk_split_launches(int n_seq, int64_t T, int H_v, bool has_cu);
+// Kernel launches launch_chunk_split issues: chunk offsets, then intra + chain per segment
+// (chunk: tokens per chunk, 16, 32 or 64).
+int chunk_split_launches(int n_seq, int64_t T, int H_v, bool has_cu, int chunk);
 
 // The same chunked prefill with its scratch in a fixed device array of the
 // library (gdn_chunk_prefill_noalloc): no allocation; final_state required.

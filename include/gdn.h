@@ -84,10 +84,13 @@ typedef struct {
  * at 0 means 64.  Any C gives the per-token rule's result up to rounding
  * (cortex GatedDeltaNet commit, "Performance note": chunk_size=64 is one
  * choice of the chunked algorithm); it trades per-chunk matrix work (which
- * grows with C) against the number of sequential chunk steps.  The CUDA-core
- * path takes all three; the tensor-core path (bf16, d = 128) is built around
- * C = 64 and returns GDN_ERR_UNSUPPORTED for the others.  Other values:
- * GDN_ERR_INVALID_ARG. */
+ * grows with C) against the number of sequential chunk steps.  Both paths take
+ * all three.  The tensor-core path (bf16, d = 128) keeps its tiles at 64 rows:
+ * a chunk of 16 or 32 tokens fills the first rows of its tile, so it costs
+ * about what a chunk of 64 does, and the call runs in more workspace segments
+ * (the same workspace size), between which the state crosses through
+ * final_state, which these chunk sizes require there (else
+ * GDN_ERR_UNSUPPORTED).  Other values: GDN_ERR_INVALID_ARG. */
 #define GDN_CHUNK(c) ((((uint32_t)(c)) & 0xffu) << 8)
 
 /* Text for a status code (static storage, never NULL). */
@@ -232,14 +235,15 @@ gdn_status_t gdn_layer_prefill_host(const void* h_qkv, const void* h_z, const vo
 gdn_status_t gdn_selftest_bounded_wait(int64_t limit_ns, void* stream);
 
 /*
- * Number of kernel launches one gdn_chunk_prefill call with these sizes
- * issues (for profiling and launch accounting; the library has no paper
+ * Number of kernel launches one gdn_chunk_prefill call with these sizes and
+ * flags issues (for profiling and launch accounting; the library has no paper
  * counterpart for it): on the tensor-core path, a chunk-offsets kernel when
  * cu_seqlens is given (has_cu_seqlens != 0), then an intra and a chain kernel
- * per workspace segment.  0 for T_tot == 0 or invalid dims.
+ * per workspace segment (more segments for GDN_CHUNK(16) and GDN_CHUNK(32);
+ * the other flag bits do not matter).  0 for T_tot == 0 or invalid dims.
  */
 int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_seqlens, gdn_dims_t dims,
-                                   gdn_dtype_t dtype);
+                                   gdn_dtype_t dtype, uint32_t flags);
 
 /*
  * Chunked gated delta rule (chunk size 64, WY/UT form) over packed sequences.
@@ -261,6 +265,7 @@ int32_t gdn_chunk_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_
  *   cu_seqlens (device) [n_seq + 1] int32 or NULL (one sequence)
  *   initial_state (device) [n_seq, H_v, d_k, d_v] f32 or NULL (zeros)
  *   final_state   (device) [n_seq, H_v, d_k, d_v] f32 or NULL; may alias initial_state
+ *               (required on the tensor-core path with GDN_CHUNK(16) or (32))
  *   ckpt_every  0 or a positive multiple of 64; state_ckpt_out (device)
  *               [gdn_ckpt_count rows, H_v, d_k, d_v] f32: state after m*ckpt_every tokens
  *   ckpt_rows   rows allocated in state_ckpt_out; rows past it are never written;
@@ -458,7 +463,7 @@ gdn_status_t gdn_chunk_prefill_norm(const void* qkv, const void* a, const void* 
  */
 size_t gdn_layer_prefill_workspace_size(int32_t n_seq, int64_t T_tot, gdn_dims_t dims, gdn_dtype_t dtype);
 int32_t gdn_layer_prefill_launches(int32_t n_seq, int64_t T_tot, int32_t has_cu_seqlens, gdn_dims_t dims,
-                                   gdn_dtype_t dtype);
+                                   gdn_dtype_t dtype, uint32_t flags);
 gdn_status_t gdn_layer_prefill(const void* x, const void* z, const void* a, const void* b, const void* conv_w,
                                const float* A_log, const float* dt_bias, const void* norm_w, float norm_eps,
                                const int32_t* cu_seqlens, int32_t n_seq, int64_t T_tot,

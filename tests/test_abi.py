@@ -139,13 +139,15 @@ def test_chunk_prefill_validation(lib):
     neu = E.GDN_QK_L2NORM | E.GDN_SOLVE_NEUMANN
     assert chunk(lib, flags=neu) == E.GDN_ERR_WORKSPACE
     assert chunk(lib, flags=neu, dt=E.GDN_F32, a=A + 0x1000, b=A + 0x2000) == E.GDN_ERR_UNSUPPORTED
-    # the chunk-size field (bits 8..15): 16, 32, 64 or 0; the tensor-core path takes 64 only
+    # the chunk-size field (bits 8..15): 16, 32, 64 or 0; on the tensor-core path
+    # 16 and 32 need final_state (the state crosses the extra segments in it)
     assert chunk(lib, flags=1 | E.GDN_CHUNK(48)) == E.GDN_ERR_INVALID_ARG
     assert chunk(lib, flags=1 | E.GDN_CHUNK(128)) == E.GDN_ERR_INVALID_ARG
     assert chunk(lib, flags=1 | E.GDN_CHUNK(8)) == E.GDN_ERR_INVALID_ARG
     assert chunk(lib, flags=1 | (1 << 16)) == E.GDN_ERR_INVALID_ARG
     assert chunk(lib, flags=1 | E.GDN_CHUNK(16)) == E.GDN_ERR_UNSUPPORTED
     assert chunk(lib, flags=1 | E.GDN_CHUNK(32)) == E.GDN_ERR_UNSUPPORTED
+    assert chunk(lib, flags=1 | E.GDN_CHUNK(32), Sf=A + 0x20000) == E.GDN_ERR_WORKSPACE  # valid
     assert chunk(lib, flags=1 | E.GDN_CHUNK(64)) == E.GDN_ERR_WORKSPACE  # valid; no workspace given
     assert chunk(lib, scale=float("nan")) == E.GDN_ERR_INVALID_ARG
     assert chunk(lib, scale=float("inf")) == E.GDN_ERR_INVALID_ARG
@@ -344,6 +346,12 @@ def test_prefill_launch_count(lib):
     assert gdn.gdn_chunk_prefill_launches(1, 262144, dims, torch.bfloat16, cu_seqlens=None) == long_run - 1
     assert gdn.gdn_chunk_prefill_launches(1, 64, gdn.GDNDims(2, 4, 16, 16), torch.float32) == 1
     assert gdn.gdn_chunk_prefill_launches(1, 0, dims, torch.bfloat16) == 0
+    # shorter chunks on the tensor-core path: the 65-chunk segments of the
+    # 4096-token call hold 129 chunks of 32 tokens in 2 segments, 257 of 16 in 4
+    assert gdn.gdn_chunk_prefill_launches(1, 4096, dims, torch.bfloat16, cu_seqlens=None, chunk=32) == 4
+    assert gdn.gdn_chunk_prefill_launches(1, 4096, dims, torch.bfloat16, cu_seqlens=None, chunk=16) == 8
+    assert gdn.gdn_layer_prefill_launches(1, 4096, dims, torch.bfloat16, cu_seqlens=None, chunk=32) == 5
+    assert gdn.gdn_chunk_prefill_launches(1, 64, gdn.GDNDims(2, 4, 16, 16), torch.float32, chunk=16) == 1
 
 
 def test_host_prefill_piece_plan(lib):

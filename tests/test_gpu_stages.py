@@ -194,12 +194,53 @@ def test_chunk_prefill_chunk_sizes(chunk, dtype, shape):
     assert torch.equal(Sf[z].cpu(), inp["S0"][z])
 
 
-def test_chunk_size_other_than_64_is_refused_on_the_tensor_core_path():
-    inp = _delta_inputs(SMALL_128, torch.bfloat16, [70], seed=17)
+@pytest.mark.parametrize("chunk", [16, 32])
+def test_chunk_prefill_chunk_sizes_tensor_core(chunk):
+    """The tensor-core path at chunk sizes 16 and 32: each chunk fills the
+    first rows of its 64-row tile, as a partial chunk does, and the call runs
+    in more workspace segments with the state carried through final_state.
+    Against the oracle at the bf16 tolerance over sequences of 0..200 tokens
+    plus two longer ones (several segments), with checkpoints every 64 tokens;
+    the layer call at the same chunk size (conv inside the chunk kernels)
+    equals the separate calls bit for bit; without final_state the call is
+    refused."""
+    shape = SMALL_128
+    lengths = LENGTHS + [1500, 700]
+    inp = _delta_inputs(shape, torch.bfloat16, lengths, seed=16)
     d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    N = len(lengths)
+    T = int(inp["mixed_qkv"].shape[0])
+    rows = gdn.gdn_ckpt_count(inp["cu_seqlens"], 64)
+    ck = torch.full((rows, shape.H_v, shape.d_k, shape.d_v), float("nan"), device="cuda")
+    Sf = torch.full((N, shape.H_v, shape.d_k, shape.d_v), float("nan"), device="cuda")
+    o = gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(shape), d["a"], d["b"], d["A_log"], d["dt_bias"],
+                              cu_seqlens=d["cu_seqlens"], initial_state=d["S0"], final_state=Sf, ckpt_every=64,
+                              state_ckpt_out=ck, chunk=chunk)
+    torch.cuda.synchronize()
+    assert gdn.gdn_chunk_prefill_launches(N, T, _dims(shape), torch.bfloat16, chunk=chunk) > \
+        gdn.gdn_chunk_prefill_launches(N, T, _dims(shape), torch.bfloat16), "expected more segments"
+    o_ref, S_ref, ck_ref = _oracle_delta(inp, shape, ckpt_every=64)
+    tol = TOL[torch.bfloat16]
+    assert_close("o", host(o), o_ref, tol, per_head_axis=1)
+    assert_close("S_final", host(Sf), S_ref, tol, per_head_axis=1)
+    assert_close("ckpt", host(ck), ck_ref, tol)
+    z = lengths.index(0)
+    assert torch.equal(Sf[z].cpu(), inp["S0"][z])
     with pytest.raises(gdn.GDNError):
-        gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(SMALL_128), d["a"], d["b"], d["A_log"], d["dt_bias"],
-                              cu_seqlens=d["cu_seqlens"], chunk=32)
+        gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(shape), d["a"], d["b"], d["A_log"], d["dt_bias"],
+                              cu_seqlens=d["cu_seqlens"], chunk=chunk)
+    # the layer call at this chunk size against the three calls
+    lay = W.layer_inputs(shape, torch.bfloat16, lengths, seed=19, init_state=True)
+    ld = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in lay.items()}
+    args = (ld["mixed_qkv"], ld["z"], ld["a"], ld["b"], ld["conv_w"], ld["A_log"], ld["dt_bias"],
+            ld["norm_w"], _dims(shape))
+    kw = dict(cu_seqlens=ld["cu_seqlens"], initial_state=ld["S0"], conv_state=ld["conv_state0"],
+              ckpt_every=64, chunk=chunk)
+    fused = gdn.gdn_layer_prefill(*args, final_state=torch.empty_like(ld["S0"]), **kw)
+    staged = gdn.gdn_layer_prefill(*args, return_intermediates=True, final_state=torch.empty_like(ld["S0"]), **kw)
+    torch.cuda.synchronize()
+    for key in ("out", "final_state", "conv_state", "state_ckpt", "conv_ckpt"):
+        assert torch.equal(fused[key], staged[key]), key
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
