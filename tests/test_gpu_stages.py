@@ -330,6 +330,24 @@ def test_chunk_prefill_decay_range_forms():
     assert_close("S_final", host(Sf), S_ref, TOL[torch.bfloat16], per_head_axis=1)
 
 
+def test_chunk_prefill_neumann_short_chunks():
+    """GDN_SOLVE_NEUMANN with 32-token chunks on the tensor-core path (the
+    product-form inverse over the first rows of each tile) against the oracle
+    at the bf16 tolerance, on N(0,1) activations with the configs' gate
+    distributions, ragged and empty sequences included."""
+    shape = SMALL_128
+    inp = _delta_inputs(shape, torch.bfloat16, LENGTHS, seed=15)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    Sf = torch.empty_like(d["S0"])
+    o = gdn.gdn_chunk_prefill(d["mixed_qkv"], _dims(shape), d["a"], d["b"], d["A_log"], d["dt_bias"],
+                              cu_seqlens=d["cu_seqlens"], initial_state=d["S0"], final_state=Sf,
+                              solve="neumann", chunk=32)
+    torch.cuda.synchronize()
+    o_ref, S_ref, _ = _oracle_delta(inp, shape)
+    assert_close("o", host(o), o_ref, TOL[torch.bfloat16], per_head_axis=1)
+    assert_close("S_final", host(Sf), S_ref, TOL[torch.bfloat16], per_head_axis=1)
+
+
 def test_chunk_prefill_neumann_solve():
     """GDN_SOLVE_NEUMANN (tensor-core path): within the bf16 tolerance of the
     oracle on N(0,1) activations with the configs' gate distributions, where
