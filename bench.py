@@ -10,7 +10,8 @@ HBM; the same line carries the other prefill workloads (Coder-Next varlen with
 resumed states; the 262144-token sequence with checkpoints every 4096 tokens
 and its 128-step decode tail) under "prefill_workloads", the decode path (the
 27B decode workload: 64 sequences, one token each per step) under "decode",
-each with the roofline of its dominant kernel, the end-to-end rate through
+each with the roofline of its dominant kernel, one rank's call under head
+sharding over 2, 4 and 8 ranks ("head_shards"), the end-to-end rate through
 host buffers ("e2e"), the oracle's CPU rate on all cores and on one
 ("cpu_baseline") and the SM clocks seen while timing.
 
@@ -468,6 +469,40 @@ def run_ours(args):
                 "l2": f"back to back over {RING} input copies (each call's inputs out of L2)"}
         for kname, t, nb in (("gdn_conv1d_fwd", conv_alone, conv_bytes),
                              ("gdn_rmsnorm_gated", norm_alone, norm_bytes))}
+
+    # ---- head sharding: the first rank's shard of a tensor-parallel group of
+    # 2, 4 and 8 ranks (head_shard), timed like the conv and norm above over the
+    # shard's slices of the input copies.  The ranks of a group run their own
+    # heads at the same time on their own GPUs, with no exchange inside the
+    # core, so the group takes one shard's time per call.
+    full_call_ms = statistics.mean(step_ms) / args.calls
+    head_shards = {}
+    for tp in (2, 4, 8):
+        sh = gdn.head_shard(dims, 0, tp)
+        ch = sh.channels.to(dev)
+        zc = slice(sh.h0 * s.d_v, sh.h1 * s.d_v)
+        sring = [{"mixed_qkv": x["mixed_qkv"][:, ch].contiguous(), "z": x["z"][:, zc].contiguous(),
+                  "a": x["a"][:, sh.h0:sh.h1].contiguous(), "b": x["b"][:, sh.h0:sh.h1].contiguous()}
+                 for x in ring]
+        s_w = d["conv_w"][ch].contiguous()
+        s_alog, s_dtb = d["A_log"][sh.h0:sh.h1].contiguous(), d["dt_bias"][sh.h0:sh.h1].contiguous()
+        s_out = [torch.empty((T, (sh.h1 - sh.h0) * s.d_v), dtype=wp.dtype, device=dev) for _ in range(RING)]
+        s_S = torch.empty((1, sh.h1 - sh.h0, s.d_k, s.d_v), dtype=torch.float32, device=dev)
+        s_cs = torch.empty((1, ch.numel(), 3), dtype=wp.dtype, device=dev)
+        s_ws = torch.empty(gdn.gdn_layer_prefill_workspace_size(1, T, sh.dims, wp.dtype), dtype=torch.uint8,
+                           device=dev)
+        t_sh = alone(lambda i: gdn.gdn_layer_prefill(
+            sring[i]["mixed_qkv"], sring[i]["z"], sring[i]["a"], sring[i]["b"], s_w, s_alog, s_dtb, d["norm_w"],
+            sh.dims, out=s_out[i], final_state=s_S, conv_state_out=s_cs, workspace=s_ws))
+        launches += (args.steps * args.calls + RING) * gdn.gdn_layer_prefill_launches(1, T, sh.dims, wp.dtype,
+                                                                                      cu_seqlens=False)
+        head_shards[f"tp{tp}"] = {
+            "key_heads": sh.dims.H_k, "value_heads": sh.dims.H_v, "ms_per_call": round(t_sh * 1e3, 4),
+            "group_tokens_per_s": round(T / t_sh, 1),
+            "speedup_over_one_gpu": round(full_call_ms / (t_sh * 1e3), 3)}
+        del sring, s_out, s_ws
+    torch.cuda.empty_cache()
+
     total_s = max_over_ranks(dist, sum(step_ms) / 1e3, dev)
     value = world * T * args.calls * args.steps / total_s
     chunk_avg = sum(chunk_ms) / len(chunk_ms) / 1e3
@@ -823,6 +858,11 @@ def run_ours(args):
             "roofline": roofline,
             "hbm_kernels": hbm_alone,
             "prefill_workloads": workloads,
+            "head_shards": {"workload": PREFILL, "rank": 0, "calls": args.steps * args.calls,
+                            "note": "one rank's shard timed on this GPU; the group's ranks run theirs "
+                                    "at the same time on their own GPUs, so the group takes one shard's "
+                                    "time per call",
+                            **head_shards},
             "decode": decode,
             "e2e": e2e,
             "cpu_baseline": cpu,
