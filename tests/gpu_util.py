@@ -1,5 +1,7 @@
 """Helpers of the GPU parity tests: moving seeded inputs to the device, slicing
-one value head out of a layer's inputs for the oracle, and tolerance checks."""
+one value head out of a layer's inputs for the oracle, the oracle's decode step
+with the activations rounded where the layer's calls hand them on, and
+tolerance checks."""
 from __future__ import annotations
 
 from concurrent.futures import ThreadPoolExecutor
@@ -73,3 +75,21 @@ def oracle_heads_prefill(inp, shape, heads, ckpt_every=0):
     with ThreadPoolExecutor(max(1, min(len(heads), oracle.max_threads()))) as ex:
         return dict(zip(heads, ex.map(lambda h: oracle_head_prefill(inp, shape, h, ckpt_every),
                                       heads)))
+
+
+def rounded_to(dtype):
+    """f64 array -> the nearest values of the activation dtype, as f64."""
+    return lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dtype).to(torch.float64).numpy()
+
+
+def oracle_step_in_activation_dtype(x, z, a, b, conv_w, A_log, dt_bias, norm_w, s, S, conv_state, rnd):
+    """One decode step of B sequences by the oracle's definitions, with the
+    conv output y and the rule's output o rounded to the activation dtype
+    where the layer's calls hand them on (each call's output is an activation
+    of that dtype).  Returns (out, S_new, conv_state_new)."""
+    cu = np.arange(x.shape[0] + 1, dtype=np.int64)
+    y, cs_new, _ = oracle.conv1d(x, conv_w, cu, conv_state, True, 0)
+    q, k, v = oracle.split_qkv(rnd(y), s.H_k, s.H_v, s.d_k, s.d_v)
+    g, beta = oracle.gates(a, b, A_log, dt_bias)
+    o, S_new, _ = oracle.delta_rule(q, k, v, g, beta, cu, S, None, True, 0)
+    return oracle.rmsnorm_gated(rnd(o), z, norm_w), S_new, cs_new

@@ -20,7 +20,7 @@ import torch
 import gated_deltanet_linear_core_gb300 as gdn
 import oracle
 import workloads as W
-from gpu_util import TOL, assert_close, host
+from gpu_util import TOL, assert_close, host, oracle_step_in_activation_dtype, rounded_to
 
 pytestmark = pytest.mark.gpu
 
@@ -58,24 +58,6 @@ def draw_case(seed: int, dtype: torch.dtype) -> dict:
 
 def _dims(s):
     return gdn.GDNDims(s.H_k, s.H_v, s.d_k, s.d_v)
-
-
-def rounded_to(dtype):
-    """f64 array -> the nearest values of the activation dtype, as f64."""
-    return lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dtype).to(torch.float64).numpy()
-
-
-def oracle_step_in_activation_dtype(x, z, a, b, conv_w, A_log, dt_bias, norm_w, s, S, conv_state, rnd):
-    """One decode step of B sequences by the oracle's definitions, with the
-    conv output y and the rule's output o rounded to the activation dtype
-    where the layer's calls hand them on (each call's output is an activation
-    of that dtype).  Returns (out, S_new, conv_state_new)."""
-    cu = np.arange(x.shape[0] + 1, dtype=np.int64)
-    y, cs_new, _ = oracle.conv1d(x, conv_w, cu, conv_state, True, 0)
-    q, k, v = oracle.split_qkv(rnd(y), s.H_k, s.H_v, s.d_k, s.d_v)
-    g, beta = oracle.gates(a, b, A_log, dt_bias)
-    o, S_new, _ = oracle.delta_rule(q, k, v, g, beta, cu, S, None, True, 0)
-    return oracle.rmsnorm_gated(rnd(o), z, norm_w), S_new, cs_new
 
 
 CASES = [(torch.bfloat16, i) for i in range(30)] + [(torch.float32, i) for i in range(30, 40)]

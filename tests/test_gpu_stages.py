@@ -12,7 +12,7 @@ import torch
 import gated_deltanet_linear_core_gb300 as gdn
 import oracle
 import workloads as W
-from gpu_util import TOL, assert_close, host, rel_l2
+from gpu_util import TOL, assert_close, host, oracle_step_in_activation_dtype, rel_l2, rounded_to
 from precision_model import chunked_bf16_operands
 
 pytestmark = pytest.mark.gpu
@@ -670,7 +670,8 @@ def test_decode_verify_equals_successive_fused_steps(dtype, shape, K):
     from slot slots[b, 0] and the states after draft token t written to slot
     slots[b, t + 1]) gives every output, state and conv state of K successive
     gdn_decode_step calls bit for bit; slot slots[b, 0] is only read (unless it
-    is repeated as slots[b, K]) and slots of no row are untouched."""
+    is repeated as slots[b, K]) and slots of no row are untouched.  The outputs
+    and the last states are also held to the oracle's K single-token steps."""
     B = 5
     n_slots = B * (K + 1) + 3
     d = W.decode_inputs(shape, dtype, B, K, seed=43)
@@ -706,6 +707,23 @@ def test_decode_verify_equals_successive_fused_steps(dtype, shape, K):
     others = [i for i in range(n_slots) if i not in slots.flatten().tolist()]
     assert torch.equal(S_v[others].cpu(), S_all[others])
     assert torch.equal(cs_v[others].cpu(), cs_all[others])
+    # and the oracle: K single-token steps from each row's first slot; the
+    # states against the plain steps, the output rows against the steps with
+    # y and o rounded to the activation dtype, as the calls hand them on
+    f = W.to_f64
+    rnd = rounded_to(dtype)
+    S_o, cs_o = f(S_all[slots[:, 0].long()]), f(cs_all[slots[:, 0].long()])
+    S_a, cs_a, refs = S_o, cs_o, []
+    for t in range(K):
+        step = (f(d["qkv"][t]), f(d["z"][t]), f(d["a"][t]), f(d["b"][t]), f(p["conv_w"]), f(p["A_log"]),
+                f(p["dt_bias"]), f(p["norm_w"]))
+        _, S_o, cs_o, _ = oracle.layer_decode_step(*step, shape.H_k, shape.H_v, shape.d_k, shape.d_v, S_o, cs_o)
+        o_a, S_a, cs_a = oracle_step_in_activation_dtype(*step, shape, S_a, cs_a, rnd)
+        refs.append(o_a)
+    tol = TOL[dtype]
+    assert_close("verify out", host(out.transpose(0, 1)), np.stack(refs), tol)
+    assert_close("verify final state", host(S_v[slots[:, K].long()]), S_o, tol)
+    assert np.array_equal(host(cs_v[slots[:, K].long()]), cs_o), "verify final conv state"
 
 
 def test_overlapped_segments_equal_sequential_segments():
