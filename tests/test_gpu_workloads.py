@@ -227,14 +227,16 @@ def _host_prefill(inp, shape):
     return r
 
 
-@pytest.mark.parametrize("T", [4096, 3000, 64])
-def test_host_streamed_prefill_equals_device_prefill(T):
+@pytest.mark.parametrize("T,init", [(4096, True), (3000, True), (64, True), (1, True), (513, False),
+                                    (1100, True), (5000, False)])
+def test_host_streamed_prefill_equals_device_prefill(T, init):
     """gdn_layer_prefill_host (pinned host buffers, pieces of 64-aligned tokens,
     copies overlapped with the kernels) gives the device path's result bit for
     bit -- the pieces cut at chunk boundaries and the states carry exactly --
-    and matches the oracle on sampled heads."""
+    and matches the oracle on sampled heads; one token, a piece and one token,
+    more tokens than the 4096-token cut, and zero initial states included."""
     shape = W.QWEN36_27B
-    inp = W.layer_inputs(shape, torch.bfloat16, [T], seed=31, init_state=True)
+    inp = W.layer_inputs(shape, torch.bfloat16, [T], seed=31, init_state=init)
     dims = _dims(shape)
     piece = gdn._lib.load().gdn_layer_prefill_host_piece(T, gdn._dims(dims), gdn._lib.GDN_BF16)
     assert piece % 64 == 0 or piece == T
