@@ -142,6 +142,26 @@ def test_more_sequences_than_the_longest_first_order_covers():
     assert np.array_equal(host(fz["conv_state"]), ref["conv_state"])
 
 
+@pytest.mark.parametrize("H_k,H_v,lengths", [(16, 128, [300, 212]), (64, 64, [200]), (2, 32, [130, 1, 66])],
+                         ids=["r8-128heads", "r1-64heads", "r16"])
+def test_head_counts_beyond_the_workloads(H_k, H_v, lengths):
+    # 128 value heads (r = 8: 256 chain CTAs as 128-column CTAs), 64 key heads
+    # at r = 1, and r = 16 (beyond what the decode kernels take): the layer call
+    # against the separate calls bit for bit and against the oracle
+    shape = W.GDNShape(H_k=H_k, H_v=H_v, d_k=128, d_v=128)
+    inp = W.layer_inputs(shape, torch.bfloat16, lengths, seed=40 + H_k, init_state=True)
+    fz = _run(inp, shape, one_call=True, ckpt_every=128)
+    sp = _run(inp, shape, one_call=False, ckpt_every=128)
+    _compare_with_separate(fz, sp)
+    ref = _oracle(inp, shape, ckpt_every=128)
+    tol = TOL[torch.bfloat16]
+    assert_close("out", host(fz["out"]), ref["out"], tol)
+    assert_close("S", host(fz["final_state"]), ref["S"], tol, per_head_axis=1)
+    if ref["S_ckpt"] is not None and ref["S_ckpt"].shape[0]:
+        assert_close("S ckpt", host(fz["state_ckpt"]), ref["S_ckpt"], tol)
+    assert np.array_equal(host(fz["conv_state"]), ref["conv_state"])
+
+
 def test_conv_state_in_place_equals_out_of_place():
     # bf16 with d = 128 runs the conv inside the chunk kernels, which then also
     # write the conv state and checkpoints -- unless the state is updated in
